@@ -11,7 +11,8 @@ with one FP16 scale and one FP16 zero-point; keys are grouped per channel
 
 What the pages leave open and the reading taken here:
 
-* zero-point and scale: z = the largest fp16 not above min(x);
+* zero-point and scale: z = the largest fp16 not above min(x) (a zero
+  minimum or maximum counts as +0.0);
   s = the smallest fp16 not below fp32(fp32(max(x) - z) / (2^b - 1)).
   The directed roundings keep z <= min and z + (2^b-1) s >= max, so the
   stored fp16 pair still covers the group and |x - x_hat| <= s/2.
@@ -68,8 +69,10 @@ def quantize_groups(x, bits):
         raise ValueError("bits must be 2, 4 or 8")
     x = np.asarray(x).astype(F32)          # fp16 / bf16 / fp32 -> fp32 is exact
     qmax = (1 << bits) - 1
-    mn = x.min(axis=-1)
-    mx = x.max(axis=-1)
+    # + 0.0 turns a -0.0 extreme into +0.0: the sign of a zero minimum or
+    # maximum is otherwise unspecified (IEEE min/max of signed zeros)
+    mn = (x.min(axis=-1) + F32(0.0)).astype(F32)
+    mx = (x.max(axis=-1) + F32(0.0)).astype(F32)
     zero = f16_round_down(mn)
     z32 = zero.astype(F32)
     span = (mx - z32).astype(F32)

@@ -162,3 +162,15 @@ def test_token_grouping_layout():
     assert float(s[0, 1]) == 2.0 and float(z[0, 1]) == 5.0
     assert int(w[0, 2]) == 0xE4E4E4E4 and int(w[0, 0]) == 0
     assert np.array_equal(quant.unpack_token(w, s, z, 2, 32), x)
+
+
+def test_signed_zero_extremes_are_canonical():
+    """A group whose minimum/maximum is -0.0 stores the same z/s bits as +0.0."""
+    a = np.zeros((2, 32), F32)
+    a[0, 5] = F32(-0.0)
+    a[1, :] = F32(-0.0)
+    a[0, 7] = F32(1.5)
+    q, s, z = quant.quantize_groups(a, 2)
+    assert z.view(np.uint16).tolist() == [0, 0]
+    assert s.view(np.uint16)[1] == 0
+    assert np.all(q[1] == 0)
