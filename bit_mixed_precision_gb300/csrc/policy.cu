@@ -1,0 +1,627 @@
+// requant_demote: the cache life cycles.
+//
+// MiniKV (review page, "Assumptions & free parameters"; verdict JSON
+// key_machinery): selection persists from the end of prefill; selected
+// tokens are packed once (per-channel INT2 keys, per-token INT2 values),
+// the newest stay at full precision in the residual and move to the packed
+// tier G at a time.
+// DiffKV (verdict JSON key_machinery, Algorithm 1 comments): significance =
+// mean attention received, max over the GQA group; K8V4 above alpha_h/N,
+// K4V2 above alpha_l/N, pruned below, decided once as a token leaves the
+// recent window.
+// MiKV (rebuttal: re-quantisation paragraph, Q1, regrouping paragraph): the
+// top share by cumulative attention is INT4, the rest INT2, nothing is
+// evicted, INT4 tokens that leave the top share are re-quantised to INT2.
+//
+// One CTA per unit for every per-unit decision; radix select with ties to
+// the lower position; tier slots are filled in a fixed order so results
+// are deterministic.
+#include "kvq_internal.h"
+#include "pack_device.cuh"
+#include "topk_device.cuh"
+
+namespace kvq {
+
+KVQ_DEFINE_STATUS(policy)
+
+namespace {
+
+__device__ __forceinline__ float unorderable(uint32_t k) {
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ float ld_act(const void* p, size_t i, bool bf) {
+    return bf ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i])
+              : __half2float(reinterpret_cast<const __half*>(p)[i]);
+}
+
+__device__ __forceinline__ void copy_act(void* dst, size_t di, const void* src, size_t si, bool bf) {
+    reinterpret_cast<uint16_t*>(dst)[di] = reinterpret_cast<const uint16_t*>(src)[si];
+    (void)bf;
+}
+
+struct TierDev {
+    int k_bits, v_bits, k_axis, cap;
+    uint32_t* k_codes;
+    uint16_t* k_scale;
+    uint16_t* k_zero;
+    uint32_t* v_codes;
+    uint16_t* v_scale;
+    uint16_t* v_zero;
+    int32_t* token_id;
+    int32_t* count;
+};
+
+struct PolicyArgs {
+    int B, Hq, Hkv, D, G, g, bf16, n_tiers, nr, hi_den;
+    TierDev tier[KVQ_MAX_TIERS];
+    void* res_k;
+    void* res_v;
+    int32_t* res_token_id;
+    int32_t* res_start;
+    int32_t* res_len;
+    int res_cap;
+    int32_t* seq_len;
+    float* win_acc;
+    float* alpha;
+    float* cum_score;
+    int score_cap;
+    // build inputs
+    const void* k_src;
+    const void* v_src;
+    int T;
+    const int32_t* sel_idx;
+    int n_sel;
+    const float* colscore;
+    const int32_t* n_high;
+    const int32_t* n_low;
+};
+
+// Quantise one token row (token grouping, any bit width) into a tier slot.
+template <typename Load>
+__device__ void quant_row(Load load, int D, int G, int bits, uint32_t* codes, uint16_t* s,
+                          uint16_t* z) {
+    for (int grp = 0; grp < D / G; ++grp)
+        quant_token_group([&](int i) { return load(grp * G + i); }, G, bits,
+                          codes + grp * (G * bits / 32), s + grp, z + grp);
+}
+
+__device__ __forceinline__ uint32_t* krow(const TierDev& t, size_t unit, int slot, int D) {
+    return t.k_codes + (unit * t.cap + slot) * (size_t)(D * t.k_bits / 32);
+}
+__device__ __forceinline__ uint32_t* vrow(const TierDev& t, size_t unit, int slot, int D) {
+    return t.v_codes + (unit * t.cap + slot) * (size_t)(D * t.v_bits / 32);
+}
+__device__ __forceinline__ size_t srow(const TierDev& t, size_t unit, int slot, int D, int G) {
+    return (unit * t.cap + slot) * (size_t)(D / G);
+}
+
+// Quantise raw token `pos` of a [units][T][D] source (or ring slot) into a
+// token-grouped tier slot.
+__device__ void put_raw_token(const PolicyArgs& a, const TierDev& t, size_t unit, int slot,
+                              const void* ksrc, const void* vsrc, size_t row_elem, int token_id) {
+    const int D = a.D, G = a.G;
+    const bool bf = a.bf16 != 0;
+    quant_row([&](int c) { return ld_act(ksrc, row_elem + c, bf); }, D, G, t.k_bits,
+              krow(t, unit, slot, D), t.k_scale + srow(t, unit, slot, D, G),
+              t.k_zero + srow(t, unit, slot, D, G));
+    quant_row([&](int c) { return ld_act(vsrc, row_elem + c, bf); }, D, G, t.v_bits,
+              vrow(t, unit, slot, D), t.v_scale + srow(t, unit, slot, D, G),
+              t.v_zero + srow(t, unit, slot, D, G));
+    t.token_id[unit * t.cap + slot] = token_id;
+}
+
+// ----------------------------------------------------------------- MiniKV
+
+// Token ids, residual and counters after the two packing launches.
+__global__ void minikv_build_tail(PolicyArgs a, int npk, int r0) {
+    const size_t unit = blockIdx.x;
+    const int b = (int)(unit / a.Hkv);
+    const int32_t* sel = a.sel_idx + unit * (size_t)a.n_sel;
+    const TierDev& t = a.tier[0];
+    for (int i = threadIdx.x; i < npk; i += blockDim.x) t.token_id[unit * t.cap + i] = sel[i];
+    const bool bf = a.bf16 != 0;
+    for (int idx = threadIdx.x; idx < r0 * a.D; idx += blockDim.x) {
+        const int i = idx / a.D, c = idx % a.D;
+        const int pos = sel[npk + i];
+        const size_t src = (unit * a.T + pos) * (size_t)a.D + c;
+        const size_t dst = (unit * a.res_cap + i) * (size_t)a.D + c;
+        copy_act(a.res_k, dst, a.k_src, src, bf);
+        copy_act(a.res_v, dst, a.v_src, src, bf);
+    }
+    for (int i = threadIdx.x; i < r0; i += blockDim.x)
+        a.res_token_id[unit * a.res_cap + i] = sel[npk + i];
+    if (threadIdx.x == 0) {
+        t.count[unit] = npk;
+        a.res_start[unit] = 0;
+        a.res_len[unit] = r0;
+        if (unit % a.Hkv == 0) a.seq_len[b] = a.T;
+    }
+}
+
+// When the residual holds nr + G tokens, its G oldest move to tier 0:
+// keys per channel (one group along tokens), values per token.
+__global__ void minikv_flush(PolicyArgs a) {
+    const size_t unit = blockIdx.x;
+    const int len = a.res_len[unit], start = a.res_start[unit];
+    const int G = a.G, D = a.D, cap = a.res_cap;
+    if (len != a.nr + G) return;
+    const TierDev& t = a.tier[0];
+    const int cnt = t.count[unit];
+    if (cnt + G > t.cap) {
+        if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
+        return;
+    }
+    const bool bf = a.bf16 != 0;
+    const size_t rb = unit * (size_t)cap;
+    if (bf) {
+        const __nv_bfloat16* rk = reinterpret_cast<const __nv_bfloat16*>(a.res_k);
+        auto row = [&](int i) { return rk + (rb + (start + i) % cap) * D; };
+        uint32_t* codes = t.k_codes + (unit * (size_t)(t.cap * t.k_bits / 32) + cnt * t.k_bits / 32) * D;
+        uint16_t* s = t.k_scale + (unit * (size_t)(t.cap / G) + cnt / G) * D;
+        uint16_t* z = t.k_zero + (unit * (size_t)(t.cap / G) + cnt / G) * D;
+        for (int c = threadIdx.x; c < D; c += blockDim.x)
+            quant_channel_group<__nv_bfloat16>(row, G, c, t.k_bits, codes, D, s + c, z + c);
+    } else {
+        const __half* rk = reinterpret_cast<const __half*>(a.res_k);
+        auto row = [&](int i) { return rk + (rb + (start + i) % cap) * D; };
+        uint32_t* codes = t.k_codes + (unit * (size_t)(t.cap * t.k_bits / 32) + cnt * t.k_bits / 32) * D;
+        uint16_t* s = t.k_scale + (unit * (size_t)(t.cap / G) + cnt / G) * D;
+        uint16_t* z = t.k_zero + (unit * (size_t)(t.cap / G) + cnt / G) * D;
+        for (int c = threadIdx.x; c < D; c += blockDim.x)
+            quant_channel_group<__half>(row, G, c, t.k_bits, codes, D, s + c, z + c);
+    }
+    const int groups = D / G;
+    for (int idx = threadIdx.x; idx < G * groups; idx += blockDim.x) {
+        const int i = idx / groups, grp = idx % groups;
+        const size_t src = (rb + (start + i) % cap) * D + (size_t)grp * G;
+        const int slot = cnt + i;
+        quant_token_group([&](int k) { return ld_act(a.res_v, src + k, bf); }, G, t.v_bits,
+                          vrow(t, unit, slot, D) + grp * (G * t.v_bits / 32),
+                          t.v_scale + srow(t, unit, slot, D, G) + grp,
+                          t.v_zero + srow(t, unit, slot, D, G) + grp);
+    }
+    for (int i = threadIdx.x; i < G; i += blockDim.x)
+        t.token_id[unit * t.cap + cnt + i] = a.res_token_id[rb + (start + i) % cap];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        t.count[unit] = cnt + G;
+        a.res_start[unit] = (start + G) % cap;
+        a.res_len[unit] = len - G;
+    }
+}
+
+// ----------------------------------------------------------------- DiffKV
+
+__global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
+    __shared__ TopkShared sh;
+    const size_t unit = blockIdx.x;
+    const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
+    const int T = a.T, W = a.nr, g = a.g, D = a.D;
+    const int nc = T - W;
+    const float* cs = a.colscore + ((size_t)b * a.Hq + (size_t)hkv * g) * T;
+    auto sig = [&](int j) -> float {
+        const float cnt = (float)(T - j);
+        float m = __fdiv_rn(cs[j], cnt);
+        for (int h = 1; h < g; ++h) m = fmaxf(m, __fdiv_rn(cs[(size_t)h * T + j], cnt));
+        return m;
+    };
+    auto key = [&](int j) { return orderable(sig(j)); };
+    int nh = a.n_high[unit], nl = a.n_low[unit];
+    nh = max(0, min(nh, nc));
+    nl = max(0, min(nl, nc - nh));
+    uint32_t k1 = 0xffffffffu, t1 = 0, k2 = 0xffffffffu, t2 = 0;
+    if (nh > 0) block_radix_select(key, nc, nh, sh, &k1, &t1);
+    if (nh + nl > 0) block_radix_select(key, nc, nh + nl, sh, &k2, &t2);
+    const float Tf = (float)T;
+    const float alpha_h = nh > 0 ? __fmul_rn(Tf, unorderable(k1)) : __int_as_float(0x7f800000);
+    const float alpha_l = nl > 0 ? __fmul_rn(Tf, unorderable(k2)) : alpha_h;
+    const TierDev& th = a.tier[0];
+    const TierDev& tl = a.tier[1];
+    uint32_t eq1_base = 0, eq2_base = 0, hi_base = 0, lo_base = 0;
+    for (int c0 = 0; c0 < nc; c0 += blockDim.x) {
+        const int j = c0 + threadIdx.x;
+        const uint32_t kv = j < nc ? key(j) : 0u;
+        const uint32_t e1 = (j < nc && nh > 0 && kv == k1) ? 1u : 0u;
+        const uint32_t e2 = (j < nc && nh + nl > 0 && kv == k2) ? 1u : 0u;
+        uint32_t tot1, tot2;
+        const uint32_t r1 = block_excl_scan(e1, sh, &tot1);
+        const uint32_t r2 = block_excl_scan(e2, sh, &tot2);
+        const bool in1 = j < nc && nh > 0 && (kv > k1 || (e1 && eq1_base + r1 < t1));
+        const bool in2 = j < nc && nh + nl > 0 && (kv > k2 || (e2 && eq2_base + r2 < t2));
+        const uint32_t is_hi = in1 ? 1u : 0u, is_lo = (in2 && !in1) ? 1u : 0u;
+        uint32_t tot_hi, tot_lo;
+        const uint32_t ph = block_excl_scan(is_hi, sh, &tot_hi);
+        const uint32_t pl = block_excl_scan(is_lo, sh, &tot_lo);
+        const size_t row = (unit * T + j) * (size_t)D;
+        if (is_hi) put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
+        if (is_lo) put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
+        eq1_base += tot1;
+        eq2_base += tot2;
+        hi_base += tot_hi;
+        lo_base += tot_lo;
+    }
+    // recent window -> ring, with the attention each head already gave it
+    const bool bf = a.bf16 != 0;
+    for (int idx = threadIdx.x; idx < W * D; idx += blockDim.x) {
+        const int i = idx / D, c = idx % D;
+        const size_t src = (unit * T + nc + i) * (size_t)D + c;
+        const size_t dst = (unit * a.res_cap + i) * (size_t)D + c;
+        copy_act(a.res_k, dst, a.k_src, src, bf);
+        copy_act(a.res_v, dst, a.v_src, src, bf);
+    }
+    for (int idx = threadIdx.x; idx < W * g; idx += blockDim.x) {
+        const int i = idx / g, h = idx % g;
+        a.win_acc[((size_t)b * a.Hq + (size_t)hkv * g + h) * a.res_cap + i] = cs[(size_t)h * T + nc + i];
+    }
+    for (int i = threadIdx.x; i < W; i += blockDim.x) a.res_token_id[unit * a.res_cap + i] = nc + i;
+    if (threadIdx.x == 0) {
+        th.count[unit] = (int)hi_base;
+        tl.count[unit] = (int)lo_base;
+        a.res_start[unit] = 0;
+        a.res_len[unit] = W;
+        a.alpha[unit * 2] = alpha_h;
+        a.alpha[unit * 2 + 1] = alpha_l;
+        if (hkv == 0) a.seq_len[b] = T;
+    }
+}
+
+// The oldest window token leaves: K8V4, K4V2 or pruned.
+__global__ void diffkv_exit(PolicyArgs a) {
+    const size_t unit = blockIdx.x;
+    const int len = a.res_len[unit];
+    if (len <= a.nr) return;
+    const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
+    const int start = a.res_start[unit], cap = a.res_cap, g = a.g;
+    const int tc = a.res_token_id[unit * cap + start];
+    const int N = a.seq_len[b];
+    const float cnt = (float)(N - tc);
+    float score = -__int_as_float(0x7f800000);
+    for (int h = 0; h < g; ++h)
+        score = fmaxf(score, __fdiv_rn(a.win_acc[((size_t)b * a.Hq + (size_t)hkv * g + h) * cap + start], cnt));
+    const float th_h = __fdiv_rn(a.alpha[unit * 2], (float)N);
+    const float th_l = __fdiv_rn(a.alpha[unit * 2 + 1], (float)N);
+    const int cls = score >= th_h ? 0 : (score >= th_l ? 1 : 2);
+    if (cls < 2) {
+        const TierDev& t = a.tier[cls];
+        const int slot = t.count[unit];
+        if (slot >= t.cap) {
+            if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
+        } else if (threadIdx.x == 0) {
+            put_raw_token(a, t, unit, slot, a.res_k, a.res_v, (unit * cap + start) * (size_t)a.D, tc);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (cls < 2 && a.tier[cls].count[unit] < a.tier[cls].cap) a.tier[cls].count[unit] += 1;
+        a.res_start[unit] = (start + 1) % cap;
+        a.res_len[unit] = len - 1;
+    }
+}
+
+// ----------------------------------------------------------------- MiKV
+
+__global__ void __launch_bounds__(kTopkBlock) mikv_build(PolicyArgs a) {
+    __shared__ TopkShared sh;
+    const size_t unit = blockIdx.x;
+    const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
+    const int T = a.T, g = a.g, D = a.D, nr = a.nr;
+    const int nq = max(T - nr, 0);
+    const float* cs = a.colscore + ((size_t)b * a.Hq + (size_t)hkv * g) * T;
+    float* cum = a.cum_score + unit * (size_t)a.score_cap;
+    for (int j = threadIdx.x; j < T; j += blockDim.x) {
+        float acc = 0.0f;
+        for (int h = 0; h < g; ++h) acc = __fadd_rn(acc, cs[(size_t)h * T + j]);
+        cum[j] = acc;
+    }
+    __syncthreads();
+    const int n4 = nq / a.hi_den;
+    auto key = [&](int j) { return orderable(cum[j]); };
+    uint32_t k1 = 0xffffffffu, t1 = 0;
+    if (n4 > 0) block_radix_select(key, nq, n4, sh, &k1, &t1);
+    const TierDev& th = a.tier[0];
+    const TierDev& tl = a.tier[1];
+    uint32_t eq_base = 0, hi_base = 0, lo_base = 0;
+    for (int c0 = 0; c0 < nq; c0 += blockDim.x) {
+        const int j = c0 + threadIdx.x;
+        const uint32_t kv = j < nq ? key(j) : 0u;
+        const uint32_t e1 = (j < nq && n4 > 0 && kv == k1) ? 1u : 0u;
+        uint32_t tot1;
+        const uint32_t r1 = block_excl_scan(e1, sh, &tot1);
+        const bool in1 = j < nq && n4 > 0 && (kv > k1 || (e1 && eq_base + r1 < t1));
+        const uint32_t is_hi = in1 ? 1u : 0u, is_lo = (j < nq && !in1) ? 1u : 0u;
+        uint32_t tot_hi, tot_lo;
+        const uint32_t ph = block_excl_scan(is_hi, sh, &tot_hi);
+        const uint32_t pl = block_excl_scan(is_lo, sh, &tot_lo);
+        const size_t row = (unit * T + j) * (size_t)D;
+        if (is_hi) put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
+        if (is_lo) put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
+        eq_base += tot1;
+        hi_base += tot_hi;
+        lo_base += tot_lo;
+    }
+    const bool bf = a.bf16 != 0;
+    const int r0 = T - nq;
+    for (int idx = threadIdx.x; idx < r0 * D; idx += blockDim.x) {
+        const int i = idx / D, c = idx % D;
+        const size_t src = (unit * T + nq + i) * (size_t)D + c;
+        const size_t dst = (unit * a.res_cap + i) * (size_t)D + c;
+        copy_act(a.res_k, dst, a.k_src, src, bf);
+        copy_act(a.res_v, dst, a.v_src, src, bf);
+    }
+    for (int i = threadIdx.x; i < r0; i += blockDim.x) a.res_token_id[unit * a.res_cap + i] = nq + i;
+    if (threadIdx.x == 0) {
+        th.count[unit] = (int)hi_base;
+        tl.count[unit] = (int)lo_base;
+        a.res_start[unit] = 0;
+        a.res_len[unit] = r0;
+        if (hkv == 0) a.seq_len[b] = T;
+    }
+}
+
+struct MikvShared {
+    TopkShared tk;
+    uint32_t cnt_eq;
+};
+
+// Oldest residual token leaves; the top floor(N_q / hi_den) by cumulative
+// score (ties to the lower position) is recomputed; INT4 tokens outside it
+// are re-quantised to INT2 from their dequantised values.
+__global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a) {
+    __shared__ MikvShared sh;
+    extern __shared__ int32_t holes[];                 // [cap of tier 0]
+    const size_t unit = blockIdx.x;
+    const int len = a.res_len[unit];
+    if (len <= a.nr) return;
+    const int D = a.D, G = a.G, cap = a.res_cap;
+    const bool bf = a.bf16 != 0;
+    const int start = a.res_start[unit];
+    const int e_id = a.res_token_id[unit * cap + start];
+    const TierDev& th = a.tier[0];
+    const TierDev& tl = a.tier[1];
+    const int c0 = th.count[unit], c1 = tl.count[unit];
+    const int nq = c0 + c1 + 1;
+    const int n4 = nq / a.hi_den;
+    const float* cum = a.cum_score + unit * (size_t)a.score_cap;
+    auto id_of = [&](int i) -> int {
+        return i < c0 ? th.token_id[unit * th.cap + i]
+                      : (i < c0 + c1 ? tl.token_id[unit * tl.cap + (i - c0)] : e_id);
+    };
+    auto key = [&](int i) { return orderable(cum[id_of(i)]); };
+    uint32_t k1 = 0xffffffffu, t1 = 0;
+    uint32_t id_star = 0xffffffffu;                    // ties: position <= id_star are in
+    if (n4 > 0) {
+        block_radix_select(key, nq, n4, sh.tk, &k1, &t1);
+        if (threadIdx.x == 0) sh.cnt_eq = 0;
+        __syncthreads();
+        uint32_t local = 0;
+        for (int i = threadIdx.x; i < nq; i += blockDim.x) local += key(i) == k1 ? 1u : 0u;
+        atomicAdd(&sh.cnt_eq, local);
+        __syncthreads();
+        const uint32_t cnt_eq = sh.cnt_eq;
+        __syncthreads();
+        if (t1 < cnt_eq) {
+            // among equal scores keep the t1 lowest positions
+            uint32_t k2, t2;
+            block_radix_select(
+                [&](int i) { return key(i) == k1 ? 0xffffffffu - (uint32_t)id_of(i) : 0u; }, nq,
+                (int)t1, sh.tk, &k2, &t2);
+            id_star = 0xffffffffu - k2;
+        }
+    }
+    auto in_top = [&](int i) -> bool {
+        if (n4 == 0) return false;
+        const uint32_t kv = key(i);
+        return kv > k1 || (kv == k1 && (uint32_t)id_of(i) <= id_star);
+    };
+    const bool e_in = in_top(nq - 1);
+    // demotions: INT4 slots outside the set, in slot order
+    uint32_t dem_base = 0;
+    const int c0_new_pred = 0;
+    (void)c0_new_pred;
+    const int lo_first = c1 + (e_in ? 0 : 1);
+    for (int s0 = 0; s0 < c0; s0 += blockDim.x) {
+        const int i = s0 + threadIdx.x;
+        const uint32_t dem = (i < c0 && !in_top(i)) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t r = block_excl_scan(dem, sh.tk, &tot);
+        if (dem) {
+            const int slot = lo_first + (int)(dem_base + r);
+            if (slot < tl.cap) {
+                const uint32_t* k4 = krow(th, unit, i, D);
+                const uint32_t* v4 = vrow(th, unit, i, D);
+                const size_t s4 = srow(th, unit, i, D, G);
+                quant_row([&](int c) {
+                              return dequant(code_at(k4, c, th.k_bits), h2f_bits(th.k_scale[s4 + c / G]),
+                                             h2f_bits(th.k_zero[s4 + c / G]));
+                          },
+                          D, G, tl.k_bits, krow(tl, unit, slot, D), tl.k_scale + srow(tl, unit, slot, D, G),
+                          tl.k_zero + srow(tl, unit, slot, D, G));
+                quant_row([&](int c) {
+                              return dequant(code_at(v4, c, th.v_bits), h2f_bits(th.v_scale[s4 + c / G]),
+                                             h2f_bits(th.v_zero[s4 + c / G]));
+                          },
+                          D, G, tl.v_bits, vrow(tl, unit, slot, D), tl.v_scale + srow(tl, unit, slot, D, G),
+                          tl.v_zero + srow(tl, unit, slot, D, G));
+                tl.token_id[unit * tl.cap + slot] = th.token_id[unit * th.cap + i];
+            } else {
+                atomicOr(&g_status_policy, kDevCheck);
+            }
+        }
+        dem_base += tot;
+    }
+    const int n_dem = (int)dem_base;
+    const int c0n = c0 - n_dem;
+    __syncthreads();
+    // fill the holes below c0n with the kept tokens at or above c0n
+    uint32_t hole_base = 0;
+    for (int s0 = 0; s0 < c0n; s0 += blockDim.x) {
+        const int i = s0 + threadIdx.x;
+        const uint32_t hole = (i < c0n && !in_top(i)) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t r = block_excl_scan(hole, sh.tk, &tot);
+        if (hole) holes[hole_base + r] = i;
+        hole_base += tot;
+    }
+    __syncthreads();
+    uint32_t mov_base = 0;
+    const int kw = D * th.k_bits / 32, vw = D * th.v_bits / 32, ng = D / G;
+    for (int s0 = c0n; s0 < c0; s0 += blockDim.x) {
+        const int i = s0 + threadIdx.x;
+        const uint32_t mov = (i < c0 && in_top(i)) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t r = block_excl_scan(mov, sh.tk, &tot);
+        if (mov) {
+            const int dst = holes[mov_base + r];
+            uint32_t* kd = krow(th, unit, dst, D);
+            const uint32_t* ks = krow(th, unit, i, D);
+            for (int w = 0; w < kw; ++w) kd[w] = ks[w];
+            uint32_t* vd = vrow(th, unit, dst, D);
+            const uint32_t* vs = vrow(th, unit, i, D);
+            for (int w = 0; w < vw; ++w) vd[w] = vs[w];
+            const size_t sd = srow(th, unit, dst, D, G), ss = srow(th, unit, i, D, G);
+            for (int w = 0; w < ng; ++w) {
+                th.k_scale[sd + w] = th.k_scale[ss + w];
+                th.k_zero[sd + w] = th.k_zero[ss + w];
+                th.v_scale[sd + w] = th.v_scale[ss + w];
+                th.v_zero[sd + w] = th.v_zero[ss + w];
+            }
+            th.token_id[unit * th.cap + dst] = th.token_id[unit * th.cap + i];
+        }
+        mov_base += tot;
+    }
+    __syncthreads();
+    // the leaving token, quantised from its full-precision values
+    if (threadIdx.x == 0) {
+        const size_t row = (unit * cap + start) * (size_t)D;
+        if (e_in) {
+            if (c0n < th.cap) put_raw_token(a, th, unit, c0n, a.res_k, a.res_v, row, e_id);
+            else atomicOr(&g_status_policy, kDevCheck);
+        } else {
+            if (c1 < tl.cap) put_raw_token(a, tl, unit, c1, a.res_k, a.res_v, row, e_id);
+            else atomicOr(&g_status_policy, kDevCheck);
+        }
+        th.count[unit] = min(c0n + (e_in ? 1 : 0), th.cap);
+        tl.count[unit] = min(c1 + n_dem + (e_in ? 0 : 1), tl.cap);
+        a.res_start[unit] = (start + 1) % cap;
+        a.res_len[unit] = len - 1;
+    }
+    (void)bf;
+}
+
+PolicyArgs make_args(const kvq_cache& c, const kvq_policy_params* p) {
+    PolicyArgs a{};
+    a.B = c.B;
+    a.Hq = c.Hq;
+    a.Hkv = c.Hkv;
+    a.D = c.D;
+    a.G = c.G;
+    a.g = c.Hq / c.Hkv;
+    a.bf16 = c.dtype == KVQ_BF16;
+    a.n_tiers = c.n_tiers;
+    a.nr = c.nr;
+    a.hi_den = c.hi_den;
+    for (int t = 0; t < c.n_tiers; ++t) {
+        const kvq_tier& s = c.tier[t];
+        TierDev& d = a.tier[t];
+        d.k_bits = s.k_bits;
+        d.v_bits = s.v_bits;
+        d.k_axis = s.k_axis;
+        d.cap = s.cap;
+        d.k_codes = s.k_codes;
+        d.k_scale = s.k_scale;
+        d.k_zero = s.k_zero;
+        d.v_codes = s.v_codes;
+        d.v_scale = s.v_scale;
+        d.v_zero = s.v_zero;
+        d.token_id = s.token_id;
+        d.count = s.count;
+    }
+    a.res_k = c.res_k;
+    a.res_v = c.res_v;
+    a.res_token_id = c.res_token_id;
+    a.res_start = c.res_start;
+    a.res_len = c.res_len;
+    a.res_cap = c.res_cap;
+    a.seq_len = c.seq_len;
+    a.win_acc = c.win_acc;
+    a.alpha = c.alpha;
+    a.cum_score = c.cum_score;
+    a.score_cap = c.score_cap;
+    if (p) {
+        a.k_src = p->k_src;
+        a.v_src = p->v_src;
+        a.T = p->T;
+        a.sel_idx = p->sel_idx;
+        a.n_sel = p->n_sel;
+        a.colscore = p->colscore;
+        a.n_high = p->n_high;
+        a.n_low = p->n_low;
+    }
+    return a;
+}
+
+kvq_status launched(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("requant_demote (%s): %s", what, cudaGetErrorString(e));
+        return KVQ_ECUDA;
+    }
+    return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, int step,
+                      cudaStream_t s) {
+    const int units = c.B * c.Hkv;
+    PolicyArgs a = make_args(c, p);
+    if (mode == KVQ_POLICY_MINIKV) {
+        if (step == 0) {
+            const int n = p->n_sel, nr = c.nr, G = c.G;
+            const int r0 = n <= nr ? n : nr + (n - nr) % G;
+            const int npk = n - r0;
+            const kvq_tier& t = c.tier[0];
+            cudaError_t e = launch_quant_pack_strided(p->k_src, c.dtype, units, p->T, c.D, p->sel_idx, n,
+                                                      npk, t.k_bits, G, KVQ_AXIS_CHANNEL, t.cap,
+                                                      t.k_codes, t.k_scale, t.k_zero, s);
+            if (e == cudaSuccess)
+                e = launch_quant_pack_strided(p->v_src, c.dtype, units, p->T, c.D, p->sel_idx, n, npk,
+                                              t.v_bits, G, KVQ_AXIS_TOKEN, t.cap, t.v_codes, t.v_scale,
+                                              t.v_zero, s);
+            if (e != cudaSuccess) {
+                set_error("requant_demote (MiniKV pack): %s", cudaGetErrorString(e));
+                return KVQ_ECUDA;
+            }
+            minikv_build_tail<<<units, 256, 0, s>>>(a, npk, r0);
+            return launched("MiniKV build");
+        }
+        minikv_flush<<<units, 128, 0, s>>>(a);
+        return launched("MiniKV flush");
+    }
+    if (mode == KVQ_POLICY_DIFFKV) {
+        if (step == 0) {
+            diffkv_build<<<units, kTopkBlock, 0, s>>>(a);
+            return launched("DiffKV build");
+        }
+        diffkv_exit<<<units, 32, 0, s>>>(a);
+        return launched("DiffKV exit");
+    }
+    if (step == 0) {
+        mikv_build<<<units, kTopkBlock, 0, s>>>(a);
+        return launched("MiKV build");
+    }
+    const size_t holes = (size_t)c.tier[0].cap * sizeof(int32_t);
+    if (holes > 48 * 1024) {
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(mikv_step, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            attr = true;
+        }
+    }
+    mikv_step<<<units, kTopkBlock, holes, s>>>(a);
+    return launched("MiKV step");
+}
+
+}  // namespace kvq

@@ -1,0 +1,571 @@
+// prefill_attn_scores: the two-pass prefill of MiniKV (review page, referee
+// minor comment 2 on section 3.2 -- pass 1 follows FlashAttention's online
+// softmax; Figure 4 caption -- two-pass kernel parallelism; verdict JSON
+// key_machinery -- output plus column-wise cumulative attention scores with
+// memory linear in the sequence length).
+//
+// GB300 design (tcgen05 + TMEM + TMA, one CTA per 128-row tile):
+//   pass 1 (row-parallel): CTA = (batch*query head, query tile of 128).
+//     warp 4 = TMA producer (Q once, K/V tiles double-buffered),
+//     warp 5 = MMA issuer: S = Q K^T into one of two TMEM S buffers, then
+//              O += P V into the TMEM O accumulator,
+//     warps 0-3 = softmax: thread r owns query row r (TMEM lane r), reads
+//              its S row, keeps the running max/sum, writes P (fp16/bf16)
+//              into a 128B-swizzled smem tile, rescales O only when its
+//              max grew by more than 2^8 (exact: the final division uses
+//              the same stale max), and finally writes O / l and lse.
+//   pass 2 (column-parallel): CTA = (batch*query head, key tile of 128),
+//     loops over the query tiles at or below the diagonal; S^T = K Q^T in
+//     TMEM; thread r owns key r and sums exp(S - lse_i) over queries, so
+//     column sums stay in registers (no atomics, no T x T buffer).
+// Every mbarrier wait is bounded (2 s, or at once after another warp gave
+// up); a timed-out CTA drains its copies and MMAs, frees TMEM and records
+// KVQ_ETIMEOUT in the device status word.
+#include <mutex>
+
+#include "kvq_common.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+KVQ_DEFINE_STATUS(prefill)
+
+namespace {
+
+constexpr int kTile = 128;                 // rows per tile (queries or keys)
+constexpr uint32_t kHalfBytes = 128 * 128;       // one 128-row x 64-column 128B-swizzled half
+constexpr uint32_t kPBytes = 2 * kHalfBytes;     // P tile: 128 rows x 128 keys
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+// Shared memory maps (offsets from a 1024-aligned base) for head dim D.
+template <int D> struct Layout {
+    static constexpr uint32_t kTileBytes = kTile * D * 2;      // D/64 halves
+    // pass 1
+    static constexpr uint32_t P1_Q = 0;
+    static constexpr uint32_t P1_K = P1_Q + kTileBytes;        // 2 stages
+    static constexpr uint32_t P1_V = P1_K + 2 * kTileBytes;    // 2 stages
+    static constexpr uint32_t P1_P = P1_V + 2 * kTileBytes;
+    static constexpr uint32_t P1_BAR = P1_P + kPBytes;
+    static constexpr uint32_t P1_SMEM = P1_BAR + 256 + 1024;   // + barriers/flags + alignment slack
+    // pass 2
+    static constexpr uint32_t P2_K = 0;
+    static constexpr uint32_t P2_Q = P2_K + kTileBytes;        // 2 stages
+    static constexpr uint32_t P2_LSE = P2_Q + 2 * kTileBytes;  // 2 x 128 floats
+    static constexpr uint32_t P2_BAR = P2_LSE + 2 * kTile * 4;
+    static constexpr uint32_t P2_SMEM = P2_BAR + 256 + 1024;
+};
+
+enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SFREE = 9, B_PF = 11, B_OD = 12,
+             B_DRAIN = 13, P1_NBAR = 14 };
+enum P2Bar { C_KF = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_SFREE = 7, C_DRAIN = 9, C_LSE = 10,
+             P2_NBAR = 12 };
+
+template <typename T> struct Pack2;
+template <> struct Pack2<__half> {
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+template <> struct Pack2<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Bounded wait whose outcome is the same for every lane of the warp, so that
+// the warp-collective tcgen05.ld/st after it stay convergent.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag)) != 0;
+}
+
+__device__ __forceinline__ void give_up(volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_status_prefill, kDevTimeout);
+}
+
+// K-major operand (rows x 128 elements as two 128B-swizzled 64-column halves):
+// descriptor of the 16-element K slice kk (0..7).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    return sdesc_sw128(tile + (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u, 16u,
+                       1024u);
+}
+
+// MN-major operand (128 K-rows of 128 N-elements, two 64-column halves):
+// descriptor of K rows 16*kk .. 16*kk+15.  LBO = stride between the N
+// halves, SBO = stride between groups of 8 K rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+    return sdesc_sw128(tile + (uint32_t)kk * 16u * 128u, kHalfBytes, 1024u);
+}
+
+template <typename T, int AB, int D>
+__global__ void __launch_bounds__(192, 1)
+    prefill_pass1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, T* __restrict__ o,
+                         float* __restrict__ lse, int T_len, int Hq, int Hkv, int n_qt,
+                         float scale_log2) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    using Lay = Layout<D>;
+    constexpr uint32_t kTileBytes = Lay::kTileBytes;
+    constexpr int kHalves = D / 64;
+    const uint32_t sQ = base + Lay::P1_Q, sK = base + Lay::P1_K, sV = base + Lay::P1_V,
+                   sP = base + Lay::P1_P;
+    const uint32_t bar0 = base + Lay::P1_BAR;
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lay::P1_BAR + 8 * P1_NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lay::P1_BAR + 8 * P1_NBAR + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int qt = n_qt - 1 - (int)blockIdx.y;
+    const int b = bh / Hq, hq = bh % Hq;
+    const int bhkv = b * Hkv + hq / (Hq / Hkv);
+    const int n_kv = qt + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_Q), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(BAR(B_KF + s), 1);
+            mbar_init(BAR(B_VF + s), 1);
+            mbar_init(BAR(B_KVE + s), 1);
+            mbar_init(BAR(B_SF + s), 1);
+            mbar_init(BAR(B_SFREE + s), 4);
+        }
+        mbar_init(BAR(B_PF), 4);
+        mbar_init(BAR(B_OD), 1);
+        mbar_init(BAR(B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tO = tmem + 256;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            mbar_expect_tx(BAR(B_Q), kTileBytes);
+            for (int hf = 0; hf < kHalves; ++hf)
+                tma_load_3d(sQ + hf * kHalfBytes, &tq, 64 * hf, qt * kTile, bh, BAR(B_Q));
+            int last[2] = {-1, -1};
+            for (int j = 0; j < n_kv; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !mbar_wait(BAR(B_KVE + st), ((j - 2) >> 1) & 1, abort_flag)) {
+                    give_up(abort_flag);
+                    break;
+                }
+                const uint32_t kdst = sK + (uint32_t)st * kTileBytes;
+                const uint32_t vdst = sV + (uint32_t)st * kTileBytes;
+                mbar_expect_tx(BAR(B_KF + st), kTileBytes);
+                for (int hf = 0; hf < kHalves; ++hf)
+                    tma_load_3d(kdst + hf * kHalfBytes, &tk, 64 * hf, j * kTile, bhkv, BAR(B_KF + st));
+                mbar_expect_tx(BAR(B_VF + st), kTileBytes);
+                for (int hf = 0; hf < kHalves; ++hf)
+                    tma_load_3d(vdst + hf * kHalfBytes, &tv, 64 * hf, j * kTile, bhkv, BAR(B_VF + st));
+                last[st] = j;
+            }
+            // every issued copy has landed before the CTA may exit
+            mbar_wait(BAR(B_Q), 0, nullptr);
+            for (int st = 0; st < 2; ++st) {
+                if (last[st] >= 0) {
+                    mbar_wait(BAR(B_KF + st), (last[st] >> 1) & 1, nullptr);
+                    mbar_wait(BAR(B_VF + st), (last[st] >> 1) & 1, nullptr);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_f16(AB, 128, 128, 0);
+            const uint32_t idPV = idesc_f16(AB, 128, D, 1);
+            bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
+            auto issue_pv = [&](int jj) -> bool {
+                if (!mbar_wait(BAR(B_PF), jj & 1, abort_flag)) return false;
+                if (!mbar_wait(BAR(B_VF + (jj & 1)), (jj >> 1) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t vt = sV + (uint32_t)(jj & 1) * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_f16(tO, kmajor_desc(sP, kk), mnmajor_desc(vt, kk), idPV,
+                               (jj > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(BAR(B_OD));
+                tc_commit(BAR(B_KVE + (jj & 1)));
+                return true;
+            };
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int st = j & 1;
+                if (!mbar_wait(BAR(B_KF + st), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (j >= 2 && !mbar_wait(BAR(B_SFREE + st), ((j - 2) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tS = tmem + (uint32_t)st * 128u;
+                const uint32_t kt = sK + (uint32_t)st * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_f16(tS, kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idS, kk > 0 ? 1u : 0u);
+                tc_commit(BAR(B_SF + st));
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok) ok = issue_pv(n_kv - 1);
+            if (!ok) give_up(abort_flag);
+            // all MMAs of this thread complete before TMEM is released
+            tc_commit(BAR(B_DRAIN));
+            mbar_wait(BAR(B_DRAIN), 0, nullptr);
+        }
+    } else {
+        // softmax warps: thread r owns query row r of the tile
+        const int r = threadIdx.x;
+        const int i = qt * kTile + r;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_used = -__int_as_float(0x7f800000);
+        float l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const int sb = j & 1;
+            if (!warp_wait(BAR(B_SF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+                tmem_ld32(tmem + lane_base + (uint32_t)sb * 128u + (uint32_t)c4 * 32u, s + c4 * 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
+
+            const int kbase = j * kTile;
+            float mx = -__int_as_float(0x7f800000);
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                float x = s[c] * scale_log2;
+                const int kidx = kbase + c;
+                if (kidx > i || kidx >= T_len) x = -__int_as_float(0x7f800000);
+                s[c] = x;
+                mx = fmaxf(mx, x);
+            }
+            const float m_new = fmaxf(m_used, mx);
+            const bool resc = m_new > m_used + kRescaleLog2;
+            if (j >= 1) {
+                if (!warp_wait(BAR(B_OD), (j - 1) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, resc && j >= 1)) {
+                const float f = (resc && j >= 1) ? ex2_approx(m_used - m_new) : 1.0f;
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    float ov[32];
+                    tmem_ld32(tO + lane_base + (uint32_t)c4 * 32u, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) ov[c] *= f;
+                    tmem_st32(tO + lane_base + (uint32_t)c4 * 32u, ov);
+                }
+                tmem_wait_st();
+            }
+            if (resc) {
+                if (j >= 1) l *= ex2_approx(m_used - m_new);
+                m_used = m_new;
+            }
+            float rs = 0.0f;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {
+                float p[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    p[e] = ex2_approx(s[c8 * 8 + e] - m_used);
+                    rs += p[e];
+                }
+                const uint32_t off = (uint32_t)(c8 >> 3) * kHalfBytes + (uint32_t)r * 128u +
+                                     ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
+                st_shared_v4(sP + off, Pack2<T>::pack(p[0], p[1]), Pack2<T>::pack(p[2], p[3]),
+                             Pack2<T>::pack(p[4], p[5]), Pack2<T>::pack(p[6], p[7]));
+            }
+            l += rs;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_PF));
+        }
+        if (ok && !warp_wait(BAR(B_OD), (n_kv - 1) & 1, abort_flag)) ok = false;
+        if (!ok) give_up(abort_flag);
+        tc_fence_after();
+        // epilogue: O / l and lse; TMEM loads stay warp-uniform
+        const float inv = ok ? 1.0f / l : 0.0f;
+        T* orow = o + ((size_t)bh * T_len + (size_t)(i < T_len ? i : 0)) * D;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+            float ov[32];
+            tmem_ld32(tO + lane_base + (uint32_t)c4 * 32u, ov);
+            tmem_wait_ld();
+            if (ok && i < T_len) {
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint4 w;
+                    w.x = Pack2<T>::pack(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
+                    w.y = Pack2<T>::pack(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
+                    w.z = Pack2<T>::pack(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
+                    w.w = Pack2<T>::pack(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
+                    *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = w;
+                }
+            }
+        }
+        if (ok && i < T_len) lse[(size_t)bh * T_len + i] = (m_used + __log2f(l)) * kLn2;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+template <typename T, int AB, int D>
+__global__ void __launch_bounds__(192, 2)
+    prefill_pass2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const float* __restrict__ lse, float* __restrict__ colscore, int T_len,
+                         int Hq, int Hkv, int n_t, float scale_log2) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    using Lay = Layout<D>;
+    constexpr uint32_t kTileBytes = Lay::kTileBytes;
+    constexpr int kHalves = D / 64;
+    const uint32_t sK = base + Lay::P2_K, sQ = base + Lay::P2_Q;
+    float* lse_s = reinterpret_cast<float*>(gbase + Lay::P2_LSE);
+    const uint32_t bar0 = base + Lay::P2_BAR;
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lay::P2_BAR + 8 * P2_NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lay::P2_BAR + 8 * P2_NBAR + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int kt = (int)blockIdx.y;
+    const int b = bh / Hq, hq = bh % Hq;
+    const int bhkv = b * Hkv + hq / (Hq / Hkv);
+    const int n_it = n_t - kt;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(C_KF), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(BAR(C_QF + s), 1);
+            mbar_init(BAR(C_QE + s), 1);
+            mbar_init(BAR(C_SF + s), 1);
+            mbar_init(BAR(C_SFREE + s), 4);
+        }
+        mbar_init(BAR(C_DRAIN), 1);
+        mbar_init(BAR(C_LSE), 128);
+        mbar_init(BAR(C_LSE + 1), 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            mbar_expect_tx(BAR(C_KF), kTileBytes);
+            for (int hf = 0; hf < kHalves; ++hf)
+                tma_load_3d(sK + hf * kHalfBytes, &tk, 64 * hf, kt * kTile, bhkv, BAR(C_KF));
+            int last[2] = {-1, -1};
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it & 1;
+                if (it >= 2 && !mbar_wait(BAR(C_QE + st), ((it - 2) >> 1) & 1, abort_flag)) {
+                    give_up(abort_flag);
+                    break;
+                }
+                const uint32_t dst = sQ + (uint32_t)st * kTileBytes;
+                mbar_expect_tx(BAR(C_QF + st), kTileBytes);
+                for (int hf = 0; hf < kHalves; ++hf)
+                    tma_load_3d(dst + hf * kHalfBytes, &tq, 64 * hf, (kt + it) * kTile, bh,
+                                BAR(C_QF + st));
+                last[st] = it;
+            }
+            mbar_wait(BAR(C_KF), 0, nullptr);
+            for (int st = 0; st < 2; ++st)
+                if (last[st] >= 0) mbar_wait(BAR(C_QF + st), (last[st] >> 1) & 1, nullptr);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idS = idesc_f16(AB, 128, 128, 0);
+            bool ok = mbar_wait(BAR(C_KF), 0, abort_flag);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it & 1;
+                if (!mbar_wait(BAR(C_QF + st), (it >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (it >= 2 && !mbar_wait(BAR(C_SFREE + st), ((it - 2) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t qtile = sQ + (uint32_t)st * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_f16(tmem + (uint32_t)st * 128u, kmajor_desc(sK, kk), kmajor_desc(qtile, kk),
+                               idS, kk > 0 ? 1u : 0u);
+                tc_commit(BAR(C_SF + st));
+                tc_commit(BAR(C_QE + st));
+            }
+            if (!ok) give_up(abort_flag);
+            tc_commit(BAR(C_DRAIN));
+            mbar_wait(BAR(C_DRAIN), 0, nullptr);
+        }
+    } else {
+        const int r = threadIdx.x;
+        const int j = kt * kTile + r;                       // key position of this thread
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float acc = 0.0f;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int buf = it & 1;
+            const int qt = kt + it;
+            const int qi_own = qt * kTile + r;
+            lse_s[buf * kTile + r] =
+                qi_own < T_len ? lse[(size_t)bh * T_len + qi_own] * kLog2e : __int_as_float(0x7f800000);
+            // buffer buf is rewritten two tiles later, after every thread has
+            // arrived for the tile in between, i.e. finished reading this one
+            mbar_arrive(BAR(C_LSE + buf));
+            if (!warp_wait(BAR(C_LSE + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(BAR(C_SF + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+                tmem_ld32(tmem + lane_base + (uint32_t)buf * 128u + (uint32_t)c4 * 32u, s + c4 * 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C_SFREE + buf));
+            const float* ls = lse_s + buf * kTile;
+            float ts = 0.0f;
+            const int qbase = qt * kTile;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float x = s[c] * scale_log2 - ls[c];
+                ts += (qbase + c >= j) ? ex2_approx(x) : 0.0f;
+            }
+            acc += ts;
+        }
+        if (!ok) give_up(abort_flag);
+        if (ok && j < T_len) colscore[(size_t)bh * T_len + j] = acc;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [rows = BH][T][D] 16-bit tensor, box 64 x 128 x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int dt, int BH, int T, int D) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, dt == KVQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T, int AB, int D>
+kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int T_len,
+                     float sm_scale, void* o, float* lse, float* colscore, cudaStream_t s) {
+    using Lay = Layout<D>;
+    CUtensorMap mq, mk, mv;
+    const int dt = AB == 0 ? KVQ_F16 : KVQ_BF16;
+    if (!make_map(&mq, q, dt, B * Hq, T_len, D) || !make_map(&mk, k, dt, B * Hkv, T_len, D) ||
+        !make_map(&mv, v, dt, B * Hkv, T_len, D)) {
+        set_error("prefill_attn_scores: tensor map encoding failed");
+        return KVQ_ECUDA;
+    }
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaFuncSetAttribute(prefill_pass1_kernel<T, AB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Lay::P1_SMEM);
+        cudaFuncSetAttribute(prefill_pass2_kernel<T, AB, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Lay::P2_SMEM);
+        attr_done = true;
+    }
+    const int n_t = (T_len + kTile - 1) / kTile;
+    const float scale_log2 = sm_scale * kLog2e;
+    dim3 g1(B * Hq, n_t);
+    prefill_pass1_kernel<T, AB, D><<<g1, 192, Lay::P1_SMEM, s>>>(mq, mk, mv, (T*)o, lse, T_len, Hq,
+                                                                  Hkv, n_t, scale_log2);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("prefill pass 1 launch: %s", cudaGetErrorString(e));
+        return KVQ_ECUDA;
+    }
+    if (colscore) {
+        prefill_pass2_kernel<T, AB, D><<<g1, 192, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
+                                                                      Hkv, n_t, scale_log2);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error("prefill pass 2 launch: %s", cudaGetErrorString(e));
+            return KVQ_ECUDA;
+        }
+    }
+    return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status run_prefill(const void* q, const void* k, const void* v, int dt, int B, int Hq, int Hkv,
+                       int T, int D, float sm_scale, void* o, float* lse, float* colscore,
+                       cudaStream_t s) {
+    if (D == 64) {
+        if (dt == KVQ_F16)
+            return run_typed<__half, 0, 64>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
+        return run_typed<__nv_bfloat16, 1, 64>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
+    }
+    if (dt == KVQ_F16)
+        return run_typed<__half, 0, 128>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
+    return run_typed<__nv_bfloat16, 1, 128>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
+}
+
+}  // namespace kvq

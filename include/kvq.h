@@ -1,0 +1,258 @@
+/*
+ * kvq.h -- C ABI of libkvq.so: attention over a compressed, mixed-precision
+ * KV cache on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (web pages on the subject):
+ *  [MiniKV-J]  MiniKV verdict JSON (arXiv 2411.18077), pith_extraction fields
+ *              key_machinery / core_discovery / supporting_citations.
+ *  [MiniKV-R]  MiniKV review page: "The reading", "Assumptions & free
+ *              parameters", referee comments, Figure 1, 2, 4 captions.
+ *  [DiffKV-J]  DiffKV verdict JSON (arXiv 2412.03131): key_machinery,
+ *              referee major comment 2 and the Algorithm 1 comments.
+ *  [MiKV-R]    "Don't Discard, but Keep It Small" rebuttal page: the
+ *              re-quantisation paragraph, Q1 on long contexts, the
+ *              paragraphs on regrouping by precision and INTn x FP16 GEMV.
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument marked (device) is device memory owned by the
+ *    caller; the library allocates nothing and keeps no pointer after the
+ *    call returns.  Pointers marked (host) are read during the call only.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work on that stream and never
+ *    synchronise, except kvq_device_status().
+ *  - Arguments are validated on the host before any launch.  On a bad
+ *    argument the call returns KVQ_EINVAL / KVQ_EUNSUPPORTED /
+ *    KVQ_EWORKSPACE, launches nothing and sets kvq_last_error().  A failed
+ *    launch returns KVQ_ECUDA.  The library never aborts and never throws.
+ *  - Kernels never trap.  A bounded wait that runs out, or a device-side
+ *    bounds check that fails, sets a device status word that
+ *    kvq_device_status() reads (KVQ_ETIMEOUT / KVQ_EDEVICE).
+ *  - Activations (q, k, v, o, raw residual) are fp16 or bf16 (kvq_dtype),
+ *    row-major with the last axis (head dim D) contiguous.  Scales and
+ *    zero-points are always fp16 bit patterns (uint16_t).  Scores float32.
+ *    Indices int32.  A "unit" is one (batch element, KV head), numbered
+ *    u = b * Hkv + h.
+ *  - Quantiser (identical on every path that quantises): per group,
+ *      z = largest fp16 <= min x;  s = smallest fp16 >= fp32(fp32(max x - z)/(2^b-1));
+ *      q = clamp(rint_even(fp32(fp32(x - z)/s)), 0, 2^b-1), q = 0 when s == 0;
+ *      x_hat = fp32(q*s + z).
+ *    Packing: code i of a 32-bit word in bits [b*i, b*i+b), LSB first.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,         /* bad pointer, size, alignment or combination */
+    KVQ_EUNSUPPORTED = 2,   /* valid request this build does not implement */
+    KVQ_ECUDA = 3,          /* a CUDA runtime call or launch failed */
+    KVQ_ETIMEOUT = 4,       /* a bounded device-side wait ran out */
+    KVQ_EWORKSPACE = 5,     /* workspace missing or too small */
+    KVQ_EDEVICE = 6         /* a device-side consistency check failed */
+} kvq_status;
+
+typedef enum { KVQ_F16 = 0, KVQ_BF16 = 1 } kvq_dtype;
+
+/* Grouping axis.  CHANNEL: a group is G consecutive tokens of one channel
+ * and codes are packed along tokens (keys, [MiniKV-J] sub-channel key
+ * quantisation).  TOKEN: a group is G consecutive channels of one token and
+ * codes are packed along channels (values; per-token keys of the tiers). */
+typedef enum { KVQ_AXIS_CHANNEL = 0, KVQ_AXIS_TOKEN = 1 } kvq_axis;
+
+typedef enum {
+    KVQ_POLICY_MINIKV = 0,  /* persistent selection, residual flush of G tokens */
+    KVQ_POLICY_DIFFKV = 1,  /* K8V4 / K4V2 / prune as tokens leave the window */
+    KVQ_POLICY_MIKV = 2     /* INT4 top fraction, INT2 rest, demotion, no eviction */
+} kvq_policy;
+
+#define KVQ_MAX_TIERS 2
+
+/* One precision tier of the packed cache.  Layouts, per unit u:
+ *   k_axis CHANNEL: k_codes [u][cap*k_bits/32][D] uint32, k_scale/k_zero [u][cap/G][D]
+ *   k_axis TOKEN:   k_codes [u][cap][D*k_bits/32] uint32, k_scale/k_zero [u][cap][D/G]
+ *   values:         v_codes [u][cap][D*v_bits/32] uint32, v_scale/v_zero [u][cap][D/G]
+ *   token_id [u][cap] (position of the token in slot i), count [u] slots in use.
+ * Slots [0, count) are valid; their order is irrelevant to attention
+ * ([MiKV-R]: attention is permutation invariant after positional encoding). */
+typedef struct {
+    int32_t k_bits, v_bits;     /* 2, 4 or 8 */
+    int32_t k_axis;             /* kvq_axis */
+    int32_t cap;                /* slots per unit; multiple of G for CHANNEL keys */
+    uint32_t* k_codes;          /* (device) */
+    uint16_t* k_scale;          /* (device) */
+    uint16_t* k_zero;           /* (device) */
+    uint32_t* v_codes;          /* (device) */
+    uint16_t* v_scale;          /* (device) */
+    uint16_t* v_zero;           /* (device) */
+    int32_t* token_id;          /* (device) */
+    int32_t* count;             /* (device) */
+} kvq_tier;
+
+/* The compressed cache of one attention layer.  Plain struct of device
+ * pointers, filled by the caller (sizes from kvq_cache_bytes()).
+ *
+ * Residual: a ring of res_cap full-precision tokens per unit
+ *   res_k/res_v [u][res_cap][D] (activation dtype), res_token_id [u][res_cap],
+ *   res_start [u] (slot of the oldest token), res_len [u].
+ * nr: residual length the policy keeps ([MiniKV-R]: nr = 128 steps before
+ *   new tokens are quantised; DiffKV: the recent window W).
+ * seq_len [B]: position of the next token of each sequence.
+ * Policy state:
+ *   DiffKV: win_acc [B*Hq][res_cap] attention received by each ring slot,
+ *           per query head; alpha [u][2] = (alpha_h, alpha_l).
+ *   MiKV:   cum_score [u][score_cap], indexed by token position.
+ * dev_status: (device) one uint32 the kernels set on a failed check. */
+typedef struct {
+    int32_t B, Hq, Hkv, D, G;
+    int32_t dtype;              /* kvq_dtype of activations and residual */
+    int32_t policy;             /* kvq_policy */
+    int32_t n_tiers;
+    kvq_tier tier[KVQ_MAX_TIERS];
+    int32_t res_cap, nr;
+    void* res_k;
+    void* res_v;
+    int32_t* res_token_id;
+    int32_t* res_start;
+    int32_t* res_len;
+    int32_t* seq_len;
+    float* win_acc;
+    float* alpha;
+    float* cum_score;
+    int32_t score_cap;
+    int32_t hi_den;             /* MiKV: INT4 share is floor(N_q / hi_den); 5 = 20% */
+} kvq_cache;
+
+/* Inputs of requant_demote(step = 0), the cache build at the end of prefill. */
+typedef struct {
+    const void* k_src;          /* (device) [B, Hkv, T, D] prompt keys */
+    const void* v_src;          /* (device) [B, Hkv, T, D] prompt values */
+    int32_t T;
+    const int32_t* sel_idx;     /* (device) MiniKV: [u][n_sel] ascending positions */
+    int32_t n_sel;
+    const float* colscore;      /* (device) DiffKV/MiKV: [B, Hq, T] prefill column scores */
+    const int32_t* n_high;      /* (device) DiffKV: [u] tokens put in K8V4 */
+    const int32_t* n_low;       /* (device) DiffKV: [u] tokens put in K4V2 */
+} kvq_policy_params;
+
+/* ---------------------------------------------------------------------- */
+
+/* kv_quant_pack -- asymmetric b-bit quantisation + packing ([MiniKV-J]
+ * key_machinery: 16 INT2 codes per INT32 with FP16 scale/zero; [MiniKV-R]
+ * "Core claim": sub-channel keys, per-token values).
+ *   x          (device) [B, H, T, D] activations of type dt
+ *   gather_idx (device, nullable) [B, H, n] positions to pack, in order;
+ *              NULL means positions 0..n-1 (n <= T).  Indices outside
+ *              [0, T) are a device-checked error (KVQ_EDEVICE, slot skipped).
+ *   bits 2/4/8, group G in {16, 32, 64, 128}, axis CHANNEL or TOKEN.
+ *   CHANNEL: n % G == 0; codes [B,H,n*bits/32,D], scale/zero [B,H,n/G,D].
+ *   TOKEN:   D % G == 0; codes [B,H,n,D*bits/32], scale/zero [B,H,n,D/G].
+ * Bit-exact with the quantiser stated above. */
+kvq_status kv_quant_pack(const void* x, kvq_dtype dt, int B, int H, int T, int D,
+                         const int32_t* gather_idx, int n, int bits, int group, kvq_axis axis,
+                         uint32_t* codes, uint16_t* scale, uint16_t* zero, void* stream);
+
+/* prefill_attn_scores -- two-pass prefill attention ([MiniKV-R] referee
+ * minor comment 2 on the first pass, Figure 4 caption; [MiniKV-J]
+ * key_machinery: output plus column-wise cumulative attention scores in
+ * memory linear in T).
+ *   q (device) [B, Hq, T, D]; k, v (device) [B, Hkv, T, D]; Hq % Hkv == 0,
+ *   query head h reads KV head h / (Hq/Hkv).  D is 64 or 128.  Base pointers
+ *   16-byte aligned.
+ *   Pass 1: o (device) [B, Hq, T, D] = softmax(sm_scale * q k^T, causal) v,
+ *           lse (device) [B, Hq, T] natural-log row log-sum-exp.
+ *   Pass 2 (colscore non-NULL): colscore (device) [B, Hq, T],
+ *           colscore[j] = sum_{i >= j} exp(sm_scale q_i.k_j - lse_i).
+ *   causal must be 1.  ws/ws_bytes: unused (pass NULL, 0). */
+kvq_status prefill_attn_scores(const void* q, const void* k, const void* v, kvq_dtype dt,
+                               int B, int Hq, int Hkv, int T, int D, float sm_scale, int causal,
+                               void* o, float* lse, float* colscore,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* kvq_score_reduce -- GQA aggregation of per-query-head column scores.
+ *   mode 0 (MiKV, H2O cumulative): out[b,h,j] = sum over the g heads in head order.
+ *   mode 1 (DiffKV significance):  out[b,h,j] = max over the g heads of cs/(T - j).
+ *   colscore (device) [B, Hq, T] -> out (device) [B, Hkv, T]. */
+kvq_status kvq_score_reduce(const float* colscore, int B, int Hq, int Hkv, int T, int mode,
+                            float* out, void* stream);
+
+/* select_tokens -- heavy hitters + recent window ([MiniKV-R] "Assumptions &
+ * free parameters": heavy hitters by cumulative attention chosen once at
+ * the end of prefill, plus a recent window; Figure 2 caption).
+ *   score (device) [B, H, T] float32; k_hh (device) [B*H] heavy-hitter
+ *   budget per unit (clamped to T - w_recent); w_recent <= T.
+ *   idx_out (device) [B, H, kmax + w_recent] where kmax = max budget the
+ *   caller passes as `kmax`; per unit the first n_out[u] entries hold the
+ *   chosen positions ascending: the k largest scores among j < T - w (ties
+ *   to the lower position) followed by T-w .. T-1.  n_out (device) [B*H].
+ *   T <= 65536.  ws unused. */
+kvq_status select_tokens(const float* score, int B, int H, int T, const int32_t* k_hh, int kmax,
+                         int w_recent, int32_t* idx_out, int32_t* n_out,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* requant_demote -- the policy tail of a step ([DiffKV-J] key_machinery and
+ * Algorithm 1; [MiKV-R] re-quantisation paragraph; [MiniKV-R] nr).
+ *   step == 0: build the cache at the end of prefill from p (k_src, v_src,
+ *     T and, per policy, sel_idx/n_sel, colscore, n_high/n_low).  Tier
+ *     counts, the residual and the policy state are overwritten.
+ *   step > 0 (after decode_attn_qkv of that step):
+ *     MiniKV: if res_len == nr + G pack the G oldest residual tokens into tier 0.
+ *     DiffKV: if res_len > nr the oldest window token leaves: K8V4 (tier 0)
+ *             if score >= alpha_h/N, else K4V2 (tier 1) if score >= alpha_l/N,
+ *             else pruned; score = max over the group's heads of the mean
+ *             attention it received, N = seq_len.
+ *     MiKV:   if res_len > nr the oldest residual token leaves; the top
+ *             floor(N_q/hi_den) tokens by cumulative score (ties to the lower
+ *             position) over tiers 0,1 plus that token form the set S; it
+ *             enters INT4 (tier 0) if in S else INT2 (tier 1); INT4 tokens
+ *             outside S are re-quantised to INT2 from their dequantised values.
+ *   p may be NULL for step > 0. */
+kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params* p, int step,
+                          void* stream);
+
+/* decode_attn_qkv -- one decode step of attention over the compressed cache
+ * with in-kernel dequantisation ([MiKV-R] INTn x FP16 GEMV with on-the-fly
+ * dequantisation; [MiniKV-J] fused dequantisation in decoding).
+ *   q (device) [B, Hq, D]; k_new, v_new (device) [B, Hkv, D].
+ *   The new token (position seq_len[b]) is appended to the residual ring
+ *   and attends to itself; o (device) [B, Hq, D] = softmax(sm_scale q.k) v
+ *   over every packed tier (dequantised) and the residual.  lse_out (device,
+ *   nullable) [B, Hq].  DiffKV: win_acc += attention of the step for every
+ *   ring slot.  MiKV: cum_score[token] += sum over the group's heads of the
+ *   attention of the step.  seq_len and res_len advance by one.
+ *   ws (device) of at least kvq_decode_workspace_bytes(c) bytes, 256-byte
+ *   aligned; its content between calls is irrelevant. */
+kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
+                           float sm_scale, void* o, float* lse_out, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Bytes of decode workspace the cache needs (0 on an invalid cache). */
+size_t kvq_decode_workspace_bytes(const kvq_cache* c);
+
+/* Bytes each device array of a cache with these sizes needs; out[i] in the
+ * order of the kvq_cache fields (see kvq_cache_layout in the Python
+ * binding).  Returns the total, 0 on invalid sizes. */
+size_t kvq_tier_bytes(int units, int D, int G, int k_bits, int v_bits, int k_axis, int cap,
+                      size_t out[8]);
+
+/* Thread-local message of the last failed call of this thread. */
+const char* kvq_last_error(void);
+
+/* Synchronises `stream`, reads and clears the device status word of the
+ * current device.  *out = 0 (fine), KVQ_ETIMEOUT or KVQ_EDEVICE. */
+kvq_status kvq_device_status(void* stream, uint32_t* out);
+
+/* Library ABI version (major * 100 + minor). */
+int kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,67 @@
+"""Comparison helpers shared by the parity tests (no method arithmetic here)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# attention outputs at fp16/bf16: max-abs 2e-3 and relative 1e-2 per element
+ATTN_ATOL, ATTN_RTOL = 2e-3, 1e-2
+# cumulative scores: relative 1e-4 (plus a floor for values near zero)
+SCORE_RTOL, SCORE_ATOL = 1e-4, 1e-7
+
+
+def np_(t):
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu()
+        if t.dtype in (torch.float16, torch.bfloat16):
+            t = t.float()
+        return t.numpy()
+    return np.asarray(t)
+
+
+def u32(t):
+    return np_(t).view(np.uint32)
+
+
+def u16(t):
+    a = np_(t)
+    return a.view(np.uint16)
+
+
+def assert_attn_close(gpu, ref, what=""):
+    g = np_(gpu).astype(np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    err = np.abs(g - r)
+    bad = err > ATTN_ATOL + ATTN_RTOL * np.abs(r)
+    assert not bad.any(), f"{what}: {bad.sum()} elements outside tolerance, max abs err {err.max():.3e}"
+    return float(err.max())
+
+
+def assert_scores_close(gpu, ref, what=""):
+    g = np_(gpu).astype(np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    err = np.abs(g - r)
+    bad = err > SCORE_RTOL * np.abs(r) + SCORE_ATOL
+    assert not bad.any(), (f"{what}: {bad.sum()} scores outside tolerance, max rel err "
+                           f"{(err / np.maximum(np.abs(r), 1e-30)).max():.3e}")
+
+
+def selection_agrees(gpu_sel, ref_sel, ref_scores, k, w):
+    """True when identical; otherwise asserts the difference is a valid tie.
+
+    A position may differ only if its (oracle) score lies within the score
+    tolerance of the k-th largest candidate score, i.e. the two rankings
+    differ by rounding at the boundary.
+    """
+    g, r = set(int(x) for x in gpu_sel), set(int(x) for x in ref_sel)
+    if g == r:
+        return True
+    T = len(ref_scores)
+    cand = np.asarray(ref_scores[: T - w], dtype=np.float64)
+    bound = np.sort(cand)[::-1][k - 1]
+    for j in g.symmetric_difference(r):
+        assert j < T - w, f"window position {j} differs"
+        assert abs(cand[j] - bound) <= SCORE_RTOL * abs(bound) + SCORE_ATOL, \
+            f"position {j} (score {cand[j]}) differs far from the boundary {bound}"
+    assert len(g) == len(r)
+    return False

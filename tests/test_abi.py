@@ -1,0 +1,80 @@
+"""The C ABI library builds, loads and exports every symbol include/kvq.h declares;
+host-side validation rejects bad arguments before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_mixed_precision_gb300 import build, kvq
+    build.build()
+    return kvq.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^(?:kvq_status|size_t|int|const char\*)\s+(\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["kv_quant_pack", "prefill_attn_scores", "select_tokens", "requant_demote",
+              "decode_attn_qkv"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_struct_layout_matches_header():
+    from bit_mixed_precision_gb300 import kvq
+    # 4 int32 + 8 pointers
+    assert ctypes.sizeof(kvq.KvqTier) == 16 + 8 * 8
+    # 8 int32, 2 tiers, 2 int32, 9 pointers, 2 int32
+    assert ctypes.sizeof(kvq.KvqCache) == 32 + 2 * 80 + 8 + 9 * 8 + 8
+
+
+def test_host_validation_without_gpu(L):
+    from bit_mixed_precision_gb300 import kvq
+    vp = ctypes.c_void_p(16)
+    # null input
+    assert L.kv_quant_pack(None, 0, 1, 1, 32, 128, None, 32, 2, 32, 0, vp, vp, vp, None) == kvq.KVQ_EINVAL
+    assert b"null" in L.kvq_last_error()
+    # 3-bit codes are not a format
+    assert L.kv_quant_pack(vp, 0, 1, 1, 32, 128, None, 32, 3, 32, 0, vp, vp, vp, None) == kvq.KVQ_EINVAL
+    # channel grouping needs whole groups of tokens
+    assert L.kv_quant_pack(vp, 0, 1, 1, 40, 128, None, 40, 2, 32, 0, vp, vp, vp, None) == kvq.KVQ_EINVAL
+    # prefill head dim other than 128 is not built
+    assert L.prefill_attn_scores(vp, vp, vp, 0, 1, 2, 2, 64, 96, ctypes.c_float(0.1), 1, vp, vp,
+                                 None, None, 0, None) == kvq.KVQ_EUNSUPPORTED
+    # GQA needs Hq multiple of Hkv
+    assert L.prefill_attn_scores(vp, vp, vp, 0, 1, 3, 2, 64, 128, ctypes.c_float(0.1), 1, vp, vp,
+                                 None, None, 0, None) == kvq.KVQ_EINVAL
+    # window larger than the prompt
+    assert L.select_tokens(vp, 1, 1, 10, vp, 4, 11, vp, vp, None, 0, None) == kvq.KVQ_EINVAL
+    # empty cache descriptor
+    c = kvq.KvqCache()
+    assert L.decode_attn_qkv(vp, vp, vp, ctypes.byref(c), ctypes.c_float(0.1), vp, None, vp, 1 << 20,
+                             None) == kvq.KVQ_EINVAL
+    assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == 0
+    assert L.kvq_version() == 100
+
+
+def test_tier_byte_accounting(L):
+    from bit_mixed_precision_gb300 import kvq
+    out = (ctypes.c_size_t * 8)()
+    # one unit, 32 tokens, INT2 keys per channel and values per token, D = 128, G = 32
+    tot = L.kvq_tier_bytes(1, 128, 32, 2, 2, kvq.AXIS_CHANNEL, 32, out)
+    per_token_payload = sum(out[:6]) / 32
+    assert per_token_payload == 96             # 3 bits per scalar, keys + values
+    assert tot == sum(out)
+    assert L.kvq_tier_bytes(1, 128, 32, 2, 2, kvq.AXIS_CHANNEL, 40, out) == 0

@@ -1,0 +1,60 @@
+"""prefill_attn_scores (tcgen05 two-pass kernel) against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bit_mixed_precision_gb300 import inputs, kvq
+from oracle import attention as OA
+from tests.helpers import assert_attn_close, assert_scores_close, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(B, Hq, Hkv, T, dtype=torch.float16, seed=0, outlier_scale=10.0, n_out=3):
+    D = 128
+    x = inputs.make_qkv(B, Hq, Hkv, T, D, dtype=dtype, seed=seed,
+                        outliers=inputs.outlier_channels(Hkv, D, n_out, seed),
+                        outlier_scale=outlier_scale)
+    scale = 1.0 / math.sqrt(D)
+    o, lse, cs = kvq.prefill_attn_scores(x.q.cuda(), x.k.cuda(), x.v.cuda(), scale)
+    torch.cuda.synchronize()
+    assert kvq.device_status() == 0
+    return x, scale, o, lse, cs
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,dtype", [
+    (1, 2, 2, 256, torch.float16),       # two full tiles
+    (2, 4, 2, 300, torch.float16),       # GQA, ragged tail of 44 rows
+    (1, 4, 1, 200, torch.bfloat16),      # bf16, g = 4
+    (1, 1, 1, 1, torch.float16),         # a single token
+    (1, 5, 1, 129, torch.float16),       # g = 5, one row past a tile
+])
+def test_prefill_matches_oracle(B, Hq, Hkv, T, dtype):
+    x, scale, o, lse, cs = _run(B, Hq, Hkv, T, dtype)
+    oo, ol, oc = OA.prefill(np_(x.q), np_(x.k), np_(x.v), scale)
+    assert_attn_close(o, oo, "O")
+    assert np.allclose(np_(lse), ol, atol=1e-4, rtol=1e-5), "lse"
+    assert_scores_close(cs, oc, "colscore")
+    # the column scores of each head add up to the number of queries
+    assert np.allclose(np_(cs).sum(axis=-1), T, rtol=1e-5)
+
+
+def test_prefill_4096_sampled():
+    """The 32-head, 4096-token LLaMA2-7B-shaped layer: two heads checked in full."""
+    B, H, T, D = 1, 32, 4096, 128
+    x, scale, o, lse, cs = _run(B, H, H, T)
+    for h in (0, 31):
+        oo, ol, oc = OA.prefill_head(np_(x.q[0, h]), np_(x.k[0, h]), np_(x.v[0, h]), scale)
+        assert_attn_close(o[0, h], oo, f"O head {h}")
+        assert_scores_close(cs[0, h], oc, f"colscore head {h}")
+    assert np.allclose(np_(cs).sum(axis=-1), T, rtol=1e-4)
+
+
+def test_prefill_large_scores():
+    """Outlier channels x40 push row maxima far apart (exercises the rescale path)."""
+    x, scale, o, lse, cs = _run(1, 2, 2, 512, outlier_scale=40.0, n_out=6)
+    oo, ol, oc = OA.prefill(np_(x.q), np_(x.k), np_(x.v), scale)
+    assert_attn_close(o, oo, "O")
+    assert_scores_close(cs, oc, "colscore")
