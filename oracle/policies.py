@@ -62,6 +62,13 @@ def _f32(x):
     return np.asarray(x).astype(F32)
 
 
+def topk_by_id(scores, ids):
+    """Token ids sorted by (score descending, id ascending)."""
+    ids = np.asarray(ids, dtype=np.int64)
+    order = np.lexsort((ids, -np.asarray(scores).astype(np.float64)))
+    return ids[order]
+
+
 # ---------------------------------------------------------------------------
 # Packed token store with per-token groups (DiffKV and MiKV tiers)
 # ---------------------------------------------------------------------------
@@ -193,7 +200,8 @@ class DiffKVUnit:
         # window entries: [token id, k, v, acc per head]
         self.win = [[j, kf[j], vf[j], cs[:, j].copy()] for j in range(nc, T)]
 
-    def step(self, pos, qs, k_new, v_new, sm_scale):
+    def attend(self, pos, qs, k_new, v_new, sm_scale):
+        """Append the new token to the window, attend, add the attention to the window sums."""
         g = qs.shape[0]
         self.win.append([int(pos), _f32(k_new), _f32(v_new), np.zeros(g, F32)])
         ids, kk, vv = [], [], []
@@ -215,23 +223,28 @@ class DiffKVUnit:
             p = outs[h][2]
             for i, w in enumerate(self.win):
                 w[3][h] = F32(w[3][h] + F32(p[nq + i]))
-        decision = None
-        if len(self.win) > self.W:
-            tc, kc, vc, acc = self.win.pop(0)
-            N = pos + 1
-            score = (acc / F32(N - tc)).astype(F32).max()
-            th_h = F32(self.alpha_h / F32(N))
-            th_l = F32(self.alpha_l / F32(N))
-            if score >= th_h:
-                self.high.add_raw(tc, kc, vc)
-                decision = (tc, "high")
-            elif score >= th_l:
-                self.low.add_raw(tc, kc, vc)
-                decision = (tc, "low")
-            else:
-                self.pruned.append(tc)
-                decision = (tc, "pruned")
-        return np.array([o[0] for o in outs]), np.array([o[1] for o in outs]), decision
+        return np.array([o[0] for o in outs]), np.array([o[1] for o in outs])
+
+    def tail(self, N):
+        """The oldest window token leaves (if the window overflows); N = sequence length."""
+        if len(self.win) <= self.W:
+            return None
+        tc, kc, vc, acc = self.win.pop(0)
+        score = (acc / F32(N - tc)).astype(F32).max()
+        th_h = F32(self.alpha_h / F32(N))
+        th_l = F32(self.alpha_l / F32(N))
+        if score >= th_h:
+            self.high.add_raw(tc, kc, vc)
+            return (tc, "high")
+        if score >= th_l:
+            self.low.add_raw(tc, kc, vc)
+            return (tc, "low")
+        self.pruned.append(tc)
+        return (tc, "pruned")
+
+    def step(self, pos, qs, k_new, v_new, sm_scale):
+        o, lse = self.attend(pos, qs, k_new, v_new, sm_scale)
+        return o, lse, self.tail(pos + 1)
 
 
 # ---------------------------------------------------------------------------
@@ -268,7 +281,8 @@ class MiKVUnit:
         self.res = [(j, kf[j], vf[j]) for j in range(nq, T)]
         self.demoted = []
 
-    def step(self, pos, qs, k_new, v_new, sm_scale):
+    def attend(self, pos, qs, k_new, v_new, sm_scale):
+        """Append the new token, attend, add this step's attention to every cumulative score."""
         g = qs.shape[0]
         self.res.append((int(pos), _f32(k_new), _f32(v_new)))
         self.cs[int(pos)] = F32(0)
@@ -291,13 +305,17 @@ class MiKVUnit:
             contrib = (contrib + outs[h][2].astype(F32)).astype(F32)
         for i, t in enumerate(ids):
             self.cs[t] = F32(self.cs[t] + contrib[i])
+        return np.array([o[0] for o in outs]), np.array([o[1] for o in outs])
+
+    def tail(self):
+        """Residual exit, re-ranking and demotion; returns (entered, demoted)."""
         demoted = []
         entered = None
         if len(self.res) > self.nr:
             e, ke, ve = self.res.pop(0)
             pop = self.hi.ids() + self.lo.ids() + [e]
             sc = np.array([self.cs[t] for t in pop], F32)
-            order = np.array(pop)[topk_order(sc, np.arange(len(pop)))]
+            order = topk_by_id(sc, np.array(pop))
             top = set(int(t) for t in order[:len(pop) // self.den])
             if e in top:
                 self.hi.add_raw(e, ke, ve)
@@ -312,5 +330,9 @@ class MiKVUnit:
                     self.lo.add_raw(t, kh, vh)
                     demoted.append(t)
         self.demoted.append(demoted)
-        return (np.array([o[0] for o in outs]), np.array([o[1] for o in outs]),
-                entered, demoted)
+        return entered, demoted
+
+    def step(self, pos, qs, k_new, v_new, sm_scale):
+        o, lse = self.attend(pos, qs, k_new, v_new, sm_scale)
+        entered, demoted = self.tail()
+        return o, lse, entered, demoted

@@ -186,3 +186,17 @@ def test_tier_byte_closed_forms():
     assert acc.token_bytes(128, 4, 2, 32) == 128
     assert acc.fp16_token_bytes(128) == 512
     assert (8 + 4) / 32 == 0.375 and (4 + 2) / 32 == 0.1875     # codes only, DiffKV tiers
+
+
+def test_mikv_ties_go_to_the_lower_position():
+    """Equal cumulative scores: the lower position stays INT4 whatever tier it sits in."""
+    T, D = 12, 32
+    k, v = _kv(T + 1, D, 12)
+    # tokens 3 and 7 tie for the last INT4 place once token 10 (score 9) leaves the residual
+    cs = np.array([[0, 0, 0, 5, 0, 0, 0, 5, 0, 0, 9, 0]], F32)
+    u = P.MiKVUnit(k[:T], v[:T], cs, nr=2, group=32)
+    assert u.hi.ids() == [3, 7]             # floor(10/5) = 2, tie 3 < 7 both in
+    _, _, e, d = u.step(T, np.zeros((1, D)), k[T], v[T], 0.3)
+    # population 11 -> 2 places: token 10 (9 + 1/13) and the lower of the tied 3 / 7
+    assert e == (10, "int4") and d == [7]
+    assert u.hi.ids() == [3, 10]
