@@ -59,6 +59,8 @@ const char* kvq_last_error(void) { return kvq::g_last_error.c_str(); }
 kvq_status kv_quant_pack(const void* x, kvq_dtype dt, int B, int H, int T, int D,
                          const int32_t* gather_idx, int n, int bits, int group, kvq_axis axis,
                          uint32_t* codes, uint16_t* scale, uint16_t* zero, void* stream) {
+    KVQ_REQUIRE(B >= 0 && H >= 0 && T >= 0 && n >= 0, KVQ_EINVAL, "kv_quant_pack: negative size");
+    if (n == 0 || B == 0 || H == 0) return KVQ_OK;     // nothing to pack
     KVQ_REQUIRE(x && codes && scale && zero, KVQ_EINVAL, "kv_quant_pack: null pointer");
     KVQ_REQUIRE(dt == KVQ_F16 || dt == KVQ_BF16, KVQ_EINVAL, "kv_quant_pack: dtype must be f16 or bf16");
     KVQ_REQUIRE(B >= 0 && H >= 0 && T >= 0 && n >= 0, KVQ_EINVAL, "kv_quant_pack: negative size");

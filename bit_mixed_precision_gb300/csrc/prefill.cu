@@ -58,7 +58,7 @@ template <int D> struct Layout {
 };
 
 enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SFREE = 9, B_PF = 11, B_OD = 12,
-             B_DRAIN = 13, P1_NBAR = 14 };
+             B_DRAIN = 13, B_VC = 14, P1_NBAR = 16 };
 enum P2Bar { C_KF = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_SFREE = 7, C_DRAIN = 9, C_LSE = 10,
              P2_NBAR = 12 };
 
@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(BAR(B_PF), 4);
         mbar_init(BAR(B_OD), 1);
         mbar_init(BAR(B_DRAIN), 1);
+        mbar_init(BAR(B_VC), 4);
+        mbar_init(BAR(B_VC + 1), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -194,11 +196,13 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 5) {
         if (lane == 0) {
             const uint32_t idS = idesc_f16(AB, 128, 128, 0);
-            const uint32_t idPV = idesc_f16(AB, 128, D, 1);
+            // P is always fp16; bf16 V tiles are converted to fp16 in smem first
+            const uint32_t idPV = idesc_f16(0, 128, D, 1);
             bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
             auto issue_pv = [&](int jj) -> bool {
                 if (!mbar_wait(BAR(B_PF), jj & 1, abort_flag)) return false;
-                if (!mbar_wait(BAR(B_VF + (jj & 1)), (jj >> 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(BAR((AB ? B_VC : B_VF) + (jj & 1)), (jj >> 1) & 1, abort_flag))
+                    return false;
                 tc_fence_after();
                 const uint32_t vt = sV + (uint32_t)(jj & 1) * kTileBytes;
 #pragma unroll
@@ -251,6 +255,26 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
+            if (AB) {
+                // bf16 -> fp16 of this thread's share of the V tile (exact for |v| < 65504)
+                if (!warp_wait(BAR(B_VF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                uint4* vt = reinterpret_cast<uint4*>(gbase + Lay::P1_V + (uint32_t)sb * kTileBytes);
+#pragma unroll 4
+                for (int c = r; c < (int)(kTileBytes / 16); c += 128) {
+                    uint4 w = vt[c];
+                    uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __nv_bfloat162 b2 = *reinterpret_cast<__nv_bfloat162*>(&e[u]);
+                        float2 f = __bfloat1622float2(b2);
+                        e[u] = Pack2<__half>::pack(f.x, f.y);
+                    }
+                    vt[c] = w;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(B_VC + sb));
+            }
 
             const int kbase = j * kTile;
             float mx = -__int_as_float(0x7f800000);
@@ -296,8 +320,8 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const uint32_t off = (uint32_t)(c8 >> 3) * kHalfBytes + (uint32_t)r * 128u +
                                      ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
-                st_shared_v4(sP + off, Pack2<T>::pack(p[0], p[1]), Pack2<T>::pack(p[2], p[3]),
-                             Pack2<T>::pack(p[4], p[5]), Pack2<T>::pack(p[6], p[7]));
+                st_shared_v4(sP + off, Pack2<__half>::pack(p[0], p[1]), Pack2<__half>::pack(p[2], p[3]),
+                             Pack2<__half>::pack(p[4], p[5]), Pack2<__half>::pack(p[6], p[7]));
             }
             l += rs;
             fence_proxy_async_smem();

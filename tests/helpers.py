@@ -65,3 +65,29 @@ def selection_agrees(gpu_sel, ref_sel, ref_scores, k, w):
             f"position {j} (score {cand[j]}) differs far from the boundary {bound}"
     assert len(g) == len(r)
     return False
+
+
+def gpu_tier_rows(tier, u):
+    """{token id: (k codes, k scale, k zero, v codes, v scale, v zero)} of unit u of a
+    per-token tier, as uint32 / uint16 arrays."""
+    c = int(tier.count[u].item())
+    ids = tier.token_id[u, :c].cpu().numpy()
+    kc, ks, kz = u32(tier.k_codes[u, :c]), u16(tier.k_scale[u, :c]), u16(tier.k_zero[u, :c])
+    vc, vs, vz = u32(tier.v_codes[u, :c]), u16(tier.v_scale[u, :c]), u16(tier.v_zero[u, :c])
+    return {int(ids[i]): (kc[i], ks[i], kz[i], vc[i], vs[i], vz[i]) for i in range(c)}
+
+
+def oracle_tier_rows(tt):
+    """Same view of an oracle TokenTier."""
+    out = {}
+    for tid, (kc, ks, kz, vc, vs, vz) in tt.rows.items():
+        out[int(tid)] = (kc.view(np.uint32), ks.view(np.uint16), kz.view(np.uint16),
+                         vc.view(np.uint32), vs.view(np.uint16), vz.view(np.uint16))
+    return out
+
+
+def assert_tiers_equal(gpu_rows, ref_rows, what=""):
+    assert sorted(gpu_rows) == sorted(ref_rows), f"{what}: token sets differ"
+    for tid, row in ref_rows.items():
+        for a, b in zip(gpu_rows[tid], row):
+            assert np.array_equal(a, b), f"{what}: token {tid} payload differs"

@@ -48,6 +48,7 @@ def test_host_validation_without_gpu(L):
     vp = ctypes.c_void_p(16)
     # null input
     assert L.kv_quant_pack(None, 0, 1, 1, 32, 128, None, 32, 2, 32, 0, vp, vp, vp, None) == kvq.KVQ_EINVAL
+    assert L.kv_quant_pack(None, 0, 1, 1, 32, 128, None, 0, 2, 32, 0, None, None, None, None) == kvq.KVQ_OK
     assert b"null" in L.kvq_last_error()
     # 3-bit codes are not a format
     assert L.kv_quant_pack(vp, 0, 1, 1, 32, 128, None, 32, 3, 32, 0, vp, vp, vp, None) == kvq.KVQ_EINVAL
