@@ -218,9 +218,8 @@ kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params
             KVQ_REQUIRE(p->T > c->nr, KVQ_EINVAL, "requant_demote: T must exceed the window/residual");
             KVQ_REQUIRE(p->T <= c->score_cap || mode == KVQ_POLICY_DIFFKV, KVQ_EINVAL, "requant_demote: score_cap < T");
             if (mode == KVQ_POLICY_DIFFKV) {
+                // n_high / n_low live on the device: tier capacities are checked there
                 KVQ_REQUIRE(p->n_high && p->n_low, KVQ_EINVAL, "requant_demote: n_high/n_low missing");
-                KVQ_REQUIRE(c->tier[0].cap + c->tier[1].cap >= p->T - c->nr, KVQ_EINVAL,
-                            "requant_demote: tiers cannot hold the candidates");
             } else {
                 KVQ_REQUIRE(c->tier[0].cap + 0 >= (p->T - c->nr) / c->hi_den && c->tier[1].cap >= p->T - c->nr - (p->T - c->nr) / c->hi_den,
                             KVQ_EINVAL, "requant_demote: tier capacity too small");

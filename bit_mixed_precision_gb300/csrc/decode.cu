@@ -23,11 +23,13 @@ KVQ_DEFINE_STATUS(decode)
 
 namespace {
 
-constexpr int kChunk = 256;     // tokens per CTA
-constexpr int kThreads = 256;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kChunk = 256;     // tokens per CTA: each warp takes 32-token groups in turn
 constexpr int kMaxG = 8;        // query heads per KV head
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
 
 struct TierArgs {
     int k_bits, v_bits, k_axis, cap;
@@ -81,187 +83,441 @@ __device__ __forceinline__ void stf(void* p, size_t i, float v, bool bf16) {
         reinterpret_cast<__half*>(p)[i] = __float2half_rn(v);
 }
 
-// Dequantised key element (token slot j, channel c) of a tier.
-template <int KB, int KAX>
-__device__ __forceinline__ float key_at(const TierArgs& t, size_t unit, int j, int c, int D, int G) {
-    if (KAX == KVQ_AXIS_CHANNEL) {
-        constexpr int per = 32 / KB;
-        const uint32_t w = t.k_codes[(unit * (size_t)(t.cap / per) + j / per) * D + c];
-        const uint32_t q = (w >> (KB * (j % per))) & ((1u << KB) - 1u);
-        const size_t si = (unit * (size_t)(t.cap / G) + j / G) * D + c;
-        return fmaf((float)q, h2f_bits(t.k_scale[si]), h2f_bits(t.k_zero[si]));
-    } else {
-        const uint32_t* row = t.k_codes + (unit * t.cap + j) * (size_t)(D * KB / 32);
-        const uint32_t q = code_at(row, c, KB);
-        const size_t si = (unit * t.cap + j) * (size_t)(D / G) + c / G;
-        return fmaf((float)q, h2f_bits(t.k_scale[si]), h2f_bits(t.k_zero[si]));
-    }
+// Code i (KB bits) of a packed word as the float 1 + c * 2^-KB: one rotate
+// moves the code to the top of the mantissa, one LOP3 masks it and sets the
+// exponent of 1.0.  fma(x, y * 2^KB, acc) then adds y * 2^KB + c * y; the
+// constant y * 2^KB is removed once per dot product.
+template <int KB>
+__device__ __forceinline__ float code_f(uint32_t w, int i) {
+    const int rot = ((23 - KB - KB * i) % 32 + 32) % 32;
+    const uint32_t x = __funnelshift_l(w, w, rot);
+    constexpr uint32_t mask = ((1u << KB) - 1u) << (23 - KB);
+    return __uint_as_float((x & mask) | 0x3F800000u);
 }
 
-template <int VB>
-__device__ __forceinline__ float value_at(const TierArgs& t, size_t unit, int j, int c, int D, int G) {
-    const uint32_t* row = t.v_codes + (unit * t.cap + j) * (size_t)(D * VB / 32);
-    const uint32_t q = code_at(row, c, VB);
-    const size_t si = (unit * t.cap + j) * (size_t)(D / G) + c / G;
-    return fmaf((float)q, h2f_bits(t.v_scale[si]), h2f_bits(t.v_zero[si]));
+// 32 lanes each hold v[0..31]; afterwards v[0] of lane t = sum over lanes of v[t].
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
 }
 
 struct Smem {
-    float q[kMaxG][128];
-    float lg[kMaxG][kChunk];
-    float red[kMaxG][kThreads / 32];
-    float m[kMaxG];
-    float opart[4][kMaxG][128];
+    float q[kMaxG][128];                 // query rows, pre-scaled to base-2 logits
+    float wm[kWarps][kMaxG];
+    float wl[kWarps][kMaxG];
+    float wo[kWarps][kMaxG][128];
+    float lg[kWarps][kMaxG][32];         // logits of the warp's current group
     int last;
 };
 
-// Logits and P.V of one chunk of n tokens.  KeyFn(i, c) / ValFn(i, c) give
-// the dequantised (or full-precision) element of chunk token i.
-template <typename KeyFn, typename ValFn>
-__device__ void chunk_attend(const DecodeArgs& a, Smem& sm, int n, KeyFn key, ValFn val,
-                             float* part_out /* [g][total_chunks][D+2] at this chunk */,
-                             float* lg_out /* [g][slots] at this chunk's first slot, or null */) {
+// Online-softmax state of one warp for NG heads; o holds the lane's share.
+template <int NG, int NO>
+struct WarpAcc {
+    float m[NG], l[NG];
+    float o[NG][NO];
+    float off[NG], zs[NG];               // packed V: sum p*s*2^VB and sum p*z over this lane
+};
+
+// Logits of the group (lane t holds token t, -inf past nt) -> rescale the
+// accumulators, return p_h(t) in lg and write logits out when asked.
+template <int NG, int NO>
+__device__ __forceinline__ void group_softmax(WarpAcc<NG, NO>& acc, float (&lg)[NG], int nt,
+                                              float* lg_out, int slots) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        const float s = lane < nt ? lg[h] : kNegInf;
+        if (lg_out && lane < nt) lg_out[(size_t)h * slots + lane] = s;
+        const float mg = warp_max(s);
+        const float mn = fmaxf(acc.m[h], mg);
+        const float corr = acc.m[h] == kNegInf ? 0.0f : ex2_approx(acc.m[h] - mn);
+        const float p = lane < nt ? ex2_approx(s - mn) : 0.0f;
+        acc.l[h] = acc.l[h] * corr + warp_sum(p);
+#pragma unroll
+        for (int i = 0; i < NO; ++i) acc.o[h][i] *= corr;
+        acc.off[h] *= corr;
+        acc.zs[h] *= corr;
+        acc.m[h] = mn;
+        lg[h] = p;
+    }
+}
+
+// ---- key paths: each returns this lane's token logit for every head
+
+// Keys grouped per channel (packed along tokens): lane owns CPL channels;
+// partial dot products of 32 tokens, then a reduce-scatter across lanes.
+template <int KB, int CPL, int NG>
+__device__ __forceinline__ void logits_channel(const TierArgs& t, size_t unit, int tb, const Smem& sm,
+                                               int G, float (&lg)[NG]) {
+    constexpr int D = CPL * 32;
+    constexpr int per = 32 / KB;          // tokens per word
+    constexpr int rows = 32 / per;        // word rows per 32-token group
+    const int lane = threadIdx.x & 31;
+    const int c0 = lane * CPL;
+    const size_t srow_i = (unit * (size_t)(t.cap / G) + tb / G) * D + c0;
+    float s[CPL], z[CPL];
+#pragma unroll
+    for (int ci = 0; ci < CPL; ++ci) {
+        s[ci] = h2f_bits(t.k_scale[srow_i + ci]);
+        z[ci] = h2f_bits(t.k_zero[srow_i + ci]);
+    }
+    uint32_t w[rows][CPL];
+    const uint32_t* base = t.k_codes + (unit * (size_t)(t.cap / per) + tb / per) * D + c0;
+#pragma unroll
+    for (int r = 0; r < rows; ++r) {
+        if (CPL == 4) {
+            const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * D));
+            w[r][0] = v4.x; w[r][1] = v4.y; w[r][2] = v4.z; w[r][3] = v4.w;
+        } else {
+            const uint2 v2 = __ldg(reinterpret_cast<const uint2*>(base + (size_t)r * D));
+            w[r][0] = v2.x; w[r][CPL - 1] = v2.y;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        float qs[CPL], off = 0.0f, bias = 0.0f;
+#pragma unroll
+        for (int ci = 0; ci < CPL; ++ci) {
+            const float qv = sm.q[h][c0 + ci];
+            qs[ci] = qv * s[ci] * (float)(1 << KB);
+            off += qs[ci];
+            bias = fmaf(qv, z[ci], bias);
+        }
+        float part[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) part[k] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < rows; ++r)
+#pragma unroll
+            for (int ci = 0; ci < CPL; ++ci)
+#pragma unroll
+                for (int i = 0; i < per; ++i)
+                    part[r * per + i] = fmaf(code_f<KB>(w[r][ci], i), qs[ci], part[r * per + i]);
+        const float raw = reduce_scatter32(part);
+        lg[h] = raw + warp_sum(bias - off);
+    }
+}
+
+// Keys grouped per token (packed along channels): lane owns one word of a
+// token row; dot over the word, scaled by the token's group scale, summed
+// over the lanes of the token.
+template <int KB, int D, int NG>
+__device__ __forceinline__ void logits_token(const TierArgs& t, size_t unit, int tb, int nt, Smem& sm,
+                                             int G, float (&lg)[NG]) {
+    constexpr int lpt = D * KB / 32;      // words (lanes) per token
+    constexpr int tpp = 32 / lpt;         // tokens per pass
+    constexpr int cpw = 32 / KB;          // channels per word
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wi = lane % lpt, to = lane / lpt;
+    const int c0 = wi * cpw, grp = c0 / G;
+    float q4[NG][cpw], off[NG], qsum[NG];
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        off[h] = 0.0f;
+        qsum[h] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < cpw; ++i) {
+            const float qv = sm.q[h][c0 + i];
+            q4[h][i] = qv * (float)(1 << KB);
+            off[h] += q4[h][i];
+            qsum[h] += qv;
+        }
+    }
+#pragma unroll 4
+    for (int ps = 0; ps < lpt; ++ps) {
+        const int tk = ps * tpp + to;
+        float c[NG];
+#pragma unroll
+        for (int h = 0; h < NG; ++h) c[h] = 0.0f;
+        if (tk < nt) {
+            const size_t row = unit * (size_t)t.cap + tb + tk;
+            const uint32_t w = __ldg(t.k_codes + row * lpt + wi);
+            const float sc = h2f_bits(__ldg(t.k_scale + row * (D / G) + grp));
+            const float zc = h2f_bits(__ldg(t.k_zero + row * (D / G) + grp));
+#pragma unroll
+            for (int h = 0; h < NG; ++h) {
+                float d = 0.0f;
+#pragma unroll
+                for (int i = 0; i < cpw; ++i) d = fmaf(code_f<KB>(w, i), q4[h][i], d);
+                c[h] = fmaf(sc, d - off[h], zc * qsum[h]);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < NG; ++h) {
+#pragma unroll
+            for (int o = lpt / 2; o; o >>= 1) c[h] += __shfl_xor_sync(0xffffffffu, c[h], o);
+            if (wi == 0) sm.lg[warp][h][tk] = c[h];
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < NG; ++h) lg[h] = sm.lg[warp][h][lane];
+    __syncwarp();
+}
+
+// ---- value paths
+
+// Values grouped per token: lane owns word wi of the tokens to, to + tpp, ...
+template <int VB, int D, int NG>
+__device__ __forceinline__ void values_token(const TierArgs& t, size_t unit, int tb, int nt,
+                                             const float (&p)[NG], int G,
+                                             WarpAcc<NG, 32 / VB>& acc) {
+    constexpr int lpt = D * VB / 32, tpp = 32 / lpt, cpw = 32 / VB;
+    const int lane = threadIdx.x & 31;
+    const int wi = lane % lpt, to = lane / lpt;
+    const int grp = (wi * cpw) / G;
+#pragma unroll 2
+    for (int ps = 0; ps < lpt; ++ps) {
+        const int tk = ps * tpp + to;
+        float pk[NG];
+#pragma unroll
+        for (int h = 0; h < NG; ++h) pk[h] = __shfl_sync(0xffffffffu, p[h], tk);
+        if (tk < nt) {
+            const size_t row = unit * (size_t)t.cap + tb + tk;
+            const uint32_t w = __ldg(t.v_codes + row * lpt + wi);
+            const float sc = h2f_bits(__ldg(t.v_scale + row * (D / G) + grp));
+            const float zc = h2f_bits(__ldg(t.v_zero + row * (D / G) + grp));
+#pragma unroll
+            for (int h = 0; h < NG; ++h) {
+                const float ps4 = pk[h] * sc * (float)(1 << VB);
+                acc.off[h] += ps4;
+                acc.zs[h] = fmaf(pk[h], zc, acc.zs[h]);
+#pragma unroll
+                for (int i = 0; i < cpw; ++i) acc.o[h][i] = fmaf(code_f<VB>(w, i), ps4, acc.o[h][i]);
+            }
+        }
+    }
+}
+
+// Finish a packed-V warp: remove the constants, sum the lanes that share a
+// word, publish to smem.
+template <int VB, int D, int NG>
+__device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, Smem& sm) {
+    constexpr int lpt = D * VB / 32, cpw = 32 / VB;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wi = lane % lpt, to = lane / lpt;
+#pragma unroll
+    for (int h = 0; h < NG; ++h)
+#pragma unroll
+        for (int i = 0; i < cpw; ++i) {
+            float v = acc.o[h][i] - acc.off[h] + acc.zs[h];
+#pragma unroll
+            for (int o = lpt; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (to == 0) sm.wo[warp][h][wi * cpw + i] = v;
+        }
+}
+
+// ---- residual (full precision ring + the new token)
+
+template <int CPL>
+__device__ __forceinline__ void load_row(const void* base, size_t elem, bool bf, float (&x)[CPL]) {
+    if (CPL == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + elem));
+        const uint32_t e[2] = {u.x, u.y};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (bf) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&e[k]));
+                x[2 * k] = f.x; x[2 * k + 1] = f.y;
+            } else {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&e[k]));
+                x[2 * k] = f.x; x[2 * k + 1] = f.y;
+            }
+        }
+    } else {
+        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(base) + elem));
+        if (bf) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+            x[0] = f.x; x[CPL - 1] = f.y;
+        } else {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+            x[0] = f.x; x[CPL - 1] = f.y;
+        }
+    }
+}
+
+template <int CPL, int NG>
+__device__ void warp_residual(const DecodeArgs& a, Smem& sm, size_t unit, int len, int start,
+                              int j0, int n, float* lg_out) {
+    constexpr int D = CPL * 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c0 = lane * CPL;
+    const bool bf = a.bf16 != 0;
+    const int cap = a.res_cap;
+    const size_t rbase = unit * (size_t)cap;
+    WarpAcc<NG, CPL> acc;
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        acc.m[h] = kNegInf;
+        acc.l[h] = 0.0f;
+        acc.off[h] = 0.0f;
+        acc.zs[h] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) acc.o[h][i] = 0.0f;
+    }
+    for (int gi = warp; gi * 32 < n; gi += kWarps) {
+        const int tb = j0 + gi * 32;
+        const int nt = min(32, n - gi * 32);
+        auto elem_of = [&](int k, bool kk) -> size_t {
+            const int li = tb + k;
+            return li < len ? (rbase + (start + li) % cap) * D + c0 : unit * (size_t)D + c0;
+        };
+        float lg[NG];
+#pragma unroll
+        for (int h = 0; h < NG; ++h) {
+            float part[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                part[k] = 0.0f;
+                if (k < nt) {
+                    float x[CPL];
+                    load_row<CPL>(tb + k < len ? a.res_k : a.k_new, elem_of(k, true), bf, x);
+#pragma unroll
+                    for (int ci = 0; ci < CPL; ++ci) part[k] = fmaf(sm.q[h][c0 + ci], x[ci], part[k]);
+                }
+            }
+            lg[h] = reduce_scatter32(part);
+        }
+        group_softmax(acc, lg, nt, lg_out ? lg_out + (tb - j0) : nullptr, a.slots);
+        for (int k = 0; k < nt; ++k) {
+            float x[CPL];
+            load_row<CPL>(tb + k < len ? a.res_v : a.v_new, elem_of(k, false), bf, x);
+#pragma unroll
+            for (int h = 0; h < NG; ++h) {
+                const float pk = __shfl_sync(0xffffffffu, lg[h], k);
+#pragma unroll
+                for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] = fmaf(pk, x[ci], acc.o[h][ci]);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        if (lane == 0) {
+            sm.wm[warp][h] = acc.m[h];
+            sm.wl[warp][h] = acc.l[h];
+        }
+#pragma unroll
+        for (int ci = 0; ci < CPL; ++ci) sm.wo[warp][h][c0 + ci] = acc.o[h][ci];
+    }
+}
+
+template <int KB, int KAX, int VB, int D, int NG>
+__device__ void warp_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, size_t unit, int j0,
+                          int n, float* lg_out) {
+    constexpr int cpw = 32 / VB;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    WarpAcc<NG, cpw> acc;
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        acc.m[h] = kNegInf;
+        acc.l[h] = 0.0f;
+        acc.off[h] = 0.0f;
+        acc.zs[h] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < cpw; ++i) acc.o[h][i] = 0.0f;
+    }
+    for (int gi = warp; gi * 32 < n; gi += kWarps) {
+        const int tb = j0 + gi * 32;
+        const int nt = min(32, n - gi * 32);
+        float lg[NG];
+        if (KAX == KVQ_AXIS_CHANNEL)
+            logits_channel<KB, D / 32, NG>(t, unit, tb, sm, a.G, lg);
+        else
+            logits_token<KB, D, NG>(t, unit, tb, nt, sm, a.G, lg);
+        group_softmax(acc, lg, nt, lg_out ? lg_out + (tb - j0) : nullptr, a.slots);
+        values_token<VB, D, NG>(t, unit, tb, nt, lg, a.G, acc);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < NG; ++h) {
+            sm.wm[warp][h] = acc.m[h];
+            sm.wl[warp][h] = acc.l[h];
+        }
+    }
+    finish_token_values<VB, D, NG>(acc, sm);
+}
+
+// Merge the four warps of the CTA into the chunk partial (m, l, o[D]) per head.
+__device__ void cta_partial(const DecodeArgs& a, Smem& sm, float* part_out) {
     const int D = a.D, g = a.g;
-    // phase 1: logits (base-2 units), one token per thread
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        float acc[kMaxG];
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h) acc[h] = 0.0f;
-        for (int c = 0; c < D; ++c) {
-            const float x = key(i, c);
-#pragma unroll
-            for (int h = 0; h < kMaxG; ++h)
-                if (h < g) acc[h] = fmaf(sm.q[h][c], x, acc[h]);
-        }
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h)
-            if (h < g) sm.lg[h][i] = acc[h];
-    }
-    __syncthreads();
-    // phase 2: chunk max per head
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = 0; h < g; ++h) {
-        float mx = -__int_as_float(0x7f800000);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) mx = fmaxf(mx, sm.lg[h][i]);
-        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) sm.red[h][warp] = mx;
-    }
-    __syncthreads();
-    if (threadIdx.x < g) {
-        float mx = -__int_as_float(0x7f800000);
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mx = fmaxf(mx, sm.red[threadIdx.x][w]);
-        sm.m[threadIdx.x] = mx;
-    }
-    __syncthreads();
-    // logits out (for score accumulation), then p in place
-    for (int h = 0; h < g; ++h)
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const float s = sm.lg[h][i];
-            if (lg_out) lg_out[(size_t)h * a.slots + i] = s;
-            sm.lg[h][i] = ex2_approx(s - sm.m[h]);
-        }
-    __syncthreads();
-    // phase 3: P.V, channel c per thread, tokens split over blockDim / D groups
-    const int nsplit = blockDim.x / D;
-    const int c = threadIdx.x % D, sp = threadIdx.x / D;
-    if (sp < nsplit && sp < 4) {
-        float ov[kMaxG];
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h) ov[h] = 0.0f;
-        for (int i = sp; i < n; i += nsplit) {
-            const float x = val(i, c);
-#pragma unroll
-            for (int h = 0; h < kMaxG; ++h)
-                if (h < g) ov[h] = fmaf(sm.lg[h][i], x, ov[h]);
-        }
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h)
-            if (h < g) sm.opart[sp][h][c] = ov[h];
-    }
-    __syncthreads();
     for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
-        const int h = idx / D, cc = idx % D;
-        float s = 0.0f;
-        for (int k = 0; k < nsplit && k < 4; ++k) s += sm.opart[k][h][cc];
-        part_out[(size_t)h * a.total_chunks * (D + 2) + 2 + cc] = s;
-    }
-    // row sums
-    for (int h = 0; h < g; ++h) {
-        float l = 0.0f;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) l += sm.lg[h][i];
-        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) sm.red[h][warp] = l;
-    }
-    __syncthreads();
-    if (threadIdx.x < g) {
-        float l = 0.0f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) l += sm.red[threadIdx.x][w];
-        float* po = part_out + (size_t)threadIdx.x * a.total_chunks * (D + 2);
-        po[0] = sm.m[threadIdx.x];
-        po[1] = l;
+        const int h = idx / D, c = idx % D;
+        float M = kNegInf;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+        float L = 0.0f, O = 0.0f;
+        if (M != kNegInf) {
+            for (int w = 0; w < kWarps; ++w) {
+                if (sm.wm[w][h] == kNegInf) continue;
+                const float f = ex2_approx(sm.wm[w][h] - M);
+                L = fmaf(sm.wl[w][h], f, L);
+                O = fmaf(sm.wo[w][h][c], f, O);
+            }
+        }
+        float* po = part_out + (size_t)h * a.total_chunks * (D + 2);
+        po[2 + c] = O;
+        if (c == 0) {
+            po[0] = M;
+            po[1] = L;
+        }
     }
 }
 
-template <int KB, int KAX, int VB>
-__device__ void tier_chunk(const DecodeArgs& a, Smem& sm, const TierArgs& t, size_t unit, int chunk,
-                           float* part_out, float* lg_out) {
-    const int cnt = min(t.count[unit], t.cap);
-    const int j0 = chunk * kChunk;
-    const int n = min(kChunk, cnt - j0);
-    const int D = a.D, G = a.G;
-    auto key = [&](int i, int c) { return key_at<KB, KAX>(t, unit, j0 + i, c, D, G); };
-    auto val = [&](int i, int c) { return value_at<VB>(t, unit, j0 + i, c, D, G); };
-    chunk_attend(a, sm, n, key, val, part_out, lg_out ? lg_out + j0 : nullptr);
-}
-
-__device__ void dispatch_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, size_t unit,
-                              int chunk, float* part_out, float* lg_out) {
+template <int NG, int D>
+__device__ bool dispatch_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, size_t unit, int j0,
+                              int n, float* lg_out) {
     const int kb = t.k_bits, vb = t.v_bits, ax = t.k_axis;
-    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2)
-        tier_chunk<2, KVQ_AXIS_CHANNEL, 2>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_CHANNEL && kb == 4 && vb == 4)
-        tier_chunk<4, KVQ_AXIS_CHANNEL, 4>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4)
-        tier_chunk<8, KVQ_AXIS_TOKEN, 4>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2)
-        tier_chunk<4, KVQ_AXIS_TOKEN, 2>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4)
-        tier_chunk<4, KVQ_AXIS_TOKEN, 4>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2)
-        tier_chunk<2, KVQ_AXIS_TOKEN, 2>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 4)
-        tier_chunk<2, KVQ_AXIS_TOKEN, 4>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 8)
-        tier_chunk<4, KVQ_AXIS_TOKEN, 8>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 8)
-        tier_chunk<8, KVQ_AXIS_TOKEN, 8>(a, sm, t, unit, chunk, part_out, lg_out);
-    else if (ax == KVQ_AXIS_CHANNEL && kb == 8 && vb == 8)
-        tier_chunk<8, KVQ_AXIS_CHANNEL, 8>(a, sm, t, unit, chunk, part_out, lg_out);
-}
-
-__device__ void empty_partial(const DecodeArgs& a, float* part_out) {
-    if (threadIdx.x < a.g) {
-        float* po = part_out + (size_t)threadIdx.x * a.total_chunks * (a.D + 2);
-        po[0] = -__int_as_float(0x7f800000);
-        po[1] = 0.0f;
+    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
+    if (D == 128) {
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { warp_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { warp_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { warp_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
     }
+    return false;
 }
 
+template <int NG, int D>
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const size_t unit = blockIdx.y;
     const int units = gridDim.y;
     const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
-    const int D = a.D, g = a.g;
+    constexpr int g = NG;
     const bool bf = a.bf16 != 0;
 
-    // query rows of the group, pre-scaled to base-2 logits
     for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
         const int h = idx / D, c = idx % D;
         const size_t qi = ((size_t)b * a.Hq + (size_t)hkv * g + h) * D + c;
         sm.q[h][c] = ldf(a.q, qi, bf) * a.scale_log2;
     }
+    for (int idx = threadIdx.x; idx < kWarps * kMaxG; idx += blockDim.x) {
+        sm.wm[idx / kMaxG][idx % kMaxG] = kNegInf;
+        sm.wl[idx / kMaxG][idx % kMaxG] = 0.0f;
+    }
+    for (int idx = threadIdx.x; idx < kWarps * kMaxG * 128; idx += blockDim.x)
+        (&sm.wo[0][0][0])[idx] = 0.0f;
     __syncthreads();
 
     float* part_out = a.part + (unit * g * a.total_chunks + blockIdx.x) * (size_t)(D + 2);
@@ -271,41 +527,29 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         if (chunk < a.tier[t].chunks) { tier = t; break; }
         chunk -= a.tier[t].chunks;
     }
+    const int j0 = chunk * kChunk;
     if (tier >= 0) {
         const TierArgs& t = a.tier[tier];
         if (t.count[unit] > t.cap && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
-        if (chunk * kChunk < min(t.count[unit], t.cap))
-            dispatch_tier(a, sm, t, unit, chunk, part_out,
-                          (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base : nullptr);
-        else
-            empty_partial(a, part_out);
+        const int cnt = min(t.count[unit], t.cap);
+        const int n = min(kChunk, cnt - j0);
+        if (n > 0) {
+            float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
+            if (!dispatch_tier<NG, D>(a, sm, t, unit, j0, n, lg) && threadIdx.x == 0)
+                atomicOr(&g_status_decode, kDevCheck);
+        }
     } else {
         const int cap = a.res_cap;
         const int len = min(max(a.res_len[unit], 0), cap - 1), start = a.res_start[unit];
         if (a.res_len[unit] != len && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
-        const int j0 = chunk * kChunk;
         const int n = min(kChunk, len + 1 - j0);
-        const size_t rbase = unit * (size_t)cap;
         if (n > 0) {
-            auto key = [&](int i, int c) -> float {
-                const int li = j0 + i;
-                return li < len ? ldf(a.res_k, (rbase + (start + li) % cap) * D + c, bf)
-                                : ldf(a.k_new, unit * D + c, bf);
-            };
-            auto val = [&](int i, int c) -> float {
-                const int li = j0 + i;
-                return li < len ? ldf(a.res_v, (rbase + (start + li) % cap) * D + c, bf)
-                                : ldf(a.v_new, unit * D + c, bf);
-            };
-            chunk_attend(a, sm, n, key, val, part_out,
-                         (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0
-                                                                    : nullptr);
-        } else {
-            empty_partial(a, part_out);
+            float* lg = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 : nullptr;
+            warp_residual<D / 32, NG>(a, sm, unit, len, start, j0, n, lg);
         }
         if (chunk == 0) {
             // the new token joins the ring; no CTA reads this slot in this step
-            const size_t slot = rbase + (start + len) % cap;
+            const size_t slot = unit * (size_t)cap + (start + len) % cap;
             for (int c = threadIdx.x; c < D; c += blockDim.x) {
                 stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
                 stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
@@ -313,6 +557,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
             if (threadIdx.x == 0) a.res_token_id[slot] = a.seq_len[b];
         }
     }
+    __syncthreads();
+    cta_partial(a, sm, part_out);
 
     // ---- completion: the last CTA of the unit merges the partials
     __threadfence();
@@ -328,7 +574,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     const float* pu = a.part + unit * g * a.total_chunks * (size_t)(D + 2);
     if (threadIdx.x < g) {
         const float* ph = pu + (size_t)threadIdx.x * a.total_chunks * (D + 2);
-        float M = -__int_as_float(0x7f800000);
+        float M = kNegInf;
         for (int x = 0; x < a.total_chunks; ++x)
             if (__ldcg(ph + (size_t)x * (D + 2) + 1) > 0.0f) M = fmaxf(M, __ldcg(ph + (size_t)x * (D + 2)));
         float L = 0.0f;
@@ -336,16 +582,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
             const float l = __ldcg(ph + (size_t)x * (D + 2) + 1);
             if (l > 0.0f) L += l * ex2_approx(__ldcg(ph + (size_t)x * (D + 2)) - M);
         }
-        sm.red[threadIdx.x][0] = M;
-        sm.red[threadIdx.x][1] = L;
-        sm.m[threadIdx.x] = M + __log2f(L);          // base-2 lse
+        sm.wm[0][threadIdx.x] = M;
+        sm.wl[0][threadIdx.x] = L;
+        sm.wm[1][threadIdx.x] = M + __log2f(L);          // base-2 lse
         if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * g + threadIdx.x] = (M + __log2f(L)) * kLn2;
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
         const int h = idx / D, c = idx % D;
         const float* ph = pu + (size_t)h * a.total_chunks * (D + 2);
-        const float M = sm.red[h][0], L = sm.red[h][1];
+        const float M = sm.wm[0][h], L = sm.wl[0][h];
         float acc = 0.0f;
         for (int x = 0; x < a.total_chunks; ++x) {
             const float l = __ldcg(ph + (size_t)x * (D + 2) + 1);
@@ -356,6 +602,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
 
     const int cap = a.res_cap;
     const int len = min(max(a.res_len[unit], 0), cap - 1), start = a.res_start[unit];
+    const float* lse2 = sm.wm[1];
     if (a.policy == KVQ_POLICY_MIKV && lg_unit) {
         float* cs = a.cum_score + unit * (size_t)a.score_cap;
         for (int t = 0; t < a.n_tiers; ++t) {
@@ -364,7 +611,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
             for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
                 float p = 0.0f;
                 for (int h = 0; h < g; ++h)
-                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ti.slot_base + j) - sm.m[h]);
+                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ti.slot_base + j) - lse2[h]);
                 const int id = ti.token_id[unit * (size_t)ti.cap + j];
                 if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
                 else atomicOr(&g_status_decode, kDevCheck);
@@ -373,7 +620,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         for (int li = threadIdx.x; li <= len; li += blockDim.x) {
             float p = 0.0f;
             for (int h = 0; h < g; ++h)
-                p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - sm.m[h]);
+                p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
             const int id = li < len ? a.res_token_id[unit * (size_t)cap + (start + li) % cap] : a.seq_len[b];
             if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
             else cs[id] = li < len ? __fadd_rn(cs[id], p) : p;
@@ -381,7 +628,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     } else if (a.policy == KVQ_POLICY_DIFFKV && lg_unit) {
         for (int idx = threadIdx.x; idx < (len + 1) * g; idx += blockDim.x) {
             const int li = idx / g, h = idx % g;
-            const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - sm.m[h]);
+            const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
             float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * g + h) * cap + (start + li) % cap;
             *wa = li < len ? __fadd_rn(*wa, p) : p;
         }
@@ -399,6 +646,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         }
     }
 }
+
+}  // namespace
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -429,7 +678,6 @@ WsLayout ws_layout(const kvq_cache& c) {
     return w;
 }
 
-}  // namespace
 
 size_t decode_workspace_bytes(const kvq_cache& c) { return ws_layout(c).total; }
 
@@ -494,8 +742,17 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(units + 1) * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     dim3 grid(w.total_chunks, units);
-    decode_kernel<<<grid, kThreads, sizeof(Smem), s>>>(a);
-    return cudaGetLastError();
+    const size_t sh = sizeof(Smem);
+#define KVQ_DECODE_CASE(NG_, D_) \
+    if (a.g == NG_ && c.D == D_) { decode_kernel<NG_, D_><<<grid, kThreads, sh, s>>>(a); return cudaGetLastError(); }
+    KVQ_DECODE_CASE(1, 128)
+    KVQ_DECODE_CASE(1, 64)
+    KVQ_DECODE_CASE(2, 128)
+    KVQ_DECODE_CASE(4, 128)
+    KVQ_DECODE_CASE(5, 128)
+    KVQ_DECODE_CASE(8, 128)
+#undef KVQ_DECODE_CASE
+    return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace kvq

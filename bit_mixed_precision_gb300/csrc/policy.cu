@@ -235,8 +235,12 @@ __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
         const uint32_t ph = block_excl_scan(is_hi, sh, &tot_hi);
         const uint32_t pl = block_excl_scan(is_lo, sh, &tot_lo);
         const size_t row = (unit * T + j) * (size_t)D;
-        if (is_hi) put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
-        if (is_lo) put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
+        if (is_hi && hi_base + ph < (uint32_t)th.cap)
+            put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
+        if (is_lo && lo_base + pl < (uint32_t)tl.cap)
+            put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
+        if ((is_hi && hi_base + ph >= (uint32_t)th.cap) || (is_lo && lo_base + pl >= (uint32_t)tl.cap))
+            atomicOr(&g_status_policy, kDevCheck);
         eq1_base += tot1;
         eq2_base += tot2;
         hi_base += tot_hi;
@@ -257,8 +261,8 @@ __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
     }
     for (int i = threadIdx.x; i < W; i += blockDim.x) a.res_token_id[unit * a.res_cap + i] = nc + i;
     if (threadIdx.x == 0) {
-        th.count[unit] = (int)hi_base;
-        tl.count[unit] = (int)lo_base;
+        th.count[unit] = min((int)hi_base, th.cap);
+        tl.count[unit] = min((int)lo_base, tl.cap);
         a.res_start[unit] = 0;
         a.res_len[unit] = W;
         a.alpha[unit * 2] = alpha_h;
@@ -335,8 +339,12 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_build(PolicyArgs a) {
         const uint32_t ph = block_excl_scan(is_hi, sh, &tot_hi);
         const uint32_t pl = block_excl_scan(is_lo, sh, &tot_lo);
         const size_t row = (unit * T + j) * (size_t)D;
-        if (is_hi) put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
-        if (is_lo) put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
+        if (is_hi && hi_base + ph < (uint32_t)th.cap)
+            put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
+        if (is_lo && lo_base + pl < (uint32_t)tl.cap)
+            put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
+        if ((is_hi && hi_base + ph >= (uint32_t)th.cap) || (is_lo && lo_base + pl >= (uint32_t)tl.cap))
+            atomicOr(&g_status_policy, kDevCheck);
         eq_base += tot1;
         hi_base += tot_hi;
         lo_base += tot_lo;
@@ -352,8 +360,8 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_build(PolicyArgs a) {
     }
     for (int i = threadIdx.x; i < r0; i += blockDim.x) a.res_token_id[unit * a.res_cap + i] = nq + i;
     if (threadIdx.x == 0) {
-        th.count[unit] = (int)hi_base;
-        tl.count[unit] = (int)lo_base;
+        th.count[unit] = min((int)hi_base, th.cap);
+        tl.count[unit] = min((int)lo_base, tl.cap);
         a.res_start[unit] = 0;
         a.res_len[unit] = r0;
         if (hkv == 0) a.seq_len[b] = T;
