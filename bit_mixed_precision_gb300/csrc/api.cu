@@ -139,7 +139,12 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
         const kvq_tier& tr = c->tier[t];
         KVQ_REQUIRE(valid_bits(tr.k_bits) && valid_bits(tr.v_bits), KVQ_EINVAL, "%s: tier %d bits", who, t);
         KVQ_REQUIRE(tr.k_axis == KVQ_AXIS_CHANNEL || tr.k_axis == KVQ_AXIS_TOKEN, KVQ_EINVAL, "%s: tier %d axis", who, t);
-        KVQ_REQUIRE(tr.cap >= 0, KVQ_EINVAL, "%s: tier %d cap", who, t);
+        KVQ_REQUIRE(tr.cap >= 0 && tr.cap % 32 == 0, KVQ_EINVAL, "%s: tier %d cap must be a multiple of 32", who, t);
+        KVQ_REQUIRE(aligned(tr.k_codes, 16) && aligned(tr.k_scale, 16) && aligned(tr.k_zero, 16) &&
+                        aligned(tr.v_codes, 16) && aligned(tr.v_scale, 16) && aligned(tr.v_zero, 16),
+                    KVQ_EINVAL, "%s: tier %d arrays must be 16-byte aligned", who, t);
+        if (tr.k_axis == KVQ_AXIS_CHANNEL)
+            KVQ_REQUIRE(c->G % 32 == 0, KVQ_EUNSUPPORTED, "%s: per-channel keys need G %% 32 == 0", who);
         if (tr.k_axis == KVQ_AXIS_CHANNEL)
             KVQ_REQUIRE(tr.cap % c->G == 0, KVQ_EINVAL, "%s: tier %d cap must be a multiple of G", who, t);
         KVQ_REQUIRE(tr.k_codes && tr.k_scale && tr.k_zero && tr.v_codes && tr.v_scale && tr.v_zero &&
@@ -188,6 +193,8 @@ kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, 
     kvq_status st = check_cache(c, "decode_attn_qkv");
     if (st != KVQ_OK) return st;
     KVQ_REQUIRE(q && k_new && v_new && o, KVQ_EINVAL, "decode_attn_qkv: null pointer");
+    KVQ_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16) && aligned(c->res_k, 16) && aligned(c->res_v, 16),
+                KVQ_EINVAL, "decode_attn_qkv: k_new, v_new and the residual ring must be 16-byte aligned");
     const size_t need = kvq::decode_workspace_bytes(*c);
     KVQ_REQUIRE(ws && ws_bytes >= need, KVQ_EWORKSPACE,
                 "decode_attn_qkv: workspace of %zu bytes needed, %zu given", need, ws_bytes);

@@ -13,6 +13,8 @@
 // advances the residual length; the last CTA of the grid advances seq_len.
 // The tiers are read where they lie (MiKV rebuttal: attention is
 // permutation invariant, so each precision group sits in its own region).
+#include <algorithm>
+
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 #include "pack_device.cuh"
@@ -128,6 +130,7 @@ struct Smem {
     float wl[kWarps][kMaxG];
     float wo[kWarps][kMaxG][128];
     float lg[kWarps][kMaxG][32];         // logits of the warp's current group
+    unsigned long long bar;              // staging mbarrier
     int last;
 };
 
@@ -163,34 +166,138 @@ __device__ __forceinline__ void group_softmax(WarpAcc<NG, NO>& acc, float (&lg)[
     }
 }
 
+// ---- shared-memory staging: every byte a CTA needs is requested at once
+
+constexpr int kResChunk = 64;    // residual tokens per CTA (full-precision rows are large)
+
+// One chunk of packed tokens in shared memory, indexed from the chunk start.
+struct View {
+    const uint32_t* kc;   // CHANNEL keys: [n/per][D]; TOKEN keys: [n][D*KB/32]
+    const uint16_t* ks;   // CHANNEL keys: [n/G][D];   TOKEN keys: [n][D/G]
+    const uint16_t* kz;
+    const uint32_t* vc;   // [n][D*VB/32]
+    const uint16_t* vs;   // [n][D/G]
+    const uint16_t* vz;
+};
+
+__host__ __device__ __forceinline__ uint32_t a16(uint32_t x) { return (x + 15u) & ~15u; }
+
+// Bytes of one staged tier chunk of npad tokens.
+__host__ __device__ inline uint32_t tier_stage_bytes(int k_axis, int kb, int vb, int npad, int D, int G) {
+    uint32_t kc, ks;
+    if (k_axis == KVQ_AXIS_CHANNEL) {
+        kc = (uint32_t)(npad / (32 / kb)) * D * 4;
+        ks = (uint32_t)(npad / G) * D * 2;
+    } else {
+        kc = (uint32_t)npad * (D * kb / 8);
+        ks = (uint32_t)npad * (D / G) * 2;
+    }
+    const uint32_t vc = (uint32_t)npad * (D * vb / 8), vs = (uint32_t)npad * (D / G) * 2;
+    return a16(kc) + 2 * a16(ks) + a16(vc) + 2 * a16(vs);
+}
+
+// Thread 0 issues the six bulk copies of tokens [j0, j0 + npad) of a tier.
+__device__ View stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
+                           uint8_t* buf, uint32_t bar) {
+    const int kb = t.k_bits, vb = t.v_bits;
+    uint32_t kc_b, ks_b;
+    const void *kc_src, *ks_src, *kz_src;
+    if (t.k_axis == KVQ_AXIS_CHANNEL) {
+        const int per = 32 / kb;
+        kc_b = (uint32_t)(npad / per) * D * 4;
+        kc_src = t.k_codes + (unit * (size_t)(t.cap / per) + j0 / per) * D;
+        ks_b = (uint32_t)(npad / G) * D * 2;
+        const size_t so = (unit * (size_t)(t.cap / G) + j0 / G) * D;
+        ks_src = t.k_scale + so;
+        kz_src = t.k_zero + so;
+    } else {
+        kc_b = (uint32_t)npad * (D * kb / 8);
+        kc_src = t.k_codes + (unit * (size_t)t.cap + j0) * (D * kb / 32);
+        ks_b = (uint32_t)npad * (D / G) * 2;
+        const size_t so = (unit * (size_t)t.cap + j0) * (D / G);
+        ks_src = t.k_scale + so;
+        kz_src = t.k_zero + so;
+    }
+    const uint32_t vc_b = (uint32_t)npad * (D * vb / 8), vs_b = (uint32_t)npad * (D / G) * 2;
+    const size_t vo = (unit * (size_t)t.cap + j0);
+    const uint32_t o_ks = a16(kc_b), o_kz = o_ks + a16(ks_b), o_vc = o_kz + a16(ks_b);
+    const uint32_t o_vs = o_vc + a16(vc_b), o_vz = o_vs + a16(vs_b);
+    if (threadIdx.x == 0) {
+        const uint32_t d = smem_u32(buf);
+        mbar_expect_tx(bar, kc_b + 2 * ks_b + vc_b + 2 * vs_b);
+        bulk_load(d, kc_src, kc_b, bar);
+        bulk_load(d + o_ks, ks_src, ks_b, bar);
+        bulk_load(d + o_kz, kz_src, ks_b, bar);
+        bulk_load(d + o_vc, t.v_codes + vo * (D * vb / 32), vc_b, bar);
+        bulk_load(d + o_vs, t.v_scale + vo * (D / G), vs_b, bar);
+        bulk_load(d + o_vz, t.v_zero + vo * (D / G), vs_b, bar);
+    }
+    View v;
+    v.kc = reinterpret_cast<const uint32_t*>(buf);
+    v.ks = reinterpret_cast<const uint16_t*>(buf + o_ks);
+    v.kz = reinterpret_cast<const uint16_t*>(buf + o_kz);
+    v.vc = reinterpret_cast<const uint32_t*>(buf + o_vc);
+    v.vs = reinterpret_cast<const uint16_t*>(buf + o_vs);
+    v.vz = reinterpret_cast<const uint16_t*>(buf + o_vz);
+    return v;
+}
+
+// Residual rows [j0, j0 + n) in logical order (oldest first, the new token
+// last) as [n][D] 16-bit rows: K at buf, V at buf + a16(n * D * 2).
+__device__ void stage_residual(const DecodeArgs& a, size_t unit, int len, int start, int j0, int n,
+                               int D, uint8_t* buf, uint32_t bar) {
+    if (threadIdx.x != 0) return;
+    const uint32_t row = (uint32_t)D * 2;
+    const uint32_t d = smem_u32(buf), dv = d + a16((uint32_t)n * row);
+    const int cap = a.res_cap;
+    mbar_expect_tx(bar, 2u * (uint32_t)n * row);
+    const int n_old = max(0, min(j0 + n, len) - j0);
+    const int first = (start + j0) % cap;
+    const int seg1 = min(n_old, cap - first), seg2 = n_old - seg1;
+    const uint16_t* rk = reinterpret_cast<const uint16_t*>(a.res_k) + unit * (size_t)cap * D;
+    const uint16_t* rv = reinterpret_cast<const uint16_t*>(a.res_v) + unit * (size_t)cap * D;
+    if (seg1 > 0) {
+        bulk_load(d, rk + (size_t)first * D, seg1 * row, bar);
+        bulk_load(dv, rv + (size_t)first * D, seg1 * row, bar);
+    }
+    if (seg2 > 0) {
+        bulk_load(d + seg1 * row, rk, seg2 * row, bar);
+        bulk_load(dv + seg1 * row, rv, seg2 * row, bar);
+    }
+    if (len >= j0 && len < j0 + n) {
+        const uint32_t r = (uint32_t)(len - j0) * row;
+        bulk_load(d + r, reinterpret_cast<const uint16_t*>(a.k_new) + unit * (size_t)D, row, bar);
+        bulk_load(dv + r, reinterpret_cast<const uint16_t*>(a.v_new) + unit * (size_t)D, row, bar);
+    }
+}
+
 // ---- key paths: each returns this lane's token logit for every head
 
 // Keys grouped per channel (packed along tokens): lane owns CPL channels;
 // partial dot products of 32 tokens, then a reduce-scatter across lanes.
 template <int KB, int CPL, int NG>
-__device__ __forceinline__ void logits_channel(const TierArgs& t, size_t unit, int tb, const Smem& sm,
-                                               int G, float (&lg)[NG]) {
+__device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem& sm, int G,
+                                               float (&lg)[NG]) {
     constexpr int D = CPL * 32;
     constexpr int per = 32 / KB;          // tokens per word
     constexpr int rows = 32 / per;        // word rows per 32-token group
     const int lane = threadIdx.x & 31;
     const int c0 = lane * CPL;
-    const size_t srow_i = (unit * (size_t)(t.cap / G) + tb / G) * D + c0;
     float s[CPL], z[CPL];
 #pragma unroll
     for (int ci = 0; ci < CPL; ++ci) {
-        s[ci] = h2f_bits(t.k_scale[srow_i + ci]);
-        z[ci] = h2f_bits(t.k_zero[srow_i + ci]);
+        s[ci] = h2f_bits(v.ks[(tl / G) * D + c0 + ci]);
+        z[ci] = h2f_bits(v.kz[(tl / G) * D + c0 + ci]);
     }
     uint32_t w[rows][CPL];
-    const uint32_t* base = t.k_codes + (unit * (size_t)(t.cap / per) + tb / per) * D + c0;
+    const uint32_t* base = v.kc + (size_t)(tl / per) * D + c0;
 #pragma unroll
     for (int r = 0; r < rows; ++r) {
         if (CPL == 4) {
-            const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * D));
+            const uint4 v4 = *reinterpret_cast<const uint4*>(base + (size_t)r * D);
             w[r][0] = v4.x; w[r][1] = v4.y; w[r][2] = v4.z; w[r][3] = v4.w;
         } else {
-            const uint2 v2 = __ldg(reinterpret_cast<const uint2*>(base + (size_t)r * D));
+            const uint2 v2 = *reinterpret_cast<const uint2*>(base + (size_t)r * D);
             w[r][0] = v2.x; w[r][CPL - 1] = v2.y;
         }
     }
@@ -223,8 +330,8 @@ __device__ __forceinline__ void logits_channel(const TierArgs& t, size_t unit, i
 // token row; dot over the word, scaled by the token's group scale, summed
 // over the lanes of the token.
 template <int KB, int D, int NG>
-__device__ __forceinline__ void logits_token(const TierArgs& t, size_t unit, int tb, int nt, Smem& sm,
-                                             int G, float (&lg)[NG]) {
+__device__ __forceinline__ void logits_token(const View& v, int tl, int nt, Smem& sm, int G,
+                                             float (&lg)[NG]) {
     constexpr int lpt = D * KB / 32;      // words (lanes) per token
     constexpr int tpp = 32 / lpt;         // tokens per pass
     constexpr int cpw = 32 / KB;          // channels per word
@@ -247,21 +354,17 @@ __device__ __forceinline__ void logits_token(const TierArgs& t, size_t unit, int
 #pragma unroll 4
     for (int ps = 0; ps < lpt; ++ps) {
         const int tk = ps * tpp + to;
+        const int row = tl + tk;
+        const uint32_t w = v.kc[(size_t)row * lpt + wi];
+        const float sc = h2f_bits(v.ks[row * (D / G) + grp]);
+        const float zc = h2f_bits(v.kz[row * (D / G) + grp]);
         float c[NG];
 #pragma unroll
-        for (int h = 0; h < NG; ++h) c[h] = 0.0f;
-        if (tk < nt) {
-            const size_t row = unit * (size_t)t.cap + tb + tk;
-            const uint32_t w = __ldg(t.k_codes + row * lpt + wi);
-            const float sc = h2f_bits(__ldg(t.k_scale + row * (D / G) + grp));
-            const float zc = h2f_bits(__ldg(t.k_zero + row * (D / G) + grp));
+        for (int h = 0; h < NG; ++h) {
+            float d = 0.0f;
 #pragma unroll
-            for (int h = 0; h < NG; ++h) {
-                float d = 0.0f;
-#pragma unroll
-                for (int i = 0; i < cpw; ++i) d = fmaf(code_f<KB>(w, i), q4[h][i], d);
-                c[h] = fmaf(sc, d - off[h], zc * qsum[h]);
-            }
+            for (int i = 0; i < cpw; ++i) d = fmaf(code_f<KB>(w, i), q4[h][i], d);
+            c[h] = fmaf(sc, d - off[h], zc * qsum[h]);
         }
 #pragma unroll
         for (int h = 0; h < NG; ++h) {
@@ -274,30 +377,30 @@ __device__ __forceinline__ void logits_token(const TierArgs& t, size_t unit, int
 #pragma unroll
     for (int h = 0; h < NG; ++h) lg[h] = sm.lg[warp][h][lane];
     __syncwarp();
+    (void)nt;
 }
 
 // ---- value paths
 
 // Values grouped per token: lane owns word wi of the tokens to, to + tpp, ...
 template <int VB, int D, int NG>
-__device__ __forceinline__ void values_token(const TierArgs& t, size_t unit, int tb, int nt,
-                                             const float (&p)[NG], int G,
-                                             WarpAcc<NG, 32 / VB>& acc) {
+__device__ __forceinline__ void values_token(const View& v, int tl, int nt, const float (&p)[NG],
+                                             int G, WarpAcc<NG, 32 / VB>& acc) {
     constexpr int lpt = D * VB / 32, tpp = 32 / lpt, cpw = 32 / VB;
     const int lane = threadIdx.x & 31;
     const int wi = lane % lpt, to = lane / lpt;
     const int grp = (wi * cpw) / G;
-#pragma unroll 2
+#pragma unroll 4
     for (int ps = 0; ps < lpt; ++ps) {
         const int tk = ps * tpp + to;
         float pk[NG];
 #pragma unroll
         for (int h = 0; h < NG; ++h) pk[h] = __shfl_sync(0xffffffffu, p[h], tk);
         if (tk < nt) {
-            const size_t row = unit * (size_t)t.cap + tb + tk;
-            const uint32_t w = __ldg(t.v_codes + row * lpt + wi);
-            const float sc = h2f_bits(__ldg(t.v_scale + row * (D / G) + grp));
-            const float zc = h2f_bits(__ldg(t.v_zero + row * (D / G) + grp));
+            const int row = tl + tk;
+            const uint32_t w = v.vc[(size_t)row * lpt + wi];
+            const float sc = h2f_bits(v.vs[row * (D / G) + grp]);
+            const float zc = h2f_bits(v.vz[row * (D / G) + grp]);
 #pragma unroll
             for (int h = 0; h < NG; ++h) {
                 const float ps4 = pk[h] * sc * (float)(1 << VB);
@@ -321,51 +424,43 @@ __device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, S
     for (int h = 0; h < NG; ++h)
 #pragma unroll
         for (int i = 0; i < cpw; ++i) {
-            float v = acc.o[h][i] - acc.off[h] + acc.zs[h];
+            float x = acc.o[h][i] - acc.off[h] + acc.zs[h];
 #pragma unroll
-            for (int o = lpt; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (to == 0) sm.wo[warp][h][wi * cpw + i] = v;
+            for (int o = lpt; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (to == 0) sm.wo[warp][h][wi * cpw + i] = x;
         }
 }
 
-// ---- residual (full precision ring + the new token)
+// ---- residual (full precision ring + the new token), staged as [n][D] rows
 
 template <int CPL>
-__device__ __forceinline__ void load_row(const void* base, size_t elem, bool bf, float (&x)[CPL]) {
+__device__ __forceinline__ void row_vals(const uint16_t* row, bool bf, float (&x)[CPL]) {
     if (CPL == 4) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + elem));
+        const uint2 u = *reinterpret_cast<const uint2*>(row);
         const uint32_t e[2] = {u.x, u.y};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            if (bf) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&e[k]));
-                x[2 * k] = f.x; x[2 * k + 1] = f.y;
-            } else {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&e[k]));
-                x[2 * k] = f.x; x[2 * k + 1] = f.y;
-            }
+            const float2 f = bf ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&e[k]))
+                                : __half22float2(*reinterpret_cast<const __half2*>(&e[k]));
+            x[2 * k] = f.x;
+            x[2 * k + 1] = f.y;
         }
     } else {
-        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(base) + elem));
-        if (bf) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-            x[0] = f.x; x[CPL - 1] = f.y;
-        } else {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
-            x[0] = f.x; x[CPL - 1] = f.y;
-        }
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(row);
+        const float2 f = bf ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u))
+                            : __half22float2(*reinterpret_cast<const __half2*>(&u));
+        x[0] = f.x;
+        x[CPL - 1] = f.y;
     }
 }
 
 template <int CPL, int NG>
-__device__ void warp_residual(const DecodeArgs& a, Smem& sm, size_t unit, int len, int start,
-                              int j0, int n, float* lg_out) {
+__device__ void warp_residual(const DecodeArgs& a, Smem& sm, const uint16_t* rk, const uint16_t* rv,
+                              int n, float* lg_out) {
     constexpr int D = CPL * 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c0 = lane * CPL;
     const bool bf = a.bf16 != 0;
-    const int cap = a.res_cap;
-    const size_t rbase = unit * (size_t)cap;
     WarpAcc<NG, CPL> acc;
 #pragma unroll
     for (int h = 0; h < NG; ++h) {
@@ -377,12 +472,8 @@ __device__ void warp_residual(const DecodeArgs& a, Smem& sm, size_t unit, int le
         for (int i = 0; i < CPL; ++i) acc.o[h][i] = 0.0f;
     }
     for (int gi = warp; gi * 32 < n; gi += kWarps) {
-        const int tb = j0 + gi * 32;
-        const int nt = min(32, n - gi * 32);
-        auto elem_of = [&](int k, bool kk) -> size_t {
-            const int li = tb + k;
-            return li < len ? (rbase + (start + li) % cap) * D + c0 : unit * (size_t)D + c0;
-        };
+        const int tl = gi * 32;
+        const int nt = min(32, n - tl);
         float lg[NG];
 #pragma unroll
         for (int h = 0; h < NG; ++h) {
@@ -392,22 +483,25 @@ __device__ void warp_residual(const DecodeArgs& a, Smem& sm, size_t unit, int le
                 part[k] = 0.0f;
                 if (k < nt) {
                     float x[CPL];
-                    load_row<CPL>(tb + k < len ? a.res_k : a.k_new, elem_of(k, true), bf, x);
+                    row_vals<CPL>(rk + (size_t)(tl + k) * D + c0, bf, x);
 #pragma unroll
                     for (int ci = 0; ci < CPL; ++ci) part[k] = fmaf(sm.q[h][c0 + ci], x[ci], part[k]);
                 }
             }
             lg[h] = reduce_scatter32(part);
         }
-        group_softmax(acc, lg, nt, lg_out ? lg_out + (tb - j0) : nullptr, a.slots);
-        for (int k = 0; k < nt; ++k) {
-            float x[CPL];
-            load_row<CPL>(tb + k < len ? a.res_v : a.v_new, elem_of(k, false), bf, x);
+        group_softmax(acc, lg, nt, lg_out ? lg_out + tl : nullptr, a.slots);
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            if (k < nt) {
+                float x[CPL];
+                row_vals<CPL>(rv + (size_t)(tl + k) * D + c0, bf, x);
 #pragma unroll
-            for (int h = 0; h < NG; ++h) {
-                const float pk = __shfl_sync(0xffffffffu, lg[h], k);
+                for (int h = 0; h < NG; ++h) {
+                    const float pk = __shfl_sync(0xffffffffu, lg[h], k);
 #pragma unroll
-                for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] = fmaf(pk, x[ci], acc.o[h][ci]);
+                    for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] = fmaf(pk, x[ci], acc.o[h][ci]);
+                }
             }
         }
     }
@@ -423,8 +517,7 @@ __device__ void warp_residual(const DecodeArgs& a, Smem& sm, size_t unit, int le
 }
 
 template <int KB, int KAX, int VB, int D, int NG>
-__device__ void warp_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, size_t unit, int j0,
-                          int n, float* lg_out) {
+__device__ void warp_tier(const DecodeArgs& a, Smem& sm, const View& v, int n, float* lg_out) {
     constexpr int cpw = 32 / VB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpAcc<NG, cpw> acc;
@@ -438,15 +531,15 @@ __device__ void warp_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, size
         for (int i = 0; i < cpw; ++i) acc.o[h][i] = 0.0f;
     }
     for (int gi = warp; gi * 32 < n; gi += kWarps) {
-        const int tb = j0 + gi * 32;
-        const int nt = min(32, n - gi * 32);
+        const int tl = gi * 32;
+        const int nt = min(32, n - tl);
         float lg[NG];
         if (KAX == KVQ_AXIS_CHANNEL)
-            logits_channel<KB, D / 32, NG>(t, unit, tb, sm, a.G, lg);
+            logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
         else
-            logits_token<KB, D, NG>(t, unit, tb, nt, sm, a.G, lg);
-        group_softmax(acc, lg, nt, lg_out ? lg_out + (tb - j0) : nullptr, a.slots);
-        values_token<VB, D, NG>(t, unit, tb, nt, lg, a.G, acc);
+            logits_token<KB, D, NG>(v, tl, nt, sm, a.G, lg);
+        group_softmax(acc, lg, nt, lg_out ? lg_out + tl : nullptr, a.slots);
+        values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
     }
     if (lane == 0) {
 #pragma unroll
@@ -484,15 +577,15 @@ __device__ void cta_partial(const DecodeArgs& a, Smem& sm, float* part_out) {
 }
 
 template <int NG, int D>
-__device__ bool dispatch_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, size_t unit, int j0,
-                              int n, float* lg_out) {
+__device__ bool dispatch_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, const View& v, int n,
+                              float* lg_out) {
     const int kb = t.k_bits, vb = t.v_bits, ax = t.k_axis;
-    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
+    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, v, n, lg_out); return true; }
     if (D == 128) {
-        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { warp_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { warp_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { warp_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { warp_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, v, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { warp_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, v, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { warp_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, v, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, v, n, lg_out); return true; }
     }
     return false;
 }
@@ -527,25 +620,44 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         if (chunk < a.tier[t].chunks) { tier = t; break; }
         chunk -= a.tier[t].chunks;
     }
-    const int j0 = chunk * kChunk;
+    uint8_t* stage = smem_raw + ((sizeof(Smem) + 127) & ~(size_t)127);
+    const uint32_t bar = smem_u32(&sm.bar);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
     if (tier >= 0) {
         const TierArgs& t = a.tier[tier];
+        const int j0 = chunk * kChunk;
         if (t.count[unit] > t.cap && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
         const int cnt = min(t.count[unit], t.cap);
         const int n = min(kChunk, cnt - j0);
         if (n > 0) {
+            const View v = stage_tier(t, unit, j0, (n + 31) & ~31, D, a.G, stage, bar);
             float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
-            if (!dispatch_tier<NG, D>(a, sm, t, unit, j0, n, lg) && threadIdx.x == 0)
+            if (!__syncthreads_and(mbar_wait(bar, 0, nullptr))) {
+                if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
+            } else if (!dispatch_tier<NG, D>(a, sm, t, v, n, lg) && threadIdx.x == 0) {
                 atomicOr(&g_status_decode, kDevCheck);
+            }
         }
     } else {
         const int cap = a.res_cap;
         const int len = min(max(a.res_len[unit], 0), cap - 1), start = a.res_start[unit];
         if (a.res_len[unit] != len && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
-        const int n = min(kChunk, len + 1 - j0);
+        const int j0 = chunk * kResChunk;
+        const int n = min(kResChunk, len + 1 - j0);
         if (n > 0) {
+            stage_residual(a, unit, len, start, j0, n, D, stage, bar);
+            const uint16_t* rk = reinterpret_cast<const uint16_t*>(stage);
+            const uint16_t* rv = reinterpret_cast<const uint16_t*>(stage + a16((uint32_t)n * D * 2));
             float* lg = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 : nullptr;
-            warp_residual<D / 32, NG>(a, sm, unit, len, start, j0, n, lg);
+            if (!__syncthreads_and(mbar_wait(bar, 0, nullptr))) {
+                if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
+            } else {
+                warp_residual<D / 32, NG>(a, sm, rk, rv, n, lg);
+            }
         }
         if (chunk == 0) {
             // the new token joins the ring; no CTA reads this slot in this step
@@ -664,7 +776,7 @@ WsLayout ws_layout(const kvq_cache& c) {
         chunks += (c.tier[t].cap + kChunk - 1) / kChunk;
         slots += c.tier[t].cap;
     }
-    chunks += (c.res_cap + kChunk - 1) / kChunk;
+    chunks += (c.res_cap + kResChunk - 1) / kResChunk;
     slots += c.res_cap;
     w.total_chunks = chunks;
     w.slots = slots;
@@ -726,7 +838,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.res_start = c.res_start;
     a.res_len = c.res_len;
     a.res_cap = c.res_cap;
-    a.res_chunks = (c.res_cap + kChunk - 1) / kChunk;
+    a.res_chunks = (c.res_cap + kResChunk - 1) / kResChunk;
     a.res_slot_base = slot;
     a.seq_len = c.seq_len;
     a.win_acc = c.win_acc;
@@ -742,9 +854,19 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(units + 1) * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     dim3 grid(w.total_chunks, units);
-    const size_t sh = sizeof(Smem);
-#define KVQ_DECODE_CASE(NG_, D_) \
-    if (a.g == NG_ && c.D == D_) { decode_kernel<NG_, D_><<<grid, kThreads, sh, s>>>(a); return cudaGetLastError(); }
+    uint32_t stage = 2u * a16((uint32_t)kResChunk * c.D * 2);
+    for (int t = 0; t < c.n_tiers; ++t)
+        stage = std::max(stage, tier_stage_bytes(c.tier[t].k_axis, c.tier[t].k_bits, c.tier[t].v_bits,
+                                                 kChunk, c.D, c.G));
+    const size_t sh = ((sizeof(Smem) + 127) & ~(size_t)127) + stage;
+#define KVQ_DECODE_CASE(NG_, D_)                                                              \
+    if (a.g == NG_ && c.D == D_) {                                                            \
+        if (sh > 48 * 1024)                                                                   \
+            cudaFuncSetAttribute(decode_kernel<NG_, D_>,                                       \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh);       \
+        decode_kernel<NG_, D_><<<grid, kThreads, sh, s>>>(a);                                 \
+        return cudaGetLastError();                                                            \
+    }
     KVQ_DECODE_CASE(1, 128)
     KVQ_DECODE_CASE(1, 64)
     KVQ_DECODE_CASE(2, 128)

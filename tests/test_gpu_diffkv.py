@@ -70,7 +70,8 @@ def test_diffkv_decisions_bit_exact():
             assert_attn_close(od[b, h * g:(h + 1) * g], ro, f"step {t} unit {u}")
             tc = units[u].win[0][0]
             th = float(units[u].alpha_h) / N
-            vals = (r.random(g) * 2.2 * th * (N - tc)).astype(np.float32)
+            level = r.random() * 1.3 * th * (N - tc)     # spans prune / low / high
+            vals = (level * (0.5 + 0.5 * r.random(g))).astype(np.float32)
             units[u].win[0][3][:] = vals
             cache.win_acc[b * Hq + h * g:b * Hq + (h + 1) * g, start[u]] = torch.from_numpy(vals).cuda()
         kvq.requant_demote(cache, t + 1)
