@@ -861,9 +861,12 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     const size_t sh = ((sizeof(Smem) + 127) & ~(size_t)127) + stage;
 #define KVQ_DECODE_CASE(NG_, D_)                                                              \
     if (a.g == NG_ && c.D == D_) {                                                            \
-        if (sh > 48 * 1024)                                                                   \
+        static size_t attr_##NG_##_##D_ = 0;                                                  \
+        if (sh > 48 * 1024 && sh > attr_##NG_##_##D_) {                                       \
             cudaFuncSetAttribute(decode_kernel<NG_, D_>,                                       \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh);       \
+            attr_##NG_##_##D_ = sh;                                                           \
+        }                                                                                     \
         decode_kernel<NG_, D_><<<grid, kThreads, sh, s>>>(a);                                 \
         return cudaGetLastError();                                                            \
     }

@@ -293,6 +293,7 @@ class Cache:
 
 
 def _alloc_tier(units, D, G, spec, device):
+    spec = TierSpec(spec.k_bits, spec.v_bits, spec.k_axis, (spec.cap + 31) // 32 * 32)
     cap = spec.cap
     i32, i16 = torch.int32, torch.int16
     if spec.k_axis == AXIS_CHANNEL:
