@@ -4,15 +4,18 @@
 // forward_implications: fused dequantisation kernels during decoding).
 //
 // One launch per step.  Grid = (token chunks of every tier and of the
-// residual ring, units).  Each CTA computes, for the g query heads that
-// share its KV head, the base-2 logits of its chunk, the chunk max / sum
-// and the unnormalised P.V partial, and writes them to the workspace.  The
-// last CTA of a unit (atomic counter) merges the partials, writes o and
-// lse, adds this step's attention to the policy scores (DiffKV: per ring
-// slot and query head; MiKV: per token, summed over the group) and
-// advances the residual length; the last CTA of the grid advances seq_len.
-// The tiers are read where they lie (MiKV rebuttal: attention is
-// permutation invariant, so each precision group sits in its own region).
+// residual ring, units).  A CTA first requests every byte of its chunk with
+// bulk asynchronous copies into shared memory (one mbarrier), then its
+// four warps take 32-token groups: keys -> base-2 logits for the g query
+// heads of the KV head, online softmax per warp, P.V with the codes turned
+// into floats by one rotate and one LOP3 each.  The CTA writes its partial
+// (max, sum, unnormalised output); the last CTA of a unit (atomic counter)
+// merges the partials, writes o and lse, adds this step's attention to the
+// policy scores (DiffKV: per ring slot and query head; MiKV: per token,
+// summed over the group) and advances the residual length; the last CTA of
+// the grid advances seq_len.  Tiers are read where they lie (MiKV rebuttal:
+// attention is permutation invariant, so each precision group sits in its
+// own region).
 #include <algorithm>
 
 #include "kvq_common.cuh"
@@ -27,8 +30,8 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunk = 256;     // tokens per CTA: each warp takes 32-token groups in turn
-constexpr int kMaxG = 8;        // query heads per KV head
+constexpr int kChunk = 256;      // packed tokens per CTA: each warp takes 32-token groups in turn
+constexpr int kResChunk = 64;    // residual tokens per CTA (full-precision rows are large)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -87,8 +90,8 @@ __device__ __forceinline__ void stf(void* p, size_t i, float v, bool bf16) {
 
 // Code i (KB bits) of a packed word as the float 1 + c * 2^-KB: one rotate
 // moves the code to the top of the mantissa, one LOP3 masks it and sets the
-// exponent of 1.0.  fma(x, y * 2^KB, acc) then adds y * 2^KB + c * y; the
-// constant y * 2^KB is removed once per dot product.
+// exponent of 1.0.  fma(x, y, acc) adds y + c * y * 2^-KB; the constant y
+// is removed once per dot product and the result scaled by 2^KB.
 template <int KB>
 __device__ __forceinline__ float code_f(uint32_t w, int i) {
     const int rot = ((23 - KB - KB * i) % 32 + 32) % 32;
@@ -97,7 +100,7 @@ __device__ __forceinline__ float code_f(uint32_t w, int i) {
     return __uint_as_float((x & mask) | 0x3F800000u);
 }
 
-// 32 lanes each hold v[0..31]; afterwards v[0] of lane t = sum over lanes of v[t].
+// 32 lanes each hold v[0..31]; afterwards lane t returns the sum over lanes of v[t].
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -124,14 +127,15 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
+template <int NG, int D>
 struct Smem {
-    float q[kMaxG][128];                 // query rows, pre-scaled to base-2 logits
-    float wm[kWarps][kMaxG];
-    float wl[kWarps][kMaxG];
-    float wo[kWarps][kMaxG][128];
-    float lg[kWarps][kMaxG][32];         // logits of the warp's current group
+    float q[NG][D];                      // query rows, pre-scaled to base-2 logits
+    float wm[kWarps][NG];
+    float wl[kWarps][NG];
+    float wo[kWarps][NG][D];
+    float lg[kWarps][NG][32];            // logits of the warp's current group
     unsigned long long bar;              // staging mbarrier
-    int last;
+    int count, len, start, last;
 };
 
 // Online-softmax state of one warp for NG heads; o holds the lane's share.
@@ -139,11 +143,24 @@ template <int NG, int NO>
 struct WarpAcc {
     float m[NG], l[NG];
     float o[NG][NO];
-    float off[NG], zs[NG];               // packed V: sum p*s*2^VB and sum p*z over this lane
+    float off[NG], zs[NG];               // packed V: sum p*s and sum p*z over this lane's tokens
 };
 
+template <int NG, int NO>
+__device__ __forceinline__ void acc_init(WarpAcc<NG, NO>& acc) {
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        acc.m[h] = kNegInf;
+        acc.l[h] = 0.0f;
+        acc.off[h] = 0.0f;
+        acc.zs[h] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NO; ++i) acc.o[h][i] = 0.0f;
+    }
+}
+
 // Logits of the group (lane t holds token t, -inf past nt) -> rescale the
-// accumulators, return p_h(t) in lg and write logits out when asked.
+// accumulators, return p_h(t) in lg and write the logits out when asked.
 template <int NG, int NO>
 __device__ __forceinline__ void group_softmax(WarpAcc<NG, NO>& acc, float (&lg)[NG], int nt,
                                               float* lg_out, int slots) {
@@ -152,8 +169,7 @@ __device__ __forceinline__ void group_softmax(WarpAcc<NG, NO>& acc, float (&lg)[
     for (int h = 0; h < NG; ++h) {
         const float s = lane < nt ? lg[h] : kNegInf;
         if (lg_out && lane < nt) lg_out[(size_t)h * slots + lane] = s;
-        const float mg = warp_max(s);
-        const float mn = fmaxf(acc.m[h], mg);
+        const float mn = fmaxf(acc.m[h], warp_max(s));
         const float corr = acc.m[h] == kNegInf ? 0.0f : ex2_approx(acc.m[h] - mn);
         const float p = lane < nt ? ex2_approx(s - mn) : 0.0f;
         acc.l[h] = acc.l[h] * corr + warp_sum(p);
@@ -168,8 +184,6 @@ __device__ __forceinline__ void group_softmax(WarpAcc<NG, NO>& acc, float (&lg)[
 
 // ---- shared-memory staging: every byte a CTA needs is requested at once
 
-constexpr int kResChunk = 64;    // residual tokens per CTA (full-precision rows are large)
-
 // One chunk of packed tokens in shared memory, indexed from the chunk start.
 struct View {
     const uint32_t* kc;   // CHANNEL keys: [n/per][D]; TOKEN keys: [n][D*KB/32]
@@ -182,56 +196,30 @@ struct View {
 
 __host__ __device__ __forceinline__ uint32_t a16(uint32_t x) { return (x + 15u) & ~15u; }
 
-// Bytes of one staged tier chunk of npad tokens.
-__host__ __device__ inline uint32_t tier_stage_bytes(int k_axis, int kb, int vb, int npad, int D, int G) {
-    uint32_t kc, ks;
+// Byte sizes of the six arrays of a staged tier chunk of npad tokens.
+struct StageSizes {
+    uint32_t kc, ks, vc, vs;
+    __host__ __device__ uint32_t total() const { return a16(kc) + 2 * a16(ks) + a16(vc) + 2 * a16(vs); }
+};
+
+__host__ __device__ inline StageSizes tier_stage_sizes(int k_axis, int kb, int vb, int npad, int D, int G) {
+    StageSizes z;
     if (k_axis == KVQ_AXIS_CHANNEL) {
-        kc = (uint32_t)(npad / (32 / kb)) * D * 4;
-        ks = (uint32_t)(npad / G) * D * 2;
+        z.kc = (uint32_t)(npad / (32 / kb)) * D * 4;
+        z.ks = (uint32_t)(npad / G) * D * 2;
     } else {
-        kc = (uint32_t)npad * (D * kb / 8);
-        ks = (uint32_t)npad * (D / G) * 2;
+        z.kc = (uint32_t)npad * (D * kb / 8);
+        z.ks = (uint32_t)npad * (D / G) * 2;
     }
-    const uint32_t vc = (uint32_t)npad * (D * vb / 8), vs = (uint32_t)npad * (D / G) * 2;
-    return a16(kc) + 2 * a16(ks) + a16(vc) + 2 * a16(vs);
+    z.vc = (uint32_t)npad * (D * vb / 8);
+    z.vs = (uint32_t)npad * (D / G) * 2;
+    return z;
 }
 
-// Thread 0 issues the six bulk copies of tokens [j0, j0 + npad) of a tier.
-__device__ View stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
-                           uint8_t* buf, uint32_t bar) {
-    const int kb = t.k_bits, vb = t.v_bits;
-    uint32_t kc_b, ks_b;
-    const void *kc_src, *ks_src, *kz_src;
-    if (t.k_axis == KVQ_AXIS_CHANNEL) {
-        const int per = 32 / kb;
-        kc_b = (uint32_t)(npad / per) * D * 4;
-        kc_src = t.k_codes + (unit * (size_t)(t.cap / per) + j0 / per) * D;
-        ks_b = (uint32_t)(npad / G) * D * 2;
-        const size_t so = (unit * (size_t)(t.cap / G) + j0 / G) * D;
-        ks_src = t.k_scale + so;
-        kz_src = t.k_zero + so;
-    } else {
-        kc_b = (uint32_t)npad * (D * kb / 8);
-        kc_src = t.k_codes + (unit * (size_t)t.cap + j0) * (D * kb / 32);
-        ks_b = (uint32_t)npad * (D / G) * 2;
-        const size_t so = (unit * (size_t)t.cap + j0) * (D / G);
-        ks_src = t.k_scale + so;
-        kz_src = t.k_zero + so;
-    }
-    const uint32_t vc_b = (uint32_t)npad * (D * vb / 8), vs_b = (uint32_t)npad * (D / G) * 2;
-    const size_t vo = (unit * (size_t)t.cap + j0);
-    const uint32_t o_ks = a16(kc_b), o_kz = o_ks + a16(ks_b), o_vc = o_kz + a16(ks_b);
-    const uint32_t o_vs = o_vc + a16(vc_b), o_vz = o_vs + a16(vs_b);
-    if (threadIdx.x == 0) {
-        const uint32_t d = smem_u32(buf);
-        mbar_expect_tx(bar, kc_b + 2 * ks_b + vc_b + 2 * vs_b);
-        bulk_load(d, kc_src, kc_b, bar);
-        bulk_load(d + o_ks, ks_src, ks_b, bar);
-        bulk_load(d + o_kz, kz_src, ks_b, bar);
-        bulk_load(d + o_vc, t.v_codes + vo * (D * vb / 32), vc_b, bar);
-        bulk_load(d + o_vs, t.v_scale + vo * (D / G), vs_b, bar);
-        bulk_load(d + o_vz, t.v_zero + vo * (D / G), vs_b, bar);
-    }
+__device__ __forceinline__ View tier_view(const TierArgs& t, int npad, int D, int G, const uint8_t* buf) {
+    const StageSizes z = tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G);
+    const uint32_t o_ks = a16(z.kc), o_kz = o_ks + a16(z.ks), o_vc = o_kz + a16(z.ks);
+    const uint32_t o_vs = o_vc + a16(z.vc), o_vz = o_vs + a16(z.vs);
     View v;
     v.kc = reinterpret_cast<const uint32_t*>(buf);
     v.ks = reinterpret_cast<const uint16_t*>(buf + o_ks);
@@ -242,11 +230,41 @@ __device__ View stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int
     return v;
 }
 
-// Residual rows [j0, j0 + n) in logical order (oldest first, the new token
-// last) as [n][D] 16-bit rows: K at buf, V at buf + a16(n * D * 2).
+// Called by one thread: the six bulk copies of tokens [j0, j0 + npad) of a tier.
+__device__ void stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
+                           const uint8_t* buf, uint32_t bar) {
+    const StageSizes z = tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G);
+    const void *kc_src, *ks_src, *kz_src;
+    if (t.k_axis == KVQ_AXIS_CHANNEL) {
+        const int per = 32 / t.k_bits;
+        kc_src = t.k_codes + (unit * (size_t)(t.cap / per) + j0 / per) * D;
+        const size_t so = (unit * (size_t)(t.cap / G) + j0 / G) * D;
+        ks_src = t.k_scale + so;
+        kz_src = t.k_zero + so;
+    } else {
+        kc_src = t.k_codes + (unit * (size_t)t.cap + j0) * (D * t.k_bits / 32);
+        const size_t so = (unit * (size_t)t.cap + j0) * (D / G);
+        ks_src = t.k_scale + so;
+        kz_src = t.k_zero + so;
+    }
+    const size_t vo = unit * (size_t)t.cap + j0;
+    const uint32_t o_ks = a16(z.kc), o_kz = o_ks + a16(z.ks), o_vc = o_kz + a16(z.ks);
+    const uint32_t o_vs = o_vc + a16(z.vc), o_vz = o_vs + a16(z.vs);
+    const uint32_t d = smem_u32(buf);
+    mbar_expect_tx(bar, z.kc + 2 * z.ks + z.vc + 2 * z.vs);
+    bulk_load(d, kc_src, z.kc, bar);
+    bulk_load(d + o_ks, ks_src, z.ks, bar);
+    bulk_load(d + o_kz, kz_src, z.ks, bar);
+    bulk_load(d + o_vc, t.v_codes + vo * (D * t.v_bits / 32), z.vc, bar);
+    bulk_load(d + o_vs, t.v_scale + vo * (D / G), z.vs, bar);
+    bulk_load(d + o_vz, t.v_zero + vo * (D / G), z.vs, bar);
+}
+
+// Called by one thread: residual rows [j0, j0 + n) in logical order (oldest
+// first, the new token last) as [n][D] 16-bit rows, K at buf, V at
+// buf + a16(n * D * 2).
 __device__ void stage_residual(const DecodeArgs& a, size_t unit, int len, int start, int j0, int n,
-                               int D, uint8_t* buf, uint32_t bar) {
-    if (threadIdx.x != 0) return;
+                               int D, const uint8_t* buf, uint32_t bar) {
     const uint32_t row = (uint32_t)D * 2;
     const uint32_t d = smem_u32(buf), dv = d + a16((uint32_t)n * row);
     const int cap = a.res_cap;
@@ -271,13 +289,13 @@ __device__ void stage_residual(const DecodeArgs& a, size_t unit, int len, int st
     }
 }
 
-// ---- key paths: each returns this lane's token logit for every head
+// ---- key paths: each leaves this lane's token logit (base 2) for every head
 
 // Keys grouped per channel (packed along tokens): lane owns CPL channels;
 // partial dot products of 32 tokens, then a reduce-scatter across lanes.
 template <int KB, int CPL, int NG>
-__device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem& sm, int G,
-                                               float (&lg)[NG]) {
+__device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem<NG, CPL * 32>& sm,
+                                               int G, float (&lg)[NG]) {
     constexpr int D = CPL * 32;
     constexpr int per = 32 / KB;          // tokens per word
     constexpr int rows = 32 / per;        // word rows per 32-token group
@@ -301,13 +319,13 @@ __device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem
             w[r][0] = v2.x; w[r][CPL - 1] = v2.y;
         }
     }
-#pragma unroll
+#pragma unroll 1
     for (int h = 0; h < NG; ++h) {
         float qs[CPL], off = 0.0f, bias = 0.0f;
 #pragma unroll
         for (int ci = 0; ci < CPL; ++ci) {
             const float qv = sm.q[h][c0 + ci];
-            qs[ci] = qv * s[ci] * (float)(1 << KB);
+            qs[ci] = qv * s[ci];
             off += qs[ci];
             bias = fmaf(qv, z[ci], bias);
         }
@@ -322,7 +340,7 @@ __device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem
                 for (int i = 0; i < per; ++i)
                     part[r * per + i] = fmaf(code_f<KB>(w[r][ci], i), qs[ci], part[r * per + i]);
         const float raw = reduce_scatter32(part);
-        lg[h] = raw + warp_sum(bias - off);
+        lg[h] = (raw - warp_sum(off)) * (float)(1 << KB) + warp_sum(bias);
     }
 }
 
@@ -330,7 +348,7 @@ __device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem
 // token row; dot over the word, scaled by the token's group scale, summed
 // over the lanes of the token.
 template <int KB, int D, int NG>
-__device__ __forceinline__ void logits_token(const View& v, int tl, int nt, Smem& sm, int G,
+__device__ __forceinline__ void logits_token(const View& v, int tl, Smem<NG, D>& sm, int G,
                                              float (&lg)[NG]) {
     constexpr int lpt = D * KB / 32;      // words (lanes) per token
     constexpr int tpp = 32 / lpt;         // tokens per pass
@@ -338,18 +356,12 @@ __device__ __forceinline__ void logits_token(const View& v, int tl, int nt, Smem
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wi = lane % lpt, to = lane / lpt;
     const int c0 = wi * cpw, grp = c0 / G;
-    float q4[NG][cpw], off[NG], qsum[NG];
+    float qsum[NG];
 #pragma unroll
     for (int h = 0; h < NG; ++h) {
-        off[h] = 0.0f;
         qsum[h] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < cpw; ++i) {
-            const float qv = sm.q[h][c0 + i];
-            q4[h][i] = qv * (float)(1 << KB);
-            off[h] += q4[h][i];
-            qsum[h] += qv;
-        }
+        for (int i = 0; i < cpw; ++i) qsum[h] += sm.q[h][c0 + i];
     }
 #pragma unroll 4
     for (int ps = 0; ps < lpt; ++ps) {
@@ -363,8 +375,8 @@ __device__ __forceinline__ void logits_token(const View& v, int tl, int nt, Smem
         for (int h = 0; h < NG; ++h) {
             float d = 0.0f;
 #pragma unroll
-            for (int i = 0; i < cpw; ++i) d = fmaf(code_f<KB>(w, i), q4[h][i], d);
-            c[h] = fmaf(sc, d - off[h], zc * qsum[h]);
+            for (int i = 0; i < cpw; ++i) d = fmaf(code_f<KB>(w, i), sm.q[h][c0 + i], d);
+            c[h] = fmaf(sc * (float)(1 << KB), d - qsum[h], zc * qsum[h]);
         }
 #pragma unroll
         for (int h = 0; h < NG; ++h) {
@@ -377,7 +389,6 @@ __device__ __forceinline__ void logits_token(const View& v, int tl, int nt, Smem
 #pragma unroll
     for (int h = 0; h < NG; ++h) lg[h] = sm.lg[warp][h][lane];
     __syncwarp();
-    (void)nt;
 }
 
 // ---- value paths
@@ -403,11 +414,11 @@ __device__ __forceinline__ void values_token(const View& v, int tl, int nt, cons
             const float zc = h2f_bits(v.vz[row * (D / G) + grp]);
 #pragma unroll
             for (int h = 0; h < NG; ++h) {
-                const float ps4 = pk[h] * sc * (float)(1 << VB);
-                acc.off[h] += ps4;
+                const float psc = pk[h] * sc;
+                acc.off[h] += psc;
                 acc.zs[h] = fmaf(pk[h], zc, acc.zs[h]);
 #pragma unroll
-                for (int i = 0; i < cpw; ++i) acc.o[h][i] = fmaf(code_f<VB>(w, i), ps4, acc.o[h][i]);
+                for (int i = 0; i < cpw; ++i) acc.o[h][i] = fmaf(code_f<VB>(w, i), psc, acc.o[h][i]);
             }
         }
     }
@@ -416,7 +427,7 @@ __device__ __forceinline__ void values_token(const View& v, int tl, int nt, cons
 // Finish a packed-V warp: remove the constants, sum the lanes that share a
 // word, publish to smem.
 template <int VB, int D, int NG>
-__device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, Smem& sm) {
+__device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, Smem<NG, D>& sm) {
     constexpr int lpt = D * VB / 32, cpw = 32 / VB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wi = lane % lpt, to = lane / lpt;
@@ -424,7 +435,7 @@ __device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, S
     for (int h = 0; h < NG; ++h)
 #pragma unroll
         for (int i = 0; i < cpw; ++i) {
-            float x = acc.o[h][i] - acc.off[h] + acc.zs[h];
+            float x = (acc.o[h][i] - acc.off[h]) * (float)(1 << VB) + acc.zs[h];
 #pragma unroll
             for (int o = lpt; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
             if (to == 0) sm.wo[warp][h][wi * cpw + i] = x;
@@ -454,28 +465,20 @@ __device__ __forceinline__ void row_vals(const uint16_t* row, bool bf, float (&x
     }
 }
 
-template <int CPL, int NG>
-__device__ void warp_residual(const DecodeArgs& a, Smem& sm, const uint16_t* rk, const uint16_t* rv,
-                              int n, float* lg_out) {
-    constexpr int D = CPL * 32;
+template <int NG, int D>
+__device__ void warp_residual(const DecodeArgs& a, Smem<NG, D>& sm, const uint16_t* rk,
+                              const uint16_t* rv, int n, float* lg_out) {
+    constexpr int CPL = D / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c0 = lane * CPL;
     const bool bf = a.bf16 != 0;
     WarpAcc<NG, CPL> acc;
-#pragma unroll
-    for (int h = 0; h < NG; ++h) {
-        acc.m[h] = kNegInf;
-        acc.l[h] = 0.0f;
-        acc.off[h] = 0.0f;
-        acc.zs[h] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) acc.o[h][i] = 0.0f;
-    }
+    acc_init(acc);
     for (int gi = warp; gi * 32 < n; gi += kWarps) {
         const int tl = gi * 32;
         const int nt = min(32, n - tl);
         float lg[NG];
-#pragma unroll
+#pragma unroll 1
         for (int h = 0; h < NG; ++h) {
             float part[32];
 #pragma unroll
@@ -517,19 +520,11 @@ __device__ void warp_residual(const DecodeArgs& a, Smem& sm, const uint16_t* rk,
 }
 
 template <int KB, int KAX, int VB, int D, int NG>
-__device__ void warp_tier(const DecodeArgs& a, Smem& sm, const View& v, int n, float* lg_out) {
+__device__ void warp_tier(const DecodeArgs& a, Smem<NG, D>& sm, const View& v, int n, float* lg_out) {
     constexpr int cpw = 32 / VB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpAcc<NG, cpw> acc;
-#pragma unroll
-    for (int h = 0; h < NG; ++h) {
-        acc.m[h] = kNegInf;
-        acc.l[h] = 0.0f;
-        acc.off[h] = 0.0f;
-        acc.zs[h] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < cpw; ++i) acc.o[h][i] = 0.0f;
-    }
+    acc_init(acc);
     for (int gi = warp; gi * 32 < n; gi += kWarps) {
         const int tl = gi * 32;
         const int nt = min(32, n - tl);
@@ -537,7 +532,7 @@ __device__ void warp_tier(const DecodeArgs& a, Smem& sm, const View& v, int n, f
         if (KAX == KVQ_AXIS_CHANNEL)
             logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
         else
-            logits_token<KB, D, NG>(v, tl, nt, sm, a.G, lg);
+            logits_token<KB, D, NG>(v, tl, sm, a.G, lg);
         group_softmax(acc, lg, nt, lg_out ? lg_out + tl : nullptr, a.slots);
         values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
     }
@@ -551,34 +546,9 @@ __device__ void warp_tier(const DecodeArgs& a, Smem& sm, const View& v, int n, f
     finish_token_values<VB, D, NG>(acc, sm);
 }
 
-// Merge the four warps of the CTA into the chunk partial (m, l, o[D]) per head.
-__device__ void cta_partial(const DecodeArgs& a, Smem& sm, float* part_out) {
-    const int D = a.D, g = a.g;
-    for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
-        float M = kNegInf;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
-        float L = 0.0f, O = 0.0f;
-        if (M != kNegInf) {
-            for (int w = 0; w < kWarps; ++w) {
-                if (sm.wm[w][h] == kNegInf) continue;
-                const float f = ex2_approx(sm.wm[w][h] - M);
-                L = fmaf(sm.wl[w][h], f, L);
-                O = fmaf(sm.wo[w][h][c], f, O);
-            }
-        }
-        float* po = part_out + (size_t)h * a.total_chunks * (D + 2);
-        po[2 + c] = O;
-        if (c == 0) {
-            po[0] = M;
-            po[1] = L;
-        }
-    }
-}
-
 template <int NG, int D>
-__device__ bool dispatch_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, const View& v, int n,
-                              float* lg_out) {
+__device__ bool dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& t, const View& v,
+                              int n, float* lg_out) {
     const int kb = t.k_bits, vb = t.v_bits, ax = t.k_axis;
     if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, v, n, lg_out); return true; }
     if (D == 128) {
@@ -592,85 +562,113 @@ __device__ bool dispatch_tier(const DecodeArgs& a, Smem& sm, const TierArgs& t, 
 
 template <int NG, int D>
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem<NG, D>& sm = *reinterpret_cast<Smem<NG, D>*>(smem_raw);
+    const uint8_t* stage = smem_raw + ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127);
     const size_t unit = blockIdx.y;
     const int units = gridDim.y;
     const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
-    constexpr int g = NG;
     const bool bf = a.bf16 != 0;
+    const uint32_t bar = smem_u32(&sm.bar);
 
-    for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
-        const size_t qi = ((size_t)b * a.Hq + (size_t)hkv * g + h) * D + c;
-        sm.q[h][c] = ldf(a.q, qi, bf) * a.scale_log2;
-    }
-    for (int idx = threadIdx.x; idx < kWarps * kMaxG; idx += blockDim.x) {
-        sm.wm[idx / kMaxG][idx % kMaxG] = kNegInf;
-        sm.wl[idx / kMaxG][idx % kMaxG] = 0.0f;
-    }
-    for (int idx = threadIdx.x; idx < kWarps * kMaxG * 128; idx += blockDim.x)
-        (&sm.wo[0][0][0])[idx] = 0.0f;
-    __syncthreads();
-
-    float* part_out = a.part + (unit * g * a.total_chunks + blockIdx.x) * (size_t)(D + 2);
-    float* lg_unit = a.logits ? a.logits + unit * g * (size_t)a.slots : nullptr;
     int chunk = blockIdx.x, tier = -1;
     for (int t = 0; t < a.n_tiers; ++t) {
         if (chunk < a.tier[t].chunks) { tier = t; break; }
         chunk -= a.tier[t].chunks;
     }
-    uint8_t* stage = smem_raw + ((sizeof(Smem) + 127) & ~(size_t)127);
-    const uint32_t bar = smem_u32(&sm.bar);
+    // thread 0 requests the chunk's bytes before anything else
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-    }
-    __syncthreads();
-    if (tier >= 0) {
-        const TierArgs& t = a.tier[tier];
-        const int j0 = chunk * kChunk;
-        if (t.count[unit] > t.cap && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
-        const int cnt = min(t.count[unit], t.cap);
-        const int n = min(kChunk, cnt - j0);
-        if (n > 0) {
-            const View v = stage_tier(t, unit, j0, (n + 31) & ~31, D, a.G, stage, bar);
-            float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
-            if (!__syncthreads_and(mbar_wait(bar, 0, nullptr))) {
-                if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
-            } else if (!dispatch_tier<NG, D>(a, sm, t, v, n, lg) && threadIdx.x == 0) {
-                atomicOr(&g_status_decode, kDevCheck);
-            }
+        int n = 0;
+        if (tier >= 0) {
+            const TierArgs& t = a.tier[tier];
+            const int raw = t.count[unit];
+            if (raw > t.cap || raw < 0) atomicOr(&g_status_decode, kDevCheck);
+            const int j0 = chunk * kChunk;
+            n = min(kChunk, min(max(raw, 0), t.cap) - j0);
+            if (n > 0) stage_tier(t, unit, j0, (n + 31) & ~31, D, a.G, stage, bar);
+        } else {
+            const int cap = a.res_cap;
+            const int raw = a.res_len[unit];
+            const int len = min(max(raw, 0), cap - 1), start = a.res_start[unit];
+            if (raw != len || start < 0 || start >= cap) atomicOr(&g_status_decode, kDevCheck);
+            const int j0 = chunk * kResChunk;
+            n = min(kResChunk, len + 1 - j0);
+            if (n > 0 && start >= 0 && start < cap) stage_residual(a, unit, len, start, j0, n, D, stage, bar);
+            else n = 0;
         }
-    } else {
-        const int cap = a.res_cap;
-        const int len = min(max(a.res_len[unit], 0), cap - 1), start = a.res_start[unit];
-        if (a.res_len[unit] != len && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
-        const int j0 = chunk * kResChunk;
-        const int n = min(kResChunk, len + 1 - j0);
-        if (n > 0) {
-            stage_residual(a, unit, len, start, j0, n, D, stage, bar);
+        sm.count = n;
+    }
+    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx % D;
+        sm.q[h][c] = ldf(a.q, ((size_t)b * a.Hq + (size_t)hkv * NG + h) * D + c, bf) * a.scale_log2;
+    }
+    for (int idx = threadIdx.x; idx < kWarps * NG; idx += blockDim.x) {
+        sm.wm[idx / NG][idx % NG] = kNegInf;
+        sm.wl[idx / NG][idx % NG] = 0.0f;
+    }
+    for (int idx = threadIdx.x; idx < kWarps * NG * D; idx += blockDim.x) (&sm.wo[0][0][0])[idx] = 0.0f;
+    __syncthreads();
+
+    float* lg_unit = a.logits ? a.logits + unit * NG * (size_t)a.slots : nullptr;
+    const int n = sm.count;
+    if (n > 0) {
+        const bool ok = __syncthreads_and(mbar_wait(bar, 0, nullptr));
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
+        } else if (tier >= 0) {
+            const TierArgs& t = a.tier[tier];
+            const int j0 = chunk * kChunk;
+            const View v = tier_view(t, (n + 31) & ~31, D, a.G, stage);
+            float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
+            if (!dispatch_tier<NG, D>(a, sm, t, v, n, lg) && threadIdx.x == 0)
+                atomicOr(&g_status_decode, kDevCheck);
+        } else {
+            const int j0 = chunk * kResChunk;
             const uint16_t* rk = reinterpret_cast<const uint16_t*>(stage);
             const uint16_t* rv = reinterpret_cast<const uint16_t*>(stage + a16((uint32_t)n * D * 2));
             float* lg = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 : nullptr;
-            if (!__syncthreads_and(mbar_wait(bar, 0, nullptr))) {
-                if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
-            } else {
-                warp_residual<D / 32, NG>(a, sm, rk, rv, n, lg);
-            }
-        }
-        if (chunk == 0) {
-            // the new token joins the ring; no CTA reads this slot in this step
-            const size_t slot = unit * (size_t)cap + (start + len) % cap;
-            for (int c = threadIdx.x; c < D; c += blockDim.x) {
-                stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
-                stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
-            }
-            if (threadIdx.x == 0) a.res_token_id[slot] = a.seq_len[b];
+            warp_residual<NG, D>(a, sm, rk, rv, n, lg);
         }
     }
+    if (tier < 0 && chunk == 0) {
+        // the new token joins the ring; no CTA reads this slot in this step
+        const int cap = a.res_cap;
+        const int len = min(max(a.res_len[unit], 0), cap - 1);
+        const int start = min(max(a.res_start[unit], 0), cap - 1);
+        const size_t slot = unit * (size_t)cap + (start + len) % cap;
+        for (int c = threadIdx.x; c < D; c += blockDim.x) {
+            stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
+            stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
+        }
+        if (threadIdx.x == 0) a.res_token_id[slot] = a.seq_len[b];
+    }
     __syncthreads();
-    cta_partial(a, sm, part_out);
+
+    // ---- chunk partial: merge the four warps
+    float* part_out = a.part + (unit * NG * a.total_chunks + blockIdx.x) * (size_t)(D + 2);
+    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx % D;
+        float M = kNegInf;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+        float L = 0.0f, O = 0.0f;
+        if (M != kNegInf) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = sm.wm[w][h] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][h] - M);
+                L = fmaf(sm.wl[w][h], f, L);
+                O = fmaf(sm.wo[w][h][c], f, O);
+            }
+        }
+        float* po = part_out + (size_t)h * a.total_chunks * (D + 2);
+        po[2 + c] = O;
+        if (c == 0) {
+            po[0] = M;
+            po[1] = L;
+        }
+    }
 
     // ---- completion: the last CTA of the unit merges the partials
     __threadfence();
@@ -683,46 +681,55 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     if (!sm.last) return;
     __threadfence();
 
-    const float* pu = a.part + unit * g * a.total_chunks * (size_t)(D + 2);
-    if (threadIdx.x < g) {
-        const float* ph = pu + (size_t)threadIdx.x * a.total_chunks * (D + 2);
-        float M = kNegInf;
-        for (int x = 0; x < a.total_chunks; ++x)
-            if (__ldcg(ph + (size_t)x * (D + 2) + 1) > 0.0f) M = fmaxf(M, __ldcg(ph + (size_t)x * (D + 2)));
-        float L = 0.0f;
-        for (int x = 0; x < a.total_chunks; ++x) {
-            const float l = __ldcg(ph + (size_t)x * (D + 2) + 1);
-            if (l > 0.0f) L += l * ex2_approx(__ldcg(ph + (size_t)x * (D + 2)) - M);
-        }
-        sm.wm[0][threadIdx.x] = M;
-        sm.wl[0][threadIdx.x] = L;
-        sm.wm[1][threadIdx.x] = M + __log2f(L);          // base-2 lse
-        if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * g + threadIdx.x] = (M + __log2f(L)) * kLn2;
+    const int TC = a.total_chunks;
+    const float* pu = a.part + unit * NG * TC * (size_t)(D + 2);
+    // chunk maxima and sums, all loads in flight together (scratch = the stage buffer)
+    float* cm = reinterpret_cast<float*>(const_cast<uint8_t*>(stage));      // [NG][TC]
+    float* cw = cm + NG * TC;                                                  // [NG][TC]
+    for (int idx = threadIdx.x; idx < NG * TC; idx += blockDim.x) {
+        const float* ph = pu + (size_t)idx * (D + 2);
+        const float l = __ldcg(ph + 1);
+        cm[idx] = l > 0.0f ? __ldcg(ph) : kNegInf;
+        cw[idx] = l;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
-        const float* ph = pu + (size_t)h * a.total_chunks * (D + 2);
-        const float M = sm.wm[0][h], L = sm.wl[0][h];
-        float acc = 0.0f;
-        for (int x = 0; x < a.total_chunks; ++x) {
-            const float l = __ldcg(ph + (size_t)x * (D + 2) + 1);
-            if (l > 0.0f) acc += __ldcg(ph + (size_t)x * (D + 2) + 2 + c) * ex2_approx(__ldcg(ph + (size_t)x * (D + 2)) - M);
+    if (threadIdx.x < NG) {
+        const int h = threadIdx.x;
+        float M = kNegInf;
+        for (int x = 0; x < TC; ++x) M = fmaxf(M, cm[h * TC + x]);
+        float L = 0.0f;
+        for (int x = 0; x < TC; ++x) {
+            const float wgt = cm[h * TC + x] == kNegInf ? 0.0f : ex2_approx(cm[h * TC + x] - M);
+            L = fmaf(cw[h * TC + x], wgt, L);
+            cw[h * TC + x] = wgt;
         }
-        stf(a.o, ((size_t)b * a.Hq + hkv * g + h) * D + c, acc / L, bf);
+        sm.wl[0][h] = L;
+        sm.wm[0][h] = M + __log2f(L);          // base-2 lse
+        if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx % D;
+        const float* ph = pu + (size_t)h * TC * (D + 2) + 2 + c;
+        float acc = 0.0f;
+#pragma unroll 8
+        for (int x = 0; x < TC; ++x) acc = fmaf(__ldcg(ph + (size_t)x * (D + 2)), cw[h * TC + x], acc);
+        stf(a.o, ((size_t)b * a.Hq + hkv * NG + h) * D + c, acc / sm.wl[0][h], bf);
     }
 
     const int cap = a.res_cap;
-    const int len = min(max(a.res_len[unit], 0), cap - 1), start = a.res_start[unit];
-    const float* lse2 = sm.wm[1];
+    const int len = min(max(a.res_len[unit], 0), cap - 1);
+    const int start = min(max(a.res_start[unit], 0), cap - 1);
+    const float* lse2 = sm.wm[0];
     if (a.policy == KVQ_POLICY_MIKV && lg_unit) {
         float* cs = a.cum_score + unit * (size_t)a.score_cap;
         for (int t = 0; t < a.n_tiers; ++t) {
             const TierArgs& ti = a.tier[t];
-            const int cnt = min(ti.count[unit], ti.cap);
+            const int cnt = min(max(ti.count[unit], 0), ti.cap);
             for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
                 float p = 0.0f;
-                for (int h = 0; h < g; ++h)
+#pragma unroll
+                for (int h = 0; h < NG; ++h)
                     p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ti.slot_base + j) - lse2[h]);
                 const int id = ti.token_id[unit * (size_t)ti.cap + j];
                 if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
@@ -731,17 +738,18 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         }
         for (int li = threadIdx.x; li <= len; li += blockDim.x) {
             float p = 0.0f;
-            for (int h = 0; h < g; ++h)
+#pragma unroll
+            for (int h = 0; h < NG; ++h)
                 p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
             const int id = li < len ? a.res_token_id[unit * (size_t)cap + (start + li) % cap] : a.seq_len[b];
             if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
             else cs[id] = li < len ? __fadd_rn(cs[id], p) : p;
         }
     } else if (a.policy == KVQ_POLICY_DIFFKV && lg_unit) {
-        for (int idx = threadIdx.x; idx < (len + 1) * g; idx += blockDim.x) {
-            const int li = idx / g, h = idx % g;
+        for (int idx = threadIdx.x; idx < (len + 1) * NG; idx += blockDim.x) {
+            const int li = idx / NG, h = idx % NG;
             const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-            float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * g + h) * cap + (start + li) % cap;
+            float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (start + li) % cap;
             *wa = li < len ? __fadd_rn(*wa, p) : p;
         }
     }
@@ -758,8 +766,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         }
     }
 }
-
-}  // namespace
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -790,6 +796,27 @@ WsLayout ws_layout(const kvq_cache& c) {
     return w;
 }
 
+template <int NG, int D>
+cudaError_t launch_typed(const DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s) {
+    uint32_t stage = 2u * a16((uint32_t)kResChunk * D * 2);
+    for (int t = 0; t < c.n_tiers; ++t)
+        stage = std::max(stage, tier_stage_sizes(c.tier[t].k_axis, c.tier[t].k_bits, c.tier[t].v_bits,
+                                                 kChunk, D, c.G).total());
+    stage = std::max(stage, (uint32_t)(2 * NG * a.total_chunks * sizeof(float)));   // merge scratch
+    const size_t sh = ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127) + stage;
+    static size_t attr = 0;
+    if (sh > 48 * 1024 && sh > attr) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh);
+        if (e != cudaSuccess) return e;
+        attr = sh;
+    }
+    dim3 grid(a.total_chunks, units);
+    decode_kernel<NG, D><<<grid, kThreads, sh, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 size_t decode_workspace_bytes(const kvq_cache& c) { return ws_layout(c).total; }
 
@@ -853,30 +880,12 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.counters = reinterpret_cast<uint32_t*>(base + w.counters);
     cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(units + 1) * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
-    dim3 grid(w.total_chunks, units);
-    uint32_t stage = 2u * a16((uint32_t)kResChunk * c.D * 2);
-    for (int t = 0; t < c.n_tiers; ++t)
-        stage = std::max(stage, tier_stage_bytes(c.tier[t].k_axis, c.tier[t].k_bits, c.tier[t].v_bits,
-                                                 kChunk, c.D, c.G));
-    const size_t sh = ((sizeof(Smem) + 127) & ~(size_t)127) + stage;
-#define KVQ_DECODE_CASE(NG_, D_)                                                              \
-    if (a.g == NG_ && c.D == D_) {                                                            \
-        static size_t attr_##NG_##_##D_ = 0;                                                  \
-        if (sh > 48 * 1024 && sh > attr_##NG_##_##D_) {                                       \
-            cudaFuncSetAttribute(decode_kernel<NG_, D_>,                                       \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh);       \
-            attr_##NG_##_##D_ = sh;                                                           \
-        }                                                                                     \
-        decode_kernel<NG_, D_><<<grid, kThreads, sh, s>>>(a);                                 \
-        return cudaGetLastError();                                                            \
-    }
-    KVQ_DECODE_CASE(1, 128)
-    KVQ_DECODE_CASE(1, 64)
-    KVQ_DECODE_CASE(2, 128)
-    KVQ_DECODE_CASE(4, 128)
-    KVQ_DECODE_CASE(5, 128)
-    KVQ_DECODE_CASE(8, 128)
-#undef KVQ_DECODE_CASE
+    if (a.g == 1 && c.D == 128) return launch_typed<1, 128>(a, c, units, s);
+    if (a.g == 1 && c.D == 64) return launch_typed<1, 64>(a, c, units, s);
+    if (a.g == 2 && c.D == 128) return launch_typed<2, 128>(a, c, units, s);
+    if (a.g == 4 && c.D == 128) return launch_typed<4, 128>(a, c, units, s);
+    if (a.g == 5 && c.D == 128) return launch_typed<5, 128>(a, c, units, s);
+    if (a.g == 8 && c.D == 128) return launch_typed<8, 128>(a, c, units, s);
     return cudaErrorInvalidConfiguration;
 }
 
