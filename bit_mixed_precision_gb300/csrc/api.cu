@@ -205,6 +205,27 @@ kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, 
                        "decode_attn_qkv launch");
 }
 
+kvq_status decode_attn_qkv_static(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
+                                  float sm_scale, void* o, float* lse_out, void* stream) {
+    kvq_status st = check_cache(c, "decode_attn_qkv_static");
+    if (st != KVQ_OK) return st;
+    KVQ_REQUIRE(q && k_new && v_new && o, KVQ_EINVAL, "decode_attn_qkv_static: null pointer");
+    KVQ_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16) && aligned(c->res_k, 16) && aligned(c->res_v, 16),
+                KVQ_EINVAL, "decode_attn_qkv_static: k_new, v_new and the residual ring must be 16-byte aligned");
+    KVQ_REQUIRE(sm_scale > 0.0f, KVQ_EINVAL, "decode_attn_qkv_static: sm_scale must be positive");
+    const size_t need = kvq::decode_workspace_bytes(*c);
+    KVQ_REQUIRE(need <= (size_t)KVQ_STATIC_SCRATCH_BYTES, KVQ_EWORKSPACE,
+                "decode_attn_qkv_static: this cache needs %zu bytes of scratch, more than the %u bytes "
+                "built into the library; use decode_attn_qkv with a caller workspace",
+                need, (unsigned)KVQ_STATIC_SCRATCH_BYTES);
+    void* ws = nullptr;
+    kvq_status s2 = cuda_status(kvq::static_decode_scratch(&ws), "decode_attn_qkv_static scratch lookup");
+    if (s2 != KVQ_OK) return s2;
+    return cuda_status(kvq::launch_decode(q, k_new, v_new, *c, sm_scale, o, lse_out, ws,
+                                          (cudaStream_t)stream),
+                       "decode_attn_qkv_static launch");
+}
+
 kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params* p, int step,
                           void* stream) {
     kvq_status st = check_cache(c, "requant_demote");

@@ -17,6 +17,7 @@
 // attention is permutation invariant, so each precision group sits in its
 // own region).
 #include <algorithm>
+#include <mutex>
 
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
@@ -887,6 +888,36 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     if (a.g == 5 && c.D == 128) return launch_typed<5, 128>(a, c, units, s);
     if (a.g == 8 && c.D == 128) return launch_typed<8, 128>(a, c, units, s);
     return cudaErrorInvalidConfiguration;
+}
+
+// ---- workspace in the library's own device memory, for callers that cannot
+// allocate one.  The array lives in every context that loads the library,
+// for as long as the library stays loaded.  In host code its name is only a
+// host-side stand-in, so its device address is looked up once per device.
+static __device__ __align__(256) uint8_t g_decode_scratch[KVQ_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the static scratch on the current device (looked up on
+// the first call made with that device current).
+cudaError_t static_decode_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace kvq

@@ -37,6 +37,9 @@ size_t decode_workspace_bytes(const kvq_cache& c);
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, const kvq_cache& c,
                           float sm_scale, void* o, float* lse_out, void* ws, cudaStream_t s);
 
+// Device address of the library's static decode scratch on the current device.
+cudaError_t static_decode_scratch(void** out);
+
 kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, int step,
                       cudaStream_t s);
 

@@ -25,7 +25,8 @@ POLICY_MINIKV, POLICY_DIFFKV, POLICY_MIKV = 0, 1, 2
 MAX_TIERS = 2
 
 EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "kvq_score_reduce", "select_tokens",
-           "requant_demote", "decode_attn_qkv", "kvq_decode_workspace_bytes", "kvq_tier_bytes",
+           "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
+           "kvq_decode_workspace_bytes", "kvq_tier_bytes",
            "kvq_last_error", "kvq_device_status", "kvq_version"]
 
 
@@ -85,6 +86,8 @@ def lib():
         L.requant_demote.argtypes = [ctypes.POINTER(KvqCache), i32, ctypes.POINTER(KvqPolicyParams),
                                      i32, vp]
         L.decode_attn_qkv.argtypes = [vp, vp, vp, ctypes.POINTER(KvqCache), f32, vp, vp, vp, sz, vp]
+        L.decode_attn_qkv_static.argtypes = [vp, vp, vp, ctypes.POINTER(KvqCache), f32, vp, vp, vp]
+        L.decode_attn_qkv_static.restype = ctypes.c_int
         L.kvq_decode_workspace_bytes.argtypes = [ctypes.POINTER(KvqCache)]
         L.kvq_decode_workspace_bytes.restype = sz
         L.kvq_tier_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
@@ -361,4 +364,27 @@ def decode_attn_qkv(q, k_new, v_new, cache, sm_scale=None, o=None, lse=None, str
     _check(lib().decode_attn_qkv(_ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache.desc),
                                  float(sm_scale), _ptr(o), _ptr(lse), _ptr(cache.ws),
                                  cache.ws.numel() * 4, _stream(stream)))
+    return o, lse
+
+
+STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_attn_qkv_static(q, k_new, v_new, cache, sm_scale=None, o=None, lse=None, stream=None):
+    """decode_attn_qkv for callers that cannot provide scratch memory.
+
+    The library uses its own built-in device array (STATIC_SCRATCH_BYTES)
+    instead of ``cache.ws``; nothing is allocated by the call.  Calls whose
+    GPU work overlaps share that array and must not run concurrently.
+    """
+    _cuda(q, k_new, v_new)
+    B, Hq, D = q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().decode_attn_qkv_static(_ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache.desc),
+                                        float(sm_scale), _ptr(o), _ptr(lse), _stream(stream)))
     return o, lse

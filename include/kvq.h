@@ -235,6 +235,29 @@ kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, 
 /* Bytes of decode workspace the cache needs (0 on an invalid cache). */
 size_t kvq_decode_workspace_bytes(const kvq_cache* c);
 
+/* Size of the scratch array built into the library for decode_attn_qkv_static. */
+#define KVQ_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* decode_attn_qkv_static -- decode_attn_qkv without a caller workspace.
+ * No counterpart in the papers: it exists for callers that cannot hand the
+ * library any scratch memory, e.g. a serving engine whose allocator has
+ * already reserved all free device memory for its KV page pool, or plain C
+ * code that has no device allocator of its own.  The call allocates nothing
+ * (no cudaMalloc, no allocating library routine); its scratch is a
+ * KVQ_STATIC_SCRATCH_BYTES array in the library's own device memory, which
+ * every GPU that loads the library keeps until the process exits.
+ *   Arguments, results and errors as decode_attn_qkv, minus ws/ws_bytes.
+ *   A cache whose kvq_decode_workspace_bytes() exceeds
+ *   KVQ_STATIC_SCRATCH_BYTES is rejected with KVQ_EWORKSPACE.
+ *   The first call made with a given device current looks up the array's
+ *   device address on that device; make that first call before any stream
+ *   capture.
+ *   All calls share the one array (its counters are cleared at the start of
+ *   every call): two calls whose work overlaps on the GPU, on any streams,
+ *   race and give wrong results. */
+kvq_status decode_attn_qkv_static(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
+                                  float sm_scale, void* o, float* lse_out, void* stream);
+
 /* Bytes each device array of a cache with these sizes needs; out[i] in the
  * order of the kvq_cache fields (see kvq_cache_layout in the Python
  * binding).  Returns the total, 0 on invalid sizes. */
