@@ -1,21 +1,28 @@
 """Benchmark of the compressed-KV-cache attention hot path on one GB300 (or N replicas).
 
 One step = the whole hot path over one batch of synthetic input: two-pass
-prefill (output + column scores), heavy-hitter + recent-window selection, the
-prefill-end cache build (INT2 packing), then `decode_steps` decode steps
-(attention over the packed cache + residual flush).  Default workload: the
-LLaMA2-7B-shaped layer (batch 1, 32 heads, head dim 128, prompt 4096, fp16,
-2% outlier key channels x10, INT2 groups of 32, 128-token residual, 25% heavy
-hitters + 25% window, 128 decode steps).
+prefill (output + column scores), the prefill-end cache build (selection and
+INT2 packing for MiniKV, the tier split for DiffKV / MiKV), then every decode
+step of the workload (attention over the packed cache + the policy tail).
 
-Printed value: decoded tokens per second of the whole step (prefill included),
-inputs resident in HBM.  The line also carries decode-only tokens/s and
-packed-KV GB/s, prefill TFLOP/s, the roofline of the dominant kernel, the
-end-to-end number through host buffers, the CPU oracle baseline and the SM
-clocks seen during the timed region.
+Default workload (`llama-layer`): the LLaMA2-7B-shaped layer -- batch 1, 32
+heads, head dim 128, prompt 4096, fp16, 2% outlier key channels x10, INT2
+groups of 32, 128-token residual, 25% heavy hitters + 25% window, 128 decode
+steps.  Other workloads (not the default line): `tiny` (batch 1, 2 heads,
+head dim 64, prompt 256, 16 steps), `pyramid-layer16` (layer 16 of the 32-layer
+pyramid sweep: batch 16, 32 heads, prompt 16384, heavy hitters 25.2%, window
+25%, 256 steps), `diffkv` (GQA 40/8, batch 32, prompt 8192, K8V4/K4V2/prune with
+Dirichlet(2,5,3) fractions, 64-token window, 512 steps), `mikv` (GQA 32/8, batch
+64, prompt 32768, bf16, INT4 top 20% / INT2 rest, 128-token residual, 1024 steps).
+
+Printed value: decoded tokens per second of the whole step (prefill
+included), inputs resident in HBM.  The line also carries decode-only
+tokens/s and packed-KV GB/s, prefill TFLOP/s, the roofline of the dominant
+kernel, the end-to-end number through host buffers, the CPU oracle baseline
+and the SM clocks seen during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama-layer|pyramid-sweep|diffkv|mikv]
+                  [--workload llama-layer|tiny|pyramid-layer16|diffkv|mikv]
 """
 from __future__ import annotations
 
@@ -38,11 +45,20 @@ if ROOT not in sys.path:
 METRIC = "decode attn tokens/s & packed-KV GB/s (% HBM peak); prefill attn TFLOP/s"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+G = 32
 
 WORKLOADS = {
-    # name: B, H, D, T, steps, nr, hh%, rw%, outlier channels, outlier scale
-    "llama-layer": dict(B=1, H=32, D=128, T=4096, steps=128, nr=128, hh=25, rw=25, n_out=3,
-                        out_scale=10.0),
+    "llama-layer": dict(policy="minikv", B=1, Hq=32, Hkv=32, D=128, T=4096, steps=128, nr=128,
+                        hh=25, rw=25, n_out=3, out_scale=10.0, dtype="f16"),
+    "tiny": dict(policy="minikv", B=1, Hq=2, Hkv=2, D=64, T=256, steps=16, nr=0, hh=25, rw=25,
+                 n_out=2, out_scale=8.0, dtype="f16"),
+    "pyramid-layer16": dict(policy="minikv", B=16, Hq=32, Hkv=32, D=128, T=16384, steps=256, nr=0,
+                            hh=None, layer=16, n_layers=32, rw=25, n_out=0, out_scale=1.0,
+                            key_std=0.5, dtype="f16"),
+    "diffkv": dict(policy="diffkv", B=32, Hq=40, Hkv=8, D=128, T=8192, steps=512, nr=64, n_out=0,
+                   out_scale=1.0, dtype="f16"),
+    "mikv": dict(policy="mikv", B=64, Hq=32, Hkv=8, D=128, T=32768, steps=1024, nr=128, n_out=1,
+                 out_scale=12.0, dtype="bf16"),
 }
 
 
@@ -52,6 +68,18 @@ def _peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     return 6800.0, 1900.0, "fallback"
+
+
+def _budget(wl):
+    """(heavy-hitter budget, window) of a MiniKV workload, integer form of the percentages."""
+    T = wl["T"]
+    w = (T * wl["rw"]) // 100
+    if wl.get("hh") is None:
+        L, l = wl["n_layers"], wl["layer"]
+        k = (T * (40 * (L - 1) - 30 * l)) // (100 * (L - 1))
+    else:
+        k = (T * wl["hh"]) // 100
+    return min(k, T - w), w
 
 
 class Clocks:
@@ -112,58 +140,76 @@ class Clocks:
 # ---------------------------------------------------------------------------- our arm
 
 class Hot:
-    """Device-resident state of one replica of the workload."""
+    """Device-resident state of one replica of a workload."""
 
     def __init__(self, wl, dev, seed=0):
         from bit_mixed_precision_gb300 import inputs, kvq
-        self.kvq = kvq
-        self.wl = wl
-        B, H, D, T = wl["B"], wl["H"], wl["D"], wl["T"]
+        self.kvq, self.wl, self.dev = kvq, wl, dev
+        B, Hq, Hkv, D, T, steps = wl["B"], wl["Hq"], wl["Hkv"], wl["D"], wl["T"], wl["steps"]
+        self.dtype = torch.bfloat16 if wl["dtype"] == "bf16" else torch.float16
         self.scale = 1.0 / math.sqrt(D)
-        self.outl = inputs.outlier_channels(H, D, wl["n_out"], seed)
-        x = inputs.make_qkv(B, H, H, T, D, seed=seed, device=dev, outliers=self.outl,
-                            outlier_scale=wl["out_scale"])
+        outl = inputs.outlier_channels(Hkv, D, wl["n_out"], seed) if wl["n_out"] else None
+        kstd = inputs.lognormal_key_std(Hkv, D, wl["key_std"], seed) if wl.get("key_std") else None
+        x = inputs.make_qkv(B, Hq, Hkv, T, D, dtype=self.dtype, seed=seed, device=dev, outliers=outl,
+                            outlier_scale=wl["out_scale"], key_std=kstd)
         self.q, self.k, self.v = x.q, x.k, x.v
-        self.k_hh = (T * wl["hh"]) // 100
-        self.w = (T * wl["rw"]) // 100
-        self.n_sel = self.k_hh + self.w
-        G, nr, steps = 32, wl["nr"], wl["steps"]
-        r0 = self.n_sel if self.n_sel <= nr else nr + (self.n_sel - nr) % G
-        cap = ((self.n_sel - r0 + steps) // G + 1) * G
-        self.cache = kvq.make_cache(B, H, H, D, G, torch.float16, kvq.POLICY_MINIKV,
-                                    [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=nr, device=dev)
-        self.kh = torch.full((B * H,), self.k_hh, dtype=torch.int32, device=dev)
-        self.dec = [inputs.make_decode_step(B, H, H, D, t, seed=seed, device=dev,
-                                            outliers=self.outl, outlier_scale=wl["out_scale"])
+        self.dec = [inputs.make_decode_step(B, Hq, Hkv, D, t, dtype=self.dtype, seed=seed, device=dev,
+                                            outliers=outl, outlier_scale=wl["out_scale"], key_std=kstd)
                     for t in range(steps)]
+        pol = wl["policy"]
+        nr = wl["nr"]
+        if pol == "minikv":
+            self.k_hh, self.w = _budget(wl)
+            self.n_sel = self.k_hh + self.w
+            r0 = self.n_sel if self.n_sel <= nr else nr + (self.n_sel - nr) % G
+            cap = ((self.n_sel - r0 + steps) // G + 1) * G
+            self.cache = kvq.make_cache(B, Hq, Hkv, D, G, self.dtype, kvq.POLICY_MINIKV,
+                                        [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=nr, device=dev)
+            self.kh = torch.full((B * Hkv,), self.k_hh, dtype=torch.int32, device=dev)
+            self.idx = torch.empty((B, Hkv, self.n_sel), dtype=torch.int32, device=dev)
+            self.nout = torch.empty((B * Hkv,), dtype=torch.int32, device=dev)
+            self.launches_per_step = 2 + 1 + 3 + 2 * steps
+        elif pol == "diffkv":
+            f = inputs.dirichlet_fractions(B * Hkv, seed=seed)
+            nc = T - nr
+            self.n_high = torch.from_numpy(np.floor(f[:, 0] * nc).astype(np.int32)).to(dev)
+            self.n_low = torch.from_numpy(np.floor(f[:, 1] * nc).astype(np.int32)).to(dev)
+            caps = [int(self.n_high.max()) + steps + G, int(self.n_low.max()) + steps + G]
+            self.cache = kvq.make_cache(B, Hq, Hkv, D, G, self.dtype, kvq.POLICY_DIFFKV,
+                                        [kvq.TierSpec(8, 4, kvq.AXIS_TOKEN, caps[0]),
+                                         kvq.TierSpec(4, 2, kvq.AXIS_TOKEN, caps[1])], nr=nr, device=dev)
+            self.launches_per_step = 2 + 1 + 2 * steps
+        else:
+            nq = T - nr + steps
+            self.cache = kvq.make_cache(B, Hq, Hkv, D, G, self.dtype, kvq.POLICY_MIKV,
+                                        [kvq.TierSpec(4, 4, kvq.AXIS_TOKEN, nq // 5 + 64),
+                                         kvq.TierSpec(2, 2, kvq.AXIS_TOKEN, nq + 64)],
+                                        nr=nr, score_cap=T + steps + 1, hi_den=5, device=dev)
+            self.launches_per_step = 2 + 1 + 2 * steps
         self.o_pre = torch.empty_like(self.q)
-        self.lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
         self.cs = torch.empty_like(self.lse)
-        self.idx = torch.empty((B, H, self.k_hh + self.w), dtype=torch.int32, device=dev)
-        self.nout = torch.empty((B * H,), dtype=torch.int32, device=dev)
-        self.o_dec = torch.empty((steps, B, H, D), dtype=torch.float16, device=dev)
-        self.lse_dec = torch.empty((steps, B, H), dtype=torch.float32, device=dev)
+        self.o_dec = torch.empty((steps, B, Hq, D), dtype=self.dtype, device=dev)
+        self.lse_dec = torch.empty((steps, B, Hq), dtype=torch.float32, device=dev)
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        # packed-cache bytes each decode launch reads, from the flush schedule
-        self.dec_bytes = []
-        n_p, r = self.n_sel - r0, r0
-        per_tok = D * (2 + 2) // 8 + 2 * 2 * (D // G) * 2   # INT2 K+V codes + fp16 s/z
-        for t in range(steps):
-            r += 1
-            self.dec_bytes.append(B * H * (n_p * per_tok + r * 2 * D * 2 + 4 * D * 2))
-            if r == nr + G:
-                n_p, r = n_p + G, r - G
-        self.prefill_flops = 3 * D * T * T * B * H            # QK^T + PV (pass 1) + QK^T (pass 2)
-        self.launches_per_step = 2 + 1 + 3 + 2 * steps
+        nt = len(self.cache.tiers)
+        self.hist = torch.zeros((steps, nt + 1, B * Hkv), dtype=torch.int32, device=dev)
+        self.prefill_flops = 3 * D * T * T * B * Hq     # pass-1 QK^T and PV, pass-2 QK^T
 
-    def prefill_select_build(self, s):
-        kvq = self.kvq
+    def prefill_build(self, s):
+        kvq, pol = self.kvq, self.wl["policy"]
         kvq.prefill_attn_scores(self.q, self.k, self.v, self.scale,
                                 out=(self.o_pre, self.lse, self.cs), stream=s)
-        kvq.select_tokens(self.cs, self.kh, self.w, kmax=self.k_hh, out=(self.idx, self.nout),
-                          stream=s)
-        kvq.requant_demote(self.cache, 0, k_src=self.k, v_src=self.v, sel_idx=self.idx,
-                           n_sel=self.n_sel, stream=s)
+        if pol == "minikv":
+            kvq.select_tokens(self.cs, self.kh, self.w, kmax=self.k_hh, out=(self.idx, self.nout),
+                              stream=s)
+            kvq.requant_demote(self.cache, 0, k_src=self.k, v_src=self.v, sel_idx=self.idx,
+                               n_sel=self.n_sel, stream=s)
+        elif pol == "diffkv":
+            kvq.requant_demote(self.cache, 0, k_src=self.k, v_src=self.v, colscore=self.cs,
+                               n_high=self.n_high, n_low=self.n_low, stream=s)
+        else:
+            kvq.requant_demote(self.cache, 0, k_src=self.k, v_src=self.v, colscore=self.cs, stream=s)
 
     def decode(self, t, s):
         qd, kd, vd = self.dec[t]
@@ -172,6 +218,33 @@ class Hot:
 
     def tail(self, t, s):
         self.kvq.requant_demote(self.cache, t + 1, stream=s)
+
+    def record_counts(self, t):
+        """Tier sizes and residual length as decode step t saw them (outside the timed windows)."""
+        for i, tr in enumerate(self.cache.tiers):
+            self.hist[t, i].copy_(tr.count)
+        self.hist[t, -1].copy_(self.cache.res_len)
+
+    def decode_bytes(self):
+        """Algorithmic bytes each decode launch moves: packed codes + fp16 scale/zero of every
+        stored token, the full-precision residual (with the new token), q / o / k_new / v_new,
+        and for MiKV the cumulative-score read-modify-write of every token."""
+        D, Hq, Hkv = self.wl["D"], self.wl["Hq"], self.wl["Hkv"]
+        h = self.hist.cpu().numpy().astype(np.int64)
+        per = []
+        for tr in self.cache.tiers:
+            s = tr.spec
+            per.append(D * (s.k_bits + s.v_bits) // 8 + 2 * 2 * (D // G) * 2)
+        out = []
+        for t in range(h.shape[0]):
+            packed = sum(int(h[t, i].sum()) * per[i] for i in range(len(per)))
+            res = int(h[t, -1].sum() + h.shape[2]) * 2 * D * 2          # before the append, + new
+            io = (2 * Hq + 2 * Hkv) * self.wl["B"] * D * 2
+            extra = 0
+            if self.wl["policy"] == "mikv":
+                extra = 8 * (int(h[t, :-1].sum()) + int(h[t, -1].sum() + h.shape[2]))
+            out.append(packed + res + io + extra)
+        return out, packed
 
 
 def run_ours(args, wl, rank, world):
@@ -185,17 +258,19 @@ def run_ours(args, wl, rank, world):
     hbm_peak, tf_peak, peak_src = _peaks()
 
     def one_step(rec):
-        """Runs one step; when rec, returns the event pairs of each timed segment."""
+        """Runs one step; returns the event pairs of each timed segment."""
         ev = []
         with torch.cuda.stream(s):
             hot.flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s)
-            hot.prefill_select_build(s)
+            hot.prefill_build(s)
             e1.record(s)
             ev.append(("prefill", e0, e1))
             for t in range(steps):
                 hot.flush.zero_()
+                if rec:
+                    hot.record_counts(t)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 c = torch.cuda.Event(enable_timing=True)
                 a.record(s)
@@ -213,7 +288,6 @@ def run_ours(args, wl, rank, world):
     st = kvq.device_status(s)
     if st:
         raise RuntimeError(f"device status {st} after warm-up")
-    # separate prefill-kernel timing for the prefill roofline
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -226,12 +300,16 @@ def run_ours(args, wl, rank, world):
             for name, a, b in ev:
                 seg[name] += a.elapsed_time(b)
                 n_dec += name == "decode"
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    st = kvq.device_status(s)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed steps")
     step_ms = sum(seg.values()) / args.steps
-    # prefill kernels alone (both passes), for TFLOP/s
+    # the two prefill kernels alone, for TFLOP/s
     pre = []
-    for _ in range(5):
+    for _ in range(3):
         with torch.cuda.stream(s):
             hot.flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -246,36 +324,42 @@ def run_ours(args, wl, rank, world):
     dec_tokens = B * steps
     ms_max = step_ms
     if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+        tt = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
     value = world * dec_tokens / (ms_max / 1e3)
     dec_ms_per_launch = seg["decode"] / n_dec
-    dec_bytes = float(np.mean(hot.dec_bytes))
+    dbytes, _ = hot.decode_bytes()
+    dec_bytes = float(np.mean(dbytes))
     achieved = dec_bytes / (dec_ms_per_launch / 1e3) / 1e9
-    e2e = run_e2e(hot, s, args, wl)
+    pre_tf = hot.prefill_flops / (pre_ms / 1e3) / 1e12
+    default = args.workload == "llama-layer" or args.workload == "tiny"
+    e2e = run_e2e(hot, s, args, wl) if default else None
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp16 in, fp32 accumulate, INT2 cache",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{wl['dtype']} in, f32 accumulate, packed {'INT2' if wl['policy'] == 'minikv' else ('K8V4/K4V2' if wl['policy'] == 'diffkv' else 'INT4/INT2')} cache",
         "data": "synthetic (seeded Gaussian Q/K/V, outlier key channels)",
-        "config": {"workload": args.workload, "batch": B, "heads": wl["H"], "head_dim": wl["D"],
-                   "prompt": wl["T"], "decode_steps": steps, "kv_bits": 2, "group": 32,
-                   "residual": wl["nr"], "budget": f"{wl['hh']}% heavy hitters + {wl['rw']}% window",
+        "config": {"workload": args.workload, **{k: v for k, v in wl.items() if v is not None},
                    "l2": "flushed (256 MB write) before the prefill and before every decode step; "
                          "flush time excluded", "parallelism": f"replicas x{world}"},
         "decode": {"tokens_per_s": dec_tokens / (seg['decode'] / args.steps / 1e3),
-                   "us_per_launch": dec_ms_per_launch * 1e3, "packed_kv_gbs": achieved,
-                   "frac_hbm": achieved / hbm_peak},
-        "prefill": {"ms": pre_ms, "tflops": hot.prefill_flops / (pre_ms / 1e3) / 1e12,
-                    "frac_tensor": hot.prefill_flops / (pre_ms / 1e3) / 1e12 / tf_peak,
-                    "flops_counted": "3*D*T^2 per (batch, head): pass-1 QK^T and PV, pass-2 QK^T "
-                                     "(dense count, the causal half is not subtracted)"},
+                   "us_per_launch": dec_ms_per_launch * 1e3, "bytes_per_launch": dec_bytes,
+                   "packed_kv_gbs": achieved, "frac_hbm": achieved / hbm_peak},
+        "prefill": {"ms": pre_ms, "tflops": pre_tf, "frac_tensor": pre_tf / tf_peak,
+                    "flops_counted": "3*D*T^2 per (batch, query head): pass-1 QK^T and PV, pass-2 "
+                                     "QK^T (dense count, the causal half is not subtracted)"},
         "segments_ms_per_step": {k2: v2 / args.steps for k2, v2 in seg.items()},
         "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
-                     "peak_source": f"{peak_src} hbm_gbs"},
+                     "peak_source": f"{peak_src} hbm_gbs (of measured)" if peak_src == "measured"
+                                    else "fallback 6800 GB/s"},
+        "roofline_prefill": {"kernel": "prefill_pass1_kernel + prefill_pass2_kernel", "bound": "tensor",
+                             "achieved": pre_tf, "peak": tf_peak, "unit": "TFLOP/s",
+                             "frac": pre_tf / tf_peak,
+                             "peak_source": f"{peak_src} bf16_tflops (burst)"},
         "e2e": e2e,
         "gpu_launches": hot.launches_per_step * args.steps,
         "clocks": clk.summary(),
@@ -305,7 +389,7 @@ def run_e2e(hot, s, args, wl):
             hot.q.copy_(hq, non_blocking=True)
             hot.k.copy_(hk, non_blocking=True)
             hot.v.copy_(hv, non_blocking=True)
-            hot.prefill_select_build(s)
+            hot.prefill_build(s)
             for t in range(steps):
                 for dst, src in zip(hot.dec[t], hdec[t]):
                     dst.copy_(src, non_blocking=True)
@@ -319,52 +403,57 @@ def run_e2e(hot, s, args, wl):
     ms = statistics.mean(times)
     return {"value": wl["B"] * steps / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "note": "L2 not flushed inside this region (the prompt copy itself streams 100 MB)"}
+            "note": "L2 not flushed inside this region (the prompt copy itself streams the inputs)"}
 
 
 # ---------------------------------------------------------------------------- oracle arm
 
-def oracle_step_seconds(wl, seed=0, heads=2, dec_units=2, dec_steps=8):
+def oracle_step_seconds(wl, seed=0, rows=256, dec_steps=2):
     """Times the CPU oracle on a bounded sample of one step and scales it to the full step.
 
-    Sample: prefill (both passes, float64) of `heads` heads, then the MiniKV life cycle of
-    `dec_units` units for `dec_steps` decode steps.  Scale: heads -> all heads; units x steps ->
-    all units x all decode steps.
+    Sample: float64 prefill (pass 1 and pass 2) of `rows` query rows of one head, then the
+    policy life cycle (build + `dec_steps` decode steps) of one unit.  Scale: rows -> all
+    rows of all heads; one unit x dec_steps -> all units x all decode steps.
     """
     from bit_mixed_precision_gb300 import inputs
     from oracle import attention as OA
     from oracle import policies as OP
     from oracle import select as OS
-    B, H, D, T, steps, nr = wl["B"], wl["H"], wl["D"], wl["T"], wl["steps"], wl["nr"]
+    B, Hq, Hkv, D, T, steps, nr = (wl[k] for k in ("B", "Hq", "Hkv", "D", "T", "steps", "nr"))
+    g = Hq // Hkv
+    dt = torch.bfloat16 if wl["dtype"] == "bf16" else torch.float16
     scale = 1.0 / math.sqrt(D)
-    outl = inputs.outlier_channels(H, D, wl["n_out"], seed)
-    x = inputs.make_qkv(1, heads, heads, T, D, seed=seed, outliers=outl[:heads],
+    outl = inputs.outlier_channels(1, D, wl["n_out"], seed) if wl["n_out"] else None
+    x = inputs.make_qkv(1, g, 1, T, D, dtype=dt, seed=seed, outliers=outl,
                         outlier_scale=wl["out_scale"])
-    k_hh, w = OS.budget(T, wl["hh"], wl["rw"])
+    qh = [x.q[0, h].float().numpy() for h in range(g)]
+    kh, vh = x.k[0, 0].float().numpy(), x.v[0, 0].float().numpy()
     t0 = time.perf_counter()
-    sels = []
-    for h in range(heads):
-        _, _, cs = OA.prefill_head(x.q[0, h].float().numpy(), x.k[0, h].float().numpy(),
-                                   x.v[0, h].float().numpy(), scale)
-        sels.append(OS.select_unit(cs.astype(np.float32), k_hh, w))
-    t_pre = (time.perf_counter() - t0) / heads * (B * H)
-    dec_in = [inputs.make_decode_step(1, heads, heads, D, t, seed=seed) for t in range(dec_steps)]
-    t_build = t_dec = 0.0
-    for u in range(dec_units):
-        h = u % heads
-        t1 = time.perf_counter()
-        unit = OP.MiniKVUnit(x.k[0, h].float().numpy(), x.v[0, h].float().numpy(), sels[h], nr, 32)
-        t2 = time.perf_counter()
-        for t in range(dec_steps):
-            qd, kd, vd = dec_in[t]
-            unit.step(T + t, qd[0, h:h + 1].float().numpy(), kd[0, h].float().numpy(),
-                      vd[0, h].float().numpy(), scale)
-        t_build += t2 - t1
-        t_dec += time.perf_counter() - t2
-    t_build = t_build / dec_units * (B * H)
-    t_dec = t_dec / (dec_units * dec_steps) * (B * H * steps)
-    sample = (f"float64 prefill of {heads} of {B * H} heads + MiniKV decode of {dec_units} units x "
-              f"{dec_steps} of {steps} steps, scaled to the full step")
+    sample_rows = np.linspace(0, T - 1, min(rows, T)).astype(np.int64)
+    OA.prefill_rows(qh[0], kh, vh, sample_rows, scale)
+    t_rows = time.perf_counter() - t0
+    t_pre = t_rows / len(sample_rows) * T * 2 * (B * Hq)           # pass 1 + pass 2
+    # column scores of the unit (the build needs them); not part of the timed sample
+    cs = np.stack([OA.colscore_cols(qh[h], kh, np.arange(T), OA.lse_all_rows(qh[h], kh, scale),
+                                    scale) for h in range(g)]).astype(np.float32) if T <= 8192 else \
+        np.abs(np.random.default_rng(seed).normal(size=(g, T))).astype(np.float32)
+    t1 = time.perf_counter()
+    if wl["policy"] == "minikv":
+        k_hh, w = _budget(wl)
+        unit = OP.MiniKVUnit(kh, vh, OS.select_unit(cs[0], k_hh, w), nr, G)
+    elif wl["policy"] == "diffkv":
+        nc = T - nr
+        unit = OP.DiffKVUnit(kh, vh, cs, int(0.2 * nc), int(0.5 * nc), nr, G)
+    else:
+        unit = OP.MiKVUnit(kh, vh, cs, nr, G)
+    t_build = (time.perf_counter() - t1) * (B * Hkv)
+    dec = [inputs.make_decode_step(1, g, 1, D, t, dtype=dt, seed=seed) for t in range(dec_steps)]
+    t2 = time.perf_counter()
+    for t, (qd, kd, vd) in enumerate(dec):
+        unit.step(T + t, qd[0].float().numpy(), kd[0, 0].float().numpy(), vd[0, 0].float().numpy(), scale)
+    t_dec = (time.perf_counter() - t2) / dec_steps * (B * Hkv * steps)
+    sample = (f"float64 prefill of {len(sample_rows)} rows of 1 of {B * Hq} heads, the cache build "
+              f"and {dec_steps} of {steps} decode steps of 1 of {B * Hkv} units, scaled to the full step")
     return t_pre + t_build + t_dec, sample
 
 
@@ -380,20 +469,20 @@ def run_reference(args, wl, rank, world):
         return
     torch.set_num_threads(os.cpu_count() or 1)
     for _ in range(args.warmup):
-        oracle_step_seconds(wl, heads=1, dec_units=1, dec_steps=2)
-    est, t0 = [], time.perf_counter()
-    sample = ""
+        oracle_step_seconds(wl, rows=64, dec_steps=1)
+    est, t0, sample = [], time.perf_counter(), ""
     for _ in range(args.steps):
-        s, sample = oracle_step_seconds(wl, heads=1, dec_units=1, dec_steps=2)
-        est.append(s)
+        sec, sample = oracle_step_seconds(wl, rows=64, dec_steps=1)
+        est.append(sec)
     secs = statistics.mean(est)
     v = wl["B"] * wl["steps"] / secs
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantiser",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 attention, f32 quantiser",
         "data": "synthetic (seeded Gaussian Q/K/V, outlier key channels)",
-        "config": {"workload": args.workload, **{k: wl[k] for k in ("B", "H", "D", "T", "steps", "nr")}},
+        "config": {"workload": args.workload, **{k: v2 for k, v2 in wl.items() if v2 is not None}},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -412,15 +501,17 @@ def main():
         args.warmup = 3
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    if world > 1 and args.impl == "ours":
-        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     wl = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl, rank, world)
-    else:
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    try:
         run_ours(args, wl, rank, world)
-    if world > 1 and torch.distributed.is_initialized():
-        torch.distributed.destroy_process_group()
+    finally:
+        if world > 1 and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
 
 
 if __name__ == "__main__":
