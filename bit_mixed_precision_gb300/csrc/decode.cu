@@ -31,8 +31,9 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunk = 128;      // packed tokens per work item: one 32-token group per warp
-constexpr int kResChunk = 32;    // residual tokens per work item (full-precision rows are large)
+constexpr int kSub = 128;        // packed tokens per staged sub-chunk: one 32-token group per warp
+constexpr int kChunk = 4 * kSub; // packed tokens per CTA, streamed through two staging buffers
+constexpr int kResChunk = 32;    // residual tokens per CTA (full-precision rows are large)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -137,8 +138,7 @@ struct Smem {
     float wo[kWarps][NG][D];
     float lg[kWarps][NG][32];            // logits of the warp's current group
     unsigned long long bar[2];           // one staging mbarrier per buffer
-    int item_n[2], item_tier[2], item_chunk[2];
-    int last;
+    int n_total, last;
 };
 
 // Online-softmax state of one warp for NG heads; o holds the lane's share.
@@ -522,23 +522,46 @@ __device__ void warp_residual(const DecodeArgs& a, Smem<NG, D>& sm, const uint16
     }
 }
 
+// A chunk of up to kChunk tokens of one tier, streamed in kSub-token
+// sub-chunks through the two staging buffers: sub-chunk k + 2 is requested
+// as soon as sub-chunk k has been consumed.  Warp w takes the w-th 32-token
+// group of every sub-chunk; its online-softmax state spans the sub-chunks.
 template <int KB, int KAX, int VB, int D, int NG>
-__device__ void warp_tier(const DecodeArgs& a, Smem<NG, D>& sm, const View& v, int n, float* lg_out) {
+__device__ void warp_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& t, size_t unit,
+                          int j0, int n_total, uint8_t* stage_base, float* lg_out) {
     constexpr int cpw = 32 / VB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nsub = (n_total + kSub - 1) / kSub;
     WarpAcc<NG, cpw> acc;
     acc_init(acc);
-    for (int gi = warp; gi * 32 < n; gi += kWarps) {
-        const int tl = gi * 32;
-        const int nt = min(32, n - tl);
-        float lg[NG];
-        if (KAX == KVQ_AXIS_CHANNEL)
-            logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
-        else
-            logits_token<KB, D, NG>(v, tl, sm, a.G, lg);
-        group_softmax(acc, lg, nt, lg_out ? lg_out + tl : nullptr, a.slots);
-        values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
+    bool ok = true;
+    for (int sub = 0; sub < nsub; ++sub) {
+        const int buf = sub & 1;
+        uint8_t* stage = stage_base + (size_t)buf * a.stage_bytes;
+        const int n = min(kSub, n_total - sub * kSub);
+        ok = ok && __syncthreads_and(mbar_wait(smem_u32(&sm.bar[buf]), (sub >> 1) & 1, nullptr));
+        if (ok) {
+            const View v = tier_view(t, (n + 31) & ~31, D, a.G, stage);
+            const int tl = warp * 32;
+            if (tl < n) {
+                const int nt = min(32, n - tl);
+                float lg[NG];
+                if (KAX == KVQ_AXIS_CHANNEL)
+                    logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
+                else
+                    logits_token<KB, D, NG>(v, tl, sm, a.G, lg);
+                group_softmax(acc, lg, nt, lg_out ? lg_out + sub * kSub + tl : nullptr, a.slots);
+                values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
+            }
+        }
+        __syncthreads();                       // buffer consumed by every warp
+        if (threadIdx.x == 0 && sub + 2 < nsub) {
+            const int n2 = min(kSub, n_total - (sub + 2) * kSub);
+            stage_tier(t, unit, j0 + (sub + 2) * kSub, (n2 + 31) & ~31, D, a.G, stage,
+                       smem_u32(&sm.bar[buf]));
+        }
     }
+    if (!ok && threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
     if (lane == 0) {
 #pragma unroll
         for (int h = 0; h < NG; ++h) {
@@ -550,246 +573,230 @@ __device__ void warp_tier(const DecodeArgs& a, Smem<NG, D>& sm, const View& v, i
 }
 
 template <int NG, int D>
-__device__ bool dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& t, const View& v,
-                              int n, float* lg_out) {
+__device__ bool dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& t, size_t unit,
+                              int j0, int n, uint8_t* stage, float* lg_out) {
     const int kb = t.k_bits, vb = t.v_bits, ax = t.k_axis;
-    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, v, n, lg_out); return true; }
+    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
     if (D == 128) {
-        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { warp_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, v, n, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { warp_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, v, n, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { warp_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, v, n, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, v, n, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { warp_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { warp_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { warp_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
     }
     return false;
 }
 
-// Work item = (unit, chunk).  Thread 0 requests the bytes of an item into a
-// staging buffer; an item without tokens just completes its barrier phase.
-__device__ void issue_item(const DecodeArgs& a, int item, int buf, uint8_t* stage, uint32_t bar,
-                           int* item_n, int* item_tier, int* item_chunk, int D) {
-    const int TC = a.total_chunks;
-    const size_t unit = (size_t)(item / TC);
-    int chunk = item % TC, tier = -1;
-    for (int t = 0; t < a.n_tiers; ++t) {
-        if (chunk < a.tier[t].chunks) { tier = t; break; }
-        chunk -= a.tier[t].chunks;
-    }
-    int n = 0;
-    if (tier >= 0) {
-        const TierArgs& t = a.tier[tier];
-        const int raw = t.count[unit];
-        if (raw > t.cap || raw < 0) atomicOr(&g_status_decode, kDevCheck);
-        const int j0 = chunk * kChunk;
-        n = min(kChunk, min(max(raw, 0), t.cap) - j0);
-        if (n > 0) stage_tier(t, unit, j0, (n + 31) & ~31, D, a.G, stage, bar);
-    } else {
-        const int cap = a.res_cap;
-        const int raw = a.res_len[unit];
-        const int len = min(max(raw, 0), cap - 1), start = a.res_start[unit];
-        if (raw != len || start < 0 || start >= cap) atomicOr(&g_status_decode, kDevCheck);
-        const int j0 = chunk * kResChunk;
-        n = min(kResChunk, len + 1 - j0);
-        if (n > 0 && start >= 0 && start < cap) stage_residual(a, unit, len, start, j0, n, D, stage, bar);
-        else n = 0;
-    }
-    if (n <= 0) mbar_arrive(bar);        // nothing to copy: complete the phase
-    item_n[buf] = max(n, 0);
-    item_tier[buf] = tier;
-    item_chunk[buf] = chunk;
-}
-
-// Persistent grid: each CTA walks work items with stride gridDim.x; the
-// bytes of the next item are in flight while the current one is computed.
+// Grid = (chunks of every tier and of the residual ring, units).
 template <int NG, int D>
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<NG, D>& sm = *reinterpret_cast<Smem<NG, D>*>(smem_raw);
     uint8_t* stage_base = smem_raw + ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127);
-    const int units = a.B * a.Hkv;
+    const size_t unit = blockIdx.y;
+    const int units = gridDim.y;
     const int TC = a.total_chunks;
-    const int total = units * TC;
+    const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
     const bool bf = a.bf16 != 0;
 
-    if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&sm.bar[0]), 1);
-        mbar_init(smem_u32(&sm.bar[1]), 1);
-        fence_mbar_init();
-        if ((int)blockIdx.x < total)
-            issue_item(a, blockIdx.x, 0, stage_base, smem_u32(&sm.bar[0]), sm.item_n, sm.item_tier,
-                       sm.item_chunk, D);
+    int chunk = blockIdx.x, tier = -1;
+    for (int t = 0; t < a.n_tiers; ++t) {
+        if (chunk < a.tier[t].chunks) { tier = t; break; }
+        chunk -= a.tier[t].chunks;
     }
-    int it = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
-        const int buf = it & 1;
-        uint8_t* stage = stage_base + (size_t)buf * a.stage_bytes;
-        const uint32_t bar = smem_u32(&sm.bar[buf]);
-        const size_t unit = (size_t)(item / TC);
-        const int x = item % TC;
-        const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
-        if (threadIdx.x == 0 && item + (int)gridDim.x < total)
-            issue_item(a, item + gridDim.x, buf ^ 1, stage_base + (size_t)(buf ^ 1) * a.stage_bytes,
-                       smem_u32(&sm.bar[buf ^ 1]), sm.item_n, sm.item_tier, sm.item_chunk, D);
-        for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
-            const int h = idx / D, c = idx % D;
-            sm.q[h][c] = ldf(a.q, ((size_t)b * a.Hq + (size_t)hkv * NG + h) * D + c, bf) * a.scale_log2;
+    // thread 0 requests the first bytes before anything else
+    if (threadIdx.x == 0) {
+        const uint32_t b0 = smem_u32(&sm.bar[0]), b1 = smem_u32(&sm.bar[1]);
+        mbar_init(b0, 1);
+        mbar_init(b1, 1);
+        fence_mbar_init();
+        int n = 0;
+        if (tier >= 0) {
+            const TierArgs& t = a.tier[tier];
+            const int raw = t.count[unit];
+            if (raw > t.cap || raw < 0) atomicOr(&g_status_decode, kDevCheck);
+            const int j0 = chunk * kChunk;
+            n = min(kChunk, min(max(raw, 0), t.cap) - j0);
+            if (n > 0) {
+                const int n0 = min(kSub, n);
+                stage_tier(t, unit, j0, (n0 + 31) & ~31, D, a.G, stage_base, b0);
+                if (n > kSub) {
+                    const int n1 = min(kSub, n - kSub);
+                    stage_tier(t, unit, j0 + kSub, (n1 + 31) & ~31, D, a.G, stage_base + a.stage_bytes, b1);
+                }
+            }
+        } else {
+            const int cap = a.res_cap;
+            const int raw = a.res_len[unit];
+            const int len = min(max(raw, 0), cap - 1), start = a.res_start[unit];
+            if (raw != len || start < 0 || start >= cap) atomicOr(&g_status_decode, kDevCheck);
+            const int j0 = chunk * kResChunk;
+            n = min(kResChunk, len + 1 - j0);
+            if (n > 0 && start >= 0 && start < cap) stage_residual(a, unit, len, start, j0, n, D, stage_base, b0);
+            else n = 0;
         }
-        for (int idx = threadIdx.x; idx < kWarps * NG; idx += blockDim.x) {
-            sm.wm[idx / NG][idx % NG] = kNegInf;
-            sm.wl[idx / NG][idx % NG] = 0.0f;
-        }
-        for (int idx = threadIdx.x; idx < kWarps * NG * D; idx += blockDim.x) (&sm.wo[0][0][0])[idx] = 0.0f;
-        __syncthreads();
-        const int n = sm.item_n[buf], tier = sm.item_tier[buf], chunk = sm.item_chunk[buf];
-        float* lg_unit = a.logits ? a.logits + unit * NG * (size_t)a.slots : nullptr;
-        const bool ok = __syncthreads_and(mbar_wait(bar, (it >> 1) & 1, nullptr));
-        if (!ok) {
-            if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
-        } else if (n > 0) {
-            if (tier >= 0) {
-                const TierArgs& t = a.tier[tier];
-                const int j0 = chunk * kChunk;
-                const View v = tier_view(t, (n + 31) & ~31, D, a.G, stage);
-                float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
-                if (!dispatch_tier<NG, D>(a, sm, t, v, n, lg) && threadIdx.x == 0)
-                    atomicOr(&g_status_decode, kDevCheck);
+        sm.n_total = max(n, 0);
+    }
+    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx % D;
+        sm.q[h][c] = ldf(a.q, ((size_t)b * a.Hq + (size_t)hkv * NG + h) * D + c, bf) * a.scale_log2;
+    }
+    for (int idx = threadIdx.x; idx < kWarps * NG; idx += blockDim.x) {
+        sm.wm[idx / NG][idx % NG] = kNegInf;
+        sm.wl[idx / NG][idx % NG] = 0.0f;
+    }
+    for (int idx = threadIdx.x; idx < kWarps * NG * D; idx += blockDim.x) (&sm.wo[0][0][0])[idx] = 0.0f;
+    __syncthreads();
+
+    float* lg_unit = a.logits ? a.logits + unit * NG * (size_t)a.slots : nullptr;
+    const int n = sm.n_total;
+    if (n > 0) {
+        if (tier >= 0) {
+            const TierArgs& t = a.tier[tier];
+            const int j0 = chunk * kChunk;
+            float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
+            if (!dispatch_tier<NG, D>(a, sm, t, unit, j0, n, stage_base, lg) && threadIdx.x == 0)
+                atomicOr(&g_status_decode, kDevCheck);
+        } else {
+            const int j0 = chunk * kResChunk;
+            const bool ok = __syncthreads_and(mbar_wait(smem_u32(&sm.bar[0]), 0, nullptr));
+            if (!ok) {
+                if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
             } else {
-                const int j0 = chunk * kResChunk;
-                const uint16_t* rk = reinterpret_cast<const uint16_t*>(stage);
-                const uint16_t* rv = reinterpret_cast<const uint16_t*>(stage + a16((uint32_t)n * D * 2));
+                const uint16_t* rk = reinterpret_cast<const uint16_t*>(stage_base);
+                const uint16_t* rv = reinterpret_cast<const uint16_t*>(stage_base + a16((uint32_t)n * D * 2));
                 float* lg = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 : nullptr;
                 warp_residual<NG, D>(a, sm, rk, rv, n, lg);
             }
         }
-        if (tier < 0 && chunk == 0) {
-            // the new token joins the ring; no item reads this slot in this step
-            const int cap = a.res_cap;
-            const int len = min(max(a.res_len[unit], 0), cap - 1);
-            const int start = min(max(a.res_start[unit], 0), cap - 1);
-            const size_t slot = unit * (size_t)cap + (start + len) % cap;
-            for (int c = threadIdx.x; c < D; c += blockDim.x) {
-                stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
-                stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
-            }
-            if (threadIdx.x == 0) a.res_token_id[slot] = a.seq_len[b];
+    }
+    if (tier < 0 && chunk == 0) {
+        // the new token joins the ring; no CTA reads this slot in this step
+        const int cap = a.res_cap;
+        const int len = min(max(a.res_len[unit], 0), cap - 1);
+        const int start = min(max(a.res_start[unit], 0), cap - 1);
+        const size_t slot = unit * (size_t)cap + (start + len) % cap;
+        for (int c = threadIdx.x; c < D; c += blockDim.x) {
+            stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
+            stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
         }
-        __syncthreads();
+        if (threadIdx.x == 0) a.res_token_id[slot] = a.seq_len[b];
+    }
+    __syncthreads();
 
-        // ---- item partial: merge the four warps
-        float* part_out = a.part + (unit * NG * TC + x) * (size_t)(D + 2);
-        for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
-            const int h = idx / D, c = idx % D;
-            float M = kNegInf;
+    // ---- chunk partial: merge the four warps
+    float* part_out = a.part + (unit * NG * TC + blockIdx.x) * (size_t)(D + 2);
+    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx % D;
+        float M = kNegInf;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
-            float L = 0.0f, O = 0.0f;
-            if (M != kNegInf) {
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+        float L = 0.0f, O = 0.0f;
+        if (M != kNegInf) {
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float f = sm.wm[w][h] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][h] - M);
-                    L = fmaf(sm.wl[w][h], f, L);
-                    O = fmaf(sm.wo[w][h][c], f, O);
-                }
-            }
-            float* po = part_out + (size_t)h * TC * (D + 2);
-            po[2 + c] = O;
-            if (c == 0) {
-                po[0] = M;
-                po[1] = L;
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = sm.wm[w][h] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][h] - M);
+                L = fmaf(sm.wl[w][h], f, L);
+                O = fmaf(sm.wo[w][h][c], f, O);
             }
         }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t prev = atomicAdd(&a.counters[unit], 1u);
-            sm.last = (prev == (uint32_t)TC - 1u) ? 1 : 0;
+        float* po = part_out + (size_t)h * TC * (D + 2);
+        po[2 + c] = O;
+        if (c == 0) {
+            po[0] = M;
+            po[1] = L;
         }
-        __syncthreads();
-        if (sm.last) {
-            __threadfence();
-            const float* pu = a.part + unit * NG * TC * (size_t)(D + 2);
-            // chunk maxima and sums, all loads in flight together (scratch = this item's buffer)
-            float* cm = reinterpret_cast<float*>(stage);      // [NG][TC]
-            float* cw = cm + NG * TC;                          // [NG][TC]
-            for (int idx = threadIdx.x; idx < NG * TC; idx += blockDim.x) {
-                const float* ph = pu + (size_t)idx * (D + 2);
-                const float l = __ldcg(ph + 1);
-                cm[idx] = l > 0.0f ? __ldcg(ph) : kNegInf;
-                cw[idx] = l;
-            }
-            __syncthreads();
-            if (threadIdx.x < NG) {
-                const int h = threadIdx.x;
-                float M = kNegInf;
-                for (int y = 0; y < TC; ++y) M = fmaxf(M, cm[h * TC + y]);
-                float L = 0.0f;
-                for (int y = 0; y < TC; ++y) {
-                    const float wgt = cm[h * TC + y] == kNegInf ? 0.0f : ex2_approx(cm[h * TC + y] - M);
-                    L = fmaf(cw[h * TC + y], wgt, L);
-                    cw[h * TC + y] = wgt;
-                }
-                sm.wl[0][h] = L;
-                sm.wm[0][h] = M + __log2f(L);          // base-2 lse
-                if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
-            }
-            __syncthreads();
-            for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
-                const int h = idx / D, c = idx % D;
-                const float* ph = pu + (size_t)h * TC * (D + 2) + 2 + c;
-                float acc = 0.0f;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(&a.counters[unit], 1u);
+        sm.last = (prev == (uint32_t)TC - 1u) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!sm.last) return;
+    __threadfence();
+
+    const float* pu = a.part + unit * NG * TC * (size_t)(D + 2);
+    // chunk maxima and sums, all loads in flight together (scratch = the staging buffers)
+    float* cm = reinterpret_cast<float*>(stage_base);      // [NG][TC]
+    float* cw = cm + NG * TC;                               // [NG][TC]
+    for (int idx = threadIdx.x; idx < NG * TC; idx += blockDim.x) {
+        const float* ph = pu + (size_t)idx * (D + 2);
+        const float l = __ldcg(ph + 1);
+        cm[idx] = l > 0.0f ? __ldcg(ph) : kNegInf;
+        cw[idx] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x < NG) {
+        const int h = threadIdx.x;
+        float M = kNegInf;
+        for (int y = 0; y < TC; ++y) M = fmaxf(M, cm[h * TC + y]);
+        float L = 0.0f;
+        for (int y = 0; y < TC; ++y) {
+            const float wgt = cm[h * TC + y] == kNegInf ? 0.0f : ex2_approx(cm[h * TC + y] - M);
+            L = fmaf(cw[h * TC + y], wgt, L);
+            cw[h * TC + y] = wgt;
+        }
+        sm.wl[0][h] = L;
+        sm.wm[0][h] = M + __log2f(L);          // base-2 lse
+        if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx % D;
+        const float* ph = pu + (size_t)h * TC * (D + 2) + 2 + c;
+        float acc = 0.0f;
 #pragma unroll 8
-                for (int y = 0; y < TC; ++y) acc = fmaf(__ldcg(ph + (size_t)y * (D + 2)), cw[h * TC + y], acc);
-                stf(a.o, ((size_t)b * a.Hq + hkv * NG + h) * D + c, acc / sm.wl[0][h], bf);
-            }
-            const int cap = a.res_cap;
-            const int len = min(max(a.res_len[unit], 0), cap - 1);
-            const int start = min(max(a.res_start[unit], 0), cap - 1);
-            const float* lse2 = sm.wm[0];
-            if (a.policy == KVQ_POLICY_MIKV && lg_unit) {
-                float* cs = a.cum_score + unit * (size_t)a.score_cap;
-                for (int t = 0; t < a.n_tiers; ++t) {
-                    const TierArgs& ti = a.tier[t];
-                    const int cnt = min(max(ti.count[unit], 0), ti.cap);
-                    for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
-                        float p = 0.0f;
+        for (int y = 0; y < TC; ++y) acc = fmaf(__ldcg(ph + (size_t)y * (D + 2)), cw[h * TC + y], acc);
+        stf(a.o, ((size_t)b * a.Hq + hkv * NG + h) * D + c, acc / sm.wl[0][h], bf);
+    }
+    const int cap = a.res_cap;
+    const int len = min(max(a.res_len[unit], 0), cap - 1);
+    const int start = min(max(a.res_start[unit], 0), cap - 1);
+    const float* lse2 = sm.wm[0];
+    if (a.policy == KVQ_POLICY_MIKV && lg_unit) {
+        float* cs = a.cum_score + unit * (size_t)a.score_cap;
+        for (int t = 0; t < a.n_tiers; ++t) {
+            const TierArgs& ti = a.tier[t];
+            const int cnt = min(max(ti.count[unit], 0), ti.cap);
+            for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
+                float p = 0.0f;
 #pragma unroll
-                        for (int h = 0; h < NG; ++h)
-                            p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ti.slot_base + j) - lse2[h]);
-                        const int id = ti.token_id[unit * (size_t)ti.cap + j];
-                        if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
-                        else atomicOr(&g_status_decode, kDevCheck);
-                    }
-                }
-                for (int li = threadIdx.x; li <= len; li += blockDim.x) {
-                    float p = 0.0f;
-#pragma unroll
-                    for (int h = 0; h < NG; ++h)
-                        p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-                    const int id = li < len ? a.res_token_id[unit * (size_t)cap + (start + li) % cap] : a.seq_len[b];
-                    if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
-                    else cs[id] = li < len ? __fadd_rn(cs[id], p) : p;
-                }
-            } else if (a.policy == KVQ_POLICY_DIFFKV && lg_unit) {
-                for (int idx = threadIdx.x; idx < (len + 1) * NG; idx += blockDim.x) {
-                    const int li = idx / NG, h = idx % NG;
-                    const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-                    float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (start + li) % cap;
-                    *wa = li < len ? __fadd_rn(*wa, p) : p;
-                }
-            }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                a.res_len[unit] = len + 1;
-                a.counters[unit] = 0u;
-                __threadfence();
-                const uint32_t prev = atomicAdd(&a.counters[units], 1u);
-                if (prev == (uint32_t)units - 1u) {
-                    __threadfence();
-                    for (int bb = 0; bb < a.B; ++bb) a.seq_len[bb] += 1;
-                    a.counters[units] = 0u;
-                }
+                for (int h = 0; h < NG; ++h)
+                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ti.slot_base + j) - lse2[h]);
+                const int id = ti.token_id[unit * (size_t)ti.cap + j];
+                if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
+                else atomicOr(&g_status_decode, kDevCheck);
             }
         }
-        __syncthreads();
+        for (int li = threadIdx.x; li <= len; li += blockDim.x) {
+            float p = 0.0f;
+#pragma unroll
+            for (int h = 0; h < NG; ++h)
+                p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+            const int id = li < len ? a.res_token_id[unit * (size_t)cap + (start + li) % cap] : a.seq_len[b];
+            if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
+            else cs[id] = li < len ? __fadd_rn(cs[id], p) : p;
+        }
+    } else if (a.policy == KVQ_POLICY_DIFFKV && lg_unit) {
+        for (int idx = threadIdx.x; idx < (len + 1) * NG; idx += blockDim.x) {
+            const int li = idx / NG, h = idx % NG;
+            const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+            float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (start + li) % cap;
+            *wa = li < len ? __fadd_rn(*wa, p) : p;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        a.res_len[unit] = len + 1;
+        a.counters[unit] = 0u;
+        __threadfence();
+        const uint32_t prev = atomicAdd(&a.counters[units], 1u);
+        if (prev == (uint32_t)units - 1u) {
+            __threadfence();
+            for (int bb = 0; bb < a.B; ++bb) a.seq_len[bb] += 1;
+            a.counters[units] = 0u;
+        }
     }
 }
 
@@ -827,30 +834,22 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     uint32_t stage = a16((uint32_t)kResChunk * D * 2) * 2u;
     for (int t = 0; t < c.n_tiers; ++t)
         stage = std::max(stage, tier_stage_sizes(c.tier[t].k_axis, c.tier[t].k_bits, c.tier[t].v_bits,
-                                                 kChunk, D, c.G).total());
-    stage = std::max(stage, (uint32_t)(2 * NG * a.total_chunks * sizeof(float)));   // merge scratch
+                                                 kSub, D, c.G).total());
     stage = (stage + 127u) & ~127u;
     a.stage_bytes = stage;
-    const size_t sh = ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127) + 2 * (size_t)stage;
+    // the merge reuses both buffers as scratch
+    const uint32_t scratch = (uint32_t)(2 * NG * a.total_chunks * sizeof(float));
+    const size_t bufs = std::max((size_t)2 * stage, (size_t)scratch);
+    const size_t sh = ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127) + bufs;
     static size_t attr = 0;
-    static int per_sm = 0, sms = 0;
-    static size_t occ_for = 0;
     if (sh > 48 * 1024 && sh > attr) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh);
         if (e != cudaSuccess) return e;
         attr = sh;
     }
-    if (occ_for != sh) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<NG, D>, kThreads, sh);
-        occ_for = sh;
-    }
-    const long total = (long)units * a.total_chunks;
-    const long grid = std::max(1L, std::min(total, (long)std::max(per_sm, 1) * std::max(sms, 1)));
-    decode_kernel<NG, D><<<(unsigned)grid, kThreads, sh, s>>>(a);
+    dim3 grid(a.total_chunks, units);
+    decode_kernel<NG, D><<<grid, kThreads, sh, s>>>(a);
     return cudaGetLastError();
 }
 
