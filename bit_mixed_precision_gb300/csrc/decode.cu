@@ -32,7 +32,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSub = 128;        // packed tokens per staged sub-chunk: one 32-token group per warp
-constexpr int kChunk = 4 * kSub; // packed tokens per CTA, streamed through two staging buffers
+constexpr int kMaxSubs = 4;      // sub-chunks per CTA at most, streamed through two staging buffers
 constexpr int kResChunk = 32;    // residual tokens per CTA (full-precision rows are large)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -48,7 +48,7 @@ struct TierArgs {
     const uint16_t* v_zero;
     const int32_t* token_id;
     const int32_t* count;
-    int chunks;                 // ceil(cap / kChunk)
+    int chunks;                 // ceil(cap / chunk_tokens)
     int slot_base;              // offset of this tier in the logits row
 };
 
@@ -77,6 +77,7 @@ struct DecodeArgs {
     float* logits;              // [unit][g][slots] or null
     uint32_t* counters;         // [units + 1]
     uint32_t stage_bytes;       // one staging buffer (two per CTA)
+    int chunk_tokens;           // packed tokens per CTA: kSub * (1 .. kMaxSubs)
 };
 
 __device__ __forceinline__ float ldf(const void* p, size_t i, bool bf16) {
@@ -522,7 +523,7 @@ __device__ void warp_residual(const DecodeArgs& a, Smem<NG, D>& sm, const uint16
     }
 }
 
-// A chunk of up to kChunk tokens of one tier, streamed in kSub-token
+// A chunk of up to chunk_tokens tokens of one tier, streamed in kSub-token
 // sub-chunks through the two staging buffers: sub-chunk k + 2 is requested
 // as soon as sub-chunk k has been consumed.  Warp w takes the w-th 32-token
 // group of every sub-chunk; its online-softmax state spans the sub-chunks.
@@ -614,8 +615,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
             const TierArgs& t = a.tier[tier];
             const int raw = t.count[unit];
             if (raw > t.cap || raw < 0) atomicOr(&g_status_decode, kDevCheck);
-            const int j0 = chunk * kChunk;
-            n = min(kChunk, min(max(raw, 0), t.cap) - j0);
+            const int j0 = chunk * a.chunk_tokens;
+            n = min(a.chunk_tokens, min(max(raw, 0), t.cap) - j0);
             if (n > 0) {
                 const int n0 = min(kSub, n);
                 stage_tier(t, unit, j0, (n0 + 31) & ~31, D, a.G, stage_base, b0);
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     if (n > 0) {
         if (tier >= 0) {
             const TierArgs& t = a.tier[tier];
-            const int j0 = chunk * kChunk;
+            const int j0 = chunk * a.chunk_tokens;
             float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
             if (!dispatch_tier<NG, D>(a, sm, t, unit, j0, n, stage_base, lg) && threadIdx.x == 0)
                 atomicOr(&g_status_decode, kDevCheck);
@@ -807,12 +808,23 @@ struct WsLayout {
     size_t part, logits, counters, total;
 };
 
+// Packed tokens per CTA: as many sub-chunks (up to kMaxSubs) as keeps about
+// six CTAs' worth of sub-chunks per SM; small caches get one sub-chunk per
+// CTA so that every SM has work.
+int chunk_tokens_for(const kvq_cache& c) {
+    long subs = 0;
+    for (int t = 0; t < c.n_tiers; ++t) subs += (long)c.B * c.Hkv * ((c.tier[t].cap + kSub - 1) / kSub);
+    const long per = (subs + 152L * 6 - 1) / (152L * 6);
+    return kSub * (int)std::max(1L, std::min((long)kMaxSubs, per));
+}
+
 WsLayout ws_layout(const kvq_cache& c) {
     WsLayout w{};
     const int units = c.B * c.Hkv, g = c.Hq / c.Hkv;
+    const int ct = chunk_tokens_for(c);
     int chunks = 0, slots = 0;
     for (int t = 0; t < c.n_tiers; ++t) {
-        chunks += (c.tier[t].cap + kChunk - 1) / kChunk;
+        chunks += (c.tier[t].cap + ct - 1) / ct;
         slots += c.tier[t].cap;
     }
     chunks += (c.res_cap + kResChunk - 1) / kResChunk;
@@ -876,6 +888,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.n_tiers = c.n_tiers;
     a.policy = c.policy;
     a.bf16 = c.dtype == KVQ_BF16 ? 1 : 0;
+    a.chunk_tokens = chunk_tokens_for(c);
     int slot = 0;
     for (int t = 0; t < c.n_tiers; ++t) {
         const kvq_tier& ct = c.tier[t];
@@ -892,7 +905,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
         ta.v_zero = ct.v_zero;
         ta.token_id = ct.token_id;
         ta.count = ct.count;
-        ta.chunks = (ct.cap + kChunk - 1) / kChunk;
+        ta.chunks = (ct.cap + a.chunk_tokens - 1) / a.chunk_tokens;
         ta.slot_base = slot;
         slot += ct.cap;
     }
