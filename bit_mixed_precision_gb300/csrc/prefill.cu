@@ -277,15 +277,29 @@ __global__ void __launch_bounds__(192, 1)
             }
 
             const int kbase = j * kTile;
-            float mx = -__int_as_float(0x7f800000);
+            // eight independent partial maxima keep the reduction off one long chain;
+            // only the diagonal tile and a tile past the end of the prompt need the mask
+            float mxp[8];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                float x = s[c] * scale_log2;
-                const int kidx = kbase + c;
-                if (kidx > i || kidx >= T_len) x = -__int_as_float(0x7f800000);
-                s[c] = x;
-                mx = fmaxf(mx, x);
+            for (int e = 0; e < 8; ++e) mxp[e] = -__int_as_float(0x7f800000);
+            if (j == qt || kbase + kTile > T_len) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    float x = s[c] * scale_log2;
+                    const int kidx = kbase + c;
+                    if (kidx > i || kidx >= T_len) x = -__int_as_float(0x7f800000);
+                    s[c] = x;
+                    mxp[c & 7] = fmaxf(mxp[c & 7], x);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    s[c] *= scale_log2;
+                    mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
+                }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             const float m_new = fmaxf(m_used, mx);
             const bool resc = m_new > m_used + kRescaleLog2;
             if (j >= 1) {
@@ -309,21 +323,23 @@ __global__ void __launch_bounds__(192, 1)
                 if (j >= 1) l *= ex2_approx(m_used - m_new);
                 m_used = m_new;
             }
-            float rs = 0.0f;
+            float rsp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rsp[e] = 0.0f;
 #pragma unroll
             for (int c8 = 0; c8 < 16; ++c8) {
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     p[e] = ex2_approx(s[c8 * 8 + e] - m_used);
-                    rs += p[e];
+                    rsp[e] += p[e];
                 }
                 const uint32_t off = (uint32_t)(c8 >> 3) * kHalfBytes + (uint32_t)r * 128u +
                                      ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
                 st_shared_v4(sP + off, Pack2<__half>::pack(p[0], p[1]), Pack2<__half>::pack(p[2], p[3]),
                              Pack2<__half>::pack(p[4], p[5]), Pack2<__half>::pack(p[6], p[7]));
             }
-            l += rs;
+            l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -482,14 +498,23 @@ __global__ void __launch_bounds__(192, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C_SFREE + buf));
             const float* ls = lse_s + buf * kTile;
-            float ts = 0.0f;
-            const int qbase = qt * kTile;
+            // eight independent partial sums; the causal mask only matters on the
+            // diagonal tile (later query tiles hold positions >= every key here)
+            float tsp[8];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float x = s[c] * scale_log2 - ls[c];
-                ts += (qbase + c >= j) ? ex2_approx(x) : 0.0f;
+            for (int e = 0; e < 8; ++e) tsp[e] = 0.0f;
+            const int qbase = qt * kTile;
+            if (it == 0) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const float x = fmaf(s[c], scale_log2, -ls[c]);
+                    tsp[c & 7] += (qbase + c >= j) ? ex2_approx(x) : 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) tsp[c & 7] += ex2_approx(fmaf(s[c], scale_log2, -ls[c]));
             }
-            acc += ts;
+            acc += ((tsp[0] + tsp[1]) + (tsp[2] + tsp[3])) + ((tsp[4] + tsp[5]) + (tsp[6] + tsp[7]));
         }
         if (!ok) give_up(abort_flag);
         if (ok && j < T_len) colscore[(size_t)bh * T_len + j] = acc;
