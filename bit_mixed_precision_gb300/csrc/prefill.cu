@@ -34,7 +34,9 @@ namespace {
 
 constexpr int kTile = 128;                 // rows per tile (queries or keys)
 constexpr uint32_t kHalfBytes = 128 * 128;       // one 128-row x 64-column 128B-swizzled half
-constexpr uint32_t kPBytes = 2 * kHalfBytes;     // P tile: 128 rows x 128 keys
+constexpr int kBN = 64;                          // keys per K/V tile of pass 1
+constexpr uint32_t kKVHalf = kBN * 128;          // one 64-row x 64-column swizzled half
+constexpr uint32_t kPBytes = 128 * kBN * 2;      // P tile of pass 1: 128 rows x 64 keys
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -42,13 +44,16 @@ constexpr float kRescaleLog2 = 8.0f;
 // Shared memory maps (offsets from a 1024-aligned base) for head dim D.
 template <int D> struct Layout {
     static constexpr uint32_t kTileBytes = kTile * D * 2;      // D/64 halves
-    // pass 1
+    static constexpr uint32_t kKVBytes = kBN * D * 2;          // pass-1 K or V tile, D/64 halves
+    // pass 1 (about 112 KB at D = 128: two CTAs per SM)
     static constexpr uint32_t P1_Q = 0;
     static constexpr uint32_t P1_K = P1_Q + kTileBytes;        // 2 stages
-    static constexpr uint32_t P1_V = P1_K + 2 * kTileBytes;    // 2 stages
-    static constexpr uint32_t P1_P = P1_V + 2 * kTileBytes;
+    static constexpr uint32_t P1_V = P1_K + 2 * kKVBytes;      // 2 stages
+    static constexpr uint32_t P1_P = P1_V + 2 * kKVBytes;
     static constexpr uint32_t P1_BAR = P1_P + kPBytes;
-    static constexpr uint32_t P1_SMEM = P1_BAR + 256 + 1024;   // + barriers/flags + alignment slack
+    // no alignment slack: two CTAs must fit one SM, so the kernel requires (and
+    // checks) a 1024-aligned dynamic shared memory base
+    static constexpr uint32_t P1_SMEM = P1_BAR + 256;
     // pass 2
     static constexpr uint32_t P2_K = 0;
     static constexpr uint32_t P2_Q = P2_K + kTileBytes;        // 2 stages
@@ -96,30 +101,35 @@ __device__ __forceinline__ void give_up(volatile int* abort_flag) {
 
 // K-major operand (rows x 128 elements as two 128B-swizzled 64-column halves):
 // descriptor of the 16-element K slice kk (0..7).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-    return sdesc_sw128(tile + (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u, 16u,
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk, uint32_t half = kHalfBytes) {
+    return sdesc_sw128(tile + (uint32_t)(kk >> 2) * half + (uint32_t)(kk & 3) * 32u, 16u,
                        1024u);
 }
 
 // MN-major operand (128 K-rows of 128 N-elements, two 64-column halves):
 // descriptor of K rows 16*kk .. 16*kk+15.  LBO = stride between the N
 // halves, SBO = stride between groups of 8 K rows.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
-    return sdesc_sw128(tile + (uint32_t)kk * 16u * 128u, kHalfBytes, 1024u);
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk, uint32_t half = kHalfBytes) {
+    return sdesc_sw128(tile + (uint32_t)kk * 16u * 128u, half, 1024u);
 }
 
 template <typename T, int AB, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     prefill_pass1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, T* __restrict__ o,
                          float* __restrict__ lse, int T_len, int Hq, int Hkv, int n_qt,
                          float scale_log2) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (base - raw);
+    if (raw & 1023u) {                                  // layout assumption broken: do nothing
+        if (threadIdx.x == 0) atomicOr(&g_status_prefill, kDevCheck);
+        return;
+    }
+    const uint32_t base = raw;
+    uint8_t* gbase = smem_raw;
     using Lay = Layout<D>;
     constexpr uint32_t kTileBytes = Lay::kTileBytes;
+    constexpr uint32_t kKVBytes = Lay::kKVBytes;
     constexpr int kHalves = D / 64;
     const uint32_t sQ = base + Lay::P1_Q, sK = base + Lay::P1_K, sV = base + Lay::P1_V,
                    sP = base + Lay::P1_P;
@@ -133,7 +143,8 @@ __global__ void __launch_bounds__(192, 1)
     const int qt = n_qt - 1 - (int)blockIdx.y;
     const int b = bh / Hq, hq = bh % Hq;
     const int bhkv = b * Hkv + hq / (Hq / Hkv);
-    const int n_kv = qt + 1;
+    // 64-key tiles up to the diagonal, none wholly past the end of the prompt
+    const int n_kv = min(2 * (qt + 1), (T_len + kBN - 1) / kBN);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_Q), 1);
@@ -152,12 +163,12 @@ __global__ void __launch_bounds__(192, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 512);
+    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;
+    const uint32_t tO = tmem + 2 * kBN;                 // S buffers at columns 0 and 64
 
     if (warp == 4) {
         if (lane == 0) {
@@ -174,14 +185,14 @@ __global__ void __launch_bounds__(192, 1)
                     give_up(abort_flag);
                     break;
                 }
-                const uint32_t kdst = sK + (uint32_t)st * kTileBytes;
-                const uint32_t vdst = sV + (uint32_t)st * kTileBytes;
-                mbar_expect_tx(BAR(B_KF + st), kTileBytes);
+                const uint32_t kdst = sK + (uint32_t)st * kKVBytes;
+                const uint32_t vdst = sV + (uint32_t)st * kKVBytes;
+                mbar_expect_tx(BAR(B_KF + st), kKVBytes);
                 for (int hf = 0; hf < kHalves; ++hf)
-                    tma_load_3d(kdst + hf * kHalfBytes, &tk, 64 * hf, j * kTile, bhkv, BAR(B_KF + st));
-                mbar_expect_tx(BAR(B_VF + st), kTileBytes);
+                    tma_load_3d(kdst + hf * kKVHalf, &tk, 64 * hf, j * kBN, bhkv, BAR(B_KF + st));
+                mbar_expect_tx(BAR(B_VF + st), kKVBytes);
                 for (int hf = 0; hf < kHalves; ++hf)
-                    tma_load_3d(vdst + hf * kHalfBytes, &tv, 64 * hf, j * kTile, bhkv, BAR(B_VF + st));
+                    tma_load_3d(vdst + hf * kKVHalf, &tv, 64 * hf, j * kBN, bhkv, BAR(B_VF + st));
                 last[st] = j;
             }
             // every issued copy has landed before the CTA may exit
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            const uint32_t idS = idesc_f16(AB, 128, 128, 0);
+            const uint32_t idS = idesc_f16(AB, 128, kBN, 0);
             // P is always fp16; bf16 V tiles are converted to fp16 in smem first
             const uint32_t idPV = idesc_f16(0, 128, D, 1);
             bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
@@ -204,10 +215,10 @@ __global__ void __launch_bounds__(192, 1)
                 if (!mbar_wait(BAR((AB ? B_VC : B_VF) + (jj & 1)), (jj >> 1) & 1, abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t vt = sV + (uint32_t)(jj & 1) * kTileBytes;
+                const uint32_t vt = sV + (uint32_t)(jj & 1) * kKVBytes;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16(tO, kmajor_desc(sP, kk), mnmajor_desc(vt, kk), idPV,
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    tc_mma_f16(tO, kmajor_desc(sP, kk), mnmajor_desc(vt, kk, kKVHalf), idPV,
                                (jj > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(B_OD));
                 tc_commit(BAR(B_KVE + (jj & 1)));
@@ -221,11 +232,11 @@ __global__ void __launch_bounds__(192, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tS = tmem + (uint32_t)st * 128u;
-                const uint32_t kt = sK + (uint32_t)st * kTileBytes;
+                const uint32_t tS = tmem + (uint32_t)st * kBN;
+                const uint32_t kt = sK + (uint32_t)st * kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_f16(tS, kmajor_desc(sQ, kk), kmajor_desc(kt, kk), idS, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(tS, kmajor_desc(sQ, kk), kmajor_desc(kt, kk, kKVHalf), idS, kk > 0 ? 1u : 0u);
                 tc_commit(BAR(B_SF + st));
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
@@ -247,10 +258,10 @@ __global__ void __launch_bounds__(192, 1)
             const int sb = j & 1;
             if (!warp_wait(BAR(B_SF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            float s[128];
+            float s[kBN];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                tmem_ld32(tmem + lane_base + (uint32_t)sb * 128u + (uint32_t)c4 * 32u, s + c4 * 32);
+            for (int c4 = 0; c4 < kBN / 32; ++c4)
+                tmem_ld32(tmem + lane_base + (uint32_t)sb * kBN + (uint32_t)c4 * 32u, s + c4 * 32);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -258,9 +269,9 @@ __global__ void __launch_bounds__(192, 1)
             if (AB) {
                 // bf16 -> fp16 of this thread's share of the V tile (exact for |v| < 65504)
                 if (!warp_wait(BAR(B_VF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
-                uint4* vt = reinterpret_cast<uint4*>(gbase + Lay::P1_V + (uint32_t)sb * kTileBytes);
+                uint4* vt = reinterpret_cast<uint4*>(gbase + Lay::P1_V + (uint32_t)sb * kKVBytes);
 #pragma unroll 4
-                for (int c = r; c < (int)(kTileBytes / 16); c += 128) {
+                for (int c = r; c < (int)(kKVBytes / 16); c += 128) {
                     uint4 w = vt[c];
                     uint32_t* e = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
@@ -276,15 +287,15 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) mbar_arrive(BAR(B_VC + sb));
             }
 
-            const int kbase = j * kTile;
+            const int kbase = j * kBN;
             // eight independent partial maxima keep the reduction off one long chain;
             // only the diagonal tile and a tile past the end of the prompt need the mask
             float mxp[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mxp[e] = -__int_as_float(0x7f800000);
-            if (j == qt || kbase + kTile > T_len) {
+            if (kbase + kBN - 1 > qt * kTile || kbase + kBN > T_len) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
+                for (int c = 0; c < kBN; ++c) {
                     float x = s[c] * scale_log2;
                     const int kidx = kbase + c;
                     if (kidx > i || kidx >= T_len) x = -__int_as_float(0x7f800000);
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(192, 1)
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
+                for (int c = 0; c < kBN; ++c) {
                     s[c] *= scale_log2;
                     mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
                 }
@@ -327,7 +338,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) rsp[e] = 0.0f;
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
+            for (int c8 = 0; c8 < kBN / 8; ++c8) {
                 float p[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, 512);
+    if (warp == 5) tmem_dealloc(tmem, 256);
 }
 
 template <typename T, int AB, int D>
@@ -546,13 +557,13 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [rows = BH][T][D] 16-bit tensor, box 64 x 128 x 1, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, int dt, int BH, int T, int D) {
+// [rows = BH][T][D] 16-bit tensor, box 64 x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int dt, int BH, int T, int D, int box_rows = kTile) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, dt == KVQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                      3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -565,10 +576,10 @@ template <typename T, int AB, int D>
 kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int T_len,
                      float sm_scale, void* o, float* lse, float* colscore, cudaStream_t s) {
     using Lay = Layout<D>;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mk64, mv64;
     const int dt = AB == 0 ? KVQ_F16 : KVQ_BF16;
     if (!make_map(&mq, q, dt, B * Hq, T_len, D) || !make_map(&mk, k, dt, B * Hkv, T_len, D) ||
-        !make_map(&mv, v, dt, B * Hkv, T_len, D)) {
+        !make_map(&mk64, k, dt, B * Hkv, T_len, D, kBN) || !make_map(&mv64, v, dt, B * Hkv, T_len, D, kBN)) {
         set_error("prefill_attn_scores: tensor map encoding failed");
         return KVQ_ECUDA;
     }
@@ -583,7 +594,7 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
     const int n_t = (T_len + kTile - 1) / kTile;
     const float scale_log2 = sm_scale * kLog2e;
     dim3 g1(B * Hq, n_t);
-    prefill_pass1_kernel<T, AB, D><<<g1, 192, Lay::P1_SMEM, s>>>(mq, mk, mv, (T*)o, lse, T_len, Hq,
+    prefill_pass1_kernel<T, AB, D><<<g1, 192, Lay::P1_SMEM, s>>>(mq, mk64, mv64, (T*)o, lse, T_len, Hq,
                                                                   Hkv, n_t, scale_log2);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
