@@ -168,7 +168,7 @@ class Hot:
             self.kh = torch.full((B * Hkv,), self.k_hh, dtype=torch.int32, device=dev)
             self.idx = torch.empty((B, Hkv, self.n_sel), dtype=torch.int32, device=dev)
             self.nout = torch.empty((B * Hkv,), dtype=torch.int32, device=dev)
-            self.launches_per_step = 2 + 1 + 3 + 2 * steps
+            self.launches_per_step = 2 + 1 + 3 + steps       # the residual flush runs inside decode
         elif pol == "diffkv":
             f = inputs.dirichlet_fractions(B * Hkv, seed=seed)
             nc = T - nr
@@ -215,6 +215,10 @@ class Hot:
         qd, kd, vd = self.dec[t]
         self.kvq.decode_attn_qkv(qd, kd, vd, self.cache, self.scale, o=self.o_dec[t],
                                  lse=self.lse_dec[t], stream=s)
+
+    def has_tail(self):
+        """DiffKV / MiKV decide a token's tier after each step; MiniKV's flush is part of decode."""
+        return self.wl["policy"] != "minikv"
 
     def tail(self, t, s):
         self.kvq.requant_demote(self.cache, t + 1, stream=s)
@@ -276,10 +280,11 @@ def run_ours(args, wl, rank, world):
                 a.record(s)
                 hot.decode(t, s)
                 b.record(s)
-                hot.tail(t, s)
-                c.record(s)
                 ev.append(("decode", a, b))
-                ev.append(("tail", b, c))
+                if hot.has_tail():
+                    hot.tail(t, s)
+                    c.record(s)
+                    ev.append(("tail", b, c))
         return ev
 
     for _ in range(args.warmup):
@@ -394,7 +399,8 @@ def run_e2e(hot, s, args, wl):
                 for dst, src in zip(hot.dec[t], hdec[t]):
                     dst.copy_(src, non_blocking=True)
                 hot.decode(t, s)
-                hot.tail(t, s)
+                if hot.has_tail():
+                    hot.tail(t, s)
             ho.copy_(hot.o_dec, non_blocking=True)
             b.record(s)
         torch.cuda.synchronize()

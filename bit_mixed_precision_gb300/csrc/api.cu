@@ -182,7 +182,7 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
 }
 
 size_t kvq_decode_workspace_bytes(const kvq_cache* c) {
-    if (check_cache(c, "kvq_decode_workspace_bytes") != KVQ_OK) return 0;
+    if (check_cache(c, "kvq_decode_workspace_bytes") != KVQ_OK) return (size_t)-1;
     return kvq::decode_workspace_bytes(*c);
 }
 
@@ -195,9 +195,9 @@ kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, 
     KVQ_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16) && aligned(c->res_k, 16) && aligned(c->res_v, 16),
                 KVQ_EINVAL, "decode_attn_qkv: k_new, v_new and the residual ring must be 16-byte aligned");
     const size_t need = kvq::decode_workspace_bytes(*c);
-    KVQ_REQUIRE(ws && ws_bytes >= need, KVQ_EWORKSPACE,
+    KVQ_REQUIRE(need == 0 || (ws && ws_bytes >= need), KVQ_EWORKSPACE,
                 "decode_attn_qkv: workspace of %zu bytes needed, %zu given", need, ws_bytes);
-    KVQ_REQUIRE(aligned(ws, 256), KVQ_EINVAL, "decode_attn_qkv: workspace must be 256-byte aligned");
+    KVQ_REQUIRE(need == 0 || aligned(ws, 256), KVQ_EINVAL, "decode_attn_qkv: workspace must be 256-byte aligned");
     KVQ_REQUIRE(sm_scale > 0.0f, KVQ_EINVAL, "decode_attn_qkv: sm_scale must be positive");
     return cuda_status(kvq::launch_decode(q, k_new, v_new, *c, sm_scale, o, lse_out, ws,
                                           (cudaStream_t)stream),

@@ -3,19 +3,28 @@
 // FP16 GEMV paragraph: on-the-fly dequantisation; MiniKV verdict JSON
 // forward_implications: fused dequantisation kernels during decoding).
 //
-// One launch per step.  Grid = (token chunks of every tier and of the
-// residual ring, units).  A CTA first requests every byte of its chunk with
-// bulk asynchronous copies into shared memory (one mbarrier), then its
-// four warps take 32-token groups: keys -> base-2 logits for the g query
-// heads of the KV head, online softmax per warp, P.V with the codes turned
-// into floats by one rotate and one LOP3 each.  The CTA writes its partial
-// (max, sum, unnormalised output); the last CTA of a unit (atomic counter)
-// merges the partials, writes o and lse, adds this step's attention to the
-// policy scores (DiffKV: per ring slot and query head; MiKV: per token,
-// summed over the group) and advances the residual length; the last CTA of
-// the grid advances seq_len.  Tiers are read where they lie (MiKV rebuttal:
-// attention is permutation invariant, so each precision group sits in its
-// own region).
+// One launch per step.  Each (batch, KV head) unit is one thread-block
+// cluster of C CTAs (C = 1 .. 16, chosen so that the grid fills the GPU in
+// one wave).  The unit's work is a list of items: 128-token sub-chunks of
+// every packed tier, then 32-row pieces of the residual ring (the new token
+// last); CTA r of the cluster takes items r, r + C, r + 2C, ...  A CTA
+// requests each item with bulk asynchronous copies into one of two staging
+// buffers (the next-but-one item is requested as soon as one is consumed);
+// its four warps take 32 tokens (or 8 residual rows) each: keys -> base-2
+// logits for the g query heads of the KV head, online softmax per warp, P.V
+// with the codes turned into floats by one rotate and one LOP3 each.  The
+// CTA merges its warps and writes its partial (max, sum, unnormalised
+// output) into the shared memory of the cluster's leader (distributed shared
+// memory, no global round trip, no atomics).  The leader merges the C
+// partials and writes o and lse.  Then, per policy:
+//   DiffKV / MiKV: the leader broadcasts the log-sum-exp and every CTA adds
+//     this step's attention to the scores of its own tokens (DiffKV: per
+//     ring slot and query head; MiKV: per token, summed over the group);
+//   MiniKV: when the residual reaches nr + G tokens the leader packs its G
+//     oldest into tier 0 (MiniKV review, nr; verdict JSON key_machinery).
+// The leader appends the new token to the ring and advances res_len and the
+// unit's position.  Tiers are read where they lie (MiKV rebuttal: attention
+// is permutation invariant, so each precision group sits in its own region).
 #include <algorithm>
 #include <mutex>
 
@@ -31,24 +40,23 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSub = 128;        // packed tokens per staged sub-chunk: one 32-token group per warp
-constexpr int kMaxSubs = 4;      // sub-chunks per CTA at most, streamed through two staging buffers
-constexpr int kResChunk = 32;    // residual tokens per CTA (full-precision rows are large)
+constexpr int kSub = 128;        // packed tokens per item: one 32-token group per warp
+constexpr int kResItem = 32;     // residual rows per item: eight per warp
+constexpr int kMaxCluster = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
 struct TierArgs {
     int k_bits, v_bits, k_axis, cap;
-    const uint32_t* k_codes;
-    const uint16_t* k_scale;
-    const uint16_t* k_zero;
-    const uint32_t* v_codes;
-    const uint16_t* v_scale;
-    const uint16_t* v_zero;
-    const int32_t* token_id;
-    const int32_t* count;
-    int chunks;                 // ceil(cap / chunk_tokens)
+    uint32_t* k_codes;
+    uint16_t* k_scale;
+    uint16_t* k_zero;
+    uint32_t* v_codes;
+    uint16_t* v_scale;
+    uint16_t* v_zero;
+    int32_t* token_id;
+    int32_t* count;
     int slot_base;              // offset of this tier in the logits row
 };
 
@@ -58,26 +66,24 @@ struct DecodeArgs {
     const void* v_new;
     void* o;
     float* lse_out;
-    int B, Hq, Hkv, D, G, g, n_tiers, policy, bf16;
+    int B, Hq, Hkv, D, G, g, n_tiers, policy, bf16, nr;
     TierArgs tier[KVQ_MAX_TIERS];
     void* res_k;
     void* res_v;
     int32_t* res_token_id;
-    const int32_t* res_start;
+    int32_t* res_start;
     int32_t* res_len;
-    int res_cap, res_chunks, res_slot_base;
-    int32_t* seq_len;
+    int res_cap, res_slot_base;
+    int32_t* pos;               // [units] position of the next token
     float* win_acc;
     float* cum_score;
     int score_cap;
     float scale_log2;
-    int total_chunks;           // per unit
     int slots;                  // logits row length per (unit, head)
-    float* part;                // [unit][g][total_chunks][D + 2]
-    float* logits;              // [unit][g][slots] or null
-    uint32_t* counters;         // [units + 1]
+    float* logits;              // [unit][g][slots] (DiffKV, MiKV) or null
+    int cluster;                // CTAs per unit
     uint32_t stage_bytes;       // one staging buffer (two per CTA)
-    int chunk_tokens;           // packed tokens per CTA: kSub * (1 .. kMaxSubs)
+    uint32_t part_off, stage_off;  // dynamic shared memory offsets
 };
 
 __device__ __forceinline__ float ldf(const void* p, size_t i, bool bf16) {
@@ -131,15 +137,27 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
+// Per-unit state read once at the start of the launch (before any CTA of
+// the cluster can change it) and the item map derived from it.
+struct UnitState {
+    int cnt[KVQ_MAX_TIERS];              // valid slots of each tier
+    int base[KVQ_MAX_TIERS + 1];         // first item of each tier; base[n_tiers] = first residual item
+    int len, start, pos;                 // residual length and first slot, position of the new token
+    int total;                           // items of the unit
+};
+
 template <int NG, int D>
 struct Smem {
     float q[NG][D];                      // query rows, pre-scaled to base-2 logits
-    float wm[kWarps][NG];
+    float wm[kWarps][NG];                // per-warp running max / sum / output (merged across kinds)
     float wl[kWarps][NG];
     float wo[kWarps][NG][D];
     float lg[kWarps][NG][32];            // logits of the warp's current group
+    float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
+    float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
+    float lsum[NG];
     unsigned long long bar[2];           // one staging mbarrier per buffer
-    int n_total, last;
+    UnitState us;
 };
 
 // Online-softmax state of one warp for NG heads; o holds the lane's share.
@@ -428,13 +446,42 @@ __device__ __forceinline__ void values_token(const View& v, int tl, int nt, cons
     }
 }
 
-// Finish a packed-V warp: remove the constants, sum the lanes that share a
-// word, publish to smem.
+// ---- merging a warp's register state into its shared-memory state
+
+// Combines the warp's (m, l) with the stored ones; returns the factors that
+// scale the stored and the new output.  m and l are uniform over the warp.
+template <int NG, int D, int NO>
+__device__ __forceinline__ void merge_stats(Smem<NG, D>& sm, const WarpAcc<NG, NO>& acc,
+                                            float (&fo)[NG], float (&fn)[NG]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float M[NG], L[NG];
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        const float mo = sm.wm[warp][h];
+        M[h] = fmaxf(mo, acc.m[h]);
+        fo[h] = mo == kNegInf ? 0.0f : ex2_approx(mo - M[h]);
+        fn[h] = acc.m[h] == kNegInf ? 0.0f : ex2_approx(acc.m[h] - M[h]);
+        L[h] = sm.wl[warp][h] * fo[h] + acc.l[h] * fn[h];
+    }
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < NG; ++h) {
+            sm.wm[warp][h] = M[h];
+            sm.wl[warp][h] = L[h];
+        }
+    }
+}
+
+// Packed-V layout: remove the constants, sum the lanes that share a word,
+// merge into the warp's output.
 template <int VB, int D, int NG>
-__device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, Smem<NG, D>& sm) {
+__device__ __forceinline__ void flush_token_values(WarpAcc<NG, 32 / VB>& acc, Smem<NG, D>& sm) {
     constexpr int lpt = D * VB / 32, cpw = 32 / VB;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wi = lane % lpt, to = lane / lpt;
+    float fo[NG], fn[NG];
+    merge_stats(sm, acc, fo, fn);
 #pragma unroll
     for (int h = 0; h < NG; ++h)
 #pragma unroll
@@ -442,11 +489,32 @@ __device__ __forceinline__ void finish_token_values(WarpAcc<NG, 32 / VB>& acc, S
             float x = (acc.o[h][i] - acc.off[h]) * (float)(1 << VB) + acc.zs[h];
 #pragma unroll
             for (int o = lpt; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (to == 0) sm.wo[warp][h][wi * cpw + i] = x;
+            if (to == 0) {
+                float* p = &sm.wo[warp][h][wi * cpw + i];
+                *p = *p * fo[h] + x * fn[h];
+            }
         }
+    __syncwarp();
 }
 
-// ---- residual (full precision ring + the new token), staged as [n][D] rows
+// Residual layout: lane owns channels [lane * CPL, lane * CPL + CPL).
+template <int NG, int D>
+__device__ __forceinline__ void flush_lane_values(WarpAcc<NG, D / 32>& acc, Smem<NG, D>& sm) {
+    constexpr int CPL = D / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float fo[NG], fn[NG];
+    merge_stats(sm, acc, fo, fn);
+#pragma unroll
+    for (int h = 0; h < NG; ++h)
+#pragma unroll
+        for (int ci = 0; ci < CPL; ++ci) {
+            float* p = &sm.wo[warp][h][lane * CPL + ci];
+            *p = *p * fo[h] + acc.o[h][ci] * fn[h];
+        }
+    __syncwarp();
+}
+
+// ---- residual rows (full precision), eight per warp
 
 template <int CPL>
 __device__ __forceinline__ void row_vals(const uint16_t* row, bool bf, float (&x)[CPL]) {
@@ -469,80 +537,147 @@ __device__ __forceinline__ void row_vals(const uint16_t* row, bool bf, float (&x
     }
 }
 
-template <int NG, int D>
-__device__ void warp_residual(const DecodeArgs& a, Smem<NG, D>& sm, const uint16_t* rk,
-                              const uint16_t* rv, int n, float* lg_out) {
-    constexpr int CPL = D / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int c0 = lane * CPL;
-    const bool bf = a.bf16 != 0;
-    WarpAcc<NG, CPL> acc;
-    acc_init(acc);
-    for (int gi = warp; gi * 32 < n; gi += kWarps) {
-        const int tl = gi * 32;
-        const int nt = min(32, n - tl);
-        float lg[NG];
-#pragma unroll 1
-        for (int h = 0; h < NG; ++h) {
-            float part[32];
+// 32 lanes each hold v[0..7]; afterwards lanes 4t .. 4t+3 return the sum
+// over lanes of v[t].
+__device__ __forceinline__ float reduce_scatter8(float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                part[k] = 0.0f;
-                if (k < nt) {
-                    float x[CPL];
-                    row_vals<CPL>(rk + (size_t)(tl + k) * D + c0, bf, x);
+    for (int s = 16, half = 4; s >= 4; s >>= 1, half >>= 1) {
+        const bool up = (lane & s) != 0;
 #pragma unroll
-                    for (int ci = 0; ci < CPL; ++ci) part[k] = fmaf(sm.q[h][c0 + ci], x[ci], part[k]);
-                }
-            }
-            lg[h] = reduce_scatter32(part);
-        }
-        group_softmax(acc, lg, nt, lg_out ? lg_out + tl : nullptr, a.slots);
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            if (k < nt) {
-                float x[CPL];
-                row_vals<CPL>(rv + (size_t)(tl + k) * D + c0, bf, x);
-#pragma unroll
-                for (int h = 0; h < NG; ++h) {
-                    const float pk = __shfl_sync(0xffffffffu, lg[h], k);
-#pragma unroll
-                    for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] = fmaf(pk, x[ci], acc.o[h][ci]);
-                }
-            }
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
         }
     }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return v[0];
+}
+
+// Rows [0, nt) (nt <= 8) of the warp's slice: logits, online softmax and
+// P.V; the logits go to lg_out (row-indexed) when asked.
+template <int NG, int D>
+__device__ __forceinline__ void residual_rows(const Smem<NG, D>& sm, const uint16_t* rk,
+                                              const uint16_t* rv, int nt, bool bf,
+                                              WarpAcc<NG, D / 32>& acc, float* lg_out, int slots) {
+    constexpr int CPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int c0 = lane * CPL;
+    const int t = lane >> 2;                       // the row this lane reports
+    float lg[NG];
+#pragma unroll 1
+    for (int h = 0; h < NG; ++h) {
+        float part[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            part[k] = 0.0f;
+            if (k < nt) {
+                float x[CPL];
+                row_vals<CPL>(rk + (size_t)k * D + c0, bf, x);
+#pragma unroll
+                for (int ci = 0; ci < CPL; ++ci) part[k] = fmaf(sm.q[h][c0 + ci], x[ci], part[k]);
+            }
+        }
+        lg[h] = reduce_scatter8(part);
+    }
+    const bool valid = t < nt;
 #pragma unroll
     for (int h = 0; h < NG; ++h) {
-        if (lane == 0) {
-            sm.wm[warp][h] = acc.m[h];
-            sm.wl[warp][h] = acc.l[h];
-        }
+        const float s = valid ? lg[h] : kNegInf;
+        if (lg_out && valid && (lane & 3) == 0) lg_out[(size_t)h * slots + t] = s;
+        const float mn = fmaxf(acc.m[h], warp_max(s));
+        const float corr = acc.m[h] == kNegInf ? 0.0f : ex2_approx(acc.m[h] - mn);
+        const float p = valid ? ex2_approx(s - mn) : 0.0f;
+        acc.l[h] = acc.l[h] * corr + warp_sum((lane & 3) == 0 ? p : 0.0f);
 #pragma unroll
-        for (int ci = 0; ci < CPL; ++ci) sm.wo[warp][h][c0 + ci] = acc.o[h][ci];
+        for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] *= corr;
+        acc.m[h] = mn;
+        lg[h] = p;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (k < nt) {
+            float x[CPL];
+            row_vals<CPL>(rv + (size_t)k * D + c0, bf, x);
+#pragma unroll
+            for (int h = 0; h < NG; ++h) {
+                const float pk = __shfl_sync(0xffffffffu, lg[h], 4 * k);
+#pragma unroll
+                for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] = fmaf(pk, x[ci], acc.o[h][ci]);
+            }
+        }
     }
 }
 
-// A chunk of up to chunk_tokens tokens of one tier, streamed in kSub-token
-// sub-chunks through the two staging buffers: sub-chunk k + 2 is requested
-// as soon as sub-chunk k has been consumed.  Warp w takes the w-th 32-token
-// group of every sub-chunk; its online-softmax state spans the sub-chunks.
+// ---- items
+
+// Global item k of the unit: tier (or -1 for the residual) and index within it.
+__device__ __forceinline__ int item_kind(const UnitState& us, int n_tiers, int k, int& idx) {
+    for (int t = 0; t < n_tiers; ++t)
+        if (k < us.base[t + 1]) {
+            idx = k - us.base[t];
+            return t;
+        }
+    idx = k - us.base[n_tiers];
+    return -1;
+}
+
+// First local index of CTA r (items r, r + C, ...) at or after global item k.
+__device__ __forceinline__ int local_at(int k, int r, int C) { return k > r ? (k - r + C - 1) / C : 0; }
+
+// Called by one thread: the bulk copies of local item i into buffer i & 1.
+__device__ void issue_item(const DecodeArgs& a, const UnitState& us, size_t unit, int r, int i,
+                           uint8_t* stage_base, const unsigned long long* bars) {
+    const int D = a.D;
+    int idx;
+    const int t = item_kind(us, a.n_tiers, r + i * a.cluster, idx);
+    uint8_t* buf = stage_base + (size_t)(i & 1) * a.stage_bytes;
+    const uint32_t bar = smem_u32(&bars[i & 1]);
+    if (t >= 0) {
+        const int j0 = idx * kSub;
+        const int n = min(kSub, us.cnt[t] - j0);
+        stage_tier(a.tier[t], unit, j0, (n + 31) & ~31, D, a.G, buf, bar);
+    } else {
+        const int j0 = idx * kResItem;
+        const int n = min(kResItem, us.len + 1 - j0);
+        stage_residual(a, unit, us.len, us.start, j0, n, D, buf, bar);
+    }
+}
+
+// Waits for local item i; the next-but-one item is requested once every
+// warp is done with this one (in the caller, after its compute).
+__device__ __forceinline__ bool wait_item(unsigned long long* bars, int i, bool ok) {
+    return __syncthreads_and(ok && mbar_wait(smem_u32(&bars[i & 1]), (i >> 1) & 1, nullptr));
+}
+
+__device__ __forceinline__ void release_item(const DecodeArgs& a, const UnitState& us, size_t unit,
+                                             int r, int i, int n_local, bool ok, uint8_t* stage_base,
+                                             unsigned long long* bars, int& issued) {
+    __syncthreads();                           // buffer i & 1 consumed by every warp
+    if (threadIdx.x == 0 && ok && i + 2 < n_local) {
+        issue_item(a, us, unit, r, i + 2, stage_base, bars);
+        issued = i + 3;
+    }
+}
+
+// Local items [i0, i1) of one packed tier.
 template <int KB, int KAX, int VB, int D, int NG>
-__device__ void warp_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& t, size_t unit,
-                          int j0, int n_total, uint8_t* stage_base, float* lg_out) {
-    constexpr int cpw = 32 / VB;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nsub = (n_total + kSub - 1) / kSub;
-    WarpAcc<NG, cpw> acc;
+__device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t unit, int r, int i0,
+                         int i1, int n_local, uint8_t* stage_base, float* lg_unit, bool& ok,
+                         int& issued) {
+    const TierArgs& ta = a.tier[t];
+    const UnitState& us = sm.us;
+    const int warp = threadIdx.x >> 5;
+    WarpAcc<NG, 32 / VB> acc;
     acc_init(acc);
-    bool ok = true;
-    for (int sub = 0; sub < nsub; ++sub) {
-        const int buf = sub & 1;
-        uint8_t* stage = stage_base + (size_t)buf * a.stage_bytes;
-        const int n = min(kSub, n_total - sub * kSub);
-        ok = ok && __syncthreads_and(mbar_wait(smem_u32(&sm.bar[buf]), (sub >> 1) & 1, nullptr));
+    for (int i = i0; i < i1; ++i) {
+        ok = wait_item(sm.bar, i, ok);
         if (ok) {
-            const View v = tier_view(t, (n + 31) & ~31, D, a.G, stage);
+            const int j0 = (r + i * a.cluster - us.base[t]) * kSub;
+            const int n = min(kSub, us.cnt[t] - j0);
+            const View v = tier_view(ta, (n + 31) & ~31, D, a.G, stage_base + (size_t)(i & 1) * a.stage_bytes);
             const int tl = warp * 32;
             if (tl < n) {
                 const int nt = min(32, n - tl);
@@ -551,318 +686,424 @@ __device__ void warp_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& 
                     logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
                 else
                     logits_token<KB, D, NG>(v, tl, sm, a.G, lg);
-                group_softmax(acc, lg, nt, lg_out ? lg_out + sub * kSub + tl : nullptr, a.slots);
+                float* lo = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + ta.slot_base + j0 + tl : nullptr;
+                group_softmax(acc, lg, nt, lo, a.slots);
                 values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
             }
         }
-        __syncthreads();                       // buffer consumed by every warp
-        if (threadIdx.x == 0 && sub + 2 < nsub) {
-            const int n2 = min(kSub, n_total - (sub + 2) * kSub);
-            stage_tier(t, unit, j0 + (sub + 2) * kSub, (n2 + 31) & ~31, D, a.G, stage,
-                       smem_u32(&sm.bar[buf]));
-        }
+        release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
     }
-    if (!ok && threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < NG; ++h) {
-            sm.wm[warp][h] = acc.m[h];
-            sm.wl[warp][h] = acc.l[h];
-        }
-    }
-    finish_token_values<VB, D, NG>(acc, sm);
+    flush_token_values<VB, D, NG>(acc, sm);
 }
 
 template <int NG, int D>
-__device__ bool dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, const TierArgs& t, size_t unit,
-                              int j0, int n, uint8_t* stage, float* lg_out) {
-    const int kb = t.k_bits, vb = t.v_bits, ax = t.k_axis;
-    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
-    if (D == 128) {
-        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { warp_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { warp_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { warp_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { warp_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, j0, n, stage, lg_out); return true; }
+__device__ void dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t unit, int r, int i0,
+                              int i1, int n_local, uint8_t* stage, float* lg_unit, bool& ok, int& issued) {
+    const TierArgs& ta = a.tier[t];
+    const int kb = ta.k_bits, vb = ta.v_bits, ax = ta.k_axis;
+    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) {
+        run_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued);
+        return;
     }
-    return false;
+    if (D == 128) {
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+    }
+    // a format without a kernel (the host validation lists exactly the built ones):
+    // consume the items so that the staging stays in step
+    if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
+    for (int i = i0; i < i1; ++i) {
+        ok = wait_item(sm.bar, i, ok);
+        release_item(a, sm.us, unit, r, i, n_local, ok, stage, sm.bar, issued);
+    }
 }
 
-// Grid = (chunks of every tier and of the residual ring, units).
+// Local items [i0, i1) of the residual ring.
+template <int NG, int D>
+__device__ void run_residual(const DecodeArgs& a, Smem<NG, D>& sm, size_t unit, int r, int i0, int i1,
+                             int n_local, uint8_t* stage_base, float* lg_unit, bool& ok, int& issued) {
+    const UnitState& us = sm.us;
+    const int warp = threadIdx.x >> 5;
+    const bool bf = a.bf16 != 0;
+    WarpAcc<NG, D / 32> acc;
+    acc_init(acc);
+    for (int i = i0; i < i1; ++i) {
+        ok = wait_item(sm.bar, i, ok);
+        if (ok) {
+            const int j0 = (r + i * a.cluster - us.base[a.n_tiers]) * kResItem;
+            const int n = min(kResItem, us.len + 1 - j0);
+            const uint8_t* buf = stage_base + (size_t)(i & 1) * a.stage_bytes;
+            const uint16_t* rk = reinterpret_cast<const uint16_t*>(buf);
+            const uint16_t* rv = reinterpret_cast<const uint16_t*>(buf + a16((uint32_t)n * D * 2));
+            const int w0 = warp * 8;
+            if (w0 < n) {
+                float* lo = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 + w0 : nullptr;
+                residual_rows<NG, D>(sm, rk + (size_t)w0 * D, rv + (size_t)w0 * D, min(8, n - w0), bf, acc, lo,
+                                     a.slots);
+            }
+        }
+        release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
+    }
+    flush_lane_values<NG, D>(acc, sm);
+}
+
+// ---- policy work after the merge
+
+// This step's attention added to the scores of the CTA's own tokens.
+template <int NG, int D>
+__device__ void add_scores(const DecodeArgs& a, const Smem<NG, D>& sm, size_t unit, int r, int n_local,
+                           const float* lg_unit) {
+    const UnitState& us = sm.us;
+    const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
+    const int cap = a.res_cap;
+    const float* lse2 = sm.lse2;
+    float* cs = a.cum_score + unit * (size_t)a.score_cap;
+    for (int i = 0; i < n_local; ++i) {
+        int idx;
+        const int t = item_kind(us, a.n_tiers, r + i * a.cluster, idx);
+        if (t >= 0) {
+            if (a.policy != KVQ_POLICY_MIKV) continue;
+            const TierArgs& ta = a.tier[t];
+            const int j0 = idx * kSub, j1 = min(j0 + kSub, us.cnt[t]);
+            for (int j = j0 + (int)threadIdx.x; j < j1; j += blockDim.x) {
+                float p = 0.0f;
+#pragma unroll
+                for (int h = 0; h < NG; ++h)
+                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ta.slot_base + j) - lse2[h]);
+                const int id = ta.token_id[unit * (size_t)ta.cap + j];
+                if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
+                else atomicOr(&g_status_decode, kDevCheck);
+            }
+        } else {
+            const int l0 = idx * kResItem, l1 = min(l0 + kResItem, us.len + 1);
+            if (a.policy == KVQ_POLICY_MIKV) {
+                for (int li = l0 + (int)threadIdx.x; li < l1; li += blockDim.x) {
+                    float p = 0.0f;
+#pragma unroll
+                    for (int h = 0; h < NG; ++h)
+                        p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+                    const int id = li < us.len ? a.res_token_id[unit * (size_t)cap + (us.start + li) % cap] : us.pos;
+                    if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
+                    else cs[id] = li < us.len ? __fadd_rn(cs[id], p) : p;
+                }
+            } else {
+                for (int x = l0 * NG + (int)threadIdx.x; x < l1 * NG; x += blockDim.x) {
+                    const int li = x / NG, h = x % NG;
+                    const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+                    float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
+                    *wa = li < us.len ? __fadd_rn(*wa, p) : p;
+                }
+            }
+        }
+    }
+}
+
+// Leader, MiniKV: the G oldest residual tokens (the new one already in the
+// ring) move to tier 0 -- keys grouped per channel along tokens, values per
+// token along channels.  Returns false when tier 0 is full.
+template <typename T>
+__device__ bool minikv_flush(const DecodeArgs& a, size_t unit, int start, int cnt) {
+    const TierArgs& t = a.tier[0];
+    const int G = a.G, D = a.D, cap = a.res_cap;
+    if (cnt + G > t.cap) return false;
+    const T* rk = reinterpret_cast<const T*>(a.res_k);
+    const T* rv = reinterpret_cast<const T*>(a.res_v);
+    const size_t rb = unit * (size_t)cap;
+    auto row = [&](int i) { return rk + (rb + (start + i) % cap) * D; };
+    uint32_t* codes = t.k_codes + (unit * (size_t)(t.cap * t.k_bits / 32) + cnt * t.k_bits / 32) * D;
+    uint16_t* s = t.k_scale + (unit * (size_t)(t.cap / G) + cnt / G) * D;
+    uint16_t* z = t.k_zero + (unit * (size_t)(t.cap / G) + cnt / G) * D;
+    for (int c = threadIdx.x; c < D; c += blockDim.x)
+        quant_channel_group<T>(row, G, c, t.k_bits, codes, D, s + c, z + c);
+    const int groups = D / G;
+    for (int x = threadIdx.x; x < G * groups; x += blockDim.x) {
+        const int i = x / groups, grp = x % groups;
+        const T* src = rv + (rb + (start + i) % cap) * D + (size_t)grp * G;
+        const size_t slot = unit * (size_t)t.cap + cnt + i;
+        quant_token_group([&](int k) { return Elem<T>::to_f(src[k]); }, G, t.v_bits,
+                          t.v_codes + slot * (D * t.v_bits / 32) + grp * (G * t.v_bits / 32),
+                          t.v_scale + slot * groups + grp, t.v_zero + slot * groups + grp);
+    }
+    for (int i = threadIdx.x; i < G; i += blockDim.x)
+        t.token_id[unit * (size_t)t.cap + cnt + i] = a.res_token_id[rb + (start + i) % cap];
+    return true;
+}
+
+// ---- the kernel
+
+// Grid = (C, units), cluster (C, 1, 1): CTA r of the cluster of unit u.
 template <int NG, int D>
 __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<NG, D>& sm = *reinterpret_cast<Smem<NG, D>*>(smem_raw);
-    uint8_t* stage_base = smem_raw + ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127);
+    float* part = reinterpret_cast<float*>(smem_raw + a.part_off);   // leader: [C][NG][D + 2]
+    uint8_t* stage_base = smem_raw + a.stage_off;
+    const int C = a.cluster;
+    const int r = blockIdx.x;
     const size_t unit = blockIdx.y;
-    const int units = gridDim.y;
-    const int TC = a.total_chunks;
     const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
     const bool bf = a.bf16 != 0;
 
-    int chunk = blockIdx.x, tier = -1;
-    for (int t = 0; t < a.n_tiers; ++t) {
-        if (chunk < a.tier[t].chunks) { tier = t; break; }
-        chunk -= a.tier[t].chunks;
-    }
-    // thread 0 requests the first bytes before anything else
+    cluster_arrive_relaxed();                   // "started": the leader's shared memory exists
+    int issued = 0;                             // thread 0: local items requested so far
     if (threadIdx.x == 0) {
-        const uint32_t b0 = smem_u32(&sm.bar[0]), b1 = smem_u32(&sm.bar[1]);
-        mbar_init(b0, 1);
-        mbar_init(b1, 1);
-        fence_mbar_init();
-        int n = 0;
-        if (tier >= 0) {
-            const TierArgs& t = a.tier[tier];
-            const int raw = t.count[unit];
-            if (raw > t.cap || raw < 0) atomicOr(&g_status_decode, kDevCheck);
-            const int j0 = chunk * a.chunk_tokens;
-            n = min(a.chunk_tokens, min(max(raw, 0), t.cap) - j0);
-            if (n > 0) {
-                const int n0 = min(kSub, n);
-                stage_tier(t, unit, j0, (n0 + 31) & ~31, D, a.G, stage_base, b0);
-                if (n > kSub) {
-                    const int n1 = min(kSub, n - kSub);
-                    stage_tier(t, unit, j0 + kSub, (n1 + 31) & ~31, D, a.G, stage_base + a.stage_bytes, b1);
-                }
-            }
-        } else {
-            const int cap = a.res_cap;
-            const int raw = a.res_len[unit];
-            const int len = min(max(raw, 0), cap - 1), start = a.res_start[unit];
-            if (raw != len || start < 0 || start >= cap) atomicOr(&g_status_decode, kDevCheck);
-            const int j0 = chunk * kResChunk;
-            n = min(kResChunk, len + 1 - j0);
-            if (n > 0 && start >= 0 && start < cap) stage_residual(a, unit, len, start, j0, n, D, stage_base, b0);
-            else n = 0;
+        UnitState& us = sm.us;
+        bool bad = false;
+        us.base[0] = 0;
+        for (int t = 0; t < a.n_tiers; ++t) {
+            const int raw = a.tier[t].count[unit];
+            const int n = min(max(raw, 0), a.tier[t].cap);
+            bad |= raw != n;
+            us.cnt[t] = n;
+            us.base[t + 1] = us.base[t] + (n + kSub - 1) / kSub;
         }
-        sm.n_total = max(n, 0);
+        const int cap = a.res_cap;
+        const int rl = a.res_len[unit], rs = a.res_start[unit];
+        us.len = min(max(rl, 0), cap - 1);
+        us.start = min(max(rs, 0), cap - 1);
+        bad |= rl != us.len || rs != us.start;
+        us.pos = a.pos[unit];
+        us.total = us.base[a.n_tiers] + (us.len + 1 + kResItem - 1) / kResItem;
+        if (bad) atomicOr(&g_status_decode, kDevCheck);
+        mbar_init(smem_u32(&sm.bar[0]), 1);
+        mbar_init(smem_u32(&sm.bar[1]), 1);
+        fence_mbar_init();
+        const int n_local = us.total > r ? (us.total - r + C - 1) / C : 0;
+        for (int i = 0; i < 2 && i < n_local; ++i) issue_item(a, us, unit, r, i, stage_base, sm.bar);
+        issued = min(2, n_local);
     }
-    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
+    for (int x = threadIdx.x; x < NG * D; x += blockDim.x) {
+        const int h = x / D, c = x % D;
         sm.q[h][c] = ldf(a.q, ((size_t)b * a.Hq + (size_t)hkv * NG + h) * D + c, bf) * a.scale_log2;
     }
-    for (int idx = threadIdx.x; idx < kWarps * NG; idx += blockDim.x) {
-        sm.wm[idx / NG][idx % NG] = kNegInf;
-        sm.wl[idx / NG][idx % NG] = 0.0f;
+    for (int x = threadIdx.x; x < kWarps * NG; x += blockDim.x) {
+        sm.wm[x / NG][x % NG] = kNegInf;
+        sm.wl[x / NG][x % NG] = 0.0f;
     }
-    for (int idx = threadIdx.x; idx < kWarps * NG * D; idx += blockDim.x) (&sm.wo[0][0][0])[idx] = 0.0f;
+    for (int x = threadIdx.x; x < kWarps * NG * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
     __syncthreads();
 
+    const UnitState& us = sm.us;
+    const int n_local = us.total > r ? (us.total - r + C - 1) / C : 0;
     float* lg_unit = a.logits ? a.logits + unit * NG * (size_t)a.slots : nullptr;
-    const int n = sm.n_total;
-    if (n > 0) {
-        if (tier >= 0) {
-            const TierArgs& t = a.tier[tier];
-            const int j0 = chunk * a.chunk_tokens;
-            float* lg = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + t.slot_base + j0 : nullptr;
-            if (!dispatch_tier<NG, D>(a, sm, t, unit, j0, n, stage_base, lg) && threadIdx.x == 0)
-                atomicOr(&g_status_decode, kDevCheck);
-        } else {
-            const int j0 = chunk * kResChunk;
-            const bool ok = __syncthreads_and(mbar_wait(smem_u32(&sm.bar[0]), 0, nullptr));
-            if (!ok) {
-                if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevTimeout);
-            } else {
-                const uint16_t* rk = reinterpret_cast<const uint16_t*>(stage_base);
-                const uint16_t* rv = reinterpret_cast<const uint16_t*>(stage_base + a16((uint32_t)n * D * 2));
-                float* lg = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 : nullptr;
-                warp_residual<NG, D>(a, sm, rk, rv, n, lg);
+    bool ok = true;
+    for (int t = 0; t < a.n_tiers; ++t) {
+        const int i0 = local_at(us.base[t], r, C), i1 = local_at(us.base[t + 1], r, C);
+        if (i1 > i0) dispatch_tier<NG, D>(a, sm, t, unit, r, i0, i1, n_local, stage_base, lg_unit, ok, issued);
+    }
+    {
+        const int i0 = local_at(us.base[a.n_tiers], r, C);
+        if (n_local > i0) run_residual<NG, D>(a, sm, unit, r, i0, n_local, n_local, stage_base, lg_unit, ok, issued);
+    }
+    if (!ok && threadIdx.x == 0) {
+        atomicOr(&g_status_decode, kDevTimeout);
+        // let every copy still in flight land before the buffers go away
+        for (int i = 0; i < issued; ++i) mbar_wait(smem_u32(&sm.bar[i & 1]), (i >> 1) & 1, nullptr);
+    }
+    __syncthreads();
+
+    // ---- CTA partial -> slot r of the leader
+    cluster_wait_acquire();                     // every CTA of the cluster has started
+    {
+        const uint32_t slot = smem_u32(part + (size_t)r * NG * (D + 2));
+        const uint32_t dst = cluster_map(slot, 0);
+        for (int x = threadIdx.x; x < NG * D; x += blockDim.x) {
+            const int h = x / D, c = x % D;
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+            float L = 0.0f, O = 0.0f;
+            if (M != kNegInf) {
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float f = sm.wm[w][h] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][h] - M);
+                    L = fmaf(sm.wl[w][h], f, L);
+                    O = fmaf(sm.wo[w][h][c], f, O);
+                }
+            }
+            const uint32_t o = dst + (uint32_t)(h * (D + 2)) * 4u;
+            cluster_st_f32(o + (uint32_t)(2 + c) * 4u, O);
+            if (c == 0) {
+                cluster_st_f32(o, M);
+                cluster_st_f32(o + 4u, L);
             }
         }
     }
-    if (tier < 0 && chunk == 0) {
-        // the new token joins the ring; no CTA reads this slot in this step
-        const int cap = a.res_cap;
-        const int len = min(max(a.res_len[unit], 0), cap - 1);
-        const int start = min(max(a.res_start[unit], 0), cap - 1);
+    cluster_arrive_release();
+    cluster_wait_acquire();
+
+    // ---- leader: merge the C partials, write o and lse
+    if (r == 0) {
+        if (threadIdx.x < NG) {
+            const int h = threadIdx.x;
+            float M = kNegInf;
+            for (int y = 0; y < C; ++y) {
+                const float* p = part + ((size_t)y * NG + h) * (D + 2);
+                if (p[1] > 0.0f) M = fmaxf(M, p[0]);
+            }
+            float L = 0.0f;
+            for (int y = 0; y < C; ++y) {
+                const float* p = part + ((size_t)y * NG + h) * (D + 2);
+                const float w = (p[1] > 0.0f && p[0] != kNegInf) ? ex2_approx(p[0] - M) : 0.0f;
+                L = fmaf(p[1], w, L);
+                sm.cw[y][h] = w;
+            }
+            sm.lsum[h] = L;
+            sm.lse2[h] = M + __log2f(L);
+            if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
+        }
+        __syncthreads();
+        for (int x = threadIdx.x; x < NG * D; x += blockDim.x) {
+            const int h = x / D, c = x % D;
+            float acc = 0.0f;
+            for (int y = 0; y < C; ++y) acc = fmaf(part[((size_t)y * NG + h) * (D + 2) + 2 + c], sm.cw[y][h], acc);
+            stf(a.o, ((size_t)b * a.Hq + hkv * NG + h) * D + c, acc / sm.lsum[h], bf);
+        }
+    }
+
+    // ---- DiffKV / MiKV: every CTA adds the step's attention to its own tokens
+    if (a.policy != KVQ_POLICY_MINIKV && lg_unit) {
+        if (r == 0 && threadIdx.x < NG)
+            for (int y = 0; y < C; ++y)
+                cluster_st_f32(cluster_map(smem_u32(&sm.lse2[threadIdx.x]), y), sm.lse2[threadIdx.x]);
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        add_scores<NG, D>(a, sm, unit, r, n_local, lg_unit);
+    }
+
+    // ---- leader: the new token joins the ring, MiniKV flush, counters
+    if (r == 0) {
+        const int cap = a.res_cap, len = us.len, start = us.start;
         const size_t slot = unit * (size_t)cap + (start + len) % cap;
         for (int c = threadIdx.x; c < D; c += blockDim.x) {
             stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
             stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
         }
-        if (threadIdx.x == 0) a.res_token_id[slot] = a.seq_len[b];
-    }
-    __syncthreads();
-
-    // ---- chunk partial: merge the four warps
-    float* part_out = a.part + (unit * NG * TC + blockIdx.x) * (size_t)(D + 2);
-    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
-        float M = kNegInf;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
-        float L = 0.0f, O = 0.0f;
-        if (M != kNegInf) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = sm.wm[w][h] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][h] - M);
-                L = fmaf(sm.wl[w][h], f, L);
-                O = fmaf(sm.wo[w][h][c], f, O);
+        if (threadIdx.x == 0) a.res_token_id[slot] = us.pos;
+        __syncthreads();
+        bool flushed = false;
+        if (a.policy == KVQ_POLICY_MINIKV && len + 1 == a.nr + a.G) {
+            flushed = bf ? minikv_flush<__nv_bfloat16>(a, unit, start, us.cnt[0])
+                         : minikv_flush<__half>(a, unit, start, us.cnt[0]);
+            if (!flushed && threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (flushed) {
+                a.tier[0].count[unit] = us.cnt[0] + a.G;
+                a.res_start[unit] = (start + a.G) % cap;
+                a.res_len[unit] = len + 1 - a.G;
+            } else {
+                a.res_len[unit] = len + 1;
             }
-        }
-        float* po = part_out + (size_t)h * TC * (D + 2);
-        po[2 + c] = O;
-        if (c == 0) {
-            po[0] = M;
-            po[1] = L;
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t prev = atomicAdd(&a.counters[unit], 1u);
-        sm.last = (prev == (uint32_t)TC - 1u) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!sm.last) return;
-    __threadfence();
-
-    const float* pu = a.part + unit * NG * TC * (size_t)(D + 2);
-    // chunk maxima and sums, all loads in flight together (scratch = the staging buffers)
-    float* cm = reinterpret_cast<float*>(stage_base);      // [NG][TC]
-    float* cw = cm + NG * TC;                               // [NG][TC]
-    for (int idx = threadIdx.x; idx < NG * TC; idx += blockDim.x) {
-        const float* ph = pu + (size_t)idx * (D + 2);
-        const float l = __ldcg(ph + 1);
-        cm[idx] = l > 0.0f ? __ldcg(ph) : kNegInf;
-        cw[idx] = l;
-    }
-    __syncthreads();
-    if (threadIdx.x < NG) {
-        const int h = threadIdx.x;
-        float M = kNegInf;
-        for (int y = 0; y < TC; ++y) M = fmaxf(M, cm[h * TC + y]);
-        float L = 0.0f;
-        for (int y = 0; y < TC; ++y) {
-            const float wgt = cm[h * TC + y] == kNegInf ? 0.0f : ex2_approx(cm[h * TC + y] - M);
-            L = fmaf(cw[h * TC + y], wgt, L);
-            cw[h * TC + y] = wgt;
-        }
-        sm.wl[0][h] = L;
-        sm.wm[0][h] = M + __log2f(L);          // base-2 lse
-        if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < NG * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
-        const float* ph = pu + (size_t)h * TC * (D + 2) + 2 + c;
-        float acc = 0.0f;
-#pragma unroll 8
-        for (int y = 0; y < TC; ++y) acc = fmaf(__ldcg(ph + (size_t)y * (D + 2)), cw[h * TC + y], acc);
-        stf(a.o, ((size_t)b * a.Hq + hkv * NG + h) * D + c, acc / sm.wl[0][h], bf);
-    }
-    const int cap = a.res_cap;
-    const int len = min(max(a.res_len[unit], 0), cap - 1);
-    const int start = min(max(a.res_start[unit], 0), cap - 1);
-    const float* lse2 = sm.wm[0];
-    if (a.policy == KVQ_POLICY_MIKV && lg_unit) {
-        float* cs = a.cum_score + unit * (size_t)a.score_cap;
-        for (int t = 0; t < a.n_tiers; ++t) {
-            const TierArgs& ti = a.tier[t];
-            const int cnt = min(max(ti.count[unit], 0), ti.cap);
-            for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
-                float p = 0.0f;
-#pragma unroll
-                for (int h = 0; h < NG; ++h)
-                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ti.slot_base + j) - lse2[h]);
-                const int id = ti.token_id[unit * (size_t)ti.cap + j];
-                if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
-                else atomicOr(&g_status_decode, kDevCheck);
-            }
-        }
-        for (int li = threadIdx.x; li <= len; li += blockDim.x) {
-            float p = 0.0f;
-#pragma unroll
-            for (int h = 0; h < NG; ++h)
-                p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-            const int id = li < len ? a.res_token_id[unit * (size_t)cap + (start + li) % cap] : a.seq_len[b];
-            if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
-            else cs[id] = li < len ? __fadd_rn(cs[id], p) : p;
-        }
-    } else if (a.policy == KVQ_POLICY_DIFFKV && lg_unit) {
-        for (int idx = threadIdx.x; idx < (len + 1) * NG; idx += blockDim.x) {
-            const int li = idx / NG, h = idx % NG;
-            const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-            float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (start + li) % cap;
-            *wa = li < len ? __fadd_rn(*wa, p) : p;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        a.res_len[unit] = len + 1;
-        a.counters[unit] = 0u;
-        __threadfence();
-        const uint32_t prev = atomicAdd(&a.counters[units], 1u);
-        if (prev == (uint32_t)units - 1u) {
-            __threadfence();
-            for (int bb = 0; bb < a.B; ++bb) a.seq_len[bb] += 1;
-            a.counters[units] = 0u;
+            a.pos[unit] = us.pos + 1;
         }
     }
 }
-
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    int total_chunks, slots;
-    size_t part, logits, counters, total;
+    int slots;
+    size_t logits, total;
 };
-
-// Packed tokens per CTA: as many sub-chunks (up to kMaxSubs) as keeps about
-// six CTAs' worth of sub-chunks per SM; small caches get one sub-chunk per
-// CTA so that every SM has work.
-int chunk_tokens_for(const kvq_cache& c) {
-    long subs = 0;
-    for (int t = 0; t < c.n_tiers; ++t) subs += (long)c.B * c.Hkv * ((c.tier[t].cap + kSub - 1) / kSub);
-    const long per = (subs + 152L * 6 - 1) / (152L * 6);
-    return kSub * (int)std::max(1L, std::min((long)kMaxSubs, per));
-}
 
 WsLayout ws_layout(const kvq_cache& c) {
     WsLayout w{};
     const int units = c.B * c.Hkv, g = c.Hq / c.Hkv;
-    const int ct = chunk_tokens_for(c);
-    int chunks = 0, slots = 0;
-    for (int t = 0; t < c.n_tiers; ++t) {
-        chunks += (c.tier[t].cap + ct - 1) / ct;
-        slots += c.tier[t].cap;
-    }
-    chunks += (c.res_cap + kResChunk - 1) / kResChunk;
+    int slots = 0;
+    for (int t = 0; t < c.n_tiers; ++t) slots += c.tier[t].cap;
     slots += c.res_cap;
-    w.total_chunks = chunks;
     w.slots = slots;
-    w.part = 0;
-    size_t off = align256((size_t)units * g * chunks * (c.D + 2) * sizeof(float));
-    w.logits = off;
-    if (c.policy != KVQ_POLICY_MINIKV) off += align256((size_t)units * g * slots * sizeof(float));
-    w.counters = off;
-    off += align256((size_t)(units + 1) * sizeof(uint32_t));
-    w.total = off;
+    w.logits = 0;
+    w.total = c.policy != KVQ_POLICY_MINIKV ? (size_t)units * g * slots * sizeof(float) : 0;
     return w;
+}
+
+// Items of a unit at full capacity (an upper bound of the live count).
+int items_bound(const kvq_cache& c) {
+    int n = 0;
+    for (int t = 0; t < c.n_tiers; ++t) n += (c.tier[t].cap + kSub - 1) / kSub;
+    return n + (c.res_cap + kResItem - 1) / kResItem;
 }
 
 template <int NG, int D>
 cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s) {
-    uint32_t stage = a16((uint32_t)kResChunk * D * 2) * 2u;
+    uint32_t stage = 2u * a16((uint32_t)kResItem * D * 2);
     for (int t = 0; t < c.n_tiers; ++t)
         stage = std::max(stage, tier_stage_sizes(c.tier[t].k_axis, c.tier[t].k_bits, c.tier[t].v_bits,
                                                  kSub, D, c.G).total());
     stage = (stage + 127u) & ~127u;
-    a.stage_bytes = stage;
-    // the merge reuses both buffers as scratch
-    const uint32_t scratch = (uint32_t)(2 * NG * a.total_chunks * sizeof(float));
-    const size_t bufs = std::max((size_t)2 * stage, (size_t)scratch);
-    const size_t sh = ((sizeof(Smem<NG, D>) + 127) & ~(size_t)127) + bufs;
-    static size_t attr = 0;
-    if (sh > 48 * 1024 && sh > attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<NG, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sh);
+    const uint32_t sm_bytes = (uint32_t)((sizeof(Smem<NG, D>) + 127) & ~(size_t)127);
+    const uint32_t slot_bytes = (uint32_t)(NG * (D + 2) * sizeof(float));
+    auto smem_for = [&](int C) { return sm_bytes + ((C * slot_bytes + 127u) & ~127u) + 2u * stage; };
+    int cmax = kMaxCluster;
+    while (cmax > 1 && (uint32_t)cmax * slot_bytes > 32u * 1024u) cmax >>= 1;
+
+    auto kern = decode_kernel<NG, D>;
+    static bool attr_done = false, wide_ok = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem_for(kMaxCluster));
         if (e != cudaSuccess) return e;
-        attr = sh;
+        // clusters above the portable 8 CTAs, where the device allows them
+        wide_ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        if (!wide_ok) (void)cudaGetLastError();
+        attr_done = true;
     }
-    dim3 grid(a.total_chunks, units);
-    decode_kernel<NG, D><<<grid, kThreads, sh, s>>>(a);
-    return cudaGetLastError();
+    if (!wide_ok) cmax = std::min(cmax, 8);
+    // CTAs per unit: the largest power of two (at most 16) that keeps the grid
+    // within one wave of resident CTAs and gives every CTA at least one item.
+    static int last_key[4] = {-1, -1, -1, -1}, last_C = 1;
+    const int items = items_bound(c);
+    const int key[4] = {units, items, (int)stage, c.n_tiers};
+    int C = last_C;
+    if (!std::equal(key, key + 4, last_key)) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_for(cmax));
+        if (e != cudaSuccess) return e;
+        const long resident = (long)std::max(per_sm, 1) * sms;
+        C = 1;
+        while (C * 2 <= cmax && (long)units * C * 2 <= resident && C * 2 <= items) C *= 2;
+        for (; C > 1; C >>= 1) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = (unsigned)C;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)C, (unsigned)units);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem_for(C);
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int ncl = 0;
+            if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) == cudaSuccess && ncl > 0) break;
+            (void)cudaGetLastError();
+        }
+        std::copy(key, key + 4, last_key);
+        last_C = C;
+    }
+    a.cluster = C;
+    a.stage_bytes = stage;
+    a.part_off = sm_bytes;
+    a.stage_off = sm_bytes + ((C * slot_bytes + 127u) & ~127u);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)C, (unsigned)units);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_for(C);
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace
@@ -873,6 +1114,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
                           float sm_scale, void* o, float* lse_out, void* ws, cudaStream_t s) {
     const WsLayout w = ws_layout(c);
     const int units = c.B * c.Hkv;
+    if (units > 65535) return cudaErrorInvalidConfiguration;
     DecodeArgs a{};
     a.q = q;
     a.k_new = k_new;
@@ -888,7 +1130,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.n_tiers = c.n_tiers;
     a.policy = c.policy;
     a.bf16 = c.dtype == KVQ_BF16 ? 1 : 0;
-    a.chunk_tokens = chunk_tokens_for(c);
+    a.nr = c.nr;
     int slot = 0;
     for (int t = 0; t < c.n_tiers; ++t) {
         const kvq_tier& ct = c.tier[t];
@@ -905,7 +1147,6 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
         ta.v_zero = ct.v_zero;
         ta.token_id = ct.token_id;
         ta.count = ct.count;
-        ta.chunks = (ct.cap + a.chunk_tokens - 1) / a.chunk_tokens;
         ta.slot_base = slot;
         slot += ct.cap;
     }
@@ -915,21 +1156,15 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.res_start = c.res_start;
     a.res_len = c.res_len;
     a.res_cap = c.res_cap;
-    a.res_chunks = (c.res_cap + kResChunk - 1) / kResChunk;
     a.res_slot_base = slot;
-    a.seq_len = c.seq_len;
+    a.pos = c.seq_len;
     a.win_acc = c.win_acc;
     a.cum_score = c.cum_score;
     a.score_cap = c.score_cap;
     a.scale_log2 = sm_scale * kLog2e;
-    a.total_chunks = w.total_chunks;
     a.slots = w.slots;
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    a.part = reinterpret_cast<float*>(base + w.part);
-    a.logits = c.policy != KVQ_POLICY_MINIKV ? reinterpret_cast<float*>(base + w.logits) : nullptr;
-    a.counters = reinterpret_cast<uint32_t*>(base + w.counters);
-    cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)(units + 1) * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
+    a.logits = c.policy != KVQ_POLICY_MINIKV ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + w.logits)
+                                             : nullptr;
     if (a.g == 1 && c.D == 128) return launch_typed<1, 128>(a, c, units, s);
     if (a.g == 1 && c.D == 64) return launch_typed<1, 64>(a, c, units, s);
     if (a.g == 2 && c.D == 128) return launch_typed<2, 128>(a, c, units, s);

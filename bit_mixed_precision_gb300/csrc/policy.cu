@@ -62,7 +62,7 @@ struct PolicyArgs {
     int32_t* res_start;
     int32_t* res_len;
     int res_cap;
-    int32_t* seq_len;
+    int32_t* seq_len;           // [units] position of the next token
     float* win_acc;
     float* alpha;
     float* cum_score;
@@ -117,7 +117,6 @@ __device__ void put_raw_token(const PolicyArgs& a, const TierDev& t, size_t unit
 // Token ids, residual and counters after the two packing launches.
 __global__ void minikv_build_tail(PolicyArgs a, int npk, int r0) {
     const size_t unit = blockIdx.x;
-    const int b = (int)(unit / a.Hkv);
     const int32_t* sel = a.sel_idx + unit * (size_t)a.n_sel;
     const TierDev& t = a.tier[0];
     for (int i = threadIdx.x; i < npk; i += blockDim.x) t.token_id[unit * t.cap + i] = sel[i];
@@ -136,59 +135,7 @@ __global__ void minikv_build_tail(PolicyArgs a, int npk, int r0) {
         t.count[unit] = npk;
         a.res_start[unit] = 0;
         a.res_len[unit] = r0;
-        if (unit % a.Hkv == 0) a.seq_len[b] = a.T;
-    }
-}
-
-// When the residual holds nr + G tokens, its G oldest move to tier 0:
-// keys per channel (one group along tokens), values per token.
-__global__ void minikv_flush(PolicyArgs a) {
-    const size_t unit = blockIdx.x;
-    const int len = a.res_len[unit], start = a.res_start[unit];
-    const int G = a.G, D = a.D, cap = a.res_cap;
-    if (len != a.nr + G) return;
-    const TierDev& t = a.tier[0];
-    const int cnt = t.count[unit];
-    if (cnt + G > t.cap) {
-        if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
-        return;
-    }
-    const bool bf = a.bf16 != 0;
-    const size_t rb = unit * (size_t)cap;
-    if (bf) {
-        const __nv_bfloat16* rk = reinterpret_cast<const __nv_bfloat16*>(a.res_k);
-        auto row = [&](int i) { return rk + (rb + (start + i) % cap) * D; };
-        uint32_t* codes = t.k_codes + (unit * (size_t)(t.cap * t.k_bits / 32) + cnt * t.k_bits / 32) * D;
-        uint16_t* s = t.k_scale + (unit * (size_t)(t.cap / G) + cnt / G) * D;
-        uint16_t* z = t.k_zero + (unit * (size_t)(t.cap / G) + cnt / G) * D;
-        for (int c = threadIdx.x; c < D; c += blockDim.x)
-            quant_channel_group<__nv_bfloat16>(row, G, c, t.k_bits, codes, D, s + c, z + c);
-    } else {
-        const __half* rk = reinterpret_cast<const __half*>(a.res_k);
-        auto row = [&](int i) { return rk + (rb + (start + i) % cap) * D; };
-        uint32_t* codes = t.k_codes + (unit * (size_t)(t.cap * t.k_bits / 32) + cnt * t.k_bits / 32) * D;
-        uint16_t* s = t.k_scale + (unit * (size_t)(t.cap / G) + cnt / G) * D;
-        uint16_t* z = t.k_zero + (unit * (size_t)(t.cap / G) + cnt / G) * D;
-        for (int c = threadIdx.x; c < D; c += blockDim.x)
-            quant_channel_group<__half>(row, G, c, t.k_bits, codes, D, s + c, z + c);
-    }
-    const int groups = D / G;
-    for (int idx = threadIdx.x; idx < G * groups; idx += blockDim.x) {
-        const int i = idx / groups, grp = idx % groups;
-        const size_t src = (rb + (start + i) % cap) * D + (size_t)grp * G;
-        const int slot = cnt + i;
-        quant_token_group([&](int k) { return ld_act(a.res_v, src + k, bf); }, G, t.v_bits,
-                          vrow(t, unit, slot, D) + grp * (G * t.v_bits / 32),
-                          t.v_scale + srow(t, unit, slot, D, G) + grp,
-                          t.v_zero + srow(t, unit, slot, D, G) + grp);
-    }
-    for (int i = threadIdx.x; i < G; i += blockDim.x)
-        t.token_id[unit * t.cap + cnt + i] = a.res_token_id[rb + (start + i) % cap];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        t.count[unit] = cnt + G;
-        a.res_start[unit] = (start + G) % cap;
-        a.res_len[unit] = len - G;
+        a.seq_len[unit] = a.T;
     }
 }
 
@@ -267,7 +214,7 @@ __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
         a.res_len[unit] = W;
         a.alpha[unit * 2] = alpha_h;
         a.alpha[unit * 2 + 1] = alpha_l;
-        if (hkv == 0) a.seq_len[b] = T;
+        a.seq_len[unit] = T;
     }
 }
 
@@ -279,7 +226,7 @@ __global__ void diffkv_exit(PolicyArgs a) {
     const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
     const int start = a.res_start[unit], cap = a.res_cap, g = a.g;
     const int tc = a.res_token_id[unit * cap + start];
-    const int N = a.seq_len[b];
+    const int N = a.seq_len[unit];
     const float cnt = (float)(N - tc);
     float score = -__int_as_float(0x7f800000);
     for (int h = 0; h < g; ++h)
@@ -364,7 +311,7 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_build(PolicyArgs a) {
         tl.count[unit] = min((int)lo_base, tl.cap);
         a.res_start[unit] = 0;
         a.res_len[unit] = r0;
-        if (hkv == 0) a.seq_len[b] = T;
+        a.seq_len[unit] = T;
     }
 }
 
@@ -605,8 +552,8 @@ kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, 
             minikv_build_tail<<<units, 256, 0, s>>>(a, npk, r0);
             return launched("MiniKV build");
         }
-        minikv_flush<<<units, 128, 0, s>>>(a);
-        return launched("MiniKV flush");
+        // the residual flush runs inside decode_attn_qkv (its last step)
+        return KVQ_OK;
     }
     if (mode == KVQ_POLICY_DIFFKV) {
         if (step == 0) {

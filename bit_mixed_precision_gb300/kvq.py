@@ -282,9 +282,10 @@ class Cache:
         d.score_cap, d.hi_den = self.score_cap, self.hi_den
         self.desc = d
         nbytes = lib().kvq_decode_workspace_bytes(ctypes.byref(d))
-        if nbytes == 0:
+        if nbytes == ctypes.c_size_t(-1).value:
             raise KvqError(KVQ_EINVAL, lib().kvq_last_error().decode())
-        self.ws = torch.empty((nbytes + 255) // 4, dtype=torch.int32, device=self.res_k.device)
+        self.ws = (torch.empty((nbytes + 255) // 4, dtype=torch.int32, device=self.res_k.device)
+                   if nbytes else None)
 
     def tier_nbytes(self):
         """Bytes held by the packed tiers (codes + scale/zero + ids), all units."""
@@ -325,7 +326,7 @@ def make_cache(B, Hq, Hkv, D, G, dtype, policy, tiers, nr, res_cap=None, score_c
               res_token_id=torch.full((units, res_cap), -1, dtype=torch.int32, device=device),
               res_start=torch.zeros((units,), dtype=torch.int32, device=device),
               res_len=torch.zeros((units,), dtype=torch.int32, device=device),
-              seq_len=torch.zeros((B,), dtype=torch.int32, device=device),
+              seq_len=torch.zeros((B * Hkv,), dtype=torch.int32, device=device),
               score_cap=score_cap, hi_den=hi_den)
     if policy == POLICY_DIFFKV:
         c.win_acc = torch.zeros((B * Hq, res_cap), dtype=torch.float32, device=device)
@@ -363,7 +364,7 @@ def decode_attn_qkv(q, k_new, v_new, cache, sm_scale=None, o=None, lse=None, str
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     _check(lib().decode_attn_qkv(_ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(cache.desc),
                                  float(sm_scale), _ptr(o), _ptr(lse), _ptr(cache.ws),
-                                 cache.ws.numel() * 4, _stream(stream)))
+                                 0 if cache.ws is None else cache.ws.numel() * 4, _stream(stream)))
     return o, lse
 
 

@@ -103,7 +103,9 @@ typedef struct {
  *   res_start [u] (slot of the oldest token), res_len [u].
  * nr: residual length the policy keeps ([MiniKV-R]: nr = 128 steps before
  *   new tokens are quantised; DiffKV: the recent window W).
- * seq_len [B]: position of the next token of each sequence.
+ * seq_len [B*Hkv]: position of the next token, per unit (every unit of a
+ *   sequence holds the same value; one entry per unit lets each unit advance
+ *   its own without waiting for the others).
  * Policy state:
  *   DiffKV: win_acc [B*Hq][res_cap] attention received by each ring slot,
  *           per query head; alpha [u][2] = (alpha_h, alpha_l).
@@ -202,11 +204,12 @@ kvq_status select_tokens(const float* score, int B, int H, int T, const int32_t*
  *     T and, per policy, sel_idx/n_sel, colscore, n_high/n_low).  Tier
  *     counts, the residual and the policy state are overwritten.
  *   step > 0 (after decode_attn_qkv of that step):
- *     MiniKV: if res_len == nr + G pack the G oldest residual tokens into tier 0.
+ *     MiniKV: nothing to do (decode_attn_qkv packs the residual, see there);
+ *             returns KVQ_OK without a launch.
  *     DiffKV: if res_len > nr the oldest window token leaves: K8V4 (tier 0)
  *             if score >= alpha_h/N, else K4V2 (tier 1) if score >= alpha_l/N,
  *             else pruned; score = max over the group's heads of the mean
- *             attention it received, N = seq_len.
+ *             attention it received, N = seq_len[u].
  *     MiKV:   if res_len > nr the oldest residual token leaves; the top
  *             floor(N_q/hi_den) tokens by cumulative score (ties to the lower
  *             position) over tiers 0,1 plus that token form the set S; it
@@ -220,19 +223,23 @@ kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params
  * with in-kernel dequantisation ([MiKV-R] INTn x FP16 GEMV with on-the-fly
  * dequantisation; [MiniKV-J] fused dequantisation in decoding).
  *   q (device) [B, Hq, D]; k_new, v_new (device) [B, Hkv, D].
- *   The new token (position seq_len[b]) is appended to the residual ring
+ *   The new token (position seq_len[u]) is appended to the residual ring
  *   and attends to itself; o (device) [B, Hq, D] = softmax(sm_scale q.k) v
  *   over every packed tier (dequantised) and the residual.  lse_out (device,
  *   nullable) [B, Hq].  DiffKV: win_acc += attention of the step for every
  *   ring slot.  MiKV: cum_score[token] += sum over the group's heads of the
- *   attention of the step.  seq_len and res_len advance by one.
+ *   attention of the step.  MiniKV: when the residual then holds nr + G
+ *   tokens its G oldest are packed into tier 0 (keys per channel, values per
+ *   token) and leave the ring.  seq_len and res_len advance by one.
  *   ws (device) of at least kvq_decode_workspace_bytes(c) bytes, 256-byte
- *   aligned; its content between calls is irrelevant. */
+ *   aligned (may be NULL when that is 0, as for MiniKV); its content between
+ *   calls is irrelevant. */
 kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
                            float sm_scale, void* o, float* lse_out, void* ws, size_t ws_bytes,
                            void* stream);
 
-/* Bytes of decode workspace the cache needs (0 on an invalid cache). */
+/* Bytes of decode workspace the cache needs (DiffKV, MiKV: the step's
+ * logits; MiniKV: 0), or (size_t)-1 on an invalid cache. */
 size_t kvq_decode_workspace_bytes(const kvq_cache* c);
 
 /* Size of the scratch array built into the library for decode_attn_qkv_static. */
@@ -252,9 +259,9 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* c);
  *   The first call made with a given device current looks up the array's
  *   device address on that device; make that first call before any stream
  *   capture.
- *   All calls share the one array (its counters are cleared at the start of
- *   every call): two calls whose work overlaps on the GPU, on any streams,
- *   race and give wrong results. */
+ *   All calls share the one array (DiffKV and MiKV keep the step's logits
+ *   there; MiniKV needs none): two DiffKV/MiKV calls whose work overlaps on
+ *   the GPU, on any streams, race and give wrong results. */
 kvq_status decode_attn_qkv_static(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
                                   float sm_scale, void* o, float* lse_out, void* stream);
 
