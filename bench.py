@@ -194,7 +194,8 @@ class Hot:
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         nt = len(self.cache.tiers)
         self.hist = torch.zeros((steps, nt + 1, B * Hkv), dtype=torch.int32, device=dev)
-        self.prefill_flops = 3 * D * T * T * B * Hq     # pass-1 QK^T and PV, pass-2 QK^T
+        # the causal half of pass-1 QK^T and PV and of pass-2 QK^T, 2 flops per multiply-add
+        self.prefill_flops = 3 * D * T * T * B * Hq
 
     def prefill_build(self, s):
         kvq, pol = self.kvq, self.wl["policy"]
@@ -353,8 +354,9 @@ def run_ours(args, wl, rank, world):
                    "us_per_launch": dec_ms_per_launch * 1e3, "bytes_per_launch": dec_bytes,
                    "packed_kv_gbs": achieved, "frac_hbm": achieved / hbm_peak},
         "prefill": {"ms": pre_ms, "tflops": pre_tf, "frac_tensor": pre_tf / tf_peak,
-                    "flops_counted": "3*D*T^2 per (batch, query head): pass-1 QK^T and PV, pass-2 "
-                                     "QK^T (dense count, the causal half is not subtracted)"},
+                    "flops_counted": "3*D*T^2 per (batch, query head): the causal half (T^2/2 "
+                                     "query-key pairs) of pass-1 QK^T and PV and of pass-2 QK^T, "
+                                     "2 flops per multiply-add"},
         "segments_ms_per_step": {k2: v2 / args.steps for k2, v2 in seg.items()},
         "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",

@@ -38,14 +38,24 @@ KVQ_DEFINE_STATUS(decode)
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kSub = 128;        // packed tokens per item: one 32-token group per warp
-constexpr int kResItem = 32;     // residual rows per item: eight per warp
+constexpr int kSub = 128;        // packed tokens per item, split evenly over the warps
+constexpr int kResItem = 32;     // residual rows per item
 constexpr int kMaxCluster = 16;
+constexpr int kMinItemsPerCta = 34;  // large caches: items a CTA streams at least (about 4k tokens)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
+
+// Four warps per CTA, 32 packed tokens each per item.
+template <int NG>
+struct Cfg {
+    static constexpr int W = 4;
+    static constexpr int kThreads = W * 32;
+    static constexpr int TPW = kSub / W;        // packed tokens per warp and item
+    static constexpr int REP = 32 / TPW;        // lanes holding one token's logit
+    static constexpr int RPW = kResItem / W;    // residual rows per warp and item
+    static constexpr int MINB = NG == 1 ? 4 : 1; // resident CTAs per SM the registers must allow
+};
 
 struct TierArgs {
     int k_bits, v_bits, k_axis, cap;
@@ -110,19 +120,23 @@ __device__ __forceinline__ float code_f(uint32_t w, int i) {
     return __uint_as_float((x & mask) | 0x3F800000u);
 }
 
-// 32 lanes each hold v[0..31]; afterwards lane t returns the sum over lanes of v[t].
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32]) {
+// 32 lanes each hold v[0..N-1] (N = 4 .. 32); afterwards the 32/N lanes
+// (32/N) t .. (32/N) t + 32/N - 1 return the sum over lanes of v[t].
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
+    for (int half = N / 2, s = 16; half >= 1; half >>= 1, s >>= 1) {
         const bool up = (lane & s) != 0;
 #pragma unroll
-        for (int i = 0; i < s; ++i) {
-            const float send = up ? v[i] : v[i + s];
-            const float keep = up ? v[i + s] : v[i];
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
         }
     }
+#pragma unroll
+    for (int s = 16 / N; s >= 1; s >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], s);
     return v[0];
 }
 
@@ -149,10 +163,11 @@ struct UnitState {
 template <int NG, int D>
 struct Smem {
     float q[NG][D];                      // query rows, pre-scaled to base-2 logits
-    float wm[kWarps][NG];                // per-warp running max / sum / output (merged across kinds)
-    float wl[kWarps][NG];
-    float wo[kWarps][NG][D];
-    float lg[kWarps][NG][32];            // logits of the warp's current group
+    float wm[Cfg<NG>::W][NG];            // per-warp running max / sum / output (merged across kinds)
+    float wl[Cfg<NG>::W][NG];
+    float wo[Cfg<NG>::W][NG][D];
+    float lg[Cfg<NG>::W][NG][32];        // logits of the warp's current group
+    uint16_t qf[Cfg<NG>::W][NG <= 4 ? 2 * NG : 1][128];  // per-channel keys: query x scales, hi / lo rows
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
     float lsum[NG];
@@ -181,20 +196,23 @@ __device__ __forceinline__ void acc_init(WarpAcc<NG, NO>& acc) {
     }
 }
 
-// Logits of the group (lane t holds token t, -inf past nt) -> rescale the
-// accumulators, return p_h(t) in lg and write the logits out when asked.
-template <int NG, int NO>
+// Logits of the warp's tokens (lanes REP t .. REP t + REP - 1 hold token t;
+// tokens from nt on are absent) -> rescale the accumulators, return p_h(t)
+// in lg and write the logits out when asked.
+template <int REP, int NG, int NO>
 __device__ __forceinline__ void group_softmax(WarpAcc<NG, NO>& acc, float (&lg)[NG], int nt,
                                               float* lg_out, int slots) {
     const int lane = threadIdx.x & 31;
+    const int tok = lane / REP;
+    const bool lead = lane % REP == 0, valid = tok < nt;
 #pragma unroll
     for (int h = 0; h < NG; ++h) {
-        const float s = lane < nt ? lg[h] : kNegInf;
-        if (lg_out && lane < nt) lg_out[(size_t)h * slots + lane] = s;
+        const float s = valid ? lg[h] : kNegInf;
+        if (lg_out && valid && lead) lg_out[(size_t)h * slots + tok] = s;
         const float mn = fmaxf(acc.m[h], warp_max(s));
         const float corr = acc.m[h] == kNegInf ? 0.0f : ex2_approx(acc.m[h] - mn);
-        const float p = lane < nt ? ex2_approx(s - mn) : 0.0f;
-        acc.l[h] = acc.l[h] * corr + warp_sum(p);
+        const float p = valid ? ex2_approx(s - mn) : 0.0f;
+        acc.l[h] = acc.l[h] * corr + warp_sum(lead ? p : 0.0f);
 #pragma unroll
         for (int i = 0; i < NO; ++i) acc.o[h][i] *= corr;
         acc.off[h] *= corr;
@@ -252,9 +270,11 @@ __device__ __forceinline__ View tier_view(const TierArgs& t, int npad, int D, in
     return v;
 }
 
-// Called by one thread: the six bulk copies of tokens [j0, j0 + npad) of a tier.
-__device__ void stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
-                           const uint8_t* buf, uint32_t bar) {
+// The six arrays of tokens [j0, j0 + npad) of a tier: fn(global source,
+// bytes, offset in the staged chunk) for each.
+template <typename Fn>
+__device__ __forceinline__ void tier_ranges(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
+                                            Fn fn) {
     const StageSizes z = tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G);
     const void *kc_src, *ks_src, *kz_src;
     if (t.k_axis == KVQ_AXIS_CHANNEL) {
@@ -272,14 +292,22 @@ __device__ void stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int
     const size_t vo = unit * (size_t)t.cap + j0;
     const uint32_t o_ks = a16(z.kc), o_kz = o_ks + a16(z.ks), o_vc = o_kz + a16(z.ks);
     const uint32_t o_vs = o_vc + a16(z.vc), o_vz = o_vs + a16(z.vs);
+    fn(kc_src, z.kc, 0u);
+    fn(ks_src, z.ks, o_ks);
+    fn(kz_src, z.ks, o_kz);
+    fn(t.v_codes + vo * (D * t.v_bits / 32), z.vc, o_vc);
+    fn(t.v_scale + vo * (D / G), z.vs, o_vs);
+    fn(t.v_zero + vo * (D / G), z.vs, o_vz);
+}
+
+// Called by one thread: the six bulk copies of tokens [j0, j0 + npad) of a tier.
+__device__ void stage_tier(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
+                           const uint8_t* buf, uint32_t bar) {
+    const StageSizes z = tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G);
     const uint32_t d = smem_u32(buf);
     mbar_expect_tx(bar, z.kc + 2 * z.ks + z.vc + 2 * z.vs);
-    bulk_load(d, kc_src, z.kc, bar);
-    bulk_load(d + o_ks, ks_src, z.ks, bar);
-    bulk_load(d + o_kz, kz_src, z.ks, bar);
-    bulk_load(d + o_vc, t.v_codes + vo * (D * t.v_bits / 32), z.vc, bar);
-    bulk_load(d + o_vs, t.v_scale + vo * (D / G), z.vs, bar);
-    bulk_load(d + o_vz, t.v_zero + vo * (D / G), z.vs, bar);
+    tier_ranges(t, unit, j0, npad, D, G,
+                [&](const void* src, uint32_t bytes, uint32_t off) { bulk_load(d + off, src, bytes, bar); });
 }
 
 // Called by one thread: residual rows [j0, j0 + n) in logical order (oldest
@@ -319,8 +347,9 @@ template <int KB, int CPL, int NG>
 __device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem<NG, CPL * 32>& sm,
                                                int G, float (&lg)[NG]) {
     constexpr int D = CPL * 32;
+    constexpr int TPW = Cfg<NG>::TPW;
     constexpr int per = 32 / KB;          // tokens per word
-    constexpr int rows = 32 / per;        // word rows per 32-token group
+    constexpr int rows = TPW / per;       // word rows per warp
     const int lane = threadIdx.x & 31;
     const int c0 = lane * CPL;
     float s[CPL], z[CPL];
@@ -351,9 +380,9 @@ __device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem
             off += qs[ci];
             bias = fmaf(qv, z[ci], bias);
         }
-        float part[32];
+        float part[TPW];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) part[k] = 0.0f;
+        for (int k = 0; k < TPW; ++k) part[k] = 0.0f;
 #pragma unroll
         for (int r = 0; r < rows; ++r)
 #pragma unroll
@@ -361,7 +390,7 @@ __device__ __forceinline__ void logits_channel(const View& v, int tl, const Smem
 #pragma unroll
                 for (int i = 0; i < per; ++i)
                     part[r * per + i] = fmaf(code_f<KB>(w[r][ci], i), qs[ci], part[r * per + i]);
-        const float raw = reduce_scatter32(part);
+        const float raw = reduce_scatter<TPW>(part);
         lg[h] = (raw - warp_sum(off)) * (float)(1 << KB) + warp_sum(bias);
     }
 }
@@ -386,7 +415,7 @@ __device__ __forceinline__ void logits_token(const View& v, int tl, Smem<NG, D>&
         for (int i = 0; i < cpw; ++i) qsum[h] += sm.q[h][c0 + i];
     }
 #pragma unroll 4
-    for (int ps = 0; ps < lpt; ++ps) {
+    for (int ps = 0; ps < Cfg<NG>::TPW / tpp; ++ps) {
         const int tk = ps * tpp + to;
         const int row = tl + tk;
         const uint32_t w = v.kc[(size_t)row * lpt + wi];
@@ -409,7 +438,7 @@ __device__ __forceinline__ void logits_token(const View& v, int tl, Smem<NG, D>&
     }
     __syncwarp();
 #pragma unroll
-    for (int h = 0; h < NG; ++h) lg[h] = sm.lg[warp][h][lane];
+    for (int h = 0; h < NG; ++h) lg[h] = sm.lg[warp][h][lane / Cfg<NG>::REP];
     __syncwarp();
 }
 
@@ -424,11 +453,11 @@ __device__ __forceinline__ void values_token(const View& v, int tl, int nt, cons
     const int wi = lane % lpt, to = lane / lpt;
     const int grp = (wi * cpw) / G;
 #pragma unroll 4
-    for (int ps = 0; ps < lpt; ++ps) {
+    for (int ps = 0; ps < Cfg<NG>::TPW / tpp; ++ps) {
         const int tk = ps * tpp + to;
         float pk[NG];
 #pragma unroll
-        for (int h = 0; h < NG; ++h) pk[h] = __shfl_sync(0xffffffffu, p[h], tk);
+        for (int h = 0; h < NG; ++h) pk[h] = __shfl_sync(0xffffffffu, p[h], tk * Cfg<NG>::REP);
         if (tk < nt) {
             const int row = tl + tk;
             const uint32_t w = v.vc[(size_t)row * lpt + wi];
@@ -537,41 +566,23 @@ __device__ __forceinline__ void row_vals(const uint16_t* row, bool bf, float (&x
     }
 }
 
-// 32 lanes each hold v[0..7]; afterwards lanes 4t .. 4t+3 return the sum
-// over lanes of v[t].
-__device__ __forceinline__ float reduce_scatter8(float (&v)[8]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int s = 16, half = 4; s >= 4; s >>= 1, half >>= 1) {
-        const bool up = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = up ? v[i] : v[i + half];
-            const float keep = up ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-    }
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-    return v[0];
-}
-
-// Rows [0, nt) (nt <= 8) of the warp's slice: logits, online softmax and
+// Rows [0, nt) (nt <= RPW) of the warp's slice: logits, online softmax and
 // P.V; the logits go to lg_out (row-indexed) when asked.
 template <int NG, int D>
 __device__ __forceinline__ void residual_rows(const Smem<NG, D>& sm, const uint16_t* rk,
                                               const uint16_t* rv, int nt, bool bf,
                                               WarpAcc<NG, D / 32>& acc, float* lg_out, int slots) {
     constexpr int CPL = D / 32;
+    constexpr int RPW = Cfg<NG>::RPW, LPR = 32 / RPW;   // rows per warp, lanes per row
     const int lane = threadIdx.x & 31;
     const int c0 = lane * CPL;
-    const int t = lane >> 2;                       // the row this lane reports
+    const int t = lane / LPR;                      // the row this lane reports
     float lg[NG];
 #pragma unroll 1
     for (int h = 0; h < NG; ++h) {
-        float part[8];
+        float part[RPW];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < RPW; ++k) {
             part[k] = 0.0f;
             if (k < nt) {
                 float x[CPL];
@@ -580,30 +591,30 @@ __device__ __forceinline__ void residual_rows(const Smem<NG, D>& sm, const uint1
                 for (int ci = 0; ci < CPL; ++ci) part[k] = fmaf(sm.q[h][c0 + ci], x[ci], part[k]);
             }
         }
-        lg[h] = reduce_scatter8(part);
+        lg[h] = reduce_scatter<RPW>(part);
     }
-    const bool valid = t < nt;
+    const bool valid = t < nt, lead = lane % LPR == 0;
 #pragma unroll
     for (int h = 0; h < NG; ++h) {
         const float s = valid ? lg[h] : kNegInf;
-        if (lg_out && valid && (lane & 3) == 0) lg_out[(size_t)h * slots + t] = s;
+        if (lg_out && valid && lead) lg_out[(size_t)h * slots + t] = s;
         const float mn = fmaxf(acc.m[h], warp_max(s));
         const float corr = acc.m[h] == kNegInf ? 0.0f : ex2_approx(acc.m[h] - mn);
         const float p = valid ? ex2_approx(s - mn) : 0.0f;
-        acc.l[h] = acc.l[h] * corr + warp_sum((lane & 3) == 0 ? p : 0.0f);
+        acc.l[h] = acc.l[h] * corr + warp_sum(lead ? p : 0.0f);
 #pragma unroll
         for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] *= corr;
         acc.m[h] = mn;
         lg[h] = p;
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < RPW; ++k) {
         if (k < nt) {
             float x[CPL];
             row_vals<CPL>(rv + (size_t)k * D + c0, bf, x);
 #pragma unroll
             for (int h = 0; h < NG; ++h) {
-                const float pk = __shfl_sync(0xffffffffu, lg[h], 4 * k);
+                const float pk = __shfl_sync(0xffffffffu, lg[h], LPR * k);
 #pragma unroll
                 for (int ci = 0; ci < CPL; ++ci) acc.o[h][ci] = fmaf(pk, x[ci], acc.o[h][ci]);
             }
@@ -627,6 +638,33 @@ __device__ __forceinline__ int item_kind(const UnitState& us, int n_tiers, int k
 // First local index of CTA r (items r, r + C, ...) at or after global item k.
 __device__ __forceinline__ int local_at(int k, int r, int C) { return k > r ? (k - r + C - 1) / C : 0; }
 
+// Called by one thread at the start, while another thread reads the unit's
+// counters: L2 prefetches of what this CTA will most likely stage first (its
+// first two sub-chunks of tier 0 at full capacity and a 1/C share of the
+// residual ring), and of the new token's rows the leader appends at the end.
+__device__ void prefetch_start(const DecodeArgs& a, size_t unit, int r) {
+    const int C = a.cluster, D = a.D;
+    const TierArgs& t0 = a.tier[0];
+    const int nsub = (t0.cap + kSub - 1) / kSub;
+    for (int k = r, i = 0; k < nsub && i < 2; k += C, ++i) {
+        const int j0 = k * kSub;
+        tier_ranges(t0, unit, j0, min(kSub, t0.cap - j0), D, a.G,
+                    [&](const void* src, uint32_t bytes, uint32_t) {
+                        if (bytes) bulk_prefetch_l2(src, bytes);
+                    });
+    }
+    const int share = (a.res_cap + C - 1) / C, r0 = r * share, n = min(share, a.res_cap - r0);
+    if (n > 0) {
+        const uint32_t bytes = (uint32_t)n * D * 2;
+        bulk_prefetch_l2(reinterpret_cast<const uint16_t*>(a.res_k) + (unit * a.res_cap + r0) * D, bytes);
+        bulk_prefetch_l2(reinterpret_cast<const uint16_t*>(a.res_v) + (unit * a.res_cap + r0) * D, bytes);
+    }
+    if (r == 0) {
+        bulk_prefetch_l2(reinterpret_cast<const uint16_t*>(a.k_new) + unit * D, (uint32_t)D * 2);
+        bulk_prefetch_l2(reinterpret_cast<const uint16_t*>(a.v_new) + unit * D, (uint32_t)D * 2);
+    }
+}
+
 // Called by one thread: the bulk copies of local item i into buffer i & 1.
 __device__ void issue_item(const DecodeArgs& a, const UnitState& us, size_t unit, int r, int i,
                            uint8_t* stage_base, const unsigned long long* bars) {
@@ -646,10 +684,17 @@ __device__ void issue_item(const DecodeArgs& a, const UnitState& us, size_t unit
     }
 }
 
-// Waits for local item i; the next-but-one item is requested once every
-// warp is done with this one (in the caller, after its compute).
+// Waits for local item i: thread 0 polls the mbarrier (bounded), the others
+// sleep in the CTA barrier and then observe the completed phase themselves
+// (one test each, which acquires the copied bytes).  The next-but-one item
+// is requested once every warp is done with this one (release_item).
 __device__ __forceinline__ bool wait_item(unsigned long long* bars, int i, bool ok) {
-    return __syncthreads_and(ok && mbar_wait(smem_u32(&bars[i & 1]), (i >> 1) & 1, nullptr));
+    const uint32_t bar = smem_u32(&bars[i & 1]), par = (uint32_t)(i >> 1) & 1u;
+    bool mine = true;
+    if (threadIdx.x == 0) mine = ok && mbar_wait(bar, par, nullptr);
+    const bool all = __syncthreads_and(mine) != 0;
+    if (all) (void)mbar_try_wait(bar, par);
+    return all;
 }
 
 __device__ __forceinline__ void release_item(const DecodeArgs& a, const UnitState& us, size_t unit,
@@ -670,6 +715,7 @@ __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t uni
     const TierArgs& ta = a.tier[t];
     const UnitState& us = sm.us;
     const int warp = threadIdx.x >> 5;
+    constexpr int TPW = Cfg<NG>::TPW;
     WarpAcc<NG, 32 / VB> acc;
     acc_init(acc);
     for (int i = i0; i < i1; ++i) {
@@ -678,16 +724,16 @@ __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t uni
             const int j0 = (r + i * a.cluster - us.base[t]) * kSub;
             const int n = min(kSub, us.cnt[t] - j0);
             const View v = tier_view(ta, (n + 31) & ~31, D, a.G, stage_base + (size_t)(i & 1) * a.stage_bytes);
-            const int tl = warp * 32;
+            const int tl = warp * TPW;
             if (tl < n) {
-                const int nt = min(32, n - tl);
+                const int nt = min(TPW, n - tl);
                 float lg[NG];
                 if (KAX == KVQ_AXIS_CHANNEL)
                     logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
                 else
                     logits_token<KB, D, NG>(v, tl, sm, a.G, lg);
                 float* lo = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + ta.slot_base + j0 + tl : nullptr;
-                group_softmax(acc, lg, nt, lo, a.slots);
+                group_softmax<Cfg<NG>::REP>(acc, lg, nt, lo, a.slots);
                 values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
             }
         }
@@ -696,16 +742,515 @@ __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t uni
     flush_token_values<VB, D, NG>(acc, sm);
 }
 
+// ---- tensor-core path for per-token tiers (GQA groups, D = 128, G = 32)
+//
+// Each warp takes 32 tokens of an item.  Logits: mma.m16n8k16 with the
+// query group as A (16 rows: row 2h holds head h's query rounded to fp16,
+// row 2h + 1 the fp16 rounding remainder, so that the pair carries the
+// float32 query) and the packed key codes as B, each code turned into the
+// fp16 value 1 + c / 2^KB by one rotate and one LOP3 (two codes per 32-bit
+// register).  The channels of a k-step are permuted so that both codes of
+// a register come from one packed word; the query side uses the same
+// permutation.  One accumulator per 32-channel group takes the token's
+// scale and zero in float32 afterwards.  P.V: the probabilities (again a
+// hi / lo row pair) are the A operand straight from the logit accumulators;
+// B holds the value codes of two tokens per register (byte permute, shift,
+// LOP3) times their fp16 scale (one fused multiply-add, one rounding); the
+// zero points are summed per group in float32.
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> f16x2 (round to nearest), lo in the low half.
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float h2lo(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x & 0xffffu))); }
+__device__ __forceinline__ float h2hi(uint32_t x) { return __half2float(__ushort_as_half((unsigned short)(x >> 16))); }
+
+// Codes j and j + 16/KB of a packed word (bits KB*j and KB*j + 16) as the
+// f16x2 pair (1 + c_j / 2^KB, 1 + c_{j+16/KB} / 2^KB).
+template <int KB>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, int j) {
+    const int rot = ((10 - KB - KB * j) % 32 + 32) % 32;
+    const uint32_t x = __funnelshift_l(w, w, rot);
+    constexpr uint32_t m = ((1u << KB) - 1u) << (10 - KB);
+    return (x & (m | (m << 16))) | 0x3C003C00u;
+}
+
+// Channels (lo, hi) of the register b (0: k 2t..2t+1, 1: k 2t+8..2t+9) of
+// thread t in k-step s, and the word of the token row that holds them.
+template <int KB>
+__device__ __forceinline__ void kchan(int s, int t, int b, int& word, int& j, int& c_lo, int& c_hi) {
+    const int grp = s >> 1, e = s & 1;
+    if (KB == 4) {                       // word 4 grp + t, pairs (j, j + 4)
+        word = 4 * grp + t;
+        j = 2 * e + b;
+        c_lo = 8 * word + j;
+        c_hi = c_lo + 4;
+    } else if (KB == 8) {                // words 8 grp + 2t + e, pairs (j, j + 2)
+        word = 8 * grp + 2 * t + e;
+        j = b;
+        c_lo = 4 * word + j;
+        c_hi = c_lo + 2;
+    } else {                             // KB == 2: word 2 grp + t/2, pairs (j, j + 8)
+        word = 2 * grp + (t >> 1);
+        j = 4 * (t & 1) + 2 * e + b;
+        c_lo = 16 * word + j;
+        c_hi = c_lo + 8;
+    }
+}
+
+template <int NG>
+struct MmaAcc {
+    static constexpr int RI = NG > 4 ? 2 : 1;   // rows g (and g + 8) in use
+    float m[RI], l[RI];
+    float o[16][4];                              // [channel n-tile][rows g, g+8 x channels 2t, 2t+1]
+    float zs[RI][4];                             // sum of p * zero per value group
+};
+
+// Query fragments for the channel permutation of KB-bit keys, and the
+// per-group sums of each fragment row.
+template <int KB, int NG, int D>
+__device__ __forceinline__ void build_qa(const Smem<NG, D>& sm, uint32_t (&qa)[8][4], float (&qs)[4][2]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    auto part = [&](int row, int c) -> float {
+        const int h = row >> 1;
+        if (h >= NG) return 0.0f;
+        const float x = sm.q[h][c];
+        const float hi = __half2float(__float2half_rn(x));
+        return (row & 1) ? __half2float(__float2half_rn(x - hi)) : hi;
+    };
+#pragma unroll
+    for (int grp = 0; grp < 4; ++grp) qs[grp][0] = qs[grp][1] = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            int word, j, c_lo, c_hi;
+            kchan<KB>(s, t, b, word, j, c_lo, c_hi);
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                const int row = g + 8 * ri;
+                const float x0 = part(row, c_lo), x1 = part(row, c_hi);
+                qa[s][2 * b + ri] = pack_h2(x0, x1);
+                qs[s >> 1][ri] += x0 + x1;
+            }
+        }
+    }
+#pragma unroll
+    for (int grp = 0; grp < 4; ++grp)
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+            qs[grp][ri] += __shfl_xor_sync(0xffffffffu, qs[grp][ri], 1);
+            qs[grp][ri] += __shfl_xor_sync(0xffffffffu, qs[grp][ri], 2);
+        }
+}
+
+// Logits of the warp's 32 tokens, keys per token (KB bits):
+// S[n-tile][rows g, g+8 x tokens 2t, 2t+1], hi and lo rows not yet summed.
+template <int KB, int NG, int NT>
+__device__ __forceinline__ void mma_logits_token(const View& v, int tl, const uint32_t (&qa)[8][4],
+                                                 const float (&qs)[4][2], float (&S)[NT][4]) {
+    constexpr int D = 128, GR = 4;                       // channels, 32-channel groups
+    constexpr int RI = MmaAcc<NG>::RI;
+    constexpr int kw = D * KB / 32;                      // words per token row
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S[n][i] = 0.0f;
+#pragma unroll
+    for (int grp = 0; grp < GR; ++grp) {
+        float R[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) R[n][i] = 0.0f;
+            const uint32_t* row = v.kc + (size_t)(tl + 8 * n + g) * kw;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                int w0, j0, c0, c1, w1, j1;
+                kchan<KB>(2 * grp + e, t, 0, w0, j0, c0, c1);
+                kchan<KB>(2 * grp + e, t, 1, w1, j1, c0, c1);
+                const uint32_t b0 = code_pair<KB>(row[w0], j0);
+                const uint32_t b1 = code_pair<KB>(row[w1], j1);
+                mma16816(R[n], qa[2 * grp + e], b0, b1);
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int tok = tl + 8 * n + 2 * t + jj;
+                const float s = h2f_bits(v.ks[tok * GR + grp]) * (float)(1 << KB);
+                const float zp = h2f_bits(v.kz[tok * GR + grp]) - s;
+#pragma unroll
+                for (int ri = 0; ri < RI; ++ri)
+                    S[n][2 * ri + jj] = fmaf(s, R[n][2 * ri + jj], fmaf(qs[grp][ri], zp, S[n][2 * ri + jj]));
+            }
+    }
+}
+
+// Logits of the warp's 32 tokens, keys per channel (INT2, one scale row for
+// the 32 tokens): the query times the channel scales, as hi / lo fp16 rows,
+// goes through the warp's shared rows qf (A operand); the codes of two
+// channels of one token meet in one register by a byte permute.
+template <int NG, int NT>
+__device__ __forceinline__ void mma_logits_channel(const View& v, int tl, int G, const float (&q)[NG][128],
+                                                   uint16_t (&qf)[2 * NG][128], float (&S)[NT][4]) {
+    constexpr int D = 128;
+    static_assert(NG <= 4, "rows g only");
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // A rows for this scale row, and the per-row constants
+    const uint16_t* ks = v.ks + (size_t)(tl / G) * D;
+    const uint16_t* kz = v.kz + (size_t)(tl / G) * D;
+    float cst[2 * NG];
+#pragma unroll
+    for (int h = 0; h < NG; ++h) {
+        float shi = 0.0f, slo = 0.0f, bias = 0.0f;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+            const int c = lane + 32 * i;
+            const float x = q[h][c] * h2f_bits(ks[c]);
+            const __half hi = __float2half_rn(x);
+            const __half lo = __float2half_rn(x - __half2float(hi));
+            qf[2 * h][c] = __half_as_ushort(hi);
+            qf[2 * h + 1][c] = __half_as_ushort(lo);
+            shi += __half2float(hi);
+            slo += __half2float(lo);
+            bias = fmaf(q[h][c], h2f_bits(kz[c]), bias);
+        }
+        // S = 4 (R - sum A) over both rows + sum q z (added once, on the hi row)
+        cst[2 * h] = warp_sum(bias) - 4.0f * warp_sum(shi);
+        cst[2 * h + 1] = -4.0f * warp_sum(slo);
+    }
+    __syncwarp();
+    float my_cst = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 2 * NG; ++r)
+        if (g == r) my_cst = cst[r];
+    uint32_t a[8][4];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        a[s][0] = g < 2 * NG ? *reinterpret_cast<const uint32_t*>(&qf[g < 2 * NG ? g : 0][16 * s + 2 * t]) : 0u;
+        a[s][2] = g < 2 * NG ? *reinterpret_cast<const uint32_t*>(&qf[g < 2 * NG ? g : 0][16 * s + 2 * t + 8]) : 0u;
+        a[s][1] = a[s][3] = 0u;
+    }
+    __syncwarp();
+    float R[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) R[n][i] = 0.0f;
+    // token 8 n + g of the warp sits in word row (tl + 8 n) / 16 at code 8 (n & 1) + g
+    const int qb = g >> 2, sh = 2 * (g & 3);
+    const uint32_t sel = (uint32_t)qb | ((uint32_t)(2 + qb) << 4) | ((uint32_t)(4 + qb) << 8) |
+                         ((uint32_t)(6 + qb) << 12);
+#pragma unroll
+    for (int rr = 0; rr < NT / 2; ++rr) {
+        const uint32_t* row = v.kc + (size_t)(tl / 16 + rr) * D;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(row + 16 * s + 2 * t);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(row + 16 * s + 2 * t + 8);
+            const uint32_t y0 = __byte_perm(w0.x, w0.y, sel), y1 = __byte_perm(w1.x, w1.y, sel);
+            // n = 2 rr (codes 0..7 of the row) and n = 2 rr + 1 (codes 8..15)
+            const uint32_t e0 = ((y0 << (8 - sh)) & 0x03000300u) | 0x3C003C00u;
+            const uint32_t e1 = ((y1 << (8 - sh)) & 0x03000300u) | 0x3C003C00u;
+            const uint32_t o0 = ((y0 >> sh) & 0x03000300u) | 0x3C003C00u;
+            const uint32_t o1 = ((y1 >> sh) & 0x03000300u) | 0x3C003C00u;
+            mma16816(R[2 * rr], a[s], e0, e1);
+            mma16816(R[2 * rr + 1], a[s], o0, o1);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) S[n][jj] = fmaf(4.0f, R[n][jj], my_cst);
+}
+
+// Online softmax of the warp's logits (hi and lo rows summed first), the
+// logits written out when asked; S holds p afterwards.
+template <int NG, int NT>
+__device__ __forceinline__ void mma_softmax(float (&S)[NT][4], int nt, MmaAcc<NG>& acc, float* lg_out,
+                                            int slots) {
+    constexpr int RI = MmaAcc<NG>::RI, GR = 4;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // hi + lo rows: lanes g = 2h and 2h + 1 both end with head h's logits
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 2 * RI; ++i) S[n][i] += __shfl_xor_sync(0xffffffffu, S[n][i], 4);
+    // ---- online softmax per row; the running max moves only when it rises by
+    // more than 2^8 (exact: the final division uses the same reference)
+#pragma unroll
+    for (int ri = 0; ri < RI; ++ri) {
+        const int h = (g + 8 * ri) >> 1;
+        float mx = kNegInf;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+                if (8 * n + 2 * t + jj < nt) mx = fmaxf(mx, S[n][2 * ri + jj]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (h < NG && (acc.m[ri] == kNegInf ? mx != kNegInf : mx > acc.m[ri] + 8.0f)) {
+            const float corr = acc.m[ri] == kNegInf ? 0.0f : ex2_approx(acc.m[ri] - mx);
+            acc.m[ri] = mx;
+            acc.l[ri] *= corr;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                acc.o[c][2 * ri] *= corr;
+                acc.o[c][2 * ri + 1] *= corr;
+            }
+#pragma unroll
+            for (int grp = 0; grp < GR; ++grp) acc.zs[ri][grp] *= corr;
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int k = 8 * n + 2 * t + jj;
+                const bool valid = h < NG && k < nt;
+                if (lg_out && valid && !(g & 1)) lg_out[(size_t)h * slots + k] = S[n][2 * ri + jj];
+                const float p = valid ? ex2_approx(S[n][2 * ri + jj] - acc.m[ri]) : 0.0f;
+                acc.l[ri] += p;
+                S[n][2 * ri + jj] = p;
+            }
+    }
+}
+
+// P.V of the warp's tokens over k-steps of 16, values per token (VB bits).
+template <int VB, int NG, int NT>
+__device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const float (&S)[NT][4], MmaAcc<NG>& acc) {
+    constexpr int D = 128, GR = 4;
+    constexpr int RI = MmaAcc<NG>::RI;
+    constexpr int vw = D * VB / 32;                      // words per token row
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const bool lo_row = (g & 1) != 0;
+#pragma unroll
+    for (int ks = 0; ks < NT / 2; ++ks) {
+        uint32_t pa[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {            // n-tiles 2ks (a0, a1) and 2ks + 1 (a2, a3)
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                uint32_t x = 0;
+                if (ri < RI) {
+                    const float p0 = S[2 * ks + half][2 * ri], p1 = S[2 * ks + half][2 * ri + 1];
+                    x = pack_h2(p0, p1);
+                    if (lo_row) x = pack_h2(p0 - h2lo(x), p1 - h2hi(x));
+                }
+                pa[2 * half + ri] = x;
+            }
+        }
+        // tokens of b0: 2t, 2t+1; of b1: 2t+8, 2t+9 (within the k-step)
+        const int ta = tl + 16 * ks + 2 * t;
+        const uint32_t* ra = v.vc + (size_t)ta * vw;
+        const uint32_t* rb = ra + vw;
+        const uint32_t* rc = ra + 8 * vw;
+        const uint32_t* rd = rc + vw;
+        // value scales of the four tokens as f16x2 pairs (b0: ta, ta+1; b1: ta+8, ta+9) x 2^VB
+        uint32_t sc0[GR], sc1[GR];
+        // tokens from nt on (stale slots of the staged chunk) get scale and zero 0:
+        // their p is 0 and their value must be an exact, finite 0
+        const int k0 = 16 * ks + 2 * t;
+        const bool va = k0 < nt, vb = k0 + 1 < nt, vc = k0 + 8 < nt, vd = k0 + 9 < nt;
+        {
+            const uint2 z2 = make_uint2(0u, 0u);
+            const uint2 sa = va ? *reinterpret_cast<const uint2*>(v.vs + ta * GR) : z2;
+            const uint2 sb = vb ? *reinterpret_cast<const uint2*>(v.vs + (ta + 1) * GR) : z2;
+            const uint2 scc = vc ? *reinterpret_cast<const uint2*>(v.vs + (ta + 8) * GR) : z2;
+            const uint2 sd = vd ? *reinterpret_cast<const uint2*>(v.vs + (ta + 9) * GR) : z2;
+            const __half2 mul = __float2half2_rn((float)(1 << VB));
+#pragma unroll
+            for (int grp = 0; grp < GR; ++grp) {
+                const uint32_t wa = grp < 2 ? sa.x : sa.y, wb = grp < 2 ? sb.x : sb.y;
+                const uint32_t wc = grp < 2 ? scc.x : scc.y, wd = grp < 2 ? sd.x : sd.y;
+                const uint32_t sel = (grp & 1) ? 0x7632u : 0x5410u;
+                const uint32_t p0 = __byte_perm(wa, wb, sel), p1 = __byte_perm(wc, wd, sel);
+                const __half2 h0 = __hmul2(*reinterpret_cast<const __half2*>(&p0), mul);
+                const __half2 h1 = __hmul2(*reinterpret_cast<const __half2*>(&p1), mul);
+                sc0[grp] = *reinterpret_cast<const uint32_t*>(&h0);
+                sc1[grp] = *reinterpret_cast<const uint32_t*>(&h1);
+            }
+        }
+        // zero points: sum of p * z per group (hi rows carry the full p)
+#pragma unroll
+        for (int ri = 0; ri < RI; ++ri)
+#pragma unroll
+            for (int grp = 0; grp < GR; ++grp) {
+                const float pa0 = S[2 * ks][2 * ri], pa1 = S[2 * ks][2 * ri + 1];
+                const float pc0 = S[2 * ks + 1][2 * ri], pc1 = S[2 * ks + 1][2 * ri + 1];
+                float z = acc.zs[ri][grp];
+                if (va) z = fmaf(pa0, h2f_bits(v.vz[ta * GR + grp]), z);
+                if (vb) z = fmaf(pa1, h2f_bits(v.vz[(ta + 1) * GR + grp]), z);
+                if (vc) z = fmaf(pc0, h2f_bits(v.vz[(ta + 8) * GR + grp]), z);
+                if (vd) z = fmaf(pc1, h2f_bits(v.vz[(ta + 9) * GR + grp]), z);
+                acc.zs[ri][grp] = z;
+            }
+        // channel c = 8 n + g of n-tile n
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const int grp = n >> 2;
+            uint32_t x0, x1;
+            if (VB == 4) {                                   // word n, nibble g of the word
+                const uint32_t sel = (uint32_t)(g >> 1) | ((uint32_t)(4 + (g >> 1)) << 8);
+                const int sh = 6 - 4 * (g & 1);
+                x0 = __byte_perm(ra[n], rb[n], sel) << sh;
+                x1 = __byte_perm(rc[n], rd[n], sel) << sh;
+                x0 = (x0 & 0x03C003C0u) | 0x3C003C00u;
+                x1 = (x1 & 0x03C003C0u) | 0x3C003C00u;
+            } else {                                         // VB == 2: word n/2, code 8 (n&1) + g
+                const int q = g >> 2;
+                const uint32_t sel = (uint32_t)q | ((uint32_t)(2 + q) << 4) | ((uint32_t)(4 + q) << 8) |
+                                     ((uint32_t)(6 + q) << 12);
+                const uint32_t y0 = __byte_perm(ra[n >> 1], rb[n >> 1], sel);
+                const uint32_t y1 = __byte_perm(rc[n >> 1], rd[n >> 1], sel);
+                const int sh = 2 * (g & 3);
+                x0 = (n & 1) ? (y0 >> sh) : (y0 << (8 - sh));
+                x1 = (n & 1) ? (y1 >> sh) : (y1 << (8 - sh));
+                x0 = (x0 & 0x03000300u) | 0x3C003C00u;
+                x1 = (x1 & 0x03000300u) | 0x3C003C00u;
+            }
+            // s * c = 2^VB s (1 + c / 2^VB) - 2^VB s, one rounding
+            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc0[grp]);
+            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc1[grp]);
+            const __half2 v0 = __hfma2(*reinterpret_cast<const __half2*>(&x0), s0, __hneg2(s0));
+            const __half2 v1 = __hfma2(*reinterpret_cast<const __half2*>(&x1), s1, __hneg2(s1));
+            mma16816(acc.o[n], pa, *reinterpret_cast<const uint32_t*>(&v0), *reinterpret_cast<const uint32_t*>(&v1));
+        }
+    }
+}
+
+// Hi + lo rows, zero points and the quad's partial sums; merge into the
+// warp's shared-memory state (lanes of the hi rows write).
 template <int NG, int D>
+__device__ __forceinline__ void flush_mma(MmaAcc<NG>& acc, Smem<NG, D>& sm) {
+    constexpr int RI = MmaAcc<NG>::RI;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int i = 0; i < 2 * RI; ++i) acc.o[n][i] += __shfl_xor_sync(0xffffffffu, acc.o[n][i], 4);
+#pragma unroll
+    for (int ri = 0; ri < RI; ++ri) {
+        acc.l[ri] += __shfl_xor_sync(0xffffffffu, acc.l[ri], 1);
+        acc.l[ri] += __shfl_xor_sync(0xffffffffu, acc.l[ri], 2);
+#pragma unroll
+        for (int grp = 0; grp < 4; ++grp) {
+            acc.zs[ri][grp] += __shfl_xor_sync(0xffffffffu, acc.zs[ri][grp], 1);
+            acc.zs[ri][grp] += __shfl_xor_sync(0xffffffffu, acc.zs[ri][grp], 2);
+        }
+    }
+    __syncwarp();
+    float fo[RI], fn[RI];
+#pragma unroll
+    for (int ri = 0; ri < RI; ++ri) {
+        const int h = (g + 8 * ri) >> 1;
+        fo[ri] = fn[ri] = 0.0f;
+        if (h < NG && !(g & 1)) {
+            const float mo = sm.wm[warp][h];
+            const float M = fmaxf(mo, acc.m[ri]);
+            fo[ri] = mo == kNegInf ? 0.0f : ex2_approx(mo - M);
+            fn[ri] = acc.m[ri] == kNegInf ? 0.0f : ex2_approx(acc.m[ri] - M);
+            const float L = sm.wl[warp][h] * fo[ri] + acc.l[ri] * fn[ri];
+            __syncwarp(0xFu << (4 * g));             // the quad has read the old state
+            if (t == 0) {
+                sm.wm[warp][h] = M;
+                sm.wl[warp][h] = L;
+            }
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int c = 8 * n + 2 * t + jj;
+                    float* p = &sm.wo[warp][h][c];
+                    *p = *p * fo[ri] + (acc.o[n][2 * ri + jj] + acc.zs[ri][n >> 2]) * fn[ri];
+                }
+        }
+    }
+    __syncwarp();
+}
+
+// Local items [i0, i1) of a tier on the tensor cores.
+template <int KB, int KAX, int VB, int NG>
+__device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size_t unit, int r, int i0,
+                             int i1, int n_local, uint8_t* stage_base, float* lg_unit, bool& ok,
+                             int& issued) {
+    constexpr int TPW = Cfg<NG>::TPW;
+    static_assert(TPW == 16 || TPW == 32, "whole n-tile pairs per warp");
+    const TierArgs& ta = a.tier[t];
+    const UnitState& us = sm.us;
+    const int warp = threadIdx.x >> 5;
+    uint32_t qa[KAX == KVQ_AXIS_TOKEN ? 8 : 1][4];
+    float qs[4][2];
+    if constexpr (KAX == KVQ_AXIS_TOKEN) build_qa<KB, NG, 128>(sm, qa, qs);
+    MmaAcc<NG> acc;
+#pragma unroll
+    for (int ri = 0; ri < MmaAcc<NG>::RI; ++ri) {
+        acc.m[ri] = kNegInf;
+        acc.l[ri] = 0.0f;
+#pragma unroll
+        for (int grp = 0; grp < 4; ++grp) acc.zs[ri][grp] = 0.0f;
+    }
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc.o[n][i] = 0.0f;
+    for (int i = i0; i < i1; ++i) {
+        ok = wait_item(sm.bar, i, ok);
+        if (ok) {
+            const int j0 = (r + i * a.cluster - us.base[t]) * kSub;
+            const int n = min(kSub, us.cnt[t] - j0);
+            const View v = tier_view(ta, (n + 31) & ~31, 128, a.G, stage_base + (size_t)(i & 1) * a.stage_bytes);
+            const int tl = warp * TPW;
+            if (tl < n) {
+                float* lo = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + ta.slot_base + j0 + tl : nullptr;
+                constexpr int NT = TPW / 8;
+                float S[NT][4];
+                if constexpr (KAX == KVQ_AXIS_CHANNEL)
+                    mma_logits_channel<NG, NT>(v, tl, a.G, sm.q, sm.qf[warp], S);
+                else
+                    mma_logits_token<KB, NG, NT>(v, tl, qa, qs, S);
+                const int nt = min(TPW, n - tl);
+                mma_softmax<NG, NT>(S, nt, acc, lo, a.slots);
+                mma_pv<VB, NG, NT>(v, tl, nt, S, acc);
+            }
+        }
+        release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
+    }
+    flush_mma<NG, 128>(acc, sm);
+}
+
+// FAM selects the formats compiled into one kernel: bit 0 keys per channel
+// (MiniKV), bit 1 keys per token (DiffKV, MiKV tiers).
+template <int NG, int D, int FAM>
 __device__ void dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t unit, int r, int i0,
                               int i1, int n_local, uint8_t* stage, float* lg_unit, bool& ok, int& issued) {
     const TierArgs& ta = a.tier[t];
     const int kb = ta.k_bits, vb = ta.v_bits, ax = ta.k_axis;
-    if (ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) {
-        run_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued);
+    if ((FAM & 1) && ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) {
+        if constexpr (D == 128 && NG <= 4)
+            run_tier_mma<2, KVQ_AXIS_CHANNEL, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued);
+        else
+            run_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued);
         return;
     }
-    if (D == 128) {
+    if constexpr ((FAM & 2) && D == 128 && NG >= 2) {
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier_mma<8, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier_mma<4, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier_mma<4, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier_mma<2, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+    } else if constexpr ((FAM & 2) && D == 128) {
         if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
@@ -737,11 +1282,11 @@ __device__ void run_residual(const DecodeArgs& a, Smem<NG, D>& sm, size_t unit, 
             const uint8_t* buf = stage_base + (size_t)(i & 1) * a.stage_bytes;
             const uint16_t* rk = reinterpret_cast<const uint16_t*>(buf);
             const uint16_t* rv = reinterpret_cast<const uint16_t*>(buf + a16((uint32_t)n * D * 2));
-            const int w0 = warp * 8;
+            const int w0 = warp * Cfg<NG>::RPW;
             if (w0 < n) {
                 float* lo = (lg_unit && a.policy != KVQ_POLICY_MINIKV) ? lg_unit + a.res_slot_base + j0 + w0 : nullptr;
-                residual_rows<NG, D>(sm, rk + (size_t)w0 * D, rv + (size_t)w0 * D, min(8, n - w0), bf, acc, lo,
-                                     a.slots);
+                residual_rows<NG, D>(sm, rk + (size_t)w0 * D, rv + (size_t)w0 * D, min(Cfg<NG>::RPW, n - w0), bf,
+                                     acc, lo, a.slots);
             }
         }
         release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
@@ -834,8 +1379,9 @@ __device__ bool minikv_flush(const DecodeArgs& a, size_t unit, int start, int cn
 // ---- the kernel
 
 // Grid = (C, units), cluster (C, 1, 1): CTA r of the cluster of unit u.
-template <int NG, int D>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
+template <int NG, int D, int FAM>
+__global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kernel(DecodeArgs a) {
+    constexpr int W = Cfg<NG>::W;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<NG, D>& sm = *reinterpret_cast<Smem<NG, D>*>(smem_raw);
     float* part = reinterpret_cast<float*>(smem_raw + a.part_off);   // leader: [C][NG][D + 2]
@@ -847,6 +1393,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     const bool bf = a.bf16 != 0;
 
     cluster_arrive_relaxed();                   // "started": the leader's shared memory exists
+    if (threadIdx.x == 32) prefetch_start(a, unit, r);
     int issued = 0;                             // thread 0: local items requested so far
     if (threadIdx.x == 0) {
         UnitState& us = sm.us;
@@ -878,11 +1425,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
         const int h = x / D, c = x % D;
         sm.q[h][c] = ldf(a.q, ((size_t)b * a.Hq + (size_t)hkv * NG + h) * D + c, bf) * a.scale_log2;
     }
-    for (int x = threadIdx.x; x < kWarps * NG; x += blockDim.x) {
+    for (int x = threadIdx.x; x < W * NG; x += blockDim.x) {
         sm.wm[x / NG][x % NG] = kNegInf;
         sm.wl[x / NG][x % NG] = 0.0f;
     }
-    for (int x = threadIdx.x; x < kWarps * NG * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
+    for (int x = threadIdx.x; x < W * NG * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
     __syncthreads();
 
     const UnitState& us = sm.us;
@@ -891,7 +1438,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
     bool ok = true;
     for (int t = 0; t < a.n_tiers; ++t) {
         const int i0 = local_at(us.base[t], r, C), i1 = local_at(us.base[t + 1], r, C);
-        if (i1 > i0) dispatch_tier<NG, D>(a, sm, t, unit, r, i0, i1, n_local, stage_base, lg_unit, ok, issued);
+        if (i1 > i0) dispatch_tier<NG, D, FAM>(a, sm, t, unit, r, i0, i1, n_local, stage_base, lg_unit, ok, issued);
     }
     {
         const int i0 = local_at(us.base[a.n_tiers], r, C);
@@ -913,11 +1460,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
             const int h = x / D, c = x % D;
             float M = kNegInf;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+            for (int w = 0; w < W; ++w) M = fmaxf(M, sm.wm[w][h]);
             float L = 0.0f, O = 0.0f;
             if (M != kNegInf) {
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
+                for (int w = 0; w < W; ++w) {
                     const float f = sm.wm[w][h] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][h] - M);
                     L = fmaf(sm.wl[w][h], f, L);
                     O = fmaf(sm.wo[w][h][c], f, O);
@@ -936,23 +1483,26 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a) {
 
     // ---- leader: merge the C partials, write o and lse
     if (r == 0) {
-        if (threadIdx.x < NG) {
-            const int h = threadIdx.x;
-            float M = kNegInf;
-            for (int y = 0; y < C; ++y) {
-                const float* p = part + ((size_t)y * NG + h) * (D + 2);
-                if (p[1] > 0.0f) M = fmaxf(M, p[0]);
+        if (threadIdx.x < 32) {
+            // lane y holds partial y (C <= 32)
+            const int y = threadIdx.x;
+            for (int h = 0; h < NG; ++h) {
+                float m = kNegInf, l = 0.0f;
+                if (y < C) {
+                    const float* p = part + ((size_t)y * NG + h) * (D + 2);
+                    l = p[1];
+                    m = l > 0.0f ? p[0] : kNegInf;
+                }
+                const float M = warp_max(m);
+                const float w = m == kNegInf ? 0.0f : ex2_approx(m - M);
+                const float L = warp_sum(l * w);
+                if (y < C) sm.cw[y][h] = w;
+                if (y == 0) {
+                    sm.lsum[h] = L;
+                    sm.lse2[h] = M + __log2f(L);
+                    if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
+                }
             }
-            float L = 0.0f;
-            for (int y = 0; y < C; ++y) {
-                const float* p = part + ((size_t)y * NG + h) * (D + 2);
-                const float w = (p[1] > 0.0f && p[0] != kNegInf) ? ex2_approx(p[0] - M) : 0.0f;
-                L = fmaf(p[1], w, L);
-                sm.cw[y][h] = w;
-            }
-            sm.lsum[h] = L;
-            sm.lse2[h] = M + __log2f(L);
-            if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
         }
         __syncthreads();
         for (int x = threadIdx.x; x < NG * D; x += blockDim.x) {
@@ -1027,7 +1577,7 @@ int items_bound(const kvq_cache& c) {
     return n + (c.res_cap + kResItem - 1) / kResItem;
 }
 
-template <int NG, int D>
+template <int NG, int D, int FAM>
 cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s) {
     uint32_t stage = 2u * a16((uint32_t)kResItem * D * 2);
     for (int t = 0; t < c.n_tiers; ++t)
@@ -1040,7 +1590,7 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     int cmax = kMaxCluster;
     while (cmax > 1 && (uint32_t)cmax * slot_bytes > 32u * 1024u) cmax >>= 1;
 
-    auto kern = decode_kernel<NG, D>;
+    auto kern = decode_kernel<NG, D, FAM>;
     static bool attr_done = false, wide_ok = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1052,8 +1602,12 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
         attr_done = true;
     }
     if (!wide_ok) cmax = std::min(cmax, 8);
-    // CTAs per unit: the largest power of two (at most 16) that keeps the grid
-    // within one wave of resident CTAs and gives every CTA at least one item.
+    // CTAs per unit (a power of two, at most cmax and at most the items): as
+    // many as one wave of resident CTAs holds (small caches: the shortest
+    // chain per CTA), or, when the units alone fill the GPU, the most that
+    // still leave every CTA kMinItemsPerCta items (large caches: enough
+    // clusters to smooth the wave tail, few enough that each CTA's fixed
+    // cost stays small against its stream).
     static int last_key[4] = {-1, -1, -1, -1}, last_C = 1;
     const int items = items_bound(c);
     const int key[4] = {units, items, (int)stage, c.n_tiers};
@@ -1063,11 +1617,14 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem_for(cmax));
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg<NG>::kThreads, smem_for(cmax));
         if (e != cudaSuccess) return e;
         const long resident = (long)std::max(per_sm, 1) * sms;
-        C = 1;
-        while (C * 2 <= cmax && (long)units * C * 2 <= resident && C * 2 <= items) C *= 2;
+        int c_fill = 1, c_items = 1;
+        while (c_fill * 2 <= std::min(cmax, items) && (long)units * c_fill * 2 <= resident) c_fill *= 2;
+        while (c_items * 2 <= std::min(cmax, items) && (items + 2 * c_items - 1) / (2 * c_items) >= kMinItemsPerCta)
+            c_items *= 2;
+        C = std::max(c_fill, c_items);
         for (; C > 1; C >>= 1) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute at[1];
@@ -1076,7 +1633,7 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
             at[0].val.clusterDim.y = 1;
             at[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3((unsigned)C, (unsigned)units);
-            cfg.blockDim = dim3(kThreads);
+            cfg.blockDim = dim3(Cfg<NG>::kThreads);
             cfg.dynamicSmemBytes = smem_for(C);
             cfg.attrs = at;
             cfg.numAttrs = 1;
@@ -1098,7 +1655,7 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)C, (unsigned)units);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Cfg<NG>::kThreads);
     cfg.dynamicSmemBytes = smem_for(C);
     cfg.stream = s;
     cfg.attrs = at;
@@ -1165,12 +1722,22 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.slots = w.slots;
     a.logits = c.policy != KVQ_POLICY_MINIKV ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + w.logits)
                                              : nullptr;
-    if (a.g == 1 && c.D == 128) return launch_typed<1, 128>(a, c, units, s);
-    if (a.g == 1 && c.D == 64) return launch_typed<1, 64>(a, c, units, s);
-    if (a.g == 2 && c.D == 128) return launch_typed<2, 128>(a, c, units, s);
-    if (a.g == 4 && c.D == 128) return launch_typed<4, 128>(a, c, units, s);
-    if (a.g == 5 && c.D == 128) return launch_typed<5, 128>(a, c, units, s);
-    if (a.g == 8 && c.D == 128) return launch_typed<8, 128>(a, c, units, s);
+    bool channel_only = true;
+    for (int t = 0; t < c.n_tiers; ++t) channel_only &= c.tier[t].k_axis == KVQ_AXIS_CHANNEL;
+    if (c.D == 64) return a.g == 1 ? launch_typed<1, 64, 1>(a, c, units, s) : cudaErrorInvalidConfiguration;
+    if (c.D != 128) return cudaErrorInvalidConfiguration;
+    switch (a.g * 2 + (channel_only ? 0 : 1)) {
+        case 2: return launch_typed<1, 128, 1>(a, c, units, s);
+        case 3: return launch_typed<1, 128, 3>(a, c, units, s);
+        case 4: return launch_typed<2, 128, 1>(a, c, units, s);
+        case 5: return launch_typed<2, 128, 3>(a, c, units, s);
+        case 8: return launch_typed<4, 128, 1>(a, c, units, s);
+        case 9: return launch_typed<4, 128, 3>(a, c, units, s);
+        case 10: return launch_typed<5, 128, 1>(a, c, units, s);
+        case 11: return launch_typed<5, 128, 3>(a, c, units, s);
+        case 16: return launch_typed<8, 128, 1>(a, c, units, s);
+        case 17: return launch_typed<8, 128, 3>(a, c, units, s);
+    }
     return cudaErrorInvalidConfiguration;
 }
 
