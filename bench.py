@@ -70,6 +70,48 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+KERNEL_SOURCES = {
+    "decode_kernel": ["bit_mixed_precision_gb300/csrc/decode.cu", "bit_mixed_precision_gb300/csrc/kvq_common.cuh",
+                      "bit_mixed_precision_gb300/csrc/pack_device.cuh"],
+}
+
+
+def sources_sha256(kernel):
+    """Hash of the source files that make up a kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json) when
+    it was taken on this workload from the kernel's current sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("workload") != workload or d.get("source_sha256") != sources_sha256(kernel):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def job_ms(step_ms, world, device):
+    """The slowest rank's step time (every rank calls this; replicas, no data exchange)."""
+    if world <= 1:
+        return step_ms
+    t = torch.tensor([step_ms], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, tokens_per_rank, ms):
+    """Whole-job decoded tokens per second: every rank decodes its own replica."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 def _budget(wl):
     """(heavy-hitter budget, window) of a MiniKV workload, integer form of the percentages."""
     T = wl["T"]
@@ -328,12 +370,8 @@ def run_ours(args, wl, rank, world):
     pre_ms = statistics.median(pre)
     B = wl["B"]
     dec_tokens = B * steps
-    ms_max = step_ms
-    if world > 1:
-        tt = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tt.item())
-    value = world * dec_tokens / (ms_max / 1e3)
+    ms_max = job_ms(step_ms, world, dev)
+    value = job_value(world, dec_tokens, ms_max)
     dec_ms_per_launch = seg["decode"] / n_dec
     dbytes, _ = hot.decode_bytes()
     dec_bytes = float(np.mean(dbytes))
@@ -360,7 +398,7 @@ def run_ours(args, wl, rank, world):
         "segments_ms_per_step": {k2: v2 / args.steps for k2, v2 in seg.items()},
         "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": _traffic("decode_kernel", args.workload),
                      "peak_source": f"{peak_src} hbm_gbs (of measured)" if peak_src == "measured"
                                     else "fallback 6800 GB/s"},
         "roofline_prefill": {"kernel": "prefill_pass1_kernel + prefill_pass2_kernel", "bound": "tensor",

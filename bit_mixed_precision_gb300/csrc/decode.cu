@@ -1397,21 +1397,26 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
     int issued = 0;                             // thread 0: local items requested so far
     if (threadIdx.x == 0) {
         UnitState& us = sm.us;
+        // all counters requested at once, then checked
+        int raw[KVQ_MAX_TIERS];
+#pragma unroll
+        for (int t = 0; t < KVQ_MAX_TIERS; ++t) raw[t] = t < a.n_tiers ? a.tier[t].count[unit] : 0;
+        const int rl = a.res_len[unit], rs = a.res_start[unit], ps = a.pos[unit];
         bool bad = false;
         us.base[0] = 0;
-        for (int t = 0; t < a.n_tiers; ++t) {
-            const int raw = a.tier[t].count[unit];
-            const int n = min(max(raw, 0), a.tier[t].cap);
-            bad |= raw != n;
+#pragma unroll
+        for (int t = 0; t < KVQ_MAX_TIERS; ++t) {
+            if (t >= a.n_tiers) break;
+            const int n = min(max(raw[t], 0), a.tier[t].cap);
+            bad |= raw[t] != n;
             us.cnt[t] = n;
             us.base[t + 1] = us.base[t] + (n + kSub - 1) / kSub;
         }
         const int cap = a.res_cap;
-        const int rl = a.res_len[unit], rs = a.res_start[unit];
         us.len = min(max(rl, 0), cap - 1);
         us.start = min(max(rs, 0), cap - 1);
         bad |= rl != us.len || rs != us.start;
-        us.pos = a.pos[unit];
+        us.pos = ps;
         us.total = us.base[a.n_tiers] + (us.len + 1 + kResItem - 1) / kResItem;
         if (bad) atomicOr(&g_status_decode, kDevCheck);
         mbar_init(smem_u32(&sm.bar[0]), 1);
