@@ -16,6 +16,8 @@
 // One CTA per unit for every per-unit decision; radix select with ties to
 // the lower position; tier slots are filled in a fixed order so results
 // are deterministic.
+#include <algorithm>
+
 #include "kvq_internal.h"
 #include "pack_device.cuh"
 #include "topk_device.cuh"
@@ -115,27 +117,45 @@ __device__ void put_raw_token(const PolicyArgs& a, const TierDev& t, size_t unit
 // ----------------------------------------------------------------- MiniKV
 
 // Token ids, residual and counters after the two packing launches.
-__global__ void minikv_build_tail(PolicyArgs a, int npk, int r0) {
+// Grid (units, row blocks): each warp copies whole residual rows with
+// 16-byte vectors; block 0 of a unit also writes the packed tokens' ids and
+// the counters.
+constexpr int kTailRows = 8;          // residual rows per CTA (one per warp)
+__global__ void __launch_bounds__(kTailRows * 32) minikv_build_tail(PolicyArgs a, int npk, int r0) {
     const size_t unit = blockIdx.x;
     const int32_t* sel = a.sel_idx + unit * (size_t)a.n_sel;
     const TierDev& t = a.tier[0];
-    for (int i = threadIdx.x; i < npk; i += blockDim.x) t.token_id[unit * t.cap + i] = sel[i];
-    const bool bf = a.bf16 != 0;
-    for (int idx = threadIdx.x; idx < r0 * a.D; idx += blockDim.x) {
-        const int i = idx / a.D, c = idx % a.D;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.y * kTailRows + warp;             // residual row of this warp
+    if (i < r0) {
         const int pos = sel[npk + i];
-        const size_t src = (unit * a.T + pos) * (size_t)a.D + c;
-        const size_t dst = (unit * a.res_cap + i) * (size_t)a.D + c;
-        copy_act(a.res_k, dst, a.k_src, src, bf);
-        copy_act(a.res_v, dst, a.v_src, src, bf);
+        if (pos < 0 || pos >= a.T) {
+            if (lane == 0) atomicOr(&g_status_policy, kDevCheck);
+        } else {
+            const int vec = a.D * 2 / 16;                    // 16-byte pieces per row
+            const uint4* ks = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const uint16_t*>(a.k_src) + (unit * a.T + pos) * (size_t)a.D);
+            const uint4* vs = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const uint16_t*>(a.v_src) + (unit * a.T + pos) * (size_t)a.D);
+            uint4* kd = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.res_k) +
+                                                 (unit * a.res_cap + i) * (size_t)a.D);
+            uint4* vd = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.res_v) +
+                                                 (unit * a.res_cap + i) * (size_t)a.D);
+            for (int e = lane; e < 2 * vec; e += 32) {
+                if (e < vec) kd[e] = ks[e];
+                else vd[e - vec] = vs[e - vec];
+            }
+            if (lane == 0) a.res_token_id[unit * a.res_cap + i] = pos;
+        }
     }
-    for (int i = threadIdx.x; i < r0; i += blockDim.x)
-        a.res_token_id[unit * a.res_cap + i] = sel[npk + i];
-    if (threadIdx.x == 0) {
-        t.count[unit] = npk;
-        a.res_start[unit] = 0;
-        a.res_len[unit] = r0;
-        a.seq_len[unit] = a.T;
+    if (blockIdx.y == 0) {
+        for (int k = threadIdx.x; k < npk; k += blockDim.x) t.token_id[unit * t.cap + k] = sel[k];
+        if (threadIdx.x == 0) {
+            t.count[unit] = npk;
+            a.res_start[unit] = 0;
+            a.res_len[unit] = r0;
+            a.seq_len[unit] = a.T;
+        }
     }
 }
 
@@ -549,7 +569,8 @@ kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, 
                 set_error("requant_demote (MiniKV pack): %s", cudaGetErrorString(e));
                 return KVQ_ECUDA;
             }
-            minikv_build_tail<<<units, 256, 0, s>>>(a, npk, r0);
+            minikv_build_tail<<<dim3(units, (unsigned)std::max(1, (r0 + kTailRows - 1) / kTailRows)),
+                                kTailRows * 32, 0, s>>>(a, npk, r0);
             return launched("MiniKV build");
         }
         // the residual flush runs inside decode_attn_qkv (its last step)

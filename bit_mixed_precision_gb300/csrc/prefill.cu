@@ -500,14 +500,6 @@ __global__ void __launch_bounds__(192, 2)
             if (!warp_wait(BAR(C_LSE + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
             if (!warp_wait(BAR(C_SF + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            float s[128];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                tmem_ld32(tmem + lane_base + (uint32_t)buf * 128u + (uint32_t)c4 * 32u, s + c4 * 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(C_SFREE + buf));
             const float* ls = lse_s + buf * kTile;
             // eight independent partial sums; the causal mask only matters on the
             // diagonal tile (later query tiles hold positions >= every key here)
@@ -515,16 +507,38 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
             for (int e = 0; e < 8; ++e) tsp[e] = 0.0f;
             const int qbase = qt * kTile;
-            if (it == 0) {
+            const bool diag = it == 0;
+            // the 128 columns in four TMEM loads of 32, the next one in flight
+            // while the current one is summed
+            auto sum32 = [&](const float (&sv)[32], int c0) {
+                if (diag) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const float x = fmaf(s[c], scale_log2, -ls[c]);
-                    tsp[c & 7] += (qbase + c >= j) ? ex2_approx(x) : 0.0f;
+                    for (int c = 0; c < 32; ++c) {
+                        const float x = fmaf(sv[c], scale_log2, -ls[c0 + c]);
+                        tsp[c & 7] += (qbase + c0 + c >= j) ? ex2_approx(x) : 0.0f;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) tsp[c & 7] += ex2_approx(fmaf(sv[c], scale_log2, -ls[c0 + c]));
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) tsp[c & 7] += ex2_approx(fmaf(s[c], scale_log2, -ls[c]));
-            }
+            };
+            const uint32_t tb = tmem + lane_base + (uint32_t)buf * 128u;
+            float s0[32], s1[32];
+            tmem_ld32(tb, s0);
+            tmem_wait_ld();
+            tmem_ld32(tb + 32u, s1);
+            sum32(s0, 0);
+            tmem_wait_ld();
+            tmem_ld32(tb + 64u, s0);
+            sum32(s1, 32);
+            tmem_wait_ld();
+            tmem_ld32(tb + 96u, s1);
+            sum32(s0, 64);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C_SFREE + buf));
+            sum32(s1, 96);
             acc += ((tsp[0] + tsp[1]) + (tsp[2] + tsp[3])) + ((tsp[4] + tsp[5]) + (tsp[6] + tsp[7]));
         }
         if (!ok) give_up(abort_flag);

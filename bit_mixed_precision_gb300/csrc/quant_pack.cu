@@ -3,7 +3,9 @@
 // codes per INT32 word; review page "Core claim": per-channel keys and
 // per-token values).  Memory-bound; one thread per (group, channel) for
 // the channel grouping (coalesced across channels) and one thread per
-// (token, group) for the token grouping (contiguous G-element runs).
+// (token, group) for the token grouping (contiguous G-element runs).  For
+// G = 32 each thread loads its group into registers once (all loads in
+// flight together); other group sizes take the generic two-pass loop.
 #include "kvq_internal.h"
 #include "pack_device.cuh"
 
@@ -71,11 +73,143 @@ __global__ void quant_token_kernel(const T* __restrict__ x, int T_len, int D,
     }
 }
 
+// ---- the configs' group of 32, values held in registers (one load each)
+
+template <int BITS>
+__device__ __forceinline__ void pack32(const float (&v)[32], const QParams& p, uint32_t* out, size_t stride) {
+    constexpr int per = 32 / BITS;
+#pragma unroll
+    for (int w = 0; w < BITS; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < per; ++k) word |= quant_code(v[w * per + k], p, BITS) << (BITS * k);
+        out[(size_t)w * stride] = word;
+    }
+}
+
+__device__ __forceinline__ QParams params32(const float (&v)[32], int bits) {
+    float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        mn = fminf(mn, v[i]);
+        mx = fmaxf(mx, v[i]);
+    }
+    return quant_params(__fadd_rn(mn, 0.0f), __fadd_rn(mx, 0.0f), bits);
+}
+
+// Channel grouping with G = 32: each thread takes one channel of the group.
+template <typename T, int BITS>
+__global__ void quant_channel32_kernel(const T* __restrict__ x, int T_len, int D,
+                                       const int32_t* __restrict__ gather, int gstride, int cap,
+                                       uint32_t* __restrict__ codes, uint16_t* __restrict__ scale,
+                                       uint16_t* __restrict__ zero) {
+    __shared__ int pos[32];
+    const int grp = blockIdx.x, unit = blockIdx.y;
+    const T* xu = x + (size_t)unit * T_len * D;
+    bool ok = true;
+    if (threadIdx.x < 32) {
+        const int t = gather ? gather[(size_t)unit * gstride + grp * 32 + threadIdx.x] : grp * 32 + threadIdx.x;
+        pos[threadIdx.x] = t;
+        ok = t >= 0 && t < T_len;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (threadIdx.x == 0) atomicOr(&g_status_quant, kDevCheck);
+        return;
+    }
+    uint32_t* cu = codes + ((size_t)unit * (cap * BITS / 32) + (size_t)grp * BITS) * D;
+    uint16_t* su = scale + ((size_t)unit * (cap / 32) + grp) * D;
+    uint16_t* zu = zero + ((size_t)unit * (cap / 32) + grp) * D;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = Elem<T>::to_f(xu[(size_t)pos[i] * D + c]);
+        const QParams p = params32(v, BITS);
+        pack32<BITS>(v, p, cu + c, D);
+        su[c] = p.s_bits;
+        zu[c] = p.z_bits;
+    }
+}
+
+// Token grouping with G = 32: each thread takes one 32-channel group of a
+// token (four 16-byte loads).
+template <typename T, int BITS>
+__global__ void quant_token32_kernel(const T* __restrict__ x, int T_len, int D,
+                                     const int32_t* __restrict__ gather, int gstride, int n, int cap,
+                                     int units, uint32_t* __restrict__ codes, uint16_t* __restrict__ scale,
+                                     uint16_t* __restrict__ zero) {
+    const int groups = D / 32;
+    const size_t total = (size_t)units * n * groups;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int g = (int)(idx % groups);
+        const size_t rowi = idx / groups;
+        const int i = (int)(rowi % n);
+        const int unit = (int)(rowi / n);
+        const size_t orow = (size_t)unit * cap + i;
+        const int t = gather ? gather[(size_t)unit * gstride + i] : i;
+        if (t < 0 || t >= T_len) {
+            atomicOr(&g_status_quant, kDevCheck);
+            continue;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(x + ((size_t)unit * T_len + t) * D + (size_t)g * 32);
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 w = src[q];
+            const T* e = reinterpret_cast<const T*>(&w);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[8 * q + k] = Elem<T>::to_f(e[k]);
+        }
+        const QParams p = params32(v, BITS);
+        pack32<BITS>(v, p, codes + orow * (D * BITS / 32) + (size_t)g * BITS, 1);
+        scale[orow * groups + g] = p.s_bits;
+        zero[orow * groups + g] = p.z_bits;
+    }
+}
+
+template <typename T, int BITS>
+void launch32(const void* x, int units, int T_len, int D, const int32_t* gather, int gstride, int n, int axis,
+              int cap, uint32_t* codes, uint16_t* scale, uint16_t* zero, cudaStream_t s) {
+    if (axis == KVQ_AXIS_CHANNEL) {
+        dim3 grid(n / 32, units);
+        const int threads = D < 256 ? ((D + 31) / 32) * 32 : 256;
+        quant_channel32_kernel<T, BITS><<<grid, threads, 0, s>>>((const T*)x, T_len, D, gather, gstride, cap, codes,
+                                                                 scale, zero);
+    } else {
+        const size_t total = (size_t)units * n * (D / 32);
+        const int threads = 128;
+        size_t blocks = (total + threads - 1) / threads;
+        if (blocks > 152 * 64) blocks = 152 * 64;
+        quant_token32_kernel<T, BITS><<<(unsigned)blocks, threads, 0, s>>>((const T*)x, T_len, D, gather, gstride, n,
+                                                                         cap, units, codes, scale, zero);
+    }
+}
+
+template <typename T>
+bool launch32_bits(const void* x, int units, int T_len, int D, const int32_t* gather, int gstride, int n, int bits,
+                   int axis, int cap, uint32_t* codes, uint16_t* scale, uint16_t* zero, cudaStream_t s) {
+    switch (bits) {
+        case 2: launch32<T, 2>(x, units, T_len, D, gather, gstride, n, axis, cap, codes, scale, zero, s); return true;
+        case 4: launch32<T, 4>(x, units, T_len, D, gather, gstride, n, axis, cap, codes, scale, zero, s); return true;
+        case 8: launch32<T, 8>(x, units, T_len, D, gather, gstride, n, axis, cap, codes, scale, zero, s); return true;
+    }
+    return false;
+}
+
 cudaError_t launch_quant_pack_strided(const void* x, int dt, int units, int T, int D,
                                       const int32_t* gather, int gstride, int n, int bits, int G,
                                       int axis, int cap, uint32_t* codes, uint16_t* scale,
                                       uint16_t* zero, cudaStream_t s) {
     if (n == 0 || units == 0) return cudaSuccess;
+    // the G = 32 path reads 16-byte vectors: rows of whole vectors, aligned base
+    if (G == 32 && reinterpret_cast<uintptr_t>(x) % 16 == 0 && (D * 2) % 16 == 0) {
+        const bool done = dt == KVQ_F16
+                              ? launch32_bits<__half>(x, units, T, D, gather, gstride, n, bits, axis, cap, codes,
+                                                      scale, zero, s)
+                              : launch32_bits<__nv_bfloat16>(x, units, T, D, gather, gstride, n, bits, axis, cap,
+                                                             codes, scale, zero, s);
+        if (done) return cudaGetLastError();
+    }
     if (axis == KVQ_AXIS_CHANNEL) {
         dim3 grid(n / G, units);
         int threads = D < 256 ? ((D + 31) / 32) * 32 : 256;
