@@ -54,7 +54,7 @@ struct Cfg {
     static constexpr int TPW = kSub / W;        // packed tokens per warp and item
     static constexpr int REP = 32 / TPW;        // lanes holding one token's logit
     static constexpr int RPW = kResItem / W;    // residual rows per warp and item
-    static constexpr int MINB = NG == 1 ? 4 : 1; // resident CTAs per SM the registers must allow
+    static constexpr int MINB = NG == 1 ? 4 : (NG <= 4 ? 3 : 2); // resident CTAs per SM the registers must allow
 };
 
 struct TierArgs {
@@ -168,6 +168,7 @@ struct Smem {
     float wo[Cfg<NG>::W][NG][D];
     float lg[Cfg<NG>::W][NG][32];        // logits of the warp's current group
     uint16_t qf[Cfg<NG>::W][NG <= 4 ? 2 * NG : 1][128];  // per-channel keys: query x scales, hi / lo rows
+    uint4 qa[8][32];                     // per-token keys: the query's A fragments, [k-step][lane]
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
     float lsum[NG];
@@ -810,16 +811,19 @@ __device__ __forceinline__ void kchan(int s, int t, int b, int& word, int& j, in
 
 template <int NG>
 struct MmaAcc {
-    static constexpr int RI = NG > 4 ? 2 : 1;   // rows g (and g + 8) in use
-    float m[RI], l[RI];
-    float o[16][4];                              // [channel n-tile][rows g, g+8 x channels 2t, 2t+1]
-    float zs[RI][4];                             // sum of p * zero per value group
+    static constexpr int RI = NG > 4 ? 2 : 1;   // blocks of 4 heads (8 hi / lo rows)
+    float m[RI], l[RI];                          // logit layout: row g + 8 ri
+    // P.V layout, D = V^T P: [16-channel m-tile][head block][channel g, g+8 x rows 2t, 2t+1],
+    // i.e. this lane holds head 4 ri + t (hi and lo rows) for channels 16 mt + g and + 8
+    float o[8][RI][4];
+    float zs[RI][4];                             // sum of p * zero per value group (logit layout)
 };
 
 // Query fragments for the channel permutation of KB-bit keys, and the
 // per-group sums of each fragment row.
 template <int KB, int NG, int D>
-__device__ __forceinline__ void build_qa(const Smem<NG, D>& sm, uint32_t (&qa)[8][4], float (&qs)[4][2]) {
+__device__ __forceinline__ void build_qa(Smem<NG, D>& sm, float (&qs)[4][2]) {
+    uint32_t qa[8][4];
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     auto part = [&](int row, int c) -> float {
         const int h = row >> 1;
@@ -852,12 +856,15 @@ __device__ __forceinline__ void build_qa(const Smem<NG, D>& sm, uint32_t (&qa)[8
             qs[grp][ri] += __shfl_xor_sync(0xffffffffu, qs[grp][ri], 1);
             qs[grp][ri] += __shfl_xor_sync(0xffffffffu, qs[grp][ri], 2);
         }
+    if (threadIdx.x < 32)                                // every warp holds the same values
+#pragma unroll
+        for (int st = 0; st < 8; ++st) sm.qa[st][lane] = make_uint4(qa[st][0], qa[st][1], qa[st][2], qa[st][3]);
 }
 
 // Logits of the warp's 32 tokens, keys per token (KB bits):
 // S[n-tile][rows g, g+8 x tokens 2t, 2t+1], hi and lo rows not yet summed.
 template <int KB, int NG, int NT>
-__device__ __forceinline__ void mma_logits_token(const View& v, int tl, const uint32_t (&qa)[8][4],
+__device__ __forceinline__ void mma_logits_token(const View& v, int tl, const uint4 (&qa)[8][32],
                                                  const float (&qs)[4][2], float (&S)[NT][4]) {
     constexpr int D = 128, GR = 4;                       // channels, 32-channel groups
     constexpr int RI = MmaAcc<NG>::RI;
@@ -882,7 +889,9 @@ __device__ __forceinline__ void mma_logits_token(const View& v, int tl, const ui
                 kchan<KB>(2 * grp + e, t, 1, w1, j1, c0, c1);
                 const uint32_t b0 = code_pair<KB>(row[w0], j0);
                 const uint32_t b1 = code_pair<KB>(row[w1], j1);
-                mma16816(R[n], qa[2 * grp + e], b0, b1);
+                const uint4 q4 = qa[2 * grp + e][lane];
+                const uint32_t af[4] = {q4.x, q4.y, q4.z, q4.w};
+                mma16816(R[n], af, b0, b1);
             }
         }
 #pragma unroll
@@ -1002,17 +1011,22 @@ __device__ __forceinline__ void mma_softmax(float (&S)[NT][4], int nt, MmaAcc<NG
                 if (8 * n + 2 * t + jj < nt) mx = fmaxf(mx, S[n][2 * ri + jj]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        float corr = 1.0f;
         if (h < NG && (acc.m[ri] == kNegInf ? mx != kNegInf : mx > acc.m[ri] + 8.0f)) {
-            const float corr = acc.m[ri] == kNegInf ? 0.0f : ex2_approx(acc.m[ri] - mx);
+            corr = acc.m[ri] == kNegInf ? 0.0f : ex2_approx(acc.m[ri] - mx);
             acc.m[ri] = mx;
             acc.l[ri] *= corr;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                acc.o[c][2 * ri] *= corr;
-                acc.o[c][2 * ri + 1] *= corr;
-            }
-#pragma unroll
             for (int grp = 0; grp < GR; ++grp) acc.zs[ri][grp] *= corr;
+        }
+        // the output of head 4 ri + t sits in this lane's column: its factor comes
+        // from row 2t of the block (lane 8t)
+        if (__any_sync(0xffffffffu, corr != 1.0f)) {
+            const float cc = __shfl_sync(0xffffffffu, corr, 8 * t);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc.o[mt][ri][i] *= cc;
         }
 #pragma unroll
         for (int n = 0; n < NT; ++n)
@@ -1028,7 +1042,10 @@ __device__ __forceinline__ void mma_softmax(float (&S)[NT][4], int nt, MmaAcc<NG
     }
 }
 
-// P.V of the warp's tokens over k-steps of 16, values per token (VB bits).
+// P.V of the warp's tokens over k-steps of 16, values per token (VB bits):
+// D = V^T P with the value codes (times their fp16 scale) as the A operand,
+// 16 channels by 16 tokens, and the probabilities (hi / lo rows) as B,
+// straight from the logit accumulators.
 template <int VB, int NG, int NT>
 __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const float (&S)[NT][4], MmaAcc<NG>& acc) {
     constexpr int D = 128, GR = 4;
@@ -1038,30 +1055,26 @@ __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const floa
     const bool lo_row = (g & 1) != 0;
 #pragma unroll
     for (int ks = 0; ks < NT / 2; ++ks) {
-        uint32_t pa[4];
+        // B: p of rows g (+ 8 ri) for tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1)
+        uint32_t pb[RI][2];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {            // n-tiles 2ks (a0, a1) and 2ks + 1 (a2, a3)
+        for (int ri = 0; ri < RI; ++ri)
 #pragma unroll
-            for (int ri = 0; ri < 2; ++ri) {
-                uint32_t x = 0;
-                if (ri < RI) {
-                    const float p0 = S[2 * ks + half][2 * ri], p1 = S[2 * ks + half][2 * ri + 1];
-                    x = pack_h2(p0, p1);
-                    if (lo_row) x = pack_h2(p0 - h2lo(x), p1 - h2hi(x));
-                }
-                pa[2 * half + ri] = x;
+            for (int half = 0; half < 2; ++half) {
+                const float p0 = S[2 * ks + half][2 * ri], p1 = S[2 * ks + half][2 * ri + 1];
+                uint32_t x = pack_h2(p0, p1);
+                if (lo_row) x = pack_h2(p0 - h2lo(x), p1 - h2hi(x));
+                pb[ri][half] = x;
             }
-        }
-        // tokens of b0: 2t, 2t+1; of b1: 2t+8, 2t+9 (within the k-step)
         const int ta = tl + 16 * ks + 2 * t;
         const uint32_t* ra = v.vc + (size_t)ta * vw;
         const uint32_t* rb = ra + vw;
         const uint32_t* rc = ra + 8 * vw;
         const uint32_t* rd = rc + vw;
-        // value scales of the four tokens as f16x2 pairs (b0: ta, ta+1; b1: ta+8, ta+9) x 2^VB
-        uint32_t sc0[GR], sc1[GR];
+        // value scales of the token pairs (ta, ta+1) and (ta+8, ta+9) as f16x2 x 2^VB;
         // tokens from nt on (stale slots of the staged chunk) get scale and zero 0:
         // their p is 0 and their value must be an exact, finite 0
+        uint32_t sc0[GR], sc1[GR];
         const int k0 = 16 * ks + 2 * t;
         const bool va = k0 < nt, vb = k0 + 1 < nt, vc = k0 + 8 < nt, vd = k0 + 9 < nt;
         {
@@ -1097,50 +1110,50 @@ __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const floa
                 if (vd) z = fmaf(pc1, h2f_bits(v.vz[(ta + 9) * GR + grp]), z);
                 acc.zs[ri][grp] = z;
             }
-        // channel c = 8 n + g of n-tile n
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const int grp = n >> 2;
-            uint32_t x0, x1;
-            if (VB == 4) {                                   // word n, nibble g of the word
+        // codes of channel c for the token pairs: f16x2 (1 + c_a / 2^VB, 1 + c_b / 2^VB)
+        auto pair = [&](uint32_t wa, uint32_t wb, bool high) -> uint32_t {
+            if (VB == 4) {                               // channel nibble g of the word
                 const uint32_t sel = (uint32_t)(g >> 1) | ((uint32_t)(4 + (g >> 1)) << 8);
-                const int sh = 6 - 4 * (g & 1);
-                x0 = __byte_perm(ra[n], rb[n], sel) << sh;
-                x1 = __byte_perm(rc[n], rd[n], sel) << sh;
-                x0 = (x0 & 0x03C003C0u) | 0x3C003C00u;
-                x1 = (x1 & 0x03C003C0u) | 0x3C003C00u;
-            } else {                                         // VB == 2: word n/2, code 8 (n&1) + g
-                const int q = g >> 2;
+                const uint32_t x = __byte_perm(wa, wb, sel) << (6 - 4 * (g & 1));
+                return (x & 0x03C003C0u) | 0x3C003C00u;
+            } else {                                     // codes g (low) and g + 8 (high) of the word
+                const int q = g >> 2, sh = 2 * (g & 3);
                 const uint32_t sel = (uint32_t)q | ((uint32_t)(2 + q) << 4) | ((uint32_t)(4 + q) << 8) |
                                      ((uint32_t)(6 + q) << 12);
-                const uint32_t y0 = __byte_perm(ra[n >> 1], rb[n >> 1], sel);
-                const uint32_t y1 = __byte_perm(rc[n >> 1], rd[n >> 1], sel);
-                const int sh = 2 * (g & 3);
-                x0 = (n & 1) ? (y0 >> sh) : (y0 << (8 - sh));
-                x1 = (n & 1) ? (y1 >> sh) : (y1 << (8 - sh));
-                x0 = (x0 & 0x03000300u) | 0x3C003C00u;
-                x1 = (x1 & 0x03000300u) | 0x3C003C00u;
+                const uint32_t y = __byte_perm(wa, wb, sel);
+                const uint32_t x = high ? (y >> sh) : (y << (8 - sh));
+                return (x & 0x03000300u) | 0x3C003C00u;
             }
-            // s * c = 2^VB s (1 + c / 2^VB) - 2^VB s, one rounding
-            const __half2 s0 = *reinterpret_cast<const __half2*>(&sc0[grp]);
-            const __half2 s1 = *reinterpret_cast<const __half2*>(&sc1[grp]);
-            const __half2 v0 = __hfma2(*reinterpret_cast<const __half2*>(&x0), s0, __hneg2(s0));
-            const __half2 v1 = __hfma2(*reinterpret_cast<const __half2*>(&x1), s1, __hneg2(s1));
-            mma16816(acc.o[n], pa, *reinterpret_cast<const uint32_t*>(&v0), *reinterpret_cast<const uint32_t*>(&v1));
+        };
+        // s * c = 2^VB s (1 + c / 2^VB) - 2^VB s, one rounding
+        auto scaled = [&](uint32_t x, uint32_t sc) -> uint32_t {
+            const __half2 s2 = *reinterpret_cast<const __half2*>(&sc);
+            const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&x), s2, __hneg2(s2));
+            return *reinterpret_cast<const uint32_t*>(&r);
+        };
+        // m-tile mt: channels 16 mt + g (rows g) and 16 mt + g + 8 (rows g + 8)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int grp = mt >> 1;
+            const int wlo = VB == 4 ? 2 * mt : mt, whi = VB == 4 ? 2 * mt + 1 : mt;
+            uint32_t af[4];
+            af[0] = scaled(pair(ra[wlo], rb[wlo], false), sc0[grp]);
+            af[1] = scaled(pair(ra[whi], rb[whi], true), sc0[grp]);
+            af[2] = scaled(pair(rc[wlo], rd[wlo], false), sc1[grp]);
+            af[3] = scaled(pair(rc[whi], rd[whi], true), sc1[grp]);
+#pragma unroll
+            for (int ri = 0; ri < RI; ++ri) mma16816(acc.o[mt][ri], af, pb[ri][0], pb[ri][1]);
         }
     }
 }
 
-// Hi + lo rows, zero points and the quad's partial sums; merge into the
-// warp's shared-memory state (lanes of the hi rows write).
+// Quad sums of l and the zero points (logit layout); then each lane takes its
+// column's head (4 ri + t): hi + lo rows of o, that head's m, l and zero sums
+// from lane 8t, and merges into the warp's shared-memory state.
 template <int NG, int D>
 __device__ __forceinline__ void flush_mma(MmaAcc<NG>& acc, Smem<NG, D>& sm) {
     constexpr int RI = MmaAcc<NG>::RI;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-#pragma unroll
-        for (int i = 0; i < 2 * RI; ++i) acc.o[n][i] += __shfl_xor_sync(0xffffffffu, acc.o[n][i], 4);
 #pragma unroll
     for (int ri = 0; ri < RI; ++ri) {
         acc.l[ri] += __shfl_xor_sync(0xffffffffu, acc.l[ri], 1);
@@ -1151,34 +1164,39 @@ __device__ __forceinline__ void flush_mma(MmaAcc<NG>& acc, Smem<NG, D>& sm) {
             acc.zs[ri][grp] += __shfl_xor_sync(0xffffffffu, acc.zs[ri][grp], 2);
         }
     }
-    __syncwarp();
-    float fo[RI], fn[RI];
 #pragma unroll
     for (int ri = 0; ri < RI; ++ri) {
-        const int h = (g + 8 * ri) >> 1;
-        fo[ri] = fn[ri] = 0.0f;
-        if (h < NG && !(g & 1)) {
+        const int h = 4 * ri + t;
+        const float m = __shfl_sync(0xffffffffu, acc.m[ri], 8 * t);
+        const float l = __shfl_sync(0xffffffffu, acc.l[ri], 8 * t);
+        float zs[4];
+#pragma unroll
+        for (int grp = 0; grp < 4; ++grp) zs[grp] = __shfl_sync(0xffffffffu, acc.zs[ri][grp], 8 * t);
+        float fo = 0.0f, fn = 0.0f, M = kNegInf, L = 0.0f;
+        if (h < NG) {
             const float mo = sm.wm[warp][h];
-            const float M = fmaxf(mo, acc.m[ri]);
-            fo[ri] = mo == kNegInf ? 0.0f : ex2_approx(mo - M);
-            fn[ri] = acc.m[ri] == kNegInf ? 0.0f : ex2_approx(acc.m[ri] - M);
-            const float L = sm.wl[warp][h] * fo[ri] + acc.l[ri] * fn[ri];
-            __syncwarp(0xFu << (4 * g));             // the quad has read the old state
-            if (t == 0) {
+            M = fmaxf(mo, m);
+            fo = mo == kNegInf ? 0.0f : ex2_approx(mo - M);
+            fn = m == kNegInf ? 0.0f : ex2_approx(m - M);
+            L = sm.wl[warp][h] * fo + l * fn;
+        }
+        __syncwarp();                                // every lane has read the old state
+        if (h < NG) {
+            if (g == 0) {
                 sm.wm[warp][h] = M;
                 sm.wl[warp][h] = L;
             }
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
+            for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int c = 8 * n + 2 * t + jj;
+                for (int hl = 0; hl < 2; ++hl) {
+                    const int c = 16 * mt + g + 8 * hl;
                     float* p = &sm.wo[warp][h][c];
-                    *p = *p * fo[ri] + (acc.o[n][2 * ri + jj] + acc.zs[ri][n >> 2]) * fn[ri];
+                    *p = *p * fo + (acc.o[mt][ri][2 * hl] + acc.o[mt][ri][2 * hl + 1] + zs[mt >> 1]) * fn;
                 }
         }
+        __syncwarp();
     }
-    __syncwarp();
 }
 
 // Local items [i0, i1) of a tier on the tensor cores.
@@ -1191,9 +1209,8 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
     const TierArgs& ta = a.tier[t];
     const UnitState& us = sm.us;
     const int warp = threadIdx.x >> 5;
-    uint32_t qa[KAX == KVQ_AXIS_TOKEN ? 8 : 1][4];
     float qs[4][2];
-    if constexpr (KAX == KVQ_AXIS_TOKEN) build_qa<KB, NG, 128>(sm, qa, qs);
+    if constexpr (KAX == KVQ_AXIS_TOKEN) build_qa<KB, NG, 128>(sm, qs);
     MmaAcc<NG> acc;
 #pragma unroll
     for (int ri = 0; ri < MmaAcc<NG>::RI; ++ri) {
@@ -1203,9 +1220,11 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
         for (int grp = 0; grp < 4; ++grp) acc.zs[ri][grp] = 0.0f;
     }
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
+    for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc.o[n][i] = 0.0f;
+        for (int ri = 0; ri < MmaAcc<NG>::RI; ++ri)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc.o[mt][ri][i] = 0.0f;
     for (int i = i0; i < i1; ++i) {
         ok = wait_item(sm.bar, i, ok);
         if (ok) {
@@ -1220,7 +1239,7 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
                 if constexpr (KAX == KVQ_AXIS_CHANNEL)
                     mma_logits_channel<NG, NT>(v, tl, a.G, sm.q, sm.qf[warp], S);
                 else
-                    mma_logits_token<KB, NG, NT>(v, tl, qa, qs, S);
+                    mma_logits_token<KB, NG, NT>(v, tl, sm.qa, qs, S);
                 const int nt = min(TPW, n - tl);
                 mma_softmax<NG, NT>(S, nt, acc, lo, a.slots);
                 mma_pv<VB, NG, NT>(v, tl, nt, S, acc);
