@@ -10,10 +10,13 @@
 //     warp 5 = MMA issuer: S = Q K^T into one of two TMEM S buffers, then
 //              O += P V into the TMEM O accumulator,
 //     warps 0-3 = softmax: thread r owns query row r (TMEM lane r), reads
-//              its S row, keeps the running max/sum, writes P (fp16/bf16)
-//              into a 128B-swizzled smem tile, rescales O only when its
-//              max grew by more than 2^8 (exact: the final division uses
-//              the same stale max), and finally writes O / l and lse.
+//              its S row, keeps the running max/sum, writes P (fp16) back
+//              over the first half of the same S buffer (the P.V MMA reads
+//              its A operand from TMEM, so P is double-buffered with S and
+//              the next tile's P never waits for this tile's P.V), rescales
+//              O only when its max grew by more than 2^8 (exact: the final
+//              division uses the same stale max), and finally writes O / l
+//              and lse.
 //   pass 2 (column-parallel): CTA = (batch*query head, key tile of 128),
 //     loops over the query tiles at or below the diagonal; S^T = K Q^T in
 //     TMEM; thread r owns key r and sums exp(S - lse_i) over queries, so
@@ -36,7 +39,6 @@ constexpr int kTile = 128;                 // rows per tile (queries or keys)
 constexpr uint32_t kHalfBytes = 128 * 128;       // one 128-row x 64-column 128B-swizzled half
 constexpr int kBN = 64;                          // keys per K/V tile of pass 1
 constexpr uint32_t kKVHalf = kBN * 128;          // one 64-row x 64-column swizzled half
-constexpr uint32_t kPBytes = 128 * kBN * 2;      // P tile of pass 1: 128 rows x 64 keys
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -45,12 +47,11 @@ constexpr float kRescaleLog2 = 8.0f;
 template <int D> struct Layout {
     static constexpr uint32_t kTileBytes = kTile * D * 2;      // D/64 halves
     static constexpr uint32_t kKVBytes = kBN * D * 2;          // pass-1 K or V tile, D/64 halves
-    // pass 1 (about 112 KB at D = 128: two CTAs per SM)
+    // pass 1 (about 96 KB at D = 128: two CTAs per SM; P lives in TMEM)
     static constexpr uint32_t P1_Q = 0;
     static constexpr uint32_t P1_K = P1_Q + kTileBytes;        // 2 stages
     static constexpr uint32_t P1_V = P1_K + 2 * kKVBytes;      // 2 stages
-    static constexpr uint32_t P1_P = P1_V + 2 * kKVBytes;
-    static constexpr uint32_t P1_BAR = P1_P + kPBytes;
+    static constexpr uint32_t P1_BAR = P1_V + 2 * kKVBytes;
     // no alignment slack: two CTAs must fit one SM, so the kernel requires (and
     // checks) a 1024-aligned dynamic shared memory base
     static constexpr uint32_t P1_SMEM = P1_BAR + 256;
@@ -62,8 +63,8 @@ template <int D> struct Layout {
     static constexpr uint32_t P2_SMEM = P2_BAR + 256 + 1024;
 };
 
-enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SFREE = 9, B_PF = 11, B_OD = 12,
-             B_DRAIN = 13, B_VC = 14, P1_NBAR = 16 };
+enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SFREE = 9, B_PF = 11, B_OD = 13,
+             B_DRAIN = 14, B_VC = 15, P1_NBAR = 17 };
 enum P2Bar { C_KF = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_SFREE = 7, C_DRAIN = 9, C_LSE = 10,
              P2_NBAR = 12 };
 
@@ -80,13 +81,6 @@ template <> struct Pack2<__nv_bfloat16> {
         return *reinterpret_cast<uint32_t*>(&h);
     }
 };
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
 
 // Bounded wait whose outcome is the same for every lane of the warp, so that
 // the warp-collective tcgen05.ld/st after it stay convergent.
@@ -131,8 +125,7 @@ __global__ void __launch_bounds__(192, 2)
     constexpr uint32_t kTileBytes = Lay::kTileBytes;
     constexpr uint32_t kKVBytes = Lay::kKVBytes;
     constexpr int kHalves = D / 64;
-    const uint32_t sQ = base + Lay::P1_Q, sK = base + Lay::P1_K, sV = base + Lay::P1_V,
-                   sP = base + Lay::P1_P;
+    const uint32_t sQ = base + Lay::P1_Q, sK = base + Lay::P1_K, sV = base + Lay::P1_V;
     const uint32_t bar0 = base + Lay::P1_BAR;
     auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Lay::P1_BAR + 8 * P1_NBAR);
@@ -153,9 +146,9 @@ __global__ void __launch_bounds__(192, 2)
             mbar_init(BAR(B_VF + s), 1);
             mbar_init(BAR(B_KVE + s), 1);
             mbar_init(BAR(B_SF + s), 1);
-            mbar_init(BAR(B_SFREE + s), 4);
+            mbar_init(BAR(B_SFREE + s), 1);              // P.V of the buffer's tile done
+            mbar_init(BAR(B_PF + s), 4);                 // P of the buffer's tile written
         }
-        mbar_init(BAR(B_PF), 4);
         mbar_init(BAR(B_OD), 1);
         mbar_init(BAR(B_DRAIN), 1);
         mbar_init(BAR(B_VC), 4);
@@ -210,18 +203,22 @@ __global__ void __launch_bounds__(192, 2)
             // P is always fp16; bf16 V tiles are converted to fp16 in smem first
             const uint32_t idPV = idesc_f16(0, 128, D, 1);
             bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
+            // O += P V with P (fp16, two keys per 32-bit column) read from the
+            // first 32 columns of the tile's S buffer
             auto issue_pv = [&](int jj) -> bool {
-                if (!mbar_wait(BAR(B_PF), jj & 1, abort_flag)) return false;
+                if (!mbar_wait(BAR(B_PF + (jj & 1)), (jj >> 1) & 1, abort_flag)) return false;
                 if (!mbar_wait(BAR((AB ? B_VC : B_VF) + (jj & 1)), (jj >> 1) & 1, abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t vt = sV + (uint32_t)(jj & 1) * kKVBytes;
+                const uint32_t tP = tmem + (uint32_t)(jj & 1) * kBN;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    tc_mma_f16(tO, kmajor_desc(sP, kk), mnmajor_desc(vt, kk, kKVHalf), idPV,
-                               (jj > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_ta(tO, tP + (uint32_t)kk * 8u, mnmajor_desc(vt, kk, kKVHalf), idPV,
+                                  (jj > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(BAR(B_OD));
                 tc_commit(BAR(B_KVE + (jj & 1)));
+                tc_commit(BAR(B_SFREE + (jj & 1)));
                 return true;
             };
             for (int j = 0; ok && j < n_kv; ++j) {
@@ -263,9 +260,6 @@ __global__ void __launch_bounds__(192, 2)
             for (int c4 = 0; c4 < kBN / 32; ++c4)
                 tmem_ld32(tmem + lane_base + (uint32_t)sb * kBN + (uint32_t)c4 * 32u, s + c4 * 32);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_SFREE + sb));
             if (AB) {
                 // bf16 -> fp16 of this thread's share of the V tile (exact for |v| < 65504)
                 if (!warp_wait(BAR(B_VF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -313,11 +307,10 @@ __global__ void __launch_bounds__(192, 2)
                                    fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             const float m_new = fmaxf(m_used, mx);
             const bool resc = m_new > m_used + kRescaleLog2;
-            if (j >= 1) {
+            if (__any_sync(0xffffffffu, resc && j >= 1)) {
+                // O is touched only after P.V of the previous tile has finished with it
                 if (!warp_wait(BAR(B_OD), (j - 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, resc && j >= 1)) {
                 const float f = (resc && j >= 1) ? ex2_approx(m_used - m_new) : 1.0f;
 #pragma unroll
                 for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -337,24 +330,22 @@ __global__ void __launch_bounds__(192, 2)
             float rsp[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) rsp[e] = 0.0f;
+            // P (fp16) over the first 32 columns of this tile's S buffer: column c
+            // holds keys 2c (low half) and 2c + 1 (high half) of row r
+            float pk[kBN / 2];
 #pragma unroll
-            for (int c8 = 0; c8 < kBN / 8; ++c8) {
-                float p[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = ex2_approx(s[c8 * 8 + e] - m_used);
-                    rsp[e] += p[e];
-                }
-                const uint32_t off = (uint32_t)(c8 >> 3) * kHalfBytes + (uint32_t)r * 128u +
-                                     ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
-                st_shared_v4(sP + off, Pack2<__half>::pack(p[0], p[1]), Pack2<__half>::pack(p[2], p[3]),
-                             Pack2<__half>::pack(p[4], p[5]), Pack2<__half>::pack(p[6], p[7]));
+            for (int c2 = 0; c2 < kBN / 2; ++c2) {
+                const float p0 = ex2_approx(s[2 * c2] - m_used), p1 = ex2_approx(s[2 * c2 + 1] - m_used);
+                rsp[(2 * c2) & 7] += p0;
+                rsp[(2 * c2 + 1) & 7] += p1;
+                pk[c2] = __uint_as_float(Pack2<__half>::pack(p0, p1));
             }
             l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-            fence_proxy_async_smem();
+            tmem_st32(tmem + lane_base + (uint32_t)sb * kBN, pk);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(B_PF));
+            if (lane == 0) mbar_arrive(BAR(B_PF + sb));
         }
         if (ok && !warp_wait(BAR(B_OD), (n_kv - 1) & 1, abort_flag)) ok = false;
         if (!ok) give_up(abort_flag);
