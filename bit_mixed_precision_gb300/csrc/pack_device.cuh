@@ -57,6 +57,30 @@ __device__ __forceinline__ void quant_token_group(Load load, int G, int bits, ui
     *z_out = p.z_bits;
 }
 
+// Groups of 32 held in registers (every value loaded once): the quantiser
+// parameters of the group, and its BITS words written at out[w * stride].
+template <int BITS>
+__device__ __forceinline__ void pack32(const float (&v)[32], const QParams& p, uint32_t* out, size_t stride) {
+    constexpr int per = 32 / BITS;
+#pragma unroll
+    for (int w = 0; w < BITS; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < per; ++k) word |= quant_code(v[w * per + k], p, BITS) << (BITS * k);
+        out[(size_t)w * stride] = word;
+    }
+}
+
+__device__ __forceinline__ QParams params32(const float (&v)[32], int bits) {
+    float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        mn = fminf(mn, v[i]);
+        mx = fmaxf(mx, v[i]);
+    }
+    return quant_params(__fadd_rn(mn, 0.0f), __fadd_rn(mx, 0.0f), bits);
+}
+
 // Code k of a token-grouped packed row.
 __device__ __forceinline__ uint32_t code_at(const uint32_t* words, int k, int bits) {
     const int per = 32 / bits;

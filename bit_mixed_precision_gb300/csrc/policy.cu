@@ -114,6 +114,40 @@ __device__ void put_raw_token(const PolicyArgs& a, const TierDev& t, size_t unit
     t.token_id[unit * t.cap + slot] = token_id;
 }
 
+// One warp: the same token into a tier slot, group-parallel for G = 32
+// (lanes 0 .. D/32 - 1 take the key groups, the next D/32 lanes the value
+// groups, each group loaded once); other group sizes run serially on lane 0.
+__device__ void put_token_warp(const PolicyArgs& a, const TierDev& t, size_t unit, int slot,
+                               const void* ksrc, const void* vsrc, size_t row_elem, int token_id) {
+    const int lane = threadIdx.x & 31;
+    const int D = a.D, G = a.G, ng = D / G;
+    if (G != 32 || 2 * ng > 32) {
+        if (lane == 0) put_raw_token(a, t, unit, slot, ksrc, vsrc, row_elem, token_id);
+        return;
+    }
+    const bool bf = a.bf16 != 0;
+    if (lane < 2 * ng) {
+        const bool isv = lane >= ng;
+        const int grp = isv ? lane - ng : lane;
+        const void* src = isv ? vsrc : ksrc;
+        const int bits = isv ? t.v_bits : t.k_bits;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = ld_act(src, row_elem + (size_t)grp * 32 + i, bf);
+        const QParams q = params32(v, bits);
+        uint32_t* codes = (isv ? vrow(t, unit, slot, D) : krow(t, unit, slot, D)) + grp * bits;
+        switch (bits) {
+            case 2: pack32<2>(v, q, codes, 1); break;
+            case 4: pack32<4>(v, q, codes, 1); break;
+            default: pack32<8>(v, q, codes, 1); break;
+        }
+        const size_t so = srow(t, unit, slot, D, G) + grp;
+        (isv ? t.v_scale : t.k_scale)[so] = q.s_bits;
+        (isv ? t.v_zero : t.k_zero)[so] = q.z_bits;
+    }
+    if (lane == 0) t.token_id[unit * t.cap + slot] = token_id;
+}
+
 // ----------------------------------------------------------------- MiniKV
 
 // Token ids, residual and counters after the two packing launches.
@@ -259,8 +293,8 @@ __global__ void diffkv_exit(PolicyArgs a) {
         const int slot = t.count[unit];
         if (slot >= t.cap) {
             if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
-        } else if (threadIdx.x == 0) {
-            put_raw_token(a, t, unit, slot, a.res_k, a.res_v, (unit * cap + start) * (size_t)a.D, tc);
+        } else {
+            put_token_warp(a, t, unit, slot, a.res_k, a.res_v, (unit * cap + start) * (size_t)a.D, tc);
         }
     }
     __syncthreads();
@@ -343,9 +377,9 @@ struct MikvShared {
 // Oldest residual token leaves; the top floor(N_q / hi_den) by cumulative
 // score (ties to the lower position) is recomputed; INT4 tokens outside it
 // are re-quantised to INT2 from their dequantised values.
-__global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a) {
+__global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a, int key_cache) {
     __shared__ MikvShared sh;
-    extern __shared__ int32_t holes[];                 // [cap of tier 0]
+    extern __shared__ int32_t holes[];                 // [cap of tier 0], then (key_cache) the keys
     const size_t unit = blockIdx.x;
     const int len = a.res_len[unit];
     if (len <= a.nr) return;
@@ -363,7 +397,14 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a) {
         return i < c0 ? th.token_id[unit * th.cap + i]
                       : (i < c0 + c1 ? tl.token_id[unit * tl.cap + (i - c0)] : e_id);
     };
-    auto key = [&](int i) { return orderable(cum[id_of(i)]); };
+    // the ranking keys of the population, gathered once into shared memory when
+    // they fit (every pass of the selection then reads them from there)
+    uint32_t* kc = reinterpret_cast<uint32_t*>(holes + th.cap);
+    if (key_cache) {
+        for (int i = threadIdx.x; i < nq; i += blockDim.x) kc[i] = orderable(cum[id_of(i)]);
+        __syncthreads();
+    }
+    auto key = [&](int i) { return key_cache ? kc[i] : orderable(cum[id_of(i)]); };
     uint32_t k1 = 0xffffffffu, t1 = 0;
     uint32_t id_star = 0xffffffffu;                    // ties: position <= id_star are in
     if (n4 > 0) {
@@ -467,16 +508,18 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a) {
         mov_base += tot;
     }
     __syncthreads();
-    // the leaving token, quantised from its full-precision values
-    if (threadIdx.x == 0) {
+    // the leaving token, quantised from its full-precision values (warp 0)
+    if (threadIdx.x < 32) {
         const size_t row = (unit * cap + start) * (size_t)D;
         if (e_in) {
-            if (c0n < th.cap) put_raw_token(a, th, unit, c0n, a.res_k, a.res_v, row, e_id);
-            else atomicOr(&g_status_policy, kDevCheck);
+            if (c0n < th.cap) put_token_warp(a, th, unit, c0n, a.res_k, a.res_v, row, e_id);
+            else if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
         } else {
-            if (c1 < tl.cap) put_raw_token(a, tl, unit, c1, a.res_k, a.res_v, row, e_id);
-            else atomicOr(&g_status_policy, kDevCheck);
+            if (c1 < tl.cap) put_token_warp(a, tl, unit, c1, a.res_k, a.res_v, row, e_id);
+            else if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
         }
+    }
+    if (threadIdx.x == 0) {
         th.count[unit] = min(c0n + (e_in ? 1 : 0), th.cap);
         tl.count[unit] = min(c1 + n_dem + (e_in ? 0 : 1), tl.cap);
         a.res_start[unit] = (start + 1) % cap;
@@ -588,15 +631,20 @@ kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, 
         mikv_build<<<units, kTopkBlock, 0, s>>>(a);
         return launched("MiKV build");
     }
+    // holes of tier 0, then the population's keys when both fit in shared memory
     const size_t holes = (size_t)c.tier[0].cap * sizeof(int32_t);
-    if (holes > 48 * 1024) {
+    const size_t keys = ((size_t)c.tier[0].cap + c.tier[1].cap + 1) * sizeof(uint32_t);
+    constexpr size_t kMaxDyn = 200 * 1024;
+    const int key_cache = holes + keys <= kMaxDyn ? 1 : 0;
+    const size_t dyn = key_cache ? holes + keys : holes;
+    if (dyn > 48 * 1024) {
         static bool attr = false;
         if (!attr) {
-            cudaFuncSetAttribute(mikv_step, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            cudaFuncSetAttribute(mikv_step, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDyn);
             attr = true;
         }
     }
-    mikv_step<<<units, kTopkBlock, holes, s>>>(a);
+    mikv_step<<<units, kTopkBlock, dyn, s>>>(a, key_cache);
     return launched("MiKV step");
 }
 

@@ -75,28 +75,6 @@ __global__ void quant_token_kernel(const T* __restrict__ x, int T_len, int D,
 
 // ---- the configs' group of 32, values held in registers (one load each)
 
-template <int BITS>
-__device__ __forceinline__ void pack32(const float (&v)[32], const QParams& p, uint32_t* out, size_t stride) {
-    constexpr int per = 32 / BITS;
-#pragma unroll
-    for (int w = 0; w < BITS; ++w) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int k = 0; k < per; ++k) word |= quant_code(v[w * per + k], p, BITS) << (BITS * k);
-        out[(size_t)w * stride] = word;
-    }
-}
-
-__device__ __forceinline__ QParams params32(const float (&v)[32], int bits) {
-    float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        mn = fminf(mn, v[i]);
-        mx = fmaxf(mx, v[i]);
-    }
-    return quant_params(__fadd_rn(mn, 0.0f), __fadd_rn(mx, 0.0f), bits);
-}
-
 // Channel grouping with G = 32: each thread takes one channel of the group.
 template <typename T, int BITS>
 __global__ void quant_channel32_kernel(const T* __restrict__ x, int T_len, int D,
