@@ -55,6 +55,10 @@ WORKLOADS = {
     "pyramid-layer16": dict(policy="minikv", B=16, Hq=32, Hkv=32, D=128, T=16384, steps=256, nr=0,
                             hh=None, layer=16, n_layers=32, rw=25, n_out=0, out_scale=1.0,
                             key_std=0.5, dtype="f16"),
+    # the whole 32-layer sweep: every layer's budget, one shared synthetic prompt
+    "pyramid": dict(policy="minikv", B=16, Hq=32, Hkv=32, D=128, T=16384, steps=256, nr=0,
+                    hh=None, layer=None, n_layers=32, rw=25, n_out=0, out_scale=1.0,
+                    key_std=0.5, dtype="f16", sweep=True),
     "diffkv": dict(policy="diffkv", B=32, Hq=40, Hkv=8, D=128, T=8192, steps=512, nr=64, n_out=0,
                    out_scale=1.0, dtype="f16"),
     "mikv": dict(policy="mikv", B=64, Hq=32, Hkv=8, D=128, T=32768, steps=1024, nr=128, n_out=1,
@@ -118,7 +122,7 @@ def _budget(wl):
     w = (T * wl["rw"]) // 100
     if wl.get("hh") is None:
         L, l = wl["n_layers"], wl["layer"]
-        k = (T * (40 * (L - 1) - 30 * l)) // (100 * (L - 1))
+        k = (T * (40 * (L - 1) - 30 * l)) // (100 * (L - 1))      # 40% at layer 0 down to 10% at L-1
     else:
         k = (T * wl["hh"]) // 100
     return min(k, T - w), w
@@ -292,6 +296,177 @@ class Hot:
                 extra = 8 * (int(h[t, :-1].sum()) + int(h[t, -1].sum() + h.shape[2]))
             out.append(packed + res + io + extra)
         return out, packed
+
+
+class Sweep:
+    """All layers of the pyramid sweep on one GPU: one synthetic prompt shared by the layers,
+    one MiniKV cache per layer with that layer's heavy-hitter budget."""
+
+    def __init__(self, wl, dev, seed=0):
+        from bit_mixed_precision_gb300 import inputs, kvq
+        self.kvq, self.wl = kvq, wl
+        B, H, D, T, steps, L = wl["B"], wl["Hq"], wl["D"], wl["T"], wl["steps"], wl["n_layers"]
+        self.scale = 1.0 / math.sqrt(D)
+        kstd = inputs.lognormal_key_std(H, D, wl["key_std"], seed)
+        x = inputs.make_qkv(B, H, H, T, D, seed=seed, device=dev, key_std=kstd)
+        self.q, self.k, self.v = x.q, x.k, x.v
+        self.o_pre = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        self.cs = torch.empty_like(self.lse)
+        self.layers = []
+        for l in range(L):
+            k_hh, w = _budget(dict(wl, layer=l))
+            n_sel = k_hh + w
+            r0 = n_sel % G                                    # nr = 0
+            cap = ((n_sel - r0 + steps) // G + 1) * G
+            cache = kvq.make_cache(B, H, H, D, G, torch.float16, kvq.POLICY_MINIKV,
+                                   [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=0, device=dev)
+            self.layers.append(dict(k_hh=k_hh, w=w, n_sel=n_sel, r0=r0, cache=cache,
+                                    kh=torch.full((B * H,), k_hh, dtype=torch.int32, device=dev),
+                                    idx=torch.empty((B, H, n_sel), dtype=torch.int32, device=dev),
+                                    nout=torch.empty((B * H,), dtype=torch.int32, device=dev)))
+        # decode inputs of one step (the same for every layer), refreshed before each step
+        self.dec = [inputs.make_decode_step(B, H, H, D, t, seed=seed, device=dev, key_std=kstd)
+                    for t in range(steps)]
+        self.qd = torch.empty_like(self.dec[0][0])
+        self.kd = torch.empty_like(self.dec[0][1])
+        self.vd = torch.empty_like(self.dec[0][2])
+        self.o_dec = torch.empty((L, B, H, D), dtype=torch.float16, device=dev)
+        self.graph = None
+        self.prefill_flops = 3 * D * T * T * B * H * L
+        self.launches_per_step = L * (2 + 1 + 3 + steps)
+
+    def prefill_build(self, s):
+        kvq = self.kvq
+        for ly in self.layers:
+            kvq.prefill_attn_scores(self.q, self.k, self.v, self.scale, out=(self.o_pre, self.lse, self.cs),
+                                    stream=s)
+            kvq.select_tokens(self.cs, ly["kh"], ly["w"], kmax=ly["k_hh"], out=(ly["idx"], ly["nout"]), stream=s)
+            kvq.requant_demote(ly["cache"], 0, k_src=self.k, v_src=self.v, sel_idx=ly["idx"],
+                               n_sel=ly["n_sel"], stream=s)
+
+    def _decode_layers(self, s):
+        for l, ly in enumerate(self.layers):
+            self.kvq.decode_attn_qkv(self.qd, self.kd, self.vd, ly["cache"], self.scale, o=self.o_dec[l], stream=s)
+
+    def capture(self, s):
+        """One decode step of every layer as a CUDA graph (all cache state is on the device)."""
+        with torch.cuda.stream(s):
+            self._decode_layers(s)                            # first launches: attributes, occupancy
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            self._decode_layers(s)
+
+    def decode_step(self, t, s):
+        qd, kd, vd = self.dec[t]
+        self.qd.copy_(qd, non_blocking=True)
+        self.kd.copy_(kd, non_blocking=True)
+        self.vd.copy_(vd, non_blocking=True)
+        self.graph.replay()
+
+    def decode_bytes(self):
+        """Mean algorithmic bytes per decode step (all layers): packed codes + scale/zero of the
+        stored tokens and the residual rows, from the flush schedule (nr = 0, G = 32)."""
+        wl = self.wl
+        B, H, D, steps = wl["B"], wl["Hq"], wl["D"], wl["steps"]
+        per_tok = D * 4 // 8 + 2 * 2 * (D // G) * 2
+        tot = 0
+        for t in range(steps):
+            for ly in self.layers:
+                packed = ly["n_sel"] - ly["r0"] + G * ((ly["r0"] + t) // G)
+                res = (ly["r0"] + t) % G + 1
+                tot += (packed * per_tok + res * 2 * D * 2) * B * H + 4 * B * H * D * 2
+        return tot / steps
+
+
+def run_sweep(args, wl, rank, world):
+    """Pyramid sweep: each step prefills and builds all layers, then decodes every layer for
+    `steps` steps (one CUDA graph of all layers per step).  The working set (every layer's
+    cache, about 13 GB) is far larger than L2, so no flush is needed between launches."""
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sw = Sweep(wl, dev, seed=rank)
+    s = torch.cuda.Stream(device=dev)
+    steps = wl["steps"]
+    hbm_peak, tf_peak, peak_src = _peaks()
+
+    def one_step():
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        with torch.cuda.stream(s):
+            ev[0].record(s)
+            sw.prefill_build(s)
+            ev[1].record(s)
+            for t in range(steps):
+                sw.decode_step(t, s)
+            ev[2].record(s)
+        return ev
+
+    with torch.cuda.stream(s):
+        sw.prefill_build(s)
+    torch.cuda.synchronize()
+    sw.capture(s)
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    st = sw.kvq.device_status(s)
+    if st:
+        raise RuntimeError(f"device status {st} after warm-up")
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    pre_ms = dec_ms = 0.0
+    with Clocks(dev.index) as clk:
+        for _ in range(args.steps):
+            ev = one_step()
+            torch.cuda.synchronize()
+            pre_ms += ev[0].elapsed_time(ev[1])
+            dec_ms += ev[1].elapsed_time(ev[2])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    st = sw.kvq.device_status(s)
+    if st:
+        raise RuntimeError(f"device status {st} after the timed steps")
+    step_ms = (pre_ms + dec_ms) / args.steps
+    ms_max = job_ms(step_ms, world, dev)
+    B = wl["B"]
+    value = job_value(world, B * steps, ms_max)
+    dec_step_ms = dec_ms / args.steps / steps
+    dbytes = sw.decode_bytes()
+    achieved = dbytes / (dec_step_ms / 1e3) / 1e9
+    pre_tf = sw.prefill_flops / (pre_ms / args.steps / 1e3) / 1e12      # includes select + build
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 in, f32 accumulate, packed INT2 cache",
+        "data": "synthetic (seeded Gaussian Q/V, keys with LogNormal(0, 0.5) per-channel std; one prompt "
+                "shared by the layers)",
+        "config": {"workload": args.workload, **{k: v for k, v in wl.items() if v is not None},
+                   "l2": "not flushed: the per-step working set (every layer's cache, about 13 GB) is "
+                         "larger than L2", "parallelism": f"replicas x{world}"},
+        "decode": {"tokens_per_s": B * steps / (dec_ms / args.steps / 1e3),
+                   "us_per_layer_step": dec_step_ms * 1e3 / wl["n_layers"],
+                   "bytes_per_step_all_layers": dbytes, "packed_kv_gbs": achieved,
+                   "frac_hbm": achieved / hbm_peak, "launch": "one CUDA graph of every layer per step"},
+        "prefill": {"ms_all_layers": pre_ms / args.steps, "tflops_incl_select_build": pre_tf,
+                    "frac_tensor": pre_tf / tf_peak},
+        "segments_ms_per_step": {"prefill_build": pre_ms / args.steps, "decode": dec_ms / args.steps},
+        "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs (of measured)"},
+        "e2e": None,
+        "gpu_launches": sw.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        cb = cpu_baseline(dict(wl, layer=wl["n_layers"] // 2), args)
+        # one layer's oracle cost (layer 16's budget) for each of the layers
+        cb["value"] /= wl["n_layers"]
+        cb["seconds_per_step_estimated"] *= wl["n_layers"]
+        cb["sample"] += f", times {wl['n_layers']} layers"
+        out["cpu_baseline"] = cb
+        print(json.dumps(out), flush=True)
 
 
 def run_ours(args, wl, rank, world):
@@ -554,7 +729,7 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     try:
-        run_ours(args, wl, rank, world)
+        (run_sweep if wl.get("sweep") else run_ours)(args, wl, rank, world)
     finally:
         if world > 1 and torch.distributed.is_initialized():
             torch.distributed.destroy_process_group()

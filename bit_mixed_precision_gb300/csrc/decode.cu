@@ -1632,11 +1632,20 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     // still leave every CTA kMinItemsPerCta items (large caches: enough
     // clusters to smooth the wave tail, few enough that each CTA's fixed
     // cost stays small against its stream).
-    static int last_key[4] = {-1, -1, -1, -1}, last_C = 1;
+    // the choice per cache shape, remembered (a model's layers differ only in capacity; the
+    // first call of each shape queries occupancy, later ones -- e.g. under stream capture --
+    // only look it up)
+    constexpr int kShapes = 64;
+    static int known[kShapes][5];
+    static int n_known = 0;
+    static std::mutex known_mu;
+    std::lock_guard<std::mutex> lock(known_mu);
     const int items = items_bound(c);
     const int key[4] = {units, items, (int)stage, c.n_tiers};
-    int C = last_C;
-    if (!std::equal(key, key + 4, last_key)) {
+    int C = 0;
+    for (int i = 0; i < n_known && !C; ++i)
+        if (std::equal(key, key + 4, known[i])) C = known[i][4];
+    if (!C) {
         int dev = 0, sms = 0, per_sm = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1665,8 +1674,9 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
             if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) == cudaSuccess && ncl > 0) break;
             (void)cudaGetLastError();
         }
-        std::copy(key, key + 4, last_key);
-        last_C = C;
+        const int slot = n_known < kShapes ? n_known++ : (int)((unsigned)items % kShapes);
+        std::copy(key, key + 4, known[slot]);
+        known[slot][4] = C;
     }
     a.cluster = C;
     a.stage_bytes = stage;
