@@ -39,8 +39,10 @@ KVQ_DEFINE_STATUS(decode)
 namespace {
 
 constexpr int kSub = 128;        // packed tokens per item, split evenly over the warps
-constexpr int kResItem = 32;     // residual rows per item
+constexpr int kResItem = 8;      // residual rows per item (small: the fp16 rows are the heaviest bytes)
 constexpr int kMaxCluster = 16;
+constexpr int kMaxStages = 4;    // staging buffers per CTA (2 or 4)
+constexpr uint32_t kSleepNs = 4000;  // longest single suspension of a waiting warp
 constexpr int kMinItemsPerCta = 34;  // large caches: items a CTA streams at least (about 4k tokens)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -92,7 +94,8 @@ struct DecodeArgs {
     int slots;                  // logits row length per (unit, head)
     float* logits;              // [unit][g][slots] (DiffKV, MiKV) or null
     int cluster;                // CTAs per unit
-    uint32_t stage_bytes;       // one staging buffer (two per CTA)
+    uint32_t stage_bytes;       // one staging buffer
+    int stages, stage_shift;    // staging buffers per CTA (2 or 4) and its log2
     uint32_t part_off, stage_off;  // dynamic shared memory offsets
 };
 
@@ -172,7 +175,9 @@ struct Smem {
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
     float lsum[NG];
-    unsigned long long bar[2];           // one staging mbarrier per buffer
+    unsigned long long bar[kMaxStages];  // one staging mbarrier per buffer
+    int issued;                          // local items requested so far (thread 0 requests)
+    int fail;                            // a wait gave up: nothing more is requested
     UnitState us;
 };
 
@@ -636,7 +641,8 @@ __device__ __forceinline__ int item_kind(const UnitState& us, int n_tiers, int k
     return -1;
 }
 
-// First local index of CTA r (items r, r + C, ...) at or after global item k.
+// First local index of the CTA of item rank r (items r, r + C, ...) at or
+// after global item k.  Item functions below take that rank as r.
 __device__ __forceinline__ int local_at(int k, int r, int C) { return k > r ? (k - r + C - 1) / C : 0; }
 
 // Called by one thread at the start, while another thread reads the unit's
@@ -666,18 +672,24 @@ __device__ void prefetch_start(const DecodeArgs& a, size_t unit, int r) {
     }
 }
 
-// Called by one thread: the bulk copies of local item i into buffer i & 1.
+// Called by one thread: the bulk copies of local item i into buffer i % S.
 __device__ void issue_item(const DecodeArgs& a, const UnitState& us, size_t unit, int r, int i,
                            uint8_t* stage_base, const unsigned long long* bars) {
     const int D = a.D;
     int idx;
     const int t = item_kind(us, a.n_tiers, r + i * a.cluster, idx);
-    uint8_t* buf = stage_base + (size_t)(i & 1) * a.stage_bytes;
-    const uint32_t bar = smem_u32(&bars[i & 1]);
+    const int sb = i & (a.stages - 1);
+    uint8_t* buf = stage_base + (size_t)sb * a.stage_bytes;
+    const uint32_t bar = smem_u32(&bars[sb]);
     if (t >= 0) {
         const int j0 = idx * kSub;
         const int n = min(kSub, us.cnt[t] - j0);
         stage_tier(a.tier[t], unit, j0, (n + 31) & ~31, D, a.G, buf, bar);
+        if (a.policy == KVQ_POLICY_MIKV) {
+            // the item's token ids, read again after the merge to add its scores
+            const int32_t* ids = a.tier[t].token_id + unit * (size_t)a.tier[t].cap + j0;
+            if ((reinterpret_cast<uintptr_t>(ids) & 15u) == 0) bulk_prefetch_l2(ids, (uint32_t)((n + 31) & ~31) * 4u);
+        }
     } else {
         const int j0 = idx * kResItem;
         const int n = min(kResItem, us.len + 1 - j0);
@@ -685,34 +697,45 @@ __device__ void issue_item(const DecodeArgs& a, const UnitState& us, size_t unit
     }
 }
 
-// Waits for local item i: thread 0 polls the mbarrier (bounded), the others
-// sleep in the CTA barrier and then observe the completed phase themselves
-// (one test each, which acquires the copied bytes).  The next-but-one item
-// is requested once every warp is done with this one (release_item).
-__device__ __forceinline__ bool wait_item(unsigned long long* bars, int i, bool ok) {
-    const uint32_t bar = smem_u32(&bars[i & 1]), par = (uint32_t)(i >> 1) & 1u;
-    bool mine = true;
-    if (threadIdx.x == 0) mine = ok && mbar_wait(bar, par, nullptr);
-    const bool all = __syncthreads_and(mine) != 0;
-    if (all) (void)mbar_try_wait(bar, par);
-    return all;
+// Buffer of local item i.
+__device__ __forceinline__ const uint8_t* item_buf(const DecodeArgs& a, const uint8_t* stage_base, int i) {
+    return stage_base + (size_t)(i & (a.stages - 1)) * a.stage_bytes;
 }
 
-__device__ __forceinline__ void release_item(const DecodeArgs& a, const UnitState& us, size_t unit,
-                                             int r, int i, int n_local, bool ok, uint8_t* stage_base,
-                                             unsigned long long* bars, int& issued) {
-    __syncthreads();                           // buffer i & 1 consumed by every warp
-    if (threadIdx.x == 0 && ok && i + 2 < n_local) {
-        issue_item(a, us, unit, r, i + 2, stage_base, bars);
-        issued = i + 3;
+// Waits for local item i (buffer i % S, phase i / S).  Each warp waits on
+// its own: lane 0 polls the mbarrier, suspended between tests (bounded, and
+// cut short once another warp has given up), then every lane tests the
+// completed phase once, which acquires the copied bytes.
+template <int NG, int D>
+__device__ __forceinline__ bool wait_item(const DecodeArgs& a, Smem<NG, D>& sm, int i, bool ok) {
+    const uint32_t bar = smem_u32(&sm.bar[i & (a.stages - 1)]), par = (uint32_t)(i >> a.stage_shift) & 1u;
+    const int lane = threadIdx.x & 31;
+    int mine = ok ? 1 : 0;
+    if (lane == 0 && ok) {
+        mine = mbar_wait_sleep(bar, par, &sm.fail, kSleepNs) ? 1 : 0;
+        if (!mine) *(volatile int*)&sm.fail = 1;
+    }
+    mine = __shfl_sync(0xffffffffu, mine, 0);
+    if (mine) (void)mbar_try_wait(bar, par);
+    return mine != 0;
+}
+
+// Every warp is done with local item i: thread 0 requests item i + S into
+// the same buffer (nothing more once a wait has given up).
+template <int NG, int D>
+__device__ __forceinline__ void release_item(const DecodeArgs& a, Smem<NG, D>& sm, size_t unit, int r, int i,
+                                             int n_local, uint8_t* stage_base) {
+    __syncthreads();
+    if (threadIdx.x == 0 && i + a.stages < n_local && !sm.fail) {
+        issue_item(a, sm.us, unit, r, i + a.stages, stage_base, sm.bar);
+        sm.issued = i + a.stages + 1;
     }
 }
 
 // Local items [i0, i1) of one packed tier.
 template <int KB, int KAX, int VB, int D, int NG>
 __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t unit, int r, int i0,
-                         int i1, int n_local, uint8_t* stage_base, float* lg_unit, bool& ok,
-                         int& issued) {
+                         int i1, int n_local, uint8_t* stage_base, float* lg_unit, bool& ok) {
     const TierArgs& ta = a.tier[t];
     const UnitState& us = sm.us;
     const int warp = threadIdx.x >> 5;
@@ -720,11 +743,11 @@ __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t uni
     WarpAcc<NG, 32 / VB> acc;
     acc_init(acc);
     for (int i = i0; i < i1; ++i) {
-        ok = wait_item(sm.bar, i, ok);
+        ok = wait_item(a, sm, i, ok);
         if (ok) {
             const int j0 = (r + i * a.cluster - us.base[t]) * kSub;
             const int n = min(kSub, us.cnt[t] - j0);
-            const View v = tier_view(ta, (n + 31) & ~31, D, a.G, stage_base + (size_t)(i & 1) * a.stage_bytes);
+            const View v = tier_view(ta, (n + 31) & ~31, D, a.G, item_buf(a, stage_base, i));
             const int tl = warp * TPW;
             if (tl < n) {
                 const int nt = min(TPW, n - tl);
@@ -738,7 +761,7 @@ __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t uni
                 values_token<VB, D, NG>(v, tl, nt, lg, a.G, acc);
             }
         }
-        release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
+        release_item(a, sm, unit, r, i, n_local, stage_base);
     }
     flush_token_values<VB, D, NG>(acc, sm);
 }
@@ -819,8 +842,9 @@ struct MmaAcc {
     float zs[RI][4];                             // sum of p * zero per value group (logit layout)
 };
 
-// Query fragments for the channel permutation of KB-bit keys, and the
-// per-group sums of each fragment row.
+// Query fragments for the channel permutation of KB-bit keys, times 2^KB
+// (exact: a power of two), and the per-group sums of each fragment row
+// (without the factor).
 template <int KB, int NG, int D>
 __device__ __forceinline__ void build_qa(Smem<NG, D>& sm, float (&qs)[4][2]) {
     uint32_t qa[8][4];
@@ -828,7 +852,7 @@ __device__ __forceinline__ void build_qa(Smem<NG, D>& sm, float (&qs)[4][2]) {
     auto part = [&](int row, int c) -> float {
         const int h = row >> 1;
         if (h >= NG) return 0.0f;
-        const float x = sm.q[h][c];
+        const float x = sm.q[h][c] * (float)(1 << KB);
         const float hi = __half2float(__float2half_rn(x));
         return (row & 1) ? __half2float(__float2half_rn(x - hi)) : hi;
     };
@@ -855,6 +879,7 @@ __device__ __forceinline__ void build_qa(Smem<NG, D>& sm, float (&qs)[4][2]) {
         for (int ri = 0; ri < 2; ++ri) {
             qs[grp][ri] += __shfl_xor_sync(0xffffffffu, qs[grp][ri], 1);
             qs[grp][ri] += __shfl_xor_sync(0xffffffffu, qs[grp][ri], 2);
+            qs[grp][ri] *= 1.0f / (float)(1 << KB);
         }
     if (threadIdx.x < 32)                                // every warp holds the same values
 #pragma unroll
@@ -898,9 +923,11 @@ __device__ __forceinline__ void mma_logits_token(const View& v, int tl, const ui
         for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
+                // R carries the factor 2^KB of the fragments: s R = (2^KB s) R_1, and
+                // zp = z - 2^KB s (both exact rewrites of the unscaled form)
                 const int tok = tl + 8 * n + 2 * t + jj;
-                const float s = h2f_bits(v.ks[tok * GR + grp]) * (float)(1 << KB);
-                const float zp = h2f_bits(v.kz[tok * GR + grp]) - s;
+                const float s = h2f_bits(v.ks[tok * GR + grp]);
+                const float zp = fmaf(-(float)(1 << KB), s, h2f_bits(v.kz[tok * GR + grp]));
 #pragma unroll
                 for (int ri = 0; ri < RI; ++ri)
                     S[n][2 * ri + jj] = fmaf(s, R[n][2 * ri + jj], fmaf(qs[grp][ri], zp, S[n][2 * ri + jj]));
@@ -1096,20 +1123,32 @@ __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const floa
                 sc1[grp] = *reinterpret_cast<const uint32_t*>(&h1);
             }
         }
-        // zero points: sum of p * z per group (hi rows carry the full p)
+        // zero points: sum of p * z per group (hi rows carry the full p); each token's
+        // four zero points in one 8-byte load
+        {
+            const uint2 z2 = make_uint2(0u, 0u);
+            const uint2 za = va ? *reinterpret_cast<const uint2*>(v.vz + ta * GR) : z2;
+            const uint2 zb = vb ? *reinterpret_cast<const uint2*>(v.vz + (ta + 1) * GR) : z2;
+            const uint2 zc = vc ? *reinterpret_cast<const uint2*>(v.vz + (ta + 8) * GR) : z2;
+            const uint2 zd = vd ? *reinterpret_cast<const uint2*>(v.vz + (ta + 9) * GR) : z2;
+            auto zf = [](const uint2& w, int grp) -> float {
+                const uint32_t x = grp < 2 ? w.x : w.y;
+                return (grp & 1) ? h2hi(x) : h2lo(x);
+            };
 #pragma unroll
-        for (int ri = 0; ri < RI; ++ri)
+            for (int ri = 0; ri < RI; ++ri)
 #pragma unroll
-            for (int grp = 0; grp < GR; ++grp) {
-                const float pa0 = S[2 * ks][2 * ri], pa1 = S[2 * ks][2 * ri + 1];
-                const float pc0 = S[2 * ks + 1][2 * ri], pc1 = S[2 * ks + 1][2 * ri + 1];
-                float z = acc.zs[ri][grp];
-                if (va) z = fmaf(pa0, h2f_bits(v.vz[ta * GR + grp]), z);
-                if (vb) z = fmaf(pa1, h2f_bits(v.vz[(ta + 1) * GR + grp]), z);
-                if (vc) z = fmaf(pc0, h2f_bits(v.vz[(ta + 8) * GR + grp]), z);
-                if (vd) z = fmaf(pc1, h2f_bits(v.vz[(ta + 9) * GR + grp]), z);
-                acc.zs[ri][grp] = z;
-            }
+                for (int grp = 0; grp < GR; ++grp) {
+                    const float pa0 = S[2 * ks][2 * ri], pa1 = S[2 * ks][2 * ri + 1];
+                    const float pc0 = S[2 * ks + 1][2 * ri], pc1 = S[2 * ks + 1][2 * ri + 1];
+                    float z = acc.zs[ri][grp];
+                    z = fmaf(pa0, zf(za, grp), z);
+                    z = fmaf(pa1, zf(zb, grp), z);
+                    z = fmaf(pc0, zf(zc, grp), z);
+                    z = fmaf(pc1, zf(zd, grp), z);
+                    acc.zs[ri][grp] = z;
+                }
+        }
         // codes of channel c for the token pairs: f16x2 (1 + c_a / 2^VB, 1 + c_b / 2^VB)
         auto pair = [&](uint32_t wa, uint32_t wb, bool high) -> uint32_t {
             if (VB == 4) {                               // channel nibble g of the word
@@ -1131,16 +1170,27 @@ __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const floa
             const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&x), s2, __hneg2(s2));
             return *reinterpret_cast<const uint32_t*>(&r);
         };
-        // m-tile mt: channels 16 mt + g (rows g) and 16 mt + g + 8 (rows g + 8)
+        // m-tile mt: channels 16 mt + g (rows g) and 16 mt + g + 8 (rows g + 8).  The code
+        // words come in 8-byte loads: words 2 mt, 2 mt + 1 (VB = 4: the low and high
+        // channels of the m-tile), or words mt, mt + 1 read once for two m-tiles (VB = 2)
+        uint2 xa = make_uint2(0u, 0u), xb = xa, xc = xa, xd = xa;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const int grp = mt >> 1;
-            const int wlo = VB == 4 ? 2 * mt : mt, whi = VB == 4 ? 2 * mt + 1 : mt;
+            if (VB == 4 || (mt & 1) == 0) {
+                const int w0 = VB == 4 ? 2 * mt : mt;
+                xa = *reinterpret_cast<const uint2*>(ra + w0);
+                xb = *reinterpret_cast<const uint2*>(rb + w0);
+                xc = *reinterpret_cast<const uint2*>(rc + w0);
+                xd = *reinterpret_cast<const uint2*>(rd + w0);
+            }
+            auto lo = [&](const uint2& x) { return VB == 4 ? x.x : ((mt & 1) ? x.y : x.x); };
+            auto hi = [&](const uint2& x) { return VB == 4 ? x.y : ((mt & 1) ? x.y : x.x); };
             uint32_t af[4];
-            af[0] = scaled(pair(ra[wlo], rb[wlo], false), sc0[grp]);
-            af[1] = scaled(pair(ra[whi], rb[whi], true), sc0[grp]);
-            af[2] = scaled(pair(rc[wlo], rd[wlo], false), sc1[grp]);
-            af[3] = scaled(pair(rc[whi], rd[whi], true), sc1[grp]);
+            af[0] = scaled(pair(lo(xa), lo(xb), false), sc0[grp]);
+            af[1] = scaled(pair(hi(xa), hi(xb), true), sc0[grp]);
+            af[2] = scaled(pair(lo(xc), lo(xd), false), sc1[grp]);
+            af[3] = scaled(pair(hi(xc), hi(xd), true), sc1[grp]);
 #pragma unroll
             for (int ri = 0; ri < RI; ++ri) mma16816(acc.o[mt][ri], af, pb[ri][0], pb[ri][1]);
         }
@@ -1202,15 +1252,18 @@ __device__ __forceinline__ void flush_mma(MmaAcc<NG>& acc, Smem<NG, D>& sm) {
 // Local items [i0, i1) of a tier on the tensor cores.
 template <int KB, int KAX, int VB, int NG>
 __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size_t unit, int r, int i0,
-                             int i1, int n_local, uint8_t* stage_base, float* lg_unit, bool& ok,
-                             int& issued) {
+                             int i1, int n_local, uint8_t* stage_base, float* lg_unit, bool& ok) {
     constexpr int TPW = Cfg<NG>::TPW;
     static_assert(TPW == 16 || TPW == 32, "whole n-tile pairs per warp");
     const TierArgs& ta = a.tier[t];
     const UnitState& us = sm.us;
     const int warp = threadIdx.x >> 5;
     float qs[4][2];
-    if constexpr (KAX == KVQ_AXIS_TOKEN) build_qa<KB, NG, 128>(sm, qs);
+    if constexpr (KAX == KVQ_AXIS_TOKEN) {
+        __syncthreads();                                 // every warp is done with the previous fragments
+        build_qa<KB, NG, 128>(sm, qs);
+        __syncthreads();
+    }
     MmaAcc<NG> acc;
 #pragma unroll
     for (int ri = 0; ri < MmaAcc<NG>::RI; ++ri) {
@@ -1226,11 +1279,11 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc.o[mt][ri][i] = 0.0f;
     for (int i = i0; i < i1; ++i) {
-        ok = wait_item(sm.bar, i, ok);
+        ok = wait_item(a, sm, i, ok);
         if (ok) {
             const int j0 = (r + i * a.cluster - us.base[t]) * kSub;
             const int n = min(kSub, us.cnt[t] - j0);
-            const View v = tier_view(ta, (n + 31) & ~31, 128, a.G, stage_base + (size_t)(i & 1) * a.stage_bytes);
+            const View v = tier_view(ta, (n + 31) & ~31, 128, a.G, item_buf(a, stage_base, i));
             const int tl = warp * TPW;
             if (tl < n) {
                 float* lo = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + ta.slot_base + j0 + tl : nullptr;
@@ -1245,7 +1298,7 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
                 mma_pv<VB, NG, NT>(v, tl, nt, S, acc);
             }
         }
-        release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
+        release_item(a, sm, unit, r, i, n_local, stage_base);
     }
     flush_mma<NG, 128>(acc, sm);
 }
@@ -1254,51 +1307,51 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
 // (MiniKV), bit 1 keys per token (DiffKV, MiKV tiers).
 template <int NG, int D, int FAM>
 __device__ void dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t unit, int r, int i0,
-                              int i1, int n_local, uint8_t* stage, float* lg_unit, bool& ok, int& issued) {
+                              int i1, int n_local, uint8_t* stage, float* lg_unit, bool& ok) {
     const TierArgs& ta = a.tier[t];
     const int kb = ta.k_bits, vb = ta.v_bits, ax = ta.k_axis;
     if ((FAM & 1) && ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) {
         if constexpr (D == 128 && NG <= 4)
-            run_tier_mma<2, KVQ_AXIS_CHANNEL, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued);
+            run_tier_mma<2, KVQ_AXIS_CHANNEL, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok);
         else
-            run_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued);
+            run_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok);
         return;
     }
     if constexpr ((FAM & 2) && D == 128 && NG >= 2) {
-        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier_mma<8, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier_mma<4, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier_mma<4, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier_mma<2, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier_mma<8, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier_mma<4, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier_mma<4, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier_mma<2, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
     } else if constexpr ((FAM & 2) && D == 128) {
-        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
-        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok, issued); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
     }
     // a format without a kernel (the host validation lists exactly the built ones):
     // consume the items so that the staging stays in step
     if (threadIdx.x == 0) atomicOr(&g_status_decode, kDevCheck);
     for (int i = i0; i < i1; ++i) {
-        ok = wait_item(sm.bar, i, ok);
-        release_item(a, sm.us, unit, r, i, n_local, ok, stage, sm.bar, issued);
+        ok = wait_item(a, sm, i, ok);
+        release_item(a, sm, unit, r, i, n_local, stage);
     }
 }
 
 // Local items [i0, i1) of the residual ring.
 template <int NG, int D>
 __device__ void run_residual(const DecodeArgs& a, Smem<NG, D>& sm, size_t unit, int r, int i0, int i1,
-                             int n_local, uint8_t* stage_base, float* lg_unit, bool& ok, int& issued) {
+                             int n_local, uint8_t* stage_base, float* lg_unit, bool& ok) {
     const UnitState& us = sm.us;
     const int warp = threadIdx.x >> 5;
     const bool bf = a.bf16 != 0;
     WarpAcc<NG, D / 32> acc;
     acc_init(acc);
     for (int i = i0; i < i1; ++i) {
-        ok = wait_item(sm.bar, i, ok);
+        ok = wait_item(a, sm, i, ok);
         if (ok) {
             const int j0 = (r + i * a.cluster - us.base[a.n_tiers]) * kResItem;
             const int n = min(kResItem, us.len + 1 - j0);
-            const uint8_t* buf = stage_base + (size_t)(i & 1) * a.stage_bytes;
+            const uint8_t* buf = item_buf(a, stage_base, i);
             const uint16_t* rk = reinterpret_cast<const uint16_t*>(buf);
             const uint16_t* rv = reinterpret_cast<const uint16_t*>(buf + a16((uint32_t)n * D * 2));
             const int w0 = warp * Cfg<NG>::RPW;
@@ -1308,7 +1361,7 @@ __device__ void run_residual(const DecodeArgs& a, Smem<NG, D>& sm, size_t unit, 
                                      acc, lo, a.slots);
             }
         }
-        release_item(a, us, unit, r, i, n_local, ok, stage_base, sm.bar, issued);
+        release_item(a, sm, unit, r, i, n_local, stage_base);
     }
     flush_lane_values<NG, D>(acc, sm);
 }
@@ -1324,41 +1377,63 @@ __device__ void add_scores(const DecodeArgs& a, const Smem<NG, D>& sm, size_t un
     const int cap = a.res_cap;
     const float* lse2 = sm.lse2;
     float* cs = a.cum_score + unit * (size_t)a.score_cap;
-    for (int i = 0; i < n_local; ++i) {
+    const int i_res = local_at(us.base[a.n_tiers], r, a.cluster);   // first local residual item
+    if (a.policy == KVQ_POLICY_MIKV) {
+        // packed tiers, one token of an item per thread, kBatch items at a time:
+        // every load of a batch is in flight before the first use
+        static_assert(Cfg<NG>::kThreads >= kSub, "one token per thread and item");
+        constexpr int kBatch = 16;
+        for (int i = 0; i < i_res && (int)threadIdx.x < kSub; i += kBatch) {
+            float p[kBatch];
+            int id[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                p[k] = 0.0f;
+                id[k] = -1;
+                int idx;
+                const int t = i + k < i_res ? item_kind(us, a.n_tiers, r + (i + k) * a.cluster, idx) : -1;
+                const int j = t >= 0 ? idx * kSub + (int)threadIdx.x : 0;
+                if (t >= 0 && j < us.cnt[t]) {
+                    const TierArgs& ta = a.tier[t];
+#pragma unroll
+                    for (int h = 0; h < NG; ++h)
+                        p[k] += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ta.slot_base + j) - lse2[h]);
+                    id[k] = ta.token_id[unit * (size_t)ta.cap + j];
+                    if (id[k] < 0 || id[k] >= a.score_cap) {
+                        atomicOr(&g_status_decode, kDevCheck);
+                        id[k] = -1;
+                    }
+                }
+            }
+            float c[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) c[k] = id[k] >= 0 ? cs[id[k]] : 0.0f;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                if (id[k] >= 0) cs[id[k]] = __fadd_rn(c[k], p[k]);
+        }
+    }
+    // the residual ring
+    for (int i = i_res; i < n_local; ++i) {
         int idx;
-        const int t = item_kind(us, a.n_tiers, r + i * a.cluster, idx);
-        if (t >= 0) {
-            if (a.policy != KVQ_POLICY_MIKV) continue;
-            const TierArgs& ta = a.tier[t];
-            const int j0 = idx * kSub, j1 = min(j0 + kSub, us.cnt[t]);
-            for (int j = j0 + (int)threadIdx.x; j < j1; j += blockDim.x) {
+        (void)item_kind(us, a.n_tiers, r + i * a.cluster, idx);
+        const int l0 = idx * kResItem, l1 = min(l0 + kResItem, us.len + 1);
+        if (a.policy == KVQ_POLICY_MIKV) {
+            for (int li = l0 + (int)threadIdx.x; li < l1; li += blockDim.x) {
                 float p = 0.0f;
 #pragma unroll
                 for (int h = 0; h < NG; ++h)
-                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ta.slot_base + j) - lse2[h]);
-                const int id = ta.token_id[unit * (size_t)ta.cap + j];
-                if (id >= 0 && id < a.score_cap) cs[id] = __fadd_rn(cs[id], p);
-                else atomicOr(&g_status_decode, kDevCheck);
+                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+                const int id = li < us.len ? a.res_token_id[unit * (size_t)cap + (us.start + li) % cap] : us.pos;
+                if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
+                else cs[id] = li < us.len ? __fadd_rn(cs[id], p) : p;
             }
         } else {
-            const int l0 = idx * kResItem, l1 = min(l0 + kResItem, us.len + 1);
-            if (a.policy == KVQ_POLICY_MIKV) {
-                for (int li = l0 + (int)threadIdx.x; li < l1; li += blockDim.x) {
-                    float p = 0.0f;
-#pragma unroll
-                    for (int h = 0; h < NG; ++h)
-                        p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-                    const int id = li < us.len ? a.res_token_id[unit * (size_t)cap + (us.start + li) % cap] : us.pos;
-                    if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
-                    else cs[id] = li < us.len ? __fadd_rn(cs[id], p) : p;
-                }
-            } else {
-                for (int x = l0 * NG + (int)threadIdx.x; x < l1 * NG; x += blockDim.x) {
-                    const int li = x / NG, h = x % NG;
-                    const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-                    float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
-                    *wa = li < us.len ? __fadd_rn(*wa, p) : p;
-                }
+            for (int x = l0 * NG + (int)threadIdx.x; x < l1 * NG; x += blockDim.x) {
+                const int li = x / NG, h = x % NG;
+                const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+                float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
+                *wa = li < us.len ? __fadd_rn(*wa, p) : p;
             }
         }
     }
@@ -1407,13 +1482,13 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
     uint8_t* stage_base = smem_raw + a.stage_off;
     const int C = a.cluster;
     const int r = blockIdx.x;
+    const int ir = C - 1 - r;                   // item rank: the leader, which also merges, takes the last share
     const size_t unit = blockIdx.y;
     const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
     const bool bf = a.bf16 != 0;
 
     cluster_arrive_relaxed();                   // "started": the leader's shared memory exists
-    if (threadIdx.x == 32) prefetch_start(a, unit, r);
-    int issued = 0;                             // thread 0: local items requested so far
+    if (threadIdx.x == 32) prefetch_start(a, unit, ir);
     if (threadIdx.x == 0) {
         UnitState& us = sm.us;
         // all counters requested at once, then checked
@@ -1438,12 +1513,12 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         us.pos = ps;
         us.total = us.base[a.n_tiers] + (us.len + 1 + kResItem - 1) / kResItem;
         if (bad) atomicOr(&g_status_decode, kDevCheck);
-        mbar_init(smem_u32(&sm.bar[0]), 1);
-        mbar_init(smem_u32(&sm.bar[1]), 1);
+        for (int st = 0; st < a.stages; ++st) mbar_init(smem_u32(&sm.bar[st]), 1);
+        sm.fail = 0;
         fence_mbar_init();
-        const int n_local = us.total > r ? (us.total - r + C - 1) / C : 0;
-        for (int i = 0; i < 2 && i < n_local; ++i) issue_item(a, us, unit, r, i, stage_base, sm.bar);
-        issued = min(2, n_local);
+        const int n_local = us.total > ir ? (us.total - ir + C - 1) / C : 0;
+        for (int i = 0; i < a.stages && i < n_local; ++i) issue_item(a, us, unit, ir, i, stage_base, sm.bar);
+        sm.issued = min(a.stages, n_local);
     }
     for (int x = threadIdx.x; x < NG * D; x += blockDim.x) {
         const int h = x / D, c = x % D;
@@ -1457,21 +1532,25 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
     __syncthreads();
 
     const UnitState& us = sm.us;
-    const int n_local = us.total > r ? (us.total - r + C - 1) / C : 0;
+    const int n_local = us.total > ir ? (us.total - ir + C - 1) / C : 0;
     float* lg_unit = a.logits ? a.logits + unit * NG * (size_t)a.slots : nullptr;
     bool ok = true;
     for (int t = 0; t < a.n_tiers; ++t) {
-        const int i0 = local_at(us.base[t], r, C), i1 = local_at(us.base[t + 1], r, C);
-        if (i1 > i0) dispatch_tier<NG, D, FAM>(a, sm, t, unit, r, i0, i1, n_local, stage_base, lg_unit, ok, issued);
+        const int i0 = local_at(us.base[t], ir, C), i1 = local_at(us.base[t + 1], ir, C);
+        if (i1 > i0) dispatch_tier<NG, D, FAM>(a, sm, t, unit, ir, i0, i1, n_local, stage_base, lg_unit, ok);
     }
     {
-        const int i0 = local_at(us.base[a.n_tiers], r, C);
-        if (n_local > i0) run_residual<NG, D>(a, sm, unit, r, i0, n_local, n_local, stage_base, lg_unit, ok, issued);
+        const int i0 = local_at(us.base[a.n_tiers], ir, C);
+        if (n_local > i0) run_residual<NG, D>(a, sm, unit, ir, i0, n_local, n_local, stage_base, lg_unit, ok);
     }
-    if (!ok && threadIdx.x == 0) {
+    __syncthreads();
+    if (sm.fail && threadIdx.x == 0) {
         atomicOr(&g_status_decode, kDevTimeout);
-        // let every copy still in flight land before the buffers go away
-        for (int i = 0; i < issued; ++i) mbar_wait(smem_u32(&sm.bar[i & 1]), (i >> 1) & 1, nullptr);
+        // let every copy still in flight land before the buffers go away: the last
+        // item requested into each buffer (items are requested in order)
+        const int S = a.stages, n = sm.issued;
+        for (int i = max(0, n - S); i < n; ++i)
+            (void)mbar_wait(smem_u32(&sm.bar[i & (S - 1)]), (uint32_t)(i >> a.stage_shift) & 1u, nullptr);
     }
     __syncthreads();
 
@@ -1544,7 +1623,7 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
                 cluster_st_f32(cluster_map(smem_u32(&sm.lse2[threadIdx.x]), y), sm.lse2[threadIdx.x]);
         cluster_arrive_release();
         cluster_wait_acquire();
-        add_scores<NG, D>(a, sm, unit, r, n_local, lg_unit);
+        add_scores<NG, D>(a, sm, unit, ir, n_local, lg_unit);
     }
 
     // ---- leader: the new token joins the ring, MiniKV flush, counters
@@ -1610,7 +1689,8 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     stage = (stage + 127u) & ~127u;
     const uint32_t sm_bytes = (uint32_t)((sizeof(Smem<NG, D>) + 127) & ~(size_t)127);
     const uint32_t slot_bytes = (uint32_t)(NG * (D + 2) * sizeof(float));
-    auto smem_for = [&](int C) { return sm_bytes + ((C * slot_bytes + 127u) & ~127u) + 2u * stage; };
+    auto smem_for = [&](int C, int S) { return sm_bytes + ((C * slot_bytes + 127u) & ~127u) + (uint32_t)S * stage; };
+    constexpr uint32_t kSmemLimit = 227u * 1024u;
     int cmax = kMaxCluster;
     while (cmax > 1 && (uint32_t)cmax * slot_bytes > 32u * 1024u) cmax >>= 1;
 
@@ -1618,7 +1698,7 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     static bool attr_done = false, wide_ok = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_for(kMaxCluster));
+                                             (int)std::min(smem_for(kMaxCluster, kMaxStages), kSmemLimit));
         if (e != cudaSuccess) return e;
         // clusters above the portable 8 CTAs, where the device allows them
         wide_ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
@@ -1636,21 +1716,24 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     // first call of each shape queries occupancy, later ones -- e.g. under stream capture --
     // only look it up)
     constexpr int kShapes = 64;
-    static int known[kShapes][5];
+    static int known[kShapes][6];
     static int n_known = 0;
     static std::mutex known_mu;
     std::lock_guard<std::mutex> lock(known_mu);
     const int items = items_bound(c);
     const int key[4] = {units, items, (int)stage, c.n_tiers};
-    int C = 0;
+    int C = 0, S = 2;
     for (int i = 0; i < n_known && !C; ++i)
-        if (std::equal(key, key + 4, known[i])) C = known[i][4];
+        if (std::equal(key, key + 4, known[i])) {
+            C = known[i][4];
+            S = known[i][5];
+        }
     if (!C) {
         int dev = 0, sms = 0, per_sm = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg<NG>::kThreads, smem_for(cmax));
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg<NG>::kThreads, smem_for(cmax, 2));
         if (e != cudaSuccess) return e;
         const long resident = (long)std::max(per_sm, 1) * sms;
         int c_fill = 1, c_items = 1;
@@ -1667,18 +1750,37 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
             at[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3((unsigned)C, (unsigned)units);
             cfg.blockDim = dim3(Cfg<NG>::kThreads);
-            cfg.dynamicSmemBytes = smem_for(C);
+            cfg.dynamicSmemBytes = smem_for(C, 2);
             cfg.attrs = at;
             cfg.numAttrs = 1;
             int ncl = 0;
             if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) == cudaSuccess && ncl > 0) break;
             (void)cudaGetLastError();
         }
+        // staging buffers: as many as fit without costing a resident CTA
+        int occ2 = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, kern, Cfg<NG>::kThreads, smem_for(C, 2)) != cudaSuccess)
+            (void)cudaGetLastError();
+        for (int s2 = kMaxStages; s2 > 2; s2 >>= 1) {
+            int o = 0;
+            if (smem_for(C, s2) > kSmemLimit) continue;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, Cfg<NG>::kThreads, smem_for(C, s2)) != cudaSuccess) {
+                (void)cudaGetLastError();
+                continue;
+            }
+            if (o >= occ2) {
+                S = s2;
+                break;
+            }
+        }
         const int slot = n_known < kShapes ? n_known++ : (int)((unsigned)items % kShapes);
         std::copy(key, key + 4, known[slot]);
         known[slot][4] = C;
+        known[slot][5] = S;
     }
     a.cluster = C;
+    a.stages = S;
+    a.stage_shift = S == 4 ? 2 : 1;
     a.stage_bytes = stage;
     a.part_off = sm_bytes;
     a.stage_off = sm_bytes + ((C * slot_bytes + 127u) & ~127u);
@@ -1690,7 +1792,7 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     at[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)C, (unsigned)units);
     cfg.blockDim = dim3(Cfg<NG>::kThreads);
-    cfg.dynamicSmemBytes = smem_for(C);
+    cfg.dynamicSmemBytes = smem_for(C, S);
     cfg.stream = s;
     cfg.attrs = at;
     cfg.numAttrs = 1;
