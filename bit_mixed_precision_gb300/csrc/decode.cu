@@ -96,7 +96,7 @@ struct DecodeArgs {
     int cluster;                // CTAs per unit
     uint32_t stage_bytes;       // one staging buffer
     int stages, stage_shift;    // staging buffers per CTA (2 or 4) and its log2
-    uint32_t part_off, stage_off;  // dynamic shared memory offsets
+    uint32_t qf_off, part_off, stage_off;  // dynamic shared memory offsets
 };
 
 __device__ __forceinline__ float ldf(const void* p, size_t i, bool bf16) {
@@ -169,8 +169,8 @@ struct Smem {
     float wm[Cfg<NG>::W][NG];            // per-warp running max / sum / output (merged across kinds)
     float wl[Cfg<NG>::W][NG];
     float wo[Cfg<NG>::W][NG][D];
-    float lg[Cfg<NG>::W][NG][32];        // logits of the warp's current group
-    uint16_t qf[Cfg<NG>::W][NG <= 4 ? 2 * NG : 1][128];  // per-channel keys: query x scales, hi / lo rows
+    // logits of the warp's current group (CUDA-core per-token path: single heads only)
+    float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 32 : 1];
     uint4 qa[8][32];                     // per-token keys: the query's A fragments, [k-step][lane]
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
@@ -752,7 +752,7 @@ __device__ void run_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_t uni
             if (tl < n) {
                 const int nt = min(TPW, n - tl);
                 float lg[NG];
-                if (KAX == KVQ_AXIS_CHANNEL)
+                if constexpr (KAX == KVQ_AXIS_CHANNEL)
                     logits_channel<KB, D / 32, NG>(v, tl, sm, a.G, lg);
                 else
                     logits_token<KB, D, NG>(v, tl, sm, a.G, lg);
@@ -1249,6 +1249,14 @@ __device__ __forceinline__ void flush_mma(MmaAcc<NG>& acc, Smem<NG, D>& sm) {
     }
 }
 
+// The warp's rows of query x key scales (per-channel keys), in the dynamic
+// shared memory the launch reserves for them when the cache has such a tier.
+template <int NG>
+__device__ __forceinline__ uint16_t (&qf_rows(const DecodeArgs& a, Smem<NG, 128>& sm, int warp))[2 * NG][128] {
+    uint8_t* base = reinterpret_cast<uint8_t*>(&sm) + a.qf_off + (size_t)warp * (2 * NG * 128 * sizeof(uint16_t));
+    return *reinterpret_cast<uint16_t (*)[2 * NG][128]>(base);
+}
+
 // Local items [i0, i1) of a tier on the tensor cores.
 template <int KB, int KAX, int VB, int NG>
 __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size_t unit, int r, int i0,
@@ -1290,7 +1298,7 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
                 constexpr int NT = TPW / 8;
                 float S[NT][4];
                 if constexpr (KAX == KVQ_AXIS_CHANNEL)
-                    mma_logits_channel<NG, NT>(v, tl, a.G, sm.q, sm.qf[warp], S);
+                    mma_logits_channel<NG, NT>(v, tl, a.G, sm.q, qf_rows<NG>(a, sm, warp), S);
                 else
                     mma_logits_token<KB, NG, NT>(v, tl, sm.qa, qs, S);
                 const int nt = min(TPW, n - tl);
@@ -1688,8 +1696,16 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
                                                  kSub, D, c.G).total());
     stage = (stage + 127u) & ~127u;
     const uint32_t sm_bytes = (uint32_t)((sizeof(Smem<NG, D>) + 127) & ~(size_t)127);
+    // per-channel keys on the tensor cores: each warp's query x scale rows
+    bool has_channel = false;
+    for (int t = 0; t < c.n_tiers; ++t) has_channel |= c.tier[t].k_axis == KVQ_AXIS_CHANNEL;
+    const uint32_t qf_bytes = (has_channel && D == 128 && NG <= 4)
+                                  ? (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t))
+                                  : 0u;
     const uint32_t slot_bytes = (uint32_t)(NG * (D + 2) * sizeof(float));
-    auto smem_for = [&](int C, int S) { return sm_bytes + ((C * slot_bytes + 127u) & ~127u) + (uint32_t)S * stage; };
+    auto smem_for = [&](int C, int S) {
+        return sm_bytes + qf_bytes + ((C * slot_bytes + 127u) & ~127u) + (uint32_t)S * stage;
+    };
     constexpr uint32_t kSmemLimit = 227u * 1024u;
     int cmax = kMaxCluster;
     while (cmax > 1 && (uint32_t)cmax * slot_bytes > 32u * 1024u) cmax >>= 1;
@@ -1697,8 +1713,10 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     auto kern = decode_kernel<NG, D, FAM>;
     static bool attr_done = false, wide_ok = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)std::min(smem_for(kMaxCluster, kMaxStages), kSmemLimit));
+        const uint32_t qf_max = NG <= 4 ? (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)) : 0u;
+        cudaError_t e = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            (int)std::min(smem_for(kMaxCluster, kMaxStages) - qf_bytes + qf_max, kSmemLimit));
         if (e != cudaSuccess) return e;
         // clusters above the portable 8 CTAs, where the device allows them
         wide_ok = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
@@ -1716,17 +1734,17 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     // first call of each shape queries occupancy, later ones -- e.g. under stream capture --
     // only look it up)
     constexpr int kShapes = 64;
-    static int known[kShapes][6];
+    static int known[kShapes][7];
     static int n_known = 0;
     static std::mutex known_mu;
     std::lock_guard<std::mutex> lock(known_mu);
     const int items = items_bound(c);
-    const int key[4] = {units, items, (int)stage, c.n_tiers};
+    const int key[5] = {units, items, (int)stage, c.n_tiers, (int)qf_bytes};
     int C = 0, S = 2;
     for (int i = 0; i < n_known && !C; ++i)
-        if (std::equal(key, key + 4, known[i])) {
-            C = known[i][4];
-            S = known[i][5];
+        if (std::equal(key, key + 5, known[i])) {
+            C = known[i][5];
+            S = known[i][6];
         }
     if (!C) {
         int dev = 0, sms = 0, per_sm = 0;
@@ -1774,16 +1792,17 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
             }
         }
         const int slot = n_known < kShapes ? n_known++ : (int)((unsigned)items % kShapes);
-        std::copy(key, key + 4, known[slot]);
-        known[slot][4] = C;
-        known[slot][5] = S;
+        std::copy(key, key + 5, known[slot]);
+        known[slot][5] = C;
+        known[slot][6] = S;
     }
     a.cluster = C;
     a.stages = S;
     a.stage_shift = S == 4 ? 2 : 1;
     a.stage_bytes = stage;
-    a.part_off = sm_bytes;
-    a.stage_off = sm_bytes + ((C * slot_bytes + 127u) & ~127u);
+    a.qf_off = sm_bytes;
+    a.part_off = sm_bytes + qf_bytes;
+    a.stage_off = a.part_off + ((C * slot_bytes + 127u) & ~127u);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
