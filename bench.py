@@ -22,7 +22,8 @@ kernel, the end-to-end number through host buffers, the CPU oracle baseline
 and the SM clocks seen during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama-layer|tiny|pyramid-layer16|diffkv|mikv]
+                  [--workload llama-layer|tiny|pyramid-layer16|pyramid|diffkv|mikv]
+                  [--batch B] [--decode-steps S]     (smaller cases, for profiling)
 """
 from __future__ import annotations
 
@@ -717,12 +718,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama-layer", choices=sorted(WORKLOADS))
+    # smaller cases of a workload's kernels (profiling): the batch and the decode steps per
+    # timed step; the JSON line's config records them
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--decode-steps", type=int, default=None)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.batch is not None:
+        wl["B"] = args.batch
+    if args.decode_steps is not None:
+        wl["steps"] = args.decode_steps
     if args.impl == "reference":
         run_reference(args, wl, rank, world)
         return

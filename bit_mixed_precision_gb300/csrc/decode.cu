@@ -43,7 +43,9 @@ constexpr int kResItem = 8;      // residual rows per item (small: the fp16 rows
 constexpr int kMaxCluster = 16;
 constexpr int kMaxStages = 4;    // staging buffers per CTA (2 or 4)
 constexpr uint32_t kSleepNs = 4000;  // longest single suspension of a waiting warp
-constexpr int kMinItemsPerCta = 34;  // large caches: items a CTA streams at least (about 4k tokens)
+// large caches: items a CTA streams at least (measured: MiKV CTAs, which also add every
+// token's score after the merge, do best with about twice as many)
+constexpr int kMinItemsPerCta = 34, kMinItemsPerCtaScores = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -1390,7 +1392,7 @@ __device__ void add_scores(const DecodeArgs& a, const Smem<NG, D>& sm, size_t un
         // packed tiers, one token of an item per thread, kBatch items at a time:
         // every load of a batch is in flight before the first use
         static_assert(Cfg<NG>::kThreads >= kSub, "one token per thread and item");
-        constexpr int kBatch = 16;
+        constexpr int kBatch = 20;
         for (int i = 0; i < i_res && (int)threadIdx.x < kSub; i += kBatch) {
             float p[kBatch];
             int id[kBatch];
@@ -1421,28 +1423,29 @@ __device__ void add_scores(const DecodeArgs& a, const Smem<NG, D>& sm, size_t un
                 if (id[k] >= 0) cs[id[k]] = __fadd_rn(c[k], p[k]);
         }
     }
-    // the residual ring
-    for (int i = i_res; i < n_local; ++i) {
+    // the residual ring: every (item, row) pair of the CTA's ring items at once
+    // (MiKV: one per row; DiffKV: one per row and head), all loads in flight together
+    const int per = a.policy == KVQ_POLICY_MIKV ? 1 : NG;
+    const int n_pairs = (n_local - i_res) * kResItem * per;
+    for (int x = threadIdx.x; x < n_pairs; x += blockDim.x) {
+        const int k = x / (kResItem * per), rem = x % (kResItem * per);
         int idx;
-        (void)item_kind(us, a.n_tiers, r + i * a.cluster, idx);
-        const int l0 = idx * kResItem, l1 = min(l0 + kResItem, us.len + 1);
+        (void)item_kind(us, a.n_tiers, r + (i_res + k) * a.cluster, idx);
+        const int li = idx * kResItem + rem / per;
+        if (li > us.len) continue;                               // past the new token
         if (a.policy == KVQ_POLICY_MIKV) {
-            for (int li = l0 + (int)threadIdx.x; li < l1; li += blockDim.x) {
-                float p = 0.0f;
+            float p = 0.0f;
 #pragma unroll
-                for (int h = 0; h < NG; ++h)
-                    p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-                const int id = li < us.len ? a.res_token_id[unit * (size_t)cap + (us.start + li) % cap] : us.pos;
-                if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
-                else cs[id] = li < us.len ? __fadd_rn(cs[id], p) : p;
-            }
+            for (int h = 0; h < NG; ++h)
+                p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+            const int id = li < us.len ? a.res_token_id[unit * (size_t)cap + (us.start + li) % cap] : us.pos;
+            if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
+            else cs[id] = li < us.len ? __fadd_rn(cs[id], p) : p;
         } else {
-            for (int x = l0 * NG + (int)threadIdx.x; x < l1 * NG; x += blockDim.x) {
-                const int li = x / NG, h = x % NG;
-                const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-                float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
-                *wa = li < us.len ? __fadd_rn(*wa, p) : p;
-            }
+            const int h = rem % per;
+            const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+            float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
+            *wa = li < us.len ? __fadd_rn(*wa, p) : p;
         }
     }
 }
@@ -1734,17 +1737,17 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     // first call of each shape queries occupancy, later ones -- e.g. under stream capture --
     // only look it up)
     constexpr int kShapes = 64;
-    static int known[kShapes][7];
+    static int known[kShapes][8];
     static int n_known = 0;
     static std::mutex known_mu;
     std::lock_guard<std::mutex> lock(known_mu);
     const int items = items_bound(c);
-    const int key[5] = {units, items, (int)stage, c.n_tiers, (int)qf_bytes};
+    const int key[6] = {units, items, (int)stage, c.n_tiers, (int)qf_bytes, c.policy};
     int C = 0, S = 2;
     for (int i = 0; i < n_known && !C; ++i)
-        if (std::equal(key, key + 5, known[i])) {
-            C = known[i][5];
-            S = known[i][6];
+        if (std::equal(key, key + 6, known[i])) {
+            C = known[i][6];
+            S = known[i][7];
         }
     if (!C) {
         int dev = 0, sms = 0, per_sm = 0;
@@ -1756,7 +1759,8 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
         const long resident = (long)std::max(per_sm, 1) * sms;
         int c_fill = 1, c_items = 1;
         while (c_fill * 2 <= std::min(cmax, items) && (long)units * c_fill * 2 <= resident) c_fill *= 2;
-        while (c_items * 2 <= std::min(cmax, items) && (items + 2 * c_items - 1) / (2 * c_items) >= kMinItemsPerCta)
+        const int min_items = c.policy == KVQ_POLICY_MIKV ? kMinItemsPerCtaScores : kMinItemsPerCta;
+        while (c_items * 2 <= std::min(cmax, items) && (items + 2 * c_items - 1) / (2 * c_items) >= min_items)
             c_items *= 2;
         C = std::max(c_fill, c_items);
         for (; C > 1; C >>= 1) {
@@ -1792,9 +1796,9 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
             }
         }
         const int slot = n_known < kShapes ? n_known++ : (int)((unsigned)items % kShapes);
-        std::copy(key, key + 5, known[slot]);
-        known[slot][5] = C;
-        known[slot][6] = S;
+        std::copy(key, key + 6, known[slot]);
+        known[slot][6] = C;
+        known[slot][7] = S;
     }
     a.cluster = C;
     a.stages = S;
