@@ -283,28 +283,25 @@ __global__ void __launch_bounds__(192, 2)
 
             const int kbase = j * kBN;
             // eight independent partial maxima keep the reduction off one long chain;
-            // only the diagonal tile and a tile past the end of the prompt need the mask
+            // only the diagonal tile and a tile past the end of the prompt need the mask.
+            // The maximum is taken over the unscaled scores (the scale is positive) and
+            // scaled once; the scale then rides in the exponent's fused multiply-add.
             float mxp[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mxp[e] = -__int_as_float(0x7f800000);
             if (kbase + kBN - 1 > qt * kTile || kbase + kBN > T_len) {
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
-                    float x = s[c] * scale_log2;
                     const int kidx = kbase + c;
-                    if (kidx > i || kidx >= T_len) x = -__int_as_float(0x7f800000);
-                    s[c] = x;
-                    mxp[c & 7] = fmaxf(mxp[c & 7], x);
+                    if (kidx > i || kidx >= T_len) s[c] = -__int_as_float(0x7f800000);
+                    mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    s[c] *= scale_log2;
-                    mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
-                }
+                for (int c = 0; c < kBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
             }
             const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]))) * scale_log2;
             const float m_new = fmaxf(m_used, mx);
             const bool resc = m_new > m_used + kRescaleLog2;
             if (__any_sync(0xffffffffu, resc && j >= 1)) {
@@ -327,19 +324,24 @@ __global__ void __launch_bounds__(192, 2)
                 if (j >= 1) l *= ex2_approx(m_used - m_new);
                 m_used = m_new;
             }
-            float rsp[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) rsp[e] = 0.0f;
             // P (fp16) over the first 32 columns of this tile's S buffer: column c
-            // holds keys 2c (low half) and 2c + 1 (high half) of row r
+            // holds keys 2c (low half) and 2c + 1 (high half) of row r.  Exponents
+            // s * scale - m and the row sum go two keys per instruction (packed
+            // float32 pairs); the eight partial sums are those of keys c mod 8.
+            unsigned long long rsp2[4] = {0ull, 0ull, 0ull, 0ull};
+            const unsigned long long sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_used, -m_used);
             float pk[kBN / 2];
 #pragma unroll
             for (int c2 = 0; c2 < kBN / 2; ++c2) {
-                const float p0 = ex2_approx(s[2 * c2] - m_used), p1 = ex2_approx(s[2 * c2 + 1] - m_used);
-                rsp[(2 * c2) & 7] += p0;
-                rsp[(2 * c2 + 1) & 7] += p1;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(s[2 * c2], s[2 * c2 + 1]), sc2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                rsp2[c2 & 3] = f2_add(rsp2[c2 & 3], f2_pack(p0, p1));
                 pk[c2] = __uint_as_float(Pack2<__half>::pack(p0, p1));
             }
+            float rsp[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f2_unpack(rsp2[e], rsp[2 * e], rsp[2 * e + 1]);
             l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
             tmem_st32(tmem + lane_base + (uint32_t)sb * kBN, pk);
             tmem_wait_st();
@@ -483,15 +485,16 @@ __global__ void __launch_bounds__(192, 2)
             const int buf = it & 1;
             const int qt = kt + it;
             const int qi_own = qt * kTile + r;
+            // minus the base-2 lse of each query (-inf past the prompt: exponent -inf)
             lse_s[buf * kTile + r] =
-                qi_own < T_len ? lse[(size_t)bh * T_len + qi_own] * kLog2e : __int_as_float(0x7f800000);
+                qi_own < T_len ? -(lse[(size_t)bh * T_len + qi_own] * kLog2e) : -__int_as_float(0x7f800000);
             // buffer buf is rewritten two tiles later, after every thread has
             // arrived for the tile in between, i.e. finished reading this one
             mbar_arrive(BAR(C_LSE + buf));
             if (!warp_wait(BAR(C_LSE + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
             if (!warp_wait(BAR(C_SF + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const float* ls = lse_s + buf * kTile;
+            const float* nls = lse_s + buf * kTile;
             // eight independent partial sums; the causal mask only matters on the
             // diagonal tile (later query tiles hold positions >= every key here)
             float tsp[8];
@@ -501,16 +504,26 @@ __global__ void __launch_bounds__(192, 2)
             const bool diag = it == 0;
             // the 128 columns in four TMEM loads of 32, the next one in flight
             // while the current one is summed
+            // off the diagonal, exponents and sums go two queries per instruction
+            // (packed float32 pairs; partial sum e of the pairs holds queries c with
+            // c mod 8 = 2e, 2e + 1)
+            unsigned long long tsp2[4] = {0ull, 0ull, 0ull, 0ull};
+            const unsigned long long sc2 = f2_pack(scale_log2, scale_log2);
             auto sum32 = [&](const float (&sv)[32], int c0) {
                 if (diag) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        const float x = fmaf(sv[c], scale_log2, -ls[c0 + c]);
+                        const float x = fmaf(sv[c], scale_log2, nls[c0 + c]);
                         tsp[c & 7] += (qbase + c0 + c >= j) ? ex2_approx(x) : 0.0f;
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) tsp[c & 7] += ex2_approx(fmaf(sv[c], scale_log2, -ls[c0 + c]));
+                    for (int c = 0; c < 32; c += 2) {
+                        const unsigned long long nl2 = *reinterpret_cast<const unsigned long long*>(nls + c0 + c);
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), sc2, nl2), x0, x1);
+                        tsp2[(c >> 1) & 3] = f2_add(tsp2[(c >> 1) & 3], f2_pack(ex2_approx(x0), ex2_approx(x1)));
+                    }
                 }
             };
             const uint32_t tb = tmem + lane_base + (uint32_t)buf * 128u;
@@ -530,6 +543,10 @@ __global__ void __launch_bounds__(192, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C_SFREE + buf));
             sum32(s1, 96);
+            if (!diag) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_unpack(tsp2[e], tsp[2 * e], tsp[2 * e + 1]);
+            }
             acc += ((tsp[0] + tsp[1]) + (tsp[2] + tsp[3])) + ((tsp[4] + tsp[5]) + (tsp[6] + tsp[7]));
         }
         if (!ok) give_up(abort_flag);
