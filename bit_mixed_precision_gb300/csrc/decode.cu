@@ -264,8 +264,20 @@ __host__ __device__ inline StageSizes tier_stage_sizes(int k_axis, int kb, int v
     return z;
 }
 
+__device__ __forceinline__ View view_of(const StageSizes& z, const uint8_t* buf);
+
 __device__ __forceinline__ View tier_view(const TierArgs& t, int npad, int D, int G, const uint8_t* buf) {
-    const StageSizes z = tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G);
+    return view_of(tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G), buf);
+}
+
+// The same view for a format known at compile time (D = 128, G = 32: the
+// sizes fold to shifts of npad).
+template <int KB, int KAX, int VB>
+__device__ __forceinline__ View tier_view_c(int npad, const uint8_t* buf) {
+    return view_of(tier_stage_sizes(KAX, KB, VB, npad, 128, 32), buf);
+}
+
+__device__ __forceinline__ View view_of(const StageSizes& z, const uint8_t* buf) {
     const uint32_t o_ks = a16(z.kc), o_kz = o_ks + a16(z.ks), o_vc = o_kz + a16(z.ks);
     const uint32_t o_vs = o_vc + a16(z.vc), o_vz = o_vs + a16(z.vs);
     View v;
@@ -921,19 +933,24 @@ __device__ __forceinline__ void mma_logits_token(const View& v, int tl, const ui
                 mma16816(R[n], af, b0, b1);
             }
         }
+        // R carries the factor 2^KB of the fragments: s R = (2^KB s) R_1, and
+        // zp = z - 2^KB s (both exact rewrites of the unscaled form).  The two
+        // tokens 2t, 2t + 1 of a row go together, on packed float32 pairs.
+        const unsigned long long mk2 = f2_pack(-(float)(1 << KB), -(float)(1 << KB));
 #pragma unroll
-        for (int n = 0; n < NT; ++n)
+        for (int n = 0; n < NT; ++n) {
+            const int tok = tl + 8 * n + 2 * t;
+            const unsigned long long s2 = f2_pack(h2f_bits(v.ks[tok * GR + grp]), h2f_bits(v.ks[(tok + 1) * GR + grp]));
+            const unsigned long long zp2 =
+                f2_fma(s2, mk2, f2_pack(h2f_bits(v.kz[tok * GR + grp]), h2f_bits(v.kz[(tok + 1) * GR + grp])));
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                // R carries the factor 2^KB of the fragments: s R = (2^KB s) R_1, and
-                // zp = z - 2^KB s (both exact rewrites of the unscaled form)
-                const int tok = tl + 8 * n + 2 * t + jj;
-                const float s = h2f_bits(v.ks[tok * GR + grp]);
-                const float zp = fmaf(-(float)(1 << KB), s, h2f_bits(v.kz[tok * GR + grp]));
-#pragma unroll
-                for (int ri = 0; ri < RI; ++ri)
-                    S[n][2 * ri + jj] = fmaf(s, R[n][2 * ri + jj], fmaf(qs[grp][ri], zp, S[n][2 * ri + jj]));
+            for (int ri = 0; ri < RI; ++ri) {
+                unsigned long long a2 = f2_pack(S[n][2 * ri], S[n][2 * ri + 1]);
+                a2 = f2_fma(f2_pack(qs[grp][ri], qs[grp][ri]), zp2, a2);
+                a2 = f2_fma(s2, f2_pack(R[n][2 * ri], R[n][2 * ri + 1]), a2);
+                f2_unpack(a2, S[n][2 * ri], S[n][2 * ri + 1]);
             }
+        }
     }
 }
 
@@ -1293,7 +1310,10 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
         if (ok) {
             const int j0 = (r + i * a.cluster - us.base[t]) * kSub;
             const int n = min(kSub, us.cnt[t] - j0);
-            const View v = tier_view(ta, (n + 31) & ~31, 128, a.G, item_buf(a, stage_base, i));
+            // per-token formats (G = 32) fold to constants; per-channel keys allow G = 32..128
+            const View v = KAX == KVQ_AXIS_TOKEN
+                               ? tier_view_c<KB, KVQ_AXIS_TOKEN, VB>((n + 31) & ~31, item_buf(a, stage_base, i))
+                               : tier_view(ta, (n + 31) & ~31, 128, a.G, item_buf(a, stage_base, i));
             const int tl = warp * TPW;
             if (tl < n) {
                 float* lo = (a.policy == KVQ_POLICY_MIKV && lg_unit) ? lg_unit + ta.slot_base + j0 + tl : nullptr;
@@ -1543,6 +1563,19 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
     __syncthreads();
 
     const UnitState& us = sm.us;
+    // the new token joins the ring now, off the leader's final path: its slot
+    // (start + len) is not among the len rows any CTA reads this step (the new
+    // row itself is read from k_new / v_new), and the leader's MiniKV flush
+    // reads it after the cluster barriers of the merge
+    if (r == C - 1) {
+        const int cap = a.res_cap;
+        const size_t slot = unit * (size_t)cap + (us.start + us.len) % cap;
+        for (int c = threadIdx.x; c < D; c += blockDim.x) {
+            stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
+            stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
+        }
+        if (threadIdx.x == 0) a.res_token_id[slot] = us.pos;
+    }
     const int n_local = us.total > ir ? (us.total - ir + C - 1) / C : 0;
     float* lg_unit = a.logits ? a.logits + unit * NG * (size_t)a.slots : nullptr;
     bool ok = true;
@@ -1637,16 +1670,10 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         add_scores<NG, D>(a, sm, unit, ir, n_local, lg_unit);
     }
 
-    // ---- leader: the new token joins the ring, MiniKV flush, counters
+    // ---- leader: MiniKV flush, counters
     if (r == 0) {
         const int cap = a.res_cap, len = us.len, start = us.start;
-        const size_t slot = unit * (size_t)cap + (start + len) % cap;
-        for (int c = threadIdx.x; c < D; c += blockDim.x) {
-            stf(a.res_k, slot * D + c, ldf(a.k_new, unit * D + c, bf), bf);
-            stf(a.res_v, slot * D + c, ldf(a.v_new, unit * D + c, bf), bf);
-        }
-        if (threadIdx.x == 0) a.res_token_id[slot] = us.pos;
-        __syncthreads();
+        __syncthreads();                        // C = 1: this CTA's own ring append is done
         bool flushed = false;
         if (a.policy == KVQ_POLICY_MINIKV && len + 1 == a.nr + a.G) {
             flushed = bf ? minikv_flush<__nv_bfloat16>(a, unit, start, us.cnt[0])

@@ -294,14 +294,12 @@ __global__ void __launch_bounds__(192, 2)
                 for (int c = 0; c < kBN; ++c) {
                     const int kidx = kbase + c;
                     if (kidx > i || kidx >= T_len) s[c] = -__int_as_float(0x7f800000);
-                    mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], s[c]);
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]))) * scale_log2;
+#pragma unroll
+            for (int c = 0; c < kBN; c += 2) mxp[(c >> 1) & 7] = fmax3(mxp[(c >> 1) & 7], s[c], s[c + 1]);
+            const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]),
+                                   fmaxf(mxp[6], mxp[7])) * scale_log2;
             const float m_new = fmaxf(m_used, mx);
             const bool resc = m_new > m_used + kRescaleLog2;
             if (__any_sync(0xffffffffu, resc && j >= 1)) {

@@ -79,3 +79,27 @@ def test_tier_byte_accounting(L):
     assert per_token_payload == 96             # 3 bits per scalar, keys + values
     assert tot == sum(out)
     assert L.kvq_tier_bytes(1, 128, 32, 2, 2, kvq.AXIS_CHANNEL, 40, out) == 0
+
+
+def test_token_tiers_need_groups_of_32(L):
+    """The decode kernels take four 32-channel groups per token: a per-token tier with
+    another group size is refused on the host (the descriptor is never dereferenced)."""
+    from bit_mixed_precision_gb300 import kvq
+    c = kvq.KvqCache()
+    c.B, c.Hq, c.Hkv, c.D, c.dtype, c.policy, c.n_tiers = 1, 4, 1, 128, kvq.F16, kvq.POLICY_MIKV, 2
+    fake = 1 << 20                                  # aligned, never read
+    for t, (kb, vb) in enumerate([(4, 4), (2, 2)]):
+        tr = c.tier[t]
+        tr.k_bits, tr.v_bits, tr.k_axis, tr.cap = kb, vb, kvq.AXIS_TOKEN, 256
+        for f in ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero", "token_id", "count"):
+            setattr(tr, f, fake)
+    c.res_cap, c.nr = 160, 128
+    for f in ("res_k", "res_v", "res_token_id", "res_start", "res_len", "seq_len", "cum_score"):
+        setattr(c, f, fake)
+    c.score_cap, c.hi_den = 1024, 5
+    size_max = ctypes.c_size_t(-1).value
+    c.G = 32
+    assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) != size_max, L.kvq_last_error()
+    c.G = 64
+    assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == size_max
+    assert b"G = 32" in L.kvq_last_error()
