@@ -4,27 +4,31 @@
 // forward_implications: fused dequantisation kernels during decoding).
 //
 // One launch per step.  Each (batch, KV head) unit is one thread-block
-// cluster of C CTAs (C = 1 .. 16, chosen so that the grid fills the GPU in
-// one wave).  The unit's work is a list of items: 128-token sub-chunks of
-// every packed tier, then 32-row pieces of the residual ring (the new token
-// last); CTA r of the cluster takes items r, r + C, r + 2C, ...  A CTA
-// requests each item with bulk asynchronous copies into one of two staging
-// buffers (the next-but-one item is requested as soon as one is consumed);
-// its four warps take 32 tokens (or 8 residual rows) each: keys -> base-2
-// logits for the g query heads of the KV head, online softmax per warp, P.V
-// with the codes turned into floats by one rotate and one LOP3 each.  The
-// CTA merges its warps and writes its partial (max, sum, unnormalised
-// output) into the shared memory of the cluster's leader (distributed shared
-// memory, no global round trip, no atomics).  The leader merges the C
-// partials and writes o and lse.  Then, per policy:
+// cluster of C CTAs (C = 1 .. 16: as many as one wave holds for small
+// caches, fewer for large ones).  The unit's work is a list of items:
+// 128-token sub-chunks of every packed tier, then 8-row pieces of the
+// residual ring (the new token last); the CTA of item rank q takes items
+// q, q + C, q + 2C, ... (the leader has the last rank).  A CTA requests
+// each item with bulk asynchronous copies into one of S staging buffers
+// (S = 2 or 4; item i + S is requested as soon as every warp is done with
+// item i); its four warps take 32 tokens (or 2 residual rows) each: keys ->
+// base-2 logits for the g query heads of the KV head (tensor cores for
+// head dim 128), online softmax per warp, P.V with the codes turned into
+// fp16 by one rotate or byte permute and one LOP3 per pair.  The CTA merges
+// its warps and writes its partial (max, sum, unnormalised output) into
+// the shared memory of the cluster's leader (distributed shared memory, no
+// global round trip, no atomics).  The leader merges the C partials and
+// writes o and lse.  Then, per policy:
 //   DiffKV / MiKV: the leader broadcasts the log-sum-exp and every CTA adds
 //     this step's attention to the scores of its own tokens (DiffKV: per
 //     ring slot and query head; MiKV: per token, summed over the group);
 //   MiniKV: when the residual reaches nr + G tokens the leader packs its G
 //     oldest into tier 0 (MiniKV review, nr; verdict JSON key_machinery).
-// The leader appends the new token to the ring and advances res_len and the
-// unit's position.  Tiers are read where they lie (MiKV rebuttal: attention
-// is permutation invariant, so each precision group sits in its own region).
+// The new token joins the ring at the start (from the cluster's last CTA;
+// its slot is not read this step) and the leader advances res_len and the
+// unit's position at the end.  Tiers are read where they lie (MiKV rebuttal:
+// attention is permutation invariant, so each precision group sits in its
+// own region).
 #include <algorithm>
 #include <mutex>
 
