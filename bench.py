@@ -232,7 +232,7 @@ class Hot:
                                         [kvq.TierSpec(4, 4, kvq.AXIS_TOKEN, nq // 5 + 64),
                                          kvq.TierSpec(2, 2, kvq.AXIS_TOKEN, nq + 64)],
                                         nr=nr, score_cap=T + steps + 1, hi_den=5, device=dev)
-            self.launches_per_step = 2 + 1 + 2 * steps
+            self.launches_per_step = 2 + 1 + 3 * steps          # decode, score update, policy step
         self.o_pre = torch.empty_like(self.q)
         self.lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
         self.cs = torch.empty_like(self.lse)

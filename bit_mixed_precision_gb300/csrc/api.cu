@@ -158,9 +158,8 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
               (tr.k_bits == 4 && tr.v_bits == 4) || (tr.k_bits == 2 && tr.v_bits == 2)));
         KVQ_REQUIRE(ok_combo, KVQ_EUNSUPPORTED, "%s: tier %d format K%dV%d axis %d not built", who, t,
                     tr.k_bits, tr.v_bits, tr.k_axis);
-        // per-token tiers: the kernels take four 32-channel groups per token
-        KVQ_REQUIRE(tr.k_axis != KVQ_AXIS_TOKEN || c->G == 32, KVQ_EUNSUPPORTED,
-                    "%s: tier %d: per-token tiers are built for G = 32", who, t);
+        // the decode kernels take value groups (and per-token key groups) of 32 channels
+        KVQ_REQUIRE(c->G == 32, KVQ_EUNSUPPORTED, "%s: tier %d: the decode kernels are built for G = 32", who, t);
     }
     KVQ_REQUIRE(c->res_cap > 0 && c->res_k && c->res_v && c->res_token_id && c->res_start && c->res_len &&
                     c->seq_len,

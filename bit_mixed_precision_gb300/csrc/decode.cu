@@ -99,6 +99,8 @@ struct DecodeArgs {
     float scale_log2;
     int slots;                  // logits row length per (unit, head)
     float* logits;              // [unit][g][slots] (DiffKV, MiKV) or null
+    float* lse2_ws;             // MiKV: [unit][8] the step's base-2 lse per head, for the score kernel
+    int32_t* meta_ws;           // MiKV: [unit][4] ring length, first slot and position before the step
     int cluster;                // CTAs per unit
     uint32_t stage_bytes;       // one staging buffer
     int stages, stage_shift;    // staging buffers per CTA (2 or 4) and its log2
@@ -703,11 +705,6 @@ __device__ void issue_item(const DecodeArgs& a, const UnitState& us, size_t unit
         const int j0 = idx * kSub;
         const int n = min(kSub, us.cnt[t] - j0);
         stage_tier(a.tier[t], unit, j0, (n + 31) & ~31, D, a.G, buf, bar);
-        if (a.policy == KVQ_POLICY_MIKV) {
-            // the item's token ids, read again after the merge to add its scores
-            const int32_t* ids = a.tier[t].token_id + unit * (size_t)a.tier[t].cap + j0;
-            if ((reinterpret_cast<uintptr_t>(ids) & 15u) == 0) bulk_prefetch_l2(ids, (uint32_t)((n + 31) & ~31) * 4u);
-        }
     } else {
         const int j0 = idx * kResItem;
         const int n = min(kResItem, us.len + 1 - j0);
@@ -1402,7 +1399,8 @@ __device__ void run_residual(const DecodeArgs& a, Smem<NG, D>& sm, size_t unit, 
 
 // ---- policy work after the merge
 
-// This step's attention added to the scores of the CTA's own tokens.
+// DiffKV: this step's attention added to the window scores of the CTA's own
+// ring rows, every (item, row, head) at once, all loads in flight together.
 template <int NG, int D>
 __device__ void add_scores(const DecodeArgs& a, const Smem<NG, D>& sm, size_t unit, int r, int n_local,
                            const float* lg_unit) {
@@ -1410,68 +1408,66 @@ __device__ void add_scores(const DecodeArgs& a, const Smem<NG, D>& sm, size_t un
     const int b = (int)(unit / a.Hkv), hkv = (int)(unit % a.Hkv);
     const int cap = a.res_cap;
     const float* lse2 = sm.lse2;
-    float* cs = a.cum_score + unit * (size_t)a.score_cap;
-    const int i_res = local_at(us.base[a.n_tiers], r, a.cluster);   // first local residual item
-    if (a.policy == KVQ_POLICY_MIKV) {
-        // packed tiers, one token of an item per thread, kBatch items at a time:
-        // every load of a batch is in flight before the first use
-        static_assert(Cfg<NG>::kThreads >= kSub, "one token per thread and item");
-        constexpr int kBatch = 20;
-        for (int i = 0; i < i_res && (int)threadIdx.x < kSub; i += kBatch) {
-            float p[kBatch];
-            int id[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                p[k] = 0.0f;
-                id[k] = -1;
-                int idx;
-                const int t = i + k < i_res ? item_kind(us, a.n_tiers, r + (i + k) * a.cluster, idx) : -1;
-                const int j = t >= 0 ? idx * kSub + (int)threadIdx.x : 0;
-                if (t >= 0 && j < us.cnt[t]) {
-                    const TierArgs& ta = a.tier[t];
-#pragma unroll
-                    for (int h = 0; h < NG; ++h)
-                        p[k] += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + ta.slot_base + j) - lse2[h]);
-                    id[k] = ta.token_id[unit * (size_t)ta.cap + j];
-                    if (id[k] < 0 || id[k] >= a.score_cap) {
-                        atomicOr(&g_status_decode, kDevCheck);
-                        id[k] = -1;
-                    }
-                }
-            }
-            float c[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) c[k] = id[k] >= 0 ? cs[id[k]] : 0.0f;
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k)
-                if (id[k] >= 0) cs[id[k]] = __fadd_rn(c[k], p[k]);
-        }
-    }
-    // the residual ring: every (item, row) pair of the CTA's ring items at once
-    // (MiKV: one per row; DiffKV: one per row and head), all loads in flight together
-    const int per = a.policy == KVQ_POLICY_MIKV ? 1 : NG;
-    const int n_pairs = (n_local - i_res) * kResItem * per;
+    const int i_res = local_at(us.base[a.n_tiers], r, a.cluster);   // first local ring item
+    const int n_pairs = (n_local - i_res) * kResItem * NG;
     for (int x = threadIdx.x; x < n_pairs; x += blockDim.x) {
-        const int k = x / (kResItem * per), rem = x % (kResItem * per);
+        const int k = x / (kResItem * NG), rem = x % (kResItem * NG);
         int idx;
         (void)item_kind(us, a.n_tiers, r + (i_res + k) * a.cluster, idx);
-        const int li = idx * kResItem + rem / per;
+        const int li = idx * kResItem + rem / NG, h = rem % NG;
         if (li > us.len) continue;                               // past the new token
-        if (a.policy == KVQ_POLICY_MIKV) {
-            float p = 0.0f;
-#pragma unroll
-            for (int h = 0; h < NG; ++h)
-                p += ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-            const int id = li < us.len ? a.res_token_id[unit * (size_t)cap + (us.start + li) % cap] : us.pos;
-            if (id < 0 || id >= a.score_cap) atomicOr(&g_status_decode, kDevCheck);
-            else cs[id] = li < us.len ? __fadd_rn(cs[id], p) : p;
-        } else {
-            const int h = rem % per;
-            const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
-            float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
-            *wa = li < us.len ? __fadd_rn(*wa, p) : p;
-        }
+        const float p = ex2_approx(__ldcg(lg_unit + (size_t)h * a.slots + a.res_slot_base + li) - lse2[h]);
+        float* wa = a.win_acc + ((size_t)b * a.Hq + hkv * NG + h) * cap + (us.start + li) % cap;
+        *wa = li < us.len ? __fadd_rn(*wa, p) : p;
     }
+}
+
+// MiKV: this step's attention added to the cumulative score of every token,
+// once the step's lse is known (written by the decode launch with the ring
+// state it saw).  One thread per logits slot of a unit: the tiers' slots,
+// then the ring's; p = sum over the group's heads of 2^(s - lse2).
+struct ScoreArgs {
+    int g, n_tiers, slots, res_cap, res_slot_base, score_cap;
+    const int32_t* token_id[KVQ_MAX_TIERS];
+    const int32_t* count[KVQ_MAX_TIERS];
+    int cap[KVQ_MAX_TIERS], slot_base[KVQ_MAX_TIERS];
+    const int32_t* res_token_id;
+    const float* logits;
+    const float* lse2;
+    const int32_t* meta;
+    float* cum_score;
+};
+
+__global__ void __launch_bounds__(256) mikv_scores_kernel(ScoreArgs s) {
+    const size_t unit = blockIdx.y;
+    const int x = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+    if (x >= s.slots) return;
+    const int32_t* meta = s.meta + unit * 4;
+    int id;
+    bool fresh = false;
+    if (x >= s.res_slot_base) {
+        const int li = x - s.res_slot_base, len = meta[0];
+        if (li > len) return;
+        id = li < len ? s.res_token_id[unit * (size_t)s.res_cap + (meta[1] + li) % s.res_cap] : meta[2];
+        fresh = li == len;                     // the step's own token: its first score
+    } else {
+        static_assert(KVQ_MAX_TIERS == 2, "two tiers at most");
+        const bool t1 = s.n_tiers > 1 && x >= s.slot_base[1];     // no indexing of the parameter arrays
+        const int cap = t1 ? s.cap[1] : s.cap[0];
+        const int j = x - (t1 ? s.slot_base[1] : s.slot_base[0]);
+        const int n = min(max((t1 ? s.count[1] : s.count[0])[unit], 0), cap);
+        if (j >= n) return;
+        id = (t1 ? s.token_id[1] : s.token_id[0])[unit * (size_t)cap + j];
+    }
+    const float* lg = s.logits + unit * (size_t)s.g * s.slots + x;
+    float p = 0.0f;
+    for (int h = 0; h < s.g; ++h) p += ex2_approx(__ldcs(lg + (size_t)h * s.slots) - s.lse2[unit * 8 + h]);
+    if (id < 0 || id >= s.score_cap) {
+        atomicOr(&g_status_decode, kDevCheck);
+        return;
+    }
+    float* cs = s.cum_score + unit * (size_t)s.score_cap + id;
+    *cs = fresh ? p : __fadd_rn(*cs, p);
 }
 
 // Leader, MiniKV: the G oldest residual tokens (the new one already in the
@@ -1652,6 +1648,7 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
                     sm.lsum[h] = L;
                     sm.lse2[h] = M + __log2f(L);
                     if (a.lse_out) a.lse_out[(size_t)b * a.Hq + hkv * NG + h] = (M + __log2f(L)) * kLn2;
+                    if (a.lse2_ws) a.lse2_ws[unit * 8 + h] = M + __log2f(L);
                 }
             }
         }
@@ -1664,8 +1661,14 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         }
     }
 
-    // ---- DiffKV / MiKV: every CTA adds the step's attention to its own tokens
-    if (a.policy != KVQ_POLICY_MINIKV && lg_unit) {
+    // ---- DiffKV: every CTA adds the step's attention to its own ring tokens (MiKV
+    // adds every token's in mikv_scores_kernel, after this launch)
+    if (r == 0 && threadIdx.x == 0 && a.meta_ws) {
+        a.meta_ws[unit * 4 + 0] = us.len;
+        a.meta_ws[unit * 4 + 1] = us.start;
+        a.meta_ws[unit * 4 + 2] = us.pos;
+    }
+    if (a.policy == KVQ_POLICY_DIFFKV && lg_unit) {
         if (r == 0 && threadIdx.x < NG)
             for (int y = 0; y < C; ++y)
                 cluster_st_f32(cluster_map(smem_u32(&sm.lse2[threadIdx.x]), y), sm.lse2[threadIdx.x]);
@@ -1700,7 +1703,7 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
 
 struct WsLayout {
     int slots;
-    size_t logits, total;
+    size_t logits, lse2, meta, total;
 };
 
 WsLayout ws_layout(const kvq_cache& c) {
@@ -1712,6 +1715,11 @@ WsLayout ws_layout(const kvq_cache& c) {
     w.slots = slots;
     w.logits = 0;
     w.total = c.policy != KVQ_POLICY_MINIKV ? (size_t)units * g * slots * sizeof(float) : 0;
+    if (c.policy == KVQ_POLICY_MIKV) {
+        w.lse2 = (w.total + 255) & ~(size_t)255;
+        w.meta = w.lse2 + (size_t)units * 8 * sizeof(float);
+        w.total = w.meta + (size_t)units * 4 * sizeof(int32_t);
+    }
     return w;
 }
 
@@ -1912,23 +1920,48 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.slots = w.slots;
     a.logits = c.policy != KVQ_POLICY_MINIKV ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + w.logits)
                                              : nullptr;
+    a.lse2_ws = c.policy == KVQ_POLICY_MIKV ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + w.lse2) : nullptr;
+    a.meta_ws = c.policy == KVQ_POLICY_MIKV ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + w.meta) : nullptr;
     bool channel_only = true;
     for (int t = 0; t < c.n_tiers; ++t) channel_only &= c.tier[t].k_axis == KVQ_AXIS_CHANNEL;
     if (c.D == 64) return a.g == 1 ? launch_typed<1, 64, 1>(a, c, units, s) : cudaErrorInvalidConfiguration;
     if (c.D != 128) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaErrorInvalidConfiguration;
     switch (a.g * 2 + (channel_only ? 0 : 1)) {
-        case 2: return launch_typed<1, 128, 1>(a, c, units, s);
-        case 3: return launch_typed<1, 128, 3>(a, c, units, s);
-        case 4: return launch_typed<2, 128, 1>(a, c, units, s);
-        case 5: return launch_typed<2, 128, 3>(a, c, units, s);
-        case 8: return launch_typed<4, 128, 1>(a, c, units, s);
-        case 9: return launch_typed<4, 128, 3>(a, c, units, s);
-        case 10: return launch_typed<5, 128, 1>(a, c, units, s);
-        case 11: return launch_typed<5, 128, 3>(a, c, units, s);
-        case 16: return launch_typed<8, 128, 1>(a, c, units, s);
-        case 17: return launch_typed<8, 128, 3>(a, c, units, s);
+        case 2: e = launch_typed<1, 128, 1>(a, c, units, s); break;
+        case 3: e = launch_typed<1, 128, 3>(a, c, units, s); break;
+        case 4: e = launch_typed<2, 128, 1>(a, c, units, s); break;
+        case 5: e = launch_typed<2, 128, 3>(a, c, units, s); break;
+        case 8: e = launch_typed<4, 128, 1>(a, c, units, s); break;
+        case 9: e = launch_typed<4, 128, 3>(a, c, units, s); break;
+        case 10: e = launch_typed<5, 128, 1>(a, c, units, s); break;
+        case 11: e = launch_typed<5, 128, 3>(a, c, units, s); break;
+        case 16: e = launch_typed<8, 128, 1>(a, c, units, s); break;
+        case 17: e = launch_typed<8, 128, 3>(a, c, units, s); break;
     }
-    return cudaErrorInvalidConfiguration;
+    if (e != cudaSuccess || c.policy != KVQ_POLICY_MIKV) return e;
+    // MiKV: every token's score, once the step's lse is known
+    ScoreArgs sa{};
+    sa.g = a.g;
+    sa.n_tiers = c.n_tiers;
+    sa.slots = w.slots;
+    sa.res_cap = c.res_cap;
+    sa.res_slot_base = a.res_slot_base;
+    sa.score_cap = c.score_cap;
+    for (int t = 0; t < c.n_tiers; ++t) {
+        sa.token_id[t] = c.tier[t].token_id;
+        sa.count[t] = c.tier[t].count;
+        sa.cap[t] = c.tier[t].cap;
+        sa.slot_base[t] = a.tier[t].slot_base;
+    }
+    sa.res_token_id = c.res_token_id;
+    sa.logits = a.logits;
+    sa.lse2 = a.lse2_ws;
+    sa.meta = a.meta_ws;
+    sa.cum_score = c.cum_score;
+    const dim3 grid((unsigned)((w.slots + 255) / 256), (unsigned)units);
+    mikv_scores_kernel<<<grid, 256, 0, s>>>(sa);
+    return cudaGetLastError();
 }
 
 // ---- workspace in the library's own device memory, for callers that cannot

@@ -97,6 +97,8 @@ typedef struct {
 
 /* The compressed cache of one attention layer.  Plain struct of device
  * pointers, filled by the caller (sizes from kvq_cache_bytes()).
+ * G: the quantisation group; the decode and policy entry points are built
+ *   for G = 32 (KVQ_EUNSUPPORTED otherwise; kv_quant_pack takes 16..128).
  *
  * Residual: a ring of res_cap full-precision tokens per unit
  *   res_k/res_v [u][res_cap][D] (activation dtype), res_token_id [u][res_cap],

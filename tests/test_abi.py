@@ -81,25 +81,32 @@ def test_tier_byte_accounting(L):
     assert L.kvq_tier_bytes(1, 128, 32, 2, 2, kvq.AXIS_CHANNEL, 40, out) == 0
 
 
-def test_token_tiers_need_groups_of_32(L):
-    """The decode kernels take four 32-channel groups per token: a per-token tier with
-    another group size is refused on the host (the descriptor is never dereferenced)."""
+def test_decode_caches_need_groups_of_32(L):
+    """The decode kernels take value groups (and per-token key groups) of 32 channels: a cache
+    with another group size is refused on the host (the descriptor is never dereferenced)."""
     from bit_mixed_precision_gb300 import kvq
-    c = kvq.KvqCache()
-    c.B, c.Hq, c.Hkv, c.D, c.dtype, c.policy, c.n_tiers = 1, 4, 1, 128, kvq.F16, kvq.POLICY_MIKV, 2
     fake = 1 << 20                                  # aligned, never read
-    for t, (kb, vb) in enumerate([(4, 4), (2, 2)]):
-        tr = c.tier[t]
-        tr.k_bits, tr.v_bits, tr.k_axis, tr.cap = kb, vb, kvq.AXIS_TOKEN, 256
-        for f in ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero", "token_id", "count"):
-            setattr(tr, f, fake)
-    c.res_cap, c.nr = 160, 128
-    for f in ("res_k", "res_v", "res_token_id", "res_start", "res_len", "seq_len", "cum_score"):
-        setattr(c, f, fake)
-    c.score_cap, c.hi_den = 1024, 5
     size_max = ctypes.c_size_t(-1).value
-    c.G = 32
-    assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) != size_max, L.kvq_last_error()
-    c.G = 64
-    assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == size_max
-    assert b"G = 32" in L.kvq_last_error()
+
+    def cache(policy, tiers, nr, res_cap):
+        c = kvq.KvqCache()
+        c.B, c.Hq, c.Hkv, c.D, c.dtype, c.policy, c.n_tiers = 1, 4, 1, 128, kvq.F16, policy, len(tiers)
+        for t, (kb, vb, ax) in enumerate(tiers):
+            tr = c.tier[t]
+            tr.k_bits, tr.v_bits, tr.k_axis, tr.cap = kb, vb, ax, 256
+            for f in ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero", "token_id", "count"):
+                setattr(tr, f, fake)
+        c.res_cap, c.nr = res_cap, nr
+        for f in ("res_k", "res_v", "res_token_id", "res_start", "res_len", "seq_len", "cum_score"):
+            setattr(c, f, fake)
+        c.score_cap, c.hi_den = 1024, 5
+        return c
+
+    mikv = cache(kvq.POLICY_MIKV, [(4, 4, kvq.AXIS_TOKEN), (2, 2, kvq.AXIS_TOKEN)], 128, 192)
+    minikv = cache(kvq.POLICY_MINIKV, [(2, 2, kvq.AXIS_CHANNEL)], 0, 128)
+    for c in (mikv, minikv):
+        c.G = 32
+        assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) != size_max, L.kvq_last_error()
+        c.G = 64
+        assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == size_max
+        assert b"G = 32" in L.kvq_last_error()

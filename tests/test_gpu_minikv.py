@@ -16,11 +16,11 @@ from tests.helpers import assert_attn_close, assert_scores_close, np_, selection
 pytestmark = pytest.mark.gpu
 
 
-def _pipeline(B, H, T, D, steps, nr, n_out, out_scale, seed, hh=25, rw=25, G=32):
+def _pipeline(B, H, T, D, steps, nr, n_out, out_scale, seed, hh=25, rw=25, G=32, dtype=torch.float16):
     dev = "cuda"
     scale = 1.0 / math.sqrt(D)
     outl = inputs.outlier_channels(H, D, n_out, seed)
-    x = inputs.make_qkv(B, H, H, T, D, seed=seed, outliers=outl, outlier_scale=out_scale)
+    x = inputs.make_qkv(B, H, H, T, D, dtype=dtype, seed=seed, outliers=outl, outlier_scale=out_scale)
     q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
     o, lse, cs = kvq.prefill_attn_scores(q, k, v, scale)
     k_hh, w = OS.budget(T, hh, rw)
@@ -38,7 +38,7 @@ def _pipeline(B, H, T, D, steps, nr, n_out, out_scale, seed, hh=25, rw=25, G=32)
     same = [selection_agrees(gsel[u], ref_sel[u], ref_cs[u], k_hh, w) for u in range(B * H)]
     r0 = n_sel if n_sel <= nr else nr + (n_sel - nr) % G
     cap = ((n_sel - r0 + steps + G - 1) // G + 1) * G
-    cache = kvq.make_cache(B, H, H, D, G, torch.float16, kvq.POLICY_MINIKV,
+    cache = kvq.make_cache(B, H, H, D, G, dtype, kvq.POLICY_MINIKV,
                            [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=nr)
     kvq.requant_demote(cache, 0, k_src=k, v_src=v, sel_idx=idx, n_sel=n_sel)
     units = [OP.MiniKVUnit(np_(x.k[u // H, u % H]), np_(x.v[u // H, u % H]), ref_sel[u], nr, G)
@@ -57,7 +57,7 @@ def _pipeline(B, H, T, D, steps, nr, n_out, out_scale, seed, hh=25, rw=25, G=32)
         assert np.array_equal(u16(t0.v_zero[u, :npk]), units[u].vze.view(np.uint16))
     max_err = 0.0
     for t in range(steps):
-        qd, kd, vd = inputs.make_decode_step(B, H, H, D, t, seed=seed, outliers=outl,
+        qd, kd, vd = inputs.make_decode_step(B, H, H, D, t, dtype=dtype, seed=seed, outliers=outl,
                                              outlier_scale=out_scale)
         od, ld = kvq.decode_attn_qkv(qd.to(dev), kd.to(dev), vd.to(dev), cache, scale)
         kvq.requant_demote(cache, t + 1)
@@ -98,3 +98,8 @@ def test_minikv_llama_layer():
     """LLaMA2-7B-shaped layer: 32 heads, prompt 4096, 2% outlier channels x10, nr = 128,
     128 decode steps (four flushes)."""
     _pipeline(B=1, H=32, T=4096, D=128, steps=128, nr=128, n_out=3, out_scale=10.0, seed=0)
+
+
+def test_minikv_bf16():
+    """bf16 prompt, decode inputs, residual ring and output (prompt 1024, 40 steps, nr = 0)."""
+    _pipeline(B=2, H=2, T=1024, D=128, steps=40, nr=0, n_out=2, out_scale=8.0, seed=4, dtype=torch.bfloat16)
