@@ -277,6 +277,11 @@ size_t kvq_tier_bytes(int units, int D, int G, int k_bits, int v_bits, int k_axi
     return tot;
 }
 
+kvq_status kvq_debug_withhold_copy(int on) {
+    kvq::set_withhold_copy(on);
+    return KVQ_OK;
+}
+
 kvq_status kvq_device_status(void* stream, uint32_t* out) {
     KVQ_REQUIRE(out, KVQ_EINVAL, "kvq_device_status: null out");
     cudaStream_t s = (cudaStream_t)stream;

@@ -30,6 +30,7 @@
 // attention is permutation invariant, so each precision group sits in its
 // own region).
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "kvq_common.cuh"
@@ -105,6 +106,7 @@ struct DecodeArgs {
     int cluster;                // CTAs per unit
     uint32_t stage_bytes;       // one staging buffer
     int stages, stage_shift;    // staging buffers per CTA (2 or 4) and its log2
+    int withhold_unit;          // failure-detection check: unit whose first CTA skips its first copy, or -1
     uint32_t qf_off, part_off, stage_off;  // dynamic shared memory offsets
 };
 
@@ -1549,7 +1551,8 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         sm.fail = 0;
         fence_mbar_init();
         const int n_local = us.total > ir ? (us.total - ir + C - 1) / C : 0;
-        for (int i = 0; i < a.stages && i < n_local; ++i) issue_item(a, us, unit, ir, i, stage_base, sm.bar);
+        for (int i = 0; i < a.stages && i < n_local; ++i)
+            if (!(i == 0 && ir == 0 && (int)unit == a.withhold_unit)) issue_item(a, us, unit, ir, i, stage_base, sm.bar);
         sm.issued = min(a.stages, n_local);
     }
     for (int x = threadIdx.x; x < NG * D; x += blockDim.x) {
@@ -1866,6 +1869,12 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
 
 size_t decode_workspace_bytes(const kvq_cache& c) { return ws_layout(c).total; }
 
+namespace {
+std::atomic<int> g_withhold_copy{0};
+}  // namespace
+
+void set_withhold_copy(int on) { g_withhold_copy.store(on ? 1 : 0); }
+
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, const kvq_cache& c,
                           float sm_scale, void* o, float* lse_out, void* ws, cudaStream_t s) {
     const WsLayout w = ws_layout(c);
@@ -1887,6 +1896,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
     a.policy = c.policy;
     a.bf16 = c.dtype == KVQ_BF16 ? 1 : 0;
     a.nr = c.nr;
+    a.withhold_unit = g_withhold_copy.load() ? 0 : -1;
     int slot = 0;
     for (int t = 0; t < c.n_tiers; ++t) {
         const kvq_tier& ct = c.tier[t];

@@ -27,7 +27,7 @@ MAX_TIERS = 2
 EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "kvq_score_reduce", "select_tokens",
            "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
            "kvq_decode_workspace_bytes", "kvq_tier_bytes",
-           "kvq_last_error", "kvq_device_status", "kvq_version"]
+           "kvq_last_error", "kvq_device_status", "kvq_debug_withhold_copy", "kvq_version"]
 
 
 class KvqError(RuntimeError):
@@ -94,8 +94,9 @@ def lib():
         L.kvq_tier_bytes.restype = sz
         L.kvq_last_error.restype = ctypes.c_char_p
         L.kvq_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.kvq_debug_withhold_copy.argtypes = [i32]
         for name in ["kv_quant_pack", "prefill_attn_scores", "kvq_score_reduce", "select_tokens",
-                     "requant_demote", "decode_attn_qkv", "kvq_device_status"]:
+                     "requant_demote", "decode_attn_qkv", "kvq_device_status", "kvq_debug_withhold_copy"]:
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -196,6 +197,12 @@ def select_tokens(score, k_hh, w_recent, kmax=None, out=None, stream=None):
     _check(lib().select_tokens(_ptr(score), B, H, T, _ptr(k_hh), kmax, w_recent, _ptr(idx),
                                _ptr(n), None, 0, _stream(stream)))
     return idx, n
+
+
+def debug_withhold_copy(on):
+    """Failure-detection check: while on, decode launches withhold one staged copy of unit 0
+    so that its bounded waits run out and device_status() reports KVQ_ETIMEOUT."""
+    _check(lib().kvq_debug_withhold_copy(1 if on else 0))
 
 
 def device_status(stream=None):

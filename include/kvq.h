@@ -280,6 +280,14 @@ const char* kvq_last_error(void);
  * current device.  *out = 0 (fine), KVQ_ETIMEOUT or KVQ_EDEVICE. */
 kvq_status kvq_device_status(void* stream, uint32_t* out);
 
+/* Failure-detection check (tests).  While on != 0, every later
+ * decode_attn_qkv launch withholds the first staged copy of one CTA of unit
+ * 0: that CTA's bounded waits run out (about 2 s, then 2 s more while it
+ * drains), it gives up, and kvq_device_status() reports KVQ_ETIMEOUT.  No
+ * copy is left in flight and the context stays usable; the outputs of unit
+ * 0 are undefined for those launches.  Process-wide; returns KVQ_OK. */
+kvq_status kvq_debug_withhold_copy(int on);
+
 /* Library ABI version (major * 100 + minor). */
 int kvq_version(void);
 
