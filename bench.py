@@ -139,7 +139,9 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # the raw samples (the JSON line carries their summary); KVQ_CLOCKS_DIR keeps them
+        out_dir = os.environ.get("KVQ_CLOCKS_DIR") or os.path.join(ROOT, "_clocks")
+        self.path = os.path.join(out_dir, f"clocks_gpu{index}.csv")
 
     def __enter__(self):
         try:
