@@ -26,7 +26,9 @@ Pins (tests/test_oracle_attention.py): a pure-Python triple loop on tiny
 inputs, rows of P summing to 1, sum_j colscore_j = number of queries,
 colscore_{T-1} = P_{T-1,T-1}, the closed form for a zero query (uniform
 attention: O_i is the running mean of v and colscore_j = H_T - H_j with H
-the harmonic numbers), permutation invariance of decode.
+the harmonic numbers), permutation invariance of decode.  Observation-window
+scores: w_obs = T gives the full column scores, w_obs = 1 the last query's
+own attention row, and every window's scores sum to w_obs.
 """
 from __future__ import annotations
 
@@ -125,6 +127,17 @@ def colscore_cols(q, k, cols, lse, sm_scale, causal=True):
     if causal:
         p = np.where(np.arange(q.shape[0])[:, None] < cols[None, :], 0.0, p)
     return p.sum(axis=0)
+
+
+def window_colscore_head(q, k, sm_scale, w_obs, causal=True):
+    """Column scores over an observation window (SnapKV-style selection; the MiniKV verdict
+    JSON names SnapKV as a LongBench baseline without its mechanism, read as: keys scored
+    by the attention of the last w_obs queries): colscore_j = sum over i >= T - w_obs of
+    P_ij, P the full softmax of the prompt (rows keep their normalisation over all keys).
+    One head: q, k [T, D]; returns [T] float64."""
+    p, _ = attention_matrix(q, k, sm_scale, causal)
+    T = p.shape[0]
+    return p[T - w_obs:].sum(axis=0)
 
 
 def decode_head(q, keys, values, sm_scale):

@@ -117,3 +117,34 @@ def test_decode_textbook_and_permutation():
     assert np.allclose(p3, p[perm])
     o4, lse4, _ = A.decode_head(np.zeros(D), k, v, 0.3)
     assert np.allclose(o4, v.mean(axis=0)) and abs(lse4 - math.log(N)) < 1e-13
+
+
+def test_window_scores_pins():
+    """Observation-window column scores: the last w queries only.  Brute force by loops for
+    every window on tiny inputs (from the textbook loops' lse), w = T reduces to the full
+    column scores, and every window sums to w."""
+    r = np.random.default_rng(5)
+    T, D = 9, 4
+    q, k, v = (r.normal(size=(T, D)) for _ in range(3))
+    _, lse, _ = _loops_attention(q.tolist(), k.tolist(), v.tolist(), 0.41)
+    for w in range(1, T + 1):
+        ref = [0.0] * T
+        for i in range(T - w, T):
+            for j in range(i + 1):
+                ref[j] += math.exp(0.41 * sum(q[i][c] * k[j][c] for c in range(D)) - lse[i])
+        got = A.window_colscore_head(q, k, 0.41, w)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-14), w
+        assert abs(got.sum() - w) < 1e-12
+    _, _, cs = A.prefill_head(q, k, v, 0.41)
+    assert np.allclose(A.window_colscore_head(q, k, 0.41, T), cs, rtol=0, atol=1e-14)
+
+
+def test_window_scores_zero_query_closed_form():
+    """q = 0: colscore_j = H_T - H_max(j, T-w) (uniform rows over the window)."""
+    r = np.random.default_rng(6)
+    T, D = 40, 8
+    H = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, T + 1))])
+    for w in (1, 7, 40):
+        got = A.window_colscore_head(np.zeros((T, D)), r.normal(size=(T, D)), 0.125, w)
+        ref = H[T] - H[np.maximum(np.arange(T), T - w)]
+        assert np.allclose(got, ref, atol=1e-13), w
