@@ -96,8 +96,26 @@ kvq_status prefill_attn_scores(const void* q, const void* k, const void* v, kvq_
     KVQ_REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(o, 16) && aligned(lse, 4),
                 KVQ_EINVAL, "prefill_attn_scores: q/k/v/o must be 16-byte aligned");
     KVQ_REQUIRE(sm_scale > 0.0f, KVQ_EINVAL, "prefill_attn_scores: sm_scale must be positive");
-    return kvq::run_prefill(q, k, v, dt, B, Hq, Hkv, T, D, sm_scale, o, lse, colscore,
+    return kvq::run_prefill(q, k, v, dt, B, Hq, Hkv, T, D, sm_scale, o, lse, colscore, 0,
                             (cudaStream_t)stream);
+}
+
+kvq_status prefill_window_scores(const void* q, const void* k, kvq_dtype dt, int B, int Hq, int Hkv, int T,
+                                 int D, float sm_scale, const float* lse, int w_obs, float* colscore,
+                                 void* stream) {
+    KVQ_REQUIRE(q && k && lse && colscore, KVQ_EINVAL, "prefill_window_scores: null pointer");
+    KVQ_REQUIRE(dt == KVQ_F16 || dt == KVQ_BF16, KVQ_EINVAL, "prefill_window_scores: dtype must be f16 or bf16");
+    KVQ_REQUIRE(B > 0 && Hq > 0 && Hkv > 0 && T > 0, KVQ_EINVAL, "prefill_window_scores: sizes must be positive");
+    KVQ_REQUIRE(Hq % Hkv == 0, KVQ_EINVAL, "prefill_window_scores: Hq %% Hkv != 0");
+    KVQ_REQUIRE(D == 64 || D == 128, KVQ_EUNSUPPORTED, "prefill_window_scores: head dim %d unsupported (64 or 128)", D);
+    KVQ_REQUIRE(w_obs >= 1 && w_obs <= T, KVQ_EINVAL, "prefill_window_scores: w_obs must be in [1, T]");
+    KVQ_REQUIRE(B * Hq <= 65535 * 1024 && T <= (1 << 30), KVQ_EINVAL, "prefill_window_scores: too large");
+    KVQ_REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(lse, 4) && aligned(colscore, 4), KVQ_EINVAL,
+                "prefill_window_scores: q/k must be 16-byte aligned");
+    KVQ_REQUIRE(sm_scale > 0.0f, KVQ_EINVAL, "prefill_window_scores: sm_scale must be positive");
+    // pass 2 alone over the last w_obs queries (k stands in for the unused value map)
+    return kvq::run_prefill(q, k, k, dt, B, Hq, Hkv, T, D, sm_scale, nullptr, const_cast<float*>(lse),
+                            colscore, T - w_obs, (cudaStream_t)stream);
 }
 
 kvq_status kvq_score_reduce(const float* colscore, int B, int Hq, int Hkv, int T, int mode,

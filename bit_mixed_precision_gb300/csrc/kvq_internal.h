@@ -23,9 +23,10 @@ cudaError_t launch_quant_pack_strided(const void* x, int dt, int units, int T, i
                                       int axis, int cap, uint32_t* codes, uint16_t* scale,
                                       uint16_t* zero, cudaStream_t s);
 
+// o == NULL: pass 2 only (lse given).  q_first: the first query counted in colscore.
 kvq_status run_prefill(const void* q, const void* k, const void* v, int dt, int B, int Hq,
                        int Hkv, int T, int D, float sm_scale, void* o, float* lse,
-                       float* colscore, cudaStream_t s);
+                       float* colscore, int q_first, cudaStream_t s);
 
 cudaError_t launch_select(const float* score, int units, int T, const int32_t* k_hh, int kmax,
                           int w, int32_t* idx_out, int32_t* n_out, cudaStream_t s);

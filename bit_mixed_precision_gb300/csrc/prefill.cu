@@ -382,7 +382,7 @@ template <typename T, int AB, int D>
 __global__ void __launch_bounds__(192, 2)
     prefill_pass2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const float* __restrict__ lse, float* __restrict__ colscore, int T_len,
-                         int Hq, int Hkv, int n_t, float scale_log2) {
+                         int Hq, int Hkv, int n_t, float scale_log2, int q_first) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -402,7 +402,10 @@ __global__ void __launch_bounds__(192, 2)
     const int kt = (int)blockIdx.y;
     const int b = bh / Hq, hq = bh % Hq;
     const int bhkv = b * Hkv + hq / (Hq / Hkv);
-    const int n_it = n_t - kt;
+    // query tiles kt + it0 .. n_t - 1: at or below the diagonal and reaching query q_first
+    // (queries before q_first count for nothing: their lse reads as +inf below)
+    const int it0 = max(0, q_first / kTile - kt);
+    const int n_it = n_t - kt - it0;
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C_KF), 1);
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(192, 2)
                 const uint32_t dst = sQ + (uint32_t)st * kTileBytes;
                 mbar_expect_tx(BAR(C_QF + st), kTileBytes);
                 for (int hf = 0; hf < kHalves; ++hf)
-                    tma_load_3d(dst + hf * kHalfBytes, &tq, 64 * hf, (kt + it) * kTile, bh,
+                    tma_load_3d(dst + hf * kHalfBytes, &tq, 64 * hf, (kt + it0 + it) * kTile, bh,
                                 BAR(C_QF + st));
                 last[st] = it;
             }
@@ -481,11 +484,12 @@ __global__ void __launch_bounds__(192, 2)
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int buf = it & 1;
-            const int qt = kt + it;
+            const int qt = kt + it0 + it;
             const int qi_own = qt * kTile + r;
             // minus the base-2 lse of each query (-inf past the prompt: exponent -inf)
-            lse_s[buf * kTile + r] =
-                qi_own < T_len ? -(lse[(size_t)bh * T_len + qi_own] * kLog2e) : -__int_as_float(0x7f800000);
+            lse_s[buf * kTile + r] = qi_own < T_len && qi_own >= q_first
+                                         ? -(lse[(size_t)bh * T_len + qi_own] * kLog2e)
+                                         : -__int_as_float(0x7f800000);
             // buffer buf is rewritten two tiles later, after every thread has
             // arrived for the tile in between, i.e. finished reading this one
             mbar_arrive(BAR(C_LSE + buf));
@@ -499,7 +503,7 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
             for (int e = 0; e < 8; ++e) tsp[e] = 0.0f;
             const int qbase = qt * kTile;
-            const bool diag = it == 0;
+            const bool diag = it0 == 0 && it == 0;
             // the 128 columns in four TMEM loads of 32, the next one in flight
             // while the current one is summed
             // off the diagonal, exponents and sums go two queries per instruction
@@ -594,7 +598,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int dt, int BH, int T, int D, int
 
 template <typename T, int AB, int D>
 kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq, int Hkv, int T_len,
-                     float sm_scale, void* o, float* lse, float* colscore, cudaStream_t s) {
+                     float sm_scale, void* o, float* lse, float* colscore, int q_first, cudaStream_t s) {
     using Lay = Layout<D>;
     CUtensorMap mq, mk, mk64, mv64;
     const int dt = AB == 0 ? KVQ_F16 : KVQ_BF16;
@@ -614,16 +618,19 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
     const int n_t = (T_len + kTile - 1) / kTile;
     const float scale_log2 = sm_scale * kLog2e;
     dim3 g1(B * Hq, n_t);
-    prefill_pass1_kernel<T, AB, D><<<g1, 192, Lay::P1_SMEM, s>>>(mq, mk64, mv64, (T*)o, lse, T_len, Hq,
-                                                                  Hkv, n_t, scale_log2);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        set_error("prefill pass 1 launch: %s", cudaGetErrorString(e));
-        return KVQ_ECUDA;
+    cudaError_t e = cudaSuccess;
+    if (o) {
+        prefill_pass1_kernel<T, AB, D><<<g1, 192, Lay::P1_SMEM, s>>>(mq, mk64, mv64, (T*)o, lse, T_len, Hq,
+                                                                      Hkv, n_t, scale_log2);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error("prefill pass 1 launch: %s", cudaGetErrorString(e));
+            return KVQ_ECUDA;
+        }
     }
     if (colscore) {
         prefill_pass2_kernel<T, AB, D><<<g1, 192, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
-                                                                      Hkv, n_t, scale_log2);
+                                                                      Hkv, n_t, scale_log2, q_first);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error("prefill pass 2 launch: %s", cudaGetErrorString(e));
@@ -636,16 +643,16 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
 }  // namespace
 
 kvq_status run_prefill(const void* q, const void* k, const void* v, int dt, int B, int Hq, int Hkv,
-                       int T, int D, float sm_scale, void* o, float* lse, float* colscore,
+                       int T, int D, float sm_scale, void* o, float* lse, float* colscore, int q_first,
                        cudaStream_t s) {
     if (D == 64) {
         if (dt == KVQ_F16)
-            return run_typed<__half, 0, 64>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
-        return run_typed<__nv_bfloat16, 1, 64>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
+            return run_typed<__half, 0, 64>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, q_first, s);
+        return run_typed<__nv_bfloat16, 1, 64>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, q_first, s);
     }
     if (dt == KVQ_F16)
-        return run_typed<__half, 0, 128>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
-    return run_typed<__nv_bfloat16, 1, 128>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, s);
+        return run_typed<__half, 0, 128>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, q_first, s);
+    return run_typed<__nv_bfloat16, 1, 128>(q, k, v, B, Hq, Hkv, T, sm_scale, o, lse, colscore, q_first, s);
 }
 
 }  // namespace kvq

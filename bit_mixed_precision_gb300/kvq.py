@@ -24,7 +24,7 @@ AXIS_CHANNEL, AXIS_TOKEN = 0, 1
 POLICY_MINIKV, POLICY_DIFFKV, POLICY_MIKV = 0, 1, 2
 MAX_TIERS = 2
 
-EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "kvq_score_reduce", "select_tokens",
+EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
            "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
            "kvq_decode_workspace_bytes", "kvq_tier_bytes",
            "kvq_last_error", "kvq_device_status", "kvq_debug_withhold_copy", "kvq_version"]
@@ -81,6 +81,7 @@ def lib():
         L.kv_quant_pack.argtypes = [vp, i32, i32, i32, i32, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.prefill_attn_scores.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp,
                                           vp, vp, sz, vp]
+        L.prefill_window_scores.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, vp]
         L.kvq_score_reduce.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp]
         L.select_tokens.argtypes = [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, sz, vp]
         L.requant_demote.argtypes = [ctypes.POINTER(KvqCache), i32, ctypes.POINTER(KvqPolicyParams),
@@ -95,7 +96,7 @@ def lib():
         L.kvq_last_error.restype = ctypes.c_char_p
         L.kvq_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.kvq_debug_withhold_copy.argtypes = [i32]
-        for name in ["kv_quant_pack", "prefill_attn_scores", "kvq_score_reduce", "select_tokens",
+        for name in ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
                      "requant_demote", "decode_attn_qkv", "kvq_device_status", "kvq_debug_withhold_copy"]:
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -171,6 +172,20 @@ def prefill_attn_scores(q, k, v, sm_scale=None, colscore=True, out=None, stream=
                                      float(sm_scale), 1, _ptr(o), _ptr(lse), _ptr(cs), None, 0,
                                      _stream(stream)))
     return o, lse, cs
+
+
+def prefill_window_scores(q, k, lse, w_obs, sm_scale=None, out=None, stream=None):
+    """Column scores over the last w_obs queries (lse from prefill_attn_scores): [B, Hq, T]."""
+    _cuda(q, k, lse)
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    _check(lib().prefill_window_scores(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, T, D, float(sm_scale), _ptr(lse),
+                                       int(w_obs), _ptr(out), _stream(stream)))
+    return out
 
 
 def kvq_score_reduce(colscore, Hkv, mode, out=None, stream=None):

@@ -179,6 +179,20 @@ kvq_status prefill_attn_scores(const void* q, const void* k, const void* v, kvq_
                                void* o, float* lse, float* colscore,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* prefill_window_scores -- column scores over an observation window of the
+ * last queries, SnapKV-style ([MiniKV-J]: SnapKV is a LongBench baseline and
+ * the SnapKV + KIVI combination the failure that drops 35 to 32 points; the
+ * pages name SnapKV without its mechanism, read here as scoring keys by the
+ * attention of the last w_obs queries, without its pooling):
+ *   colscore[j] = sum_{i >= max(j, T - w_obs)} exp(sm_scale q_i.k_j - lse_i)
+ * with lse (device) [B, Hq, T] from prefill_attn_scores (natural log).
+ * Runs pass 2 alone; q, k as for prefill_attn_scores; 1 <= w_obs <= T;
+ * colscore (device) [B, Hq, T] (keys after the window start also count
+ * only queries at or after themselves).  select_tokens then picks from it. */
+kvq_status prefill_window_scores(const void* q, const void* k, kvq_dtype dt, int B, int Hq, int Hkv, int T,
+                                 int D, float sm_scale, const float* lse, int w_obs, float* colscore,
+                                 void* stream);
+
 /* kvq_score_reduce -- GQA aggregation of per-query-head column scores.
  *   mode 0 (MiKV, H2O cumulative): out[b,h,j] = sum over the g heads in head order.
  *   mode 1 (DiffKV significance):  out[b,h,j] = max over the g heads of cs/(T - j).

@@ -58,3 +58,24 @@ def test_prefill_large_scores():
     oo, ol, oc = OA.prefill(np_(x.q), np_(x.k), np_(x.v), scale)
     assert_attn_close(o, oo, "O")
     assert_scores_close(cs, oc, "colscore")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,w_obs,dtype", [
+    (1, 2, 2, 300, 1, torch.float16),      # the last query's own row
+    (2, 4, 2, 300, 32, torch.float16),     # inside the last (ragged) tile
+    (1, 4, 1, 512, 200, torch.bfloat16),   # a window start inside a middle tile, bf16, g = 4
+    (1, 2, 2, 256, 256, torch.float16),    # the whole prompt: the full column scores
+])
+def test_window_scores_match_oracle(B, Hq, Hkv, T, w_obs, dtype):
+    """Observation-window column scores (pass 2 over the last w_obs queries) against the
+    float64 definition, with the same tolerance as the full column scores."""
+    x, scale, o, lse, cs = _run(B, Hq, Hkv, T, dtype)
+    ws = kvq.prefill_window_scores(x.q.cuda(), x.k.cuda(), lse, w_obs, scale)
+    torch.cuda.synchronize()
+    assert kvq.device_status() == 0
+    g = Hq // Hkv
+    for b in range(B):
+        for h in range(Hq):
+            ref = OA.window_colscore_head(np_(x.q[b, h]), np_(x.k[b, h // g]), scale, w_obs)
+            assert_scores_close(ws[b, h], ref, f"window scores {b},{h}")
+            assert abs(float(ws[b, h].double().sum()) - w_obs) <= 1e-4 * w_obs
