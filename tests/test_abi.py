@@ -110,3 +110,10 @@ def test_decode_caches_need_groups_of_32(L):
         c.G = 64
         assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == size_max
         assert b"G = 32" in L.kvq_last_error()
+    # workspace: MiniKV none; MiKV the step's logits [u][g][slots] (slots = tier caps + ring),
+    # then (256-byte aligned) the lse per head [u][8] and the ring state [u][4]
+    mikv.G = minikv.G = 32
+    assert L.kvq_decode_workspace_bytes(ctypes.byref(minikv)) == 0
+    slots = 256 + 256 + 192
+    logits = 1 * 4 * slots * 4
+    assert L.kvq_decode_workspace_bytes(ctypes.byref(mikv)) == (logits + 255) // 256 * 256 + 8 * 4 + 4 * 4
