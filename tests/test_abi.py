@@ -62,6 +62,13 @@ def test_host_validation_without_gpu(L):
                                  None, None, 0, None) == kvq.KVQ_EINVAL
     # window larger than the prompt
     assert L.select_tokens(vp, 1, 1, 10, vp, 4, 11, vp, vp, None, 0, None) == kvq.KVQ_EINVAL
+    # observation window outside [1, T], and a missing lse
+    for w in (0, 65):
+        assert L.prefill_window_scores(vp, vp, 0, 1, 2, 2, 64, 128, ctypes.c_float(0.1), vp, w, vp,
+                                       None) == kvq.KVQ_EINVAL
+    assert L.prefill_window_scores(vp, vp, 0, 1, 2, 2, 64, 128, ctypes.c_float(0.1), None, 8, vp,
+                                   None) == kvq.KVQ_EINVAL
+    assert b"prefill_window_scores" in L.kvq_last_error()
     # empty cache descriptor
     c = kvq.KvqCache()
     assert L.decode_attn_qkv(vp, vp, vp, ctypes.byref(c), ctypes.c_float(0.1), vp, None, vp, 1 << 20,
