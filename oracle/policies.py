@@ -79,6 +79,7 @@ class TokenTier:
     def __init__(self, k_bits, v_bits, group, d):
         self.k_bits, self.v_bits, self.group, self.d = k_bits, v_bits, group, d
         self.rows = {}   # token id -> (kc, ks, kz, vc, vs, vz)
+        self._deq = {}   # token id -> (the row it was computed from, k, v): a memo only
 
     def add_raw(self, tid, k, v):
         kc, ks, kz = quant.quant_pack_token(_f32(k)[None], self.k_bits, self.group)
@@ -86,9 +87,14 @@ class TokenTier:
         self.rows[int(tid)] = (kc[0], ks[0], kz[0], vc[0], vs[0], vz[0])
 
     def dequant(self, tid):
-        kc, ks, kz, vc, vs, vz = self.rows[int(tid)]
+        row = self.rows[int(tid)]
+        memo = self._deq.get(int(tid))
+        if memo is not None and memo[0] is row:          # same stored row: same values
+            return memo[1], memo[2]
+        kc, ks, kz, vc, vs, vz = row
         k = quant.unpack_token(kc[None], ks[None], kz[None], self.k_bits, self.group)[0]
         v = quant.unpack_token(vc[None], vs[None], vz[None], self.v_bits, self.group)[0]
+        self._deq[int(tid)] = (row, k, v)
         return k, v
 
     def ids(self):

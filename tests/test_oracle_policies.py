@@ -200,3 +200,28 @@ def test_mikv_ties_go_to_the_lower_position():
     # population 11 -> 2 places: token 10 (9 + 1/13) and the lower of the tied 3 / 7
     assert e == (10, "int4") and d == [7]
     assert u.hi.ids() == [3, 10]
+
+
+def test_mikv_gqa_group_is_summed():
+    """Two query heads that disagree: the INT4 set and every cumulative score follow the
+    SUM over the group (MiKV rebuttal, importance policy: H2O cumulative attention over
+    the heads that read the KV head).  Head 0 alone would keep {0, 2}, the max over the
+    heads {0, 1}; the sum keeps {0, 3}.  A zero query attends uniformly, so each decode
+    step adds 1/N per head, 2/N for the group; a mean over the heads would add 1/N."""
+    T, D = 12, 32
+    k, v = _kv(T + 1, D, 13)
+    cs = np.zeros((2, T), F32)
+    cs[0, [0, 2, 3, 10]] = [6, 2, 1, 3]
+    cs[1, [1, 3, 10]] = [4, 4, 2.5]
+    acc = P.mikv_cumulative(cs)
+    assert list(acc[:4]) == [6, 4, 2, 5] and acc[10] == F32(5.5)
+    u = P.MiKVUnit(k[:T], v[:T], cs, nr=2, group=32)
+    assert u.hi.ids() == [0, 3]                      # floor(10/5) = 2 places
+    q = np.zeros((2, D))
+    _, lse, e, d = u.step(T, q, k[T], v[T], 0.3)
+    assert np.allclose(lse, math.log(T + 1), atol=1e-12)
+    # population 11: 0 -> 6 + 2/13, 10 -> 5.5 + 2/13, 3 -> 5 + 2/13: token 10 enters, 3 leaves
+    assert e == (10, "int4") and d == [3]
+    assert u.hi.ids() == [0, 10]
+    for j, base in ((0, 6.0), (1, 4.0), (3, 5.0), (10, 5.5), (5, 0.0), (12, 0.0)):
+        assert abs(float(u.cs[j]) - (base + 2.0 / 13)) < 1e-6, f"token {j}"
