@@ -1,7 +1,9 @@
 """decode_attn_qkv_static: the decode entry point for callers that cannot give the
 library scratch memory (an engine whose allocator already owns all free device
-memory, or C code without a device allocator).  It must produce what
-decode_attn_qkv produces with a caller workspace, call after call.
+memory, or C code without a device allocator).  DiffKV and MiKV caches keep the
+step's logits in scratch, so those two run here: two calls in a row, each checked
+against the CPU oracle (outputs, cumulative scores, tier contents) and against the
+caller-workspace entry point on a twin cache.
 
 Collected last on purpose, so that a run stopping at the first failure has
 already run every other test."""
@@ -13,46 +15,118 @@ import pytest
 import torch
 
 from bit_mixed_precision_gb300 import inputs, kvq
-from tests.helpers import ATTN_ATOL, ATTN_RTOL, np_
+from oracle import policies as OP
+from tests.helpers import (assert_attn_close, assert_tiers_equal, gpu_tier_rows, np_,
+                           oracle_tier_rows)
 
 pytestmark = pytest.mark.gpu
 
-
-def _cache(k, v, idx, n_sel, B, H, D, nr, cap):
-    c = kvq.make_cache(B, H, H, D, 32, torch.float16, kvq.POLICY_MINIKV,
-                       [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=nr)
-    kvq.requant_demote(c, 0, k_src=k, v_src=v, sel_idx=idx, n_sel=n_sel)
-    return c
+G = 32
 
 
-def test_static_scratch_matches_caller_workspace():
-    B, H, T, D, nr = 1, 4, 512, 128, 32
-    x = inputs.make_qkv(B, H, H, T, D, seed=21, outliers=inputs.outlier_channels(H, D, 2, 21),
-                        outlier_scale=8.0)
-    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+def _scratch_used(cache):
+    need = kvq.lib().kvq_decode_workspace_bytes(ctypes.byref(cache.desc))
+    assert 0 < need <= kvq.STATIC_SCRATCH_BYTES
+    return need
+
+
+def _twin_outputs(a, b, what):
+    x, y = np_(a).astype(np.float64), np_(b).astype(np.float64)
+    assert np.all(np.abs(x - y) <= 2e-3 + 1e-2 * np.abs(y)), what
+
+
+def test_static_scratch_mikv_two_calls():
+    """MiKV, GQA 8/2, bf16: the static path's outputs and cumulative scores match the
+    oracle call after call, and its tiers after each re-ranking."""
+    B, Hq, Hkv, T, D, nr, steps = 1, 8, 2, 320, 128, 16, 2
+    g = Hq // Hkv
+    x = inputs.make_qkv(B, Hq, Hkv, T + steps, D, dtype=torch.bfloat16, seed=31,
+                        outliers=inputs.outlier_channels(Hkv, D, 1, 31), outlier_scale=12.0)
+    cs = inputs.random_scores(B, Hq, T, seed=31)
+    n_q = T - nr + steps
+
+    def make():
+        c = kvq.make_cache(B, Hq, Hkv, D, G, torch.bfloat16, kvq.POLICY_MIKV,
+                           [kvq.TierSpec(4, 4, kvq.AXIS_TOKEN, n_q // 5 + 2),
+                            kvq.TierSpec(2, 2, kvq.AXIS_TOKEN, n_q + 1)],
+                           nr=nr, score_cap=T + steps + 1, hi_den=5)
+        kvq.requant_demote(c, 0, k_src=x.k[:, :, :T].contiguous().cuda(),
+                           v_src=x.v[:, :, :T].contiguous().cuda(), colscore=cs.cuda())
+        return c
+
+    st, ws = make(), make()
+    _scratch_used(st)
+    units = [OP.MiKVUnit(np_(x.k[0, h, :T]), np_(x.v[0, h, :T]), np_(cs[0, h * g:(h + 1) * g]), nr, G)
+             for h in range(Hkv)]
     scale = 1.0 / math.sqrt(D)
-    _, _, cs = kvq.prefill_attn_scores(q, k, v, scale)
-    k_hh, w = T // 4, T // 4
-    idx, _ = kvq.select_tokens(cs, torch.full((B * H,), k_hh, dtype=torch.int32, device="cuda"), w)
-    cap = 512
-    with_ws = _cache(k, v, idx, k_hh + w, B, H, D, nr, cap)
-    no_ws = _cache(k, v, idx, k_hh + w, B, H, D, nr, cap)
-    need = kvq.lib().kvq_decode_workspace_bytes(ctypes.byref(no_ws.desc))
-    assert need <= kvq.STATIC_SCRATCH_BYTES
-    for t in range(2):                                   # two calls in a row
-        qd, kd, vd = inputs.make_decode_step(B, H, H, D, t, seed=21)
-        qd, kd, vd = qd.cuda(), kd.cuda(), vd.cuda()
-        o_ref, l_ref = kvq.decode_attn_qkv(qd, kd, vd, with_ws, scale)
-        o_st, l_st = kvq.decode_attn_qkv_static(qd, kd, vd, no_ws, scale)
-        kvq.requant_demote(with_ws, t + 1)
-        kvq.requant_demote(no_ws, t + 1)
+    for t in range(steps):                               # two calls in a row
+        qd = torch.randn((B, Hq, D), generator=torch.Generator().manual_seed(500 + t)).bfloat16()
+        kd, vd = x.k[:, :, T + t].contiguous(), x.v[:, :, T + t].contiguous()
+        o_st, _ = kvq.decode_attn_qkv_static(qd.cuda(), kd.cuda(), vd.cuda(), st, scale)
+        o_ws, _ = kvq.decode_attn_qkv(qd.cuda(), kd.cuda(), vd.cuda(), ws, scale)
         torch.cuda.synchronize()
-        a, b = np_(o_st).astype(np.float64), np_(o_ref).astype(np.float64)
-        assert np.all(np.abs(a - b) <= ATTN_ATOL + ATTN_RTOL * np.abs(b)), f"call {t}"
-        assert np.allclose(np_(l_st), np_(l_ref), atol=1e-5)
+        _twin_outputs(o_st, o_ws, f"static vs workspace, call {t}")
+        for u in range(Hkv):
+            ro, _ = units[u].attend(T + t, np_(qd[0, u * g:(u + 1) * g]), np_(kd[0, u]), np_(vd[0, u]), scale)
+            assert_attn_close(o_st[0, u * g:(u + 1) * g], ro, f"call {t} unit {u}")
+            ref = np.array([units[u].cs[j] for j in range(T + t + 1)], dtype=np.float32)
+            got = st.cum_score[u, :T + t + 1].cpu().numpy()
+            assert np.all(np.abs(got.astype(np.float64) - ref) <= 1e-4 * np.abs(ref) + 1e-6), \
+                f"cumulative scores, call {t} unit {u}"
+            # both caches continue from the oracle's float32 scores: later rankings compare bit for bit
+            st.cum_score[u, :T + t + 1] = torch.from_numpy(ref).cuda()
+            ws.cum_score[u, :T + t + 1] = torch.from_numpy(ref).cuda()
+        kvq.requant_demote(st, t + 1)
+        kvq.requant_demote(ws, t + 1)
+        for u in range(Hkv):
+            units[u].tail()
+            assert_tiers_equal(gpu_tier_rows(st.tiers[0], u), oracle_tier_rows(units[u].hi), f"INT4 u{u} call {t}")
+            assert_tiers_equal(gpu_tier_rows(st.tiers[1], u), oracle_tier_rows(units[u].lo), f"INT2 u{u} call {t}")
     assert kvq.device_status() == 0
-    assert torch.equal(with_ws.res_len, no_ws.res_len)
-    assert torch.equal(with_ws.seq_len, no_ws.seq_len)
+
+
+def test_static_scratch_diffkv_two_calls():
+    """DiffKV, GQA 10/2: the static path keeps each step's logits in the built-in array
+    and adds the window scores from there; outputs and the tiers after each window exit
+    match the oracle, and the twin cache with a caller workspace."""
+    B, Hq, Hkv, T, D, W, steps = 1, 10, 2, 384, 128, 64, 2
+    g = Hq // Hkv
+    x = inputs.make_qkv(B, Hq, Hkv, T + steps, D, seed=33)
+    cs = inputs.random_scores(B, Hq, T, seed=33) + 0.01
+    f = inputs.dirichlet_fractions(B * Hkv, seed=33)
+    n_high = np.floor(f[:, 0] * (T - W)).astype(np.int32)
+    n_low = np.floor(f[:, 1] * (T - W)).astype(np.int32)
+
+    def make():
+        c = kvq.make_cache(B, Hq, Hkv, D, G, torch.float16, kvq.POLICY_DIFFKV,
+                           [kvq.TierSpec(8, 4, kvq.AXIS_TOKEN, int(n_high.max()) + steps + 1),
+                            kvq.TierSpec(4, 2, kvq.AXIS_TOKEN, int(n_low.max()) + steps + 1)], nr=W)
+        kvq.requant_demote(c, 0, k_src=x.k[:, :, :T].contiguous().cuda(),
+                           v_src=x.v[:, :, :T].contiguous().cuda(), colscore=cs.cuda(),
+                           n_high=torch.from_numpy(n_high).cuda(), n_low=torch.from_numpy(n_low).cuda())
+        return c
+
+    st, ws = make(), make()
+    _scratch_used(st)
+    units = [OP.DiffKVUnit(np_(x.k[0, h, :T]), np_(x.v[0, h, :T]), np_(cs[0, h * g:(h + 1) * g]),
+                           int(n_high[h]), int(n_low[h]), W, G) for h in range(Hkv)]
+    scale = 1.0 / math.sqrt(D)
+    for t in range(steps):                               # two calls in a row
+        qd = torch.randn((B, Hq, D), generator=torch.Generator().manual_seed(700 + t)).half()
+        kd, vd = x.k[:, :, T + t].contiguous(), x.v[:, :, T + t].contiguous()
+        o_st, _ = kvq.decode_attn_qkv_static(qd.cuda(), kd.cuda(), vd.cuda(), st, scale)
+        o_ws, _ = kvq.decode_attn_qkv(qd.cuda(), kd.cuda(), vd.cuda(), ws, scale)
+        kvq.requant_demote(st, t + 1)
+        kvq.requant_demote(ws, t + 1)
+        torch.cuda.synchronize()
+        _twin_outputs(o_st, o_ws, f"static vs workspace, call {t}")
+        assert torch.equal(st.win_acc, ws.win_acc), f"window scores, call {t}"
+        for u in range(Hkv):
+            ro, _, _ = units[u].step(T + t, np_(qd[0, u * g:(u + 1) * g]), np_(kd[0, u]), np_(vd[0, u]), scale)
+            assert_attn_close(o_st[0, u * g:(u + 1) * g], ro, f"call {t} unit {u}")
+            assert_tiers_equal(gpu_tier_rows(st.tiers[0], u), oracle_tier_rows(units[u].high), f"K8V4 u{u}")
+            assert_tiers_equal(gpu_tier_rows(st.tiers[1], u), oracle_tier_rows(units[u].low), f"K4V2 u{u}")
+    assert kvq.device_status() == 0
 
 
 def test_static_scratch_rejects_a_cache_too_large():
