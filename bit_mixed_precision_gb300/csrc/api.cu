@@ -92,7 +92,9 @@ kvq_status prefill_attn_scores(const void* q, const void* k, const void* v, kvq_
     KVQ_REQUIRE(Hq % Hkv == 0, KVQ_EINVAL, "prefill_attn_scores: Hq %% Hkv != 0");
     KVQ_REQUIRE(D == 64 || D == 128, KVQ_EUNSUPPORTED, "prefill_attn_scores: head dim %d unsupported (64 or 128)", D);
     KVQ_REQUIRE(causal == 1, KVQ_EUNSUPPORTED, "prefill_attn_scores: only causal attention");
-    KVQ_REQUIRE(B * Hq <= 65535 * 1024 && T <= (1 << 30), KVQ_EINVAL, "prefill_attn_scores: too large");
+    KVQ_REQUIRE((long long)B * Hq <= 65535LL * 1024 && T <= (1 << 30), KVQ_EINVAL, "prefill_attn_scores: too large");
+    KVQ_REQUIRE((T + 127) / 128 <= 65535, KVQ_EUNSUPPORTED,
+                "prefill_attn_scores: T = %d needs more than 65535 tiles of 128 rows", T);
     KVQ_REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(o, 16) && aligned(lse, 4),
                 KVQ_EINVAL, "prefill_attn_scores: q/k/v/o must be 16-byte aligned");
     KVQ_REQUIRE(sm_scale > 0.0f, KVQ_EINVAL, "prefill_attn_scores: sm_scale must be positive");
@@ -109,7 +111,9 @@ kvq_status prefill_window_scores(const void* q, const void* k, kvq_dtype dt, int
     KVQ_REQUIRE(Hq % Hkv == 0, KVQ_EINVAL, "prefill_window_scores: Hq %% Hkv != 0");
     KVQ_REQUIRE(D == 64 || D == 128, KVQ_EUNSUPPORTED, "prefill_window_scores: head dim %d unsupported (64 or 128)", D);
     KVQ_REQUIRE(w_obs >= 1 && w_obs <= T, KVQ_EINVAL, "prefill_window_scores: w_obs must be in [1, T]");
-    KVQ_REQUIRE(B * Hq <= 65535 * 1024 && T <= (1 << 30), KVQ_EINVAL, "prefill_window_scores: too large");
+    KVQ_REQUIRE((long long)B * Hq <= 65535LL * 1024 && T <= (1 << 30), KVQ_EINVAL, "prefill_window_scores: too large");
+    KVQ_REQUIRE((T + 127) / 128 <= 65535, KVQ_EUNSUPPORTED,
+                "prefill_window_scores: T = %d needs more than 65535 tiles of 128 rows", T);
     KVQ_REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(lse, 4) && aligned(colscore, 4), KVQ_EINVAL,
                 "prefill_window_scores: q/k must be 16-byte aligned");
     KVQ_REQUIRE(sm_scale > 0.0f, KVQ_EINVAL, "prefill_window_scores: sm_scale must be positive");

@@ -155,9 +155,34 @@ def kv_quant_pack(x, bits, group, axis, gather_idx=None, n=None, out=None, strea
     return codes, scale, zero
 
 
+def _check_qk(q, k, v=None):
+    """q [B, Hq, T, D] and k (v) [B, Hkv, T, D] of one dtype, Hq a multiple of Hkv: the
+    kernels build their tensor maps from q's sizes, so a shorter k would be read past
+    its end."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k must be [B, H, T, D]")
+    B, Hq, T, D = q.shape
+    for x in (k, v):
+        if x is None:
+            continue
+        if x.dtype != q.dtype:
+            raise TypeError("q, k and v must share one dtype")
+        if x.shape[0] != B or x.shape[2:] != (T, D) or x.shape[1] != k.shape[1]:
+            raise ValueError(f"k/v shape {tuple(x.shape)} does not match q {tuple(q.shape)}")
+    if k.shape[1] == 0 or Hq % k.shape[1]:
+        raise ValueError("Hq must be a multiple of Hkv")
+
+
+def _check_lse(lse, q):
+    B, Hq, T, _ = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, T):
+        raise ValueError(f"lse must be float32 [{B}, {Hq}, {T}]")
+
+
 def prefill_attn_scores(q, k, v, sm_scale=None, colscore=True, out=None, stream=None):
     """Two-pass prefill: returns (o [B,Hq,T,D], lse [B,Hq,T], colscore [B,Hq,T] or None)."""
     _cuda(q, k, v)
+    _check_qk(q, k, v)
     B, Hq, T, D = q.shape
     Hkv = k.shape[1]
     if sm_scale is None:
@@ -168,6 +193,12 @@ def prefill_attn_scores(q, k, v, sm_scale=None, colscore=True, out=None, stream=
         cs = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device) if colscore else None
     else:
         o, lse, cs = out
+        _cuda(o, lse, cs)
+        if o.shape != q.shape or o.dtype != q.dtype:
+            raise ValueError("o must have q's shape and dtype")
+        _check_lse(lse, q)
+        if cs is not None:
+            _check_lse(cs, q)
     _check(lib().prefill_attn_scores(_ptr(q), _ptr(k), _ptr(v), _dt(q), B, Hq, Hkv, T, D,
                                      float(sm_scale), 1, _ptr(o), _ptr(lse), _ptr(cs), None, 0,
                                      _stream(stream)))
@@ -177,12 +208,16 @@ def prefill_attn_scores(q, k, v, sm_scale=None, colscore=True, out=None, stream=
 def prefill_window_scores(q, k, lse, w_obs, sm_scale=None, out=None, stream=None):
     """Column scores over the last w_obs queries (lse from prefill_attn_scores): [B, Hq, T]."""
     _cuda(q, k, lse)
+    _check_qk(q, k)
+    _check_lse(lse, q)
     B, Hq, T, D = q.shape
     Hkv = k.shape[1]
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    _cuda(out)
+    _check_lse(out, q)
     _check(lib().prefill_window_scores(_ptr(q), _ptr(k), _dt(q), B, Hq, Hkv, T, D, float(sm_scale), _ptr(lse),
                                        int(w_obs), _ptr(out), _stream(stream)))
     return out

@@ -273,8 +273,11 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* c);
  *   A cache whose kvq_decode_workspace_bytes() exceeds
  *   KVQ_STATIC_SCRATCH_BYTES is rejected with KVQ_EWORKSPACE.
  *   The first call made with a given device current looks up the array's
- *   device address on that device; make that first call before any stream
- *   capture.
+ *   device address on that device and keeps it for later calls; make that
+ *   first call before any stream capture.  The address belongs to the
+ *   device's context of that moment: after cudaDeviceReset (or any other
+ *   teardown of the primary context) it is stale, so a process that resets
+ *   a device must not call decode_attn_qkv_static on it again.
  *   All calls share the one array (DiffKV and MiKV keep the step's logits
  *   there; MiniKV needs none): two DiffKV/MiKV calls whose work overlaps on
  *   the GPU, on any streams, race and give wrong results. */
