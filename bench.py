@@ -5,15 +5,20 @@ prefill (output + column scores), the prefill-end cache build (selection and
 INT2 packing for MiniKV, the tier split for DiffKV / MiKV), then every decode
 step of the workload (attention over the packed cache + the policy tail).
 
-Default workload (`llama-layer`): the LLaMA2-7B-shaped layer -- batch 1, 32
-heads, head dim 128, prompt 4096, fp16, 2% outlier key channels x10, INT2
-groups of 32, 128-token residual, 25% heavy hitters + 25% window, 128 decode
-steps.  Other workloads (not the default line): `tiny` (batch 1, 2 heads,
-head dim 64, prompt 256, 16 steps), `pyramid-layer16` (layer 16 of the 32-layer
-pyramid sweep: batch 16, 32 heads, prompt 16384, heavy hitters 25.2%, window
-25%, 256 steps), `diffkv` (GQA 40/8, batch 32, prompt 8192, K8V4/K4V2/prune with
-Dirichlet(2,5,3) fractions, 64-token window, 512 steps), `mikv` (GQA 32/8, batch
-64, prompt 32768, bf16, INT4 top 20% / INT2 rest, 128-token residual, 1024 steps).
+Default workload (`pyramid`): the 32-layer MiniKV pyramid sweep -- 32 layers of
+32 heads x head dim 128, batch 16, prompt 16384, keys with LogNormal(0, 0.5)
+per-channel std, heavy-hitter budget falling linearly from 40% (layer 0) to
+10% (layer 31) plus a 25% recent window, INT2 with fp16 scale / zero in groups
+of 32, 256 decode steps of every layer (one CUDA graph of the 32 layers' decode
+launches per step).  It is the largest workload that fits one GPU (12.9 GB of
+packed cache read per decode step).  Other workloads (`--workload`):
+`llama-layer` (the LLaMA2-7B-shaped layer: batch 1, 32 heads, prompt 4096,
+2% outlier key channels x10, 128-token residual, 25% + 25% budget, 128
+steps), `tiny` (batch 1, 2 heads, head dim 64, prompt 256, 16 steps),
+`pyramid-layer16` (layer 16 of the sweep alone), `diffkv` (GQA 40/8, batch 32,
+prompt 8192, K8V4/K4V2/prune with Dirichlet(2,5,3) fractions, 64-token
+window, 512 steps), `mikv` (GQA 32/8, batch 64, prompt 32768, bf16, INT4 top
+20% / INT2 rest, 128-token residual, 1024 steps).
 
 Printed value: decoded tokens per second of the whole step (prefill
 included), inputs resident in HBM.  The line also carries decode-only
@@ -22,7 +27,7 @@ kernel, the end-to-end number through host buffers, the CPU oracle baseline
 and the SM clocks seen during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload llama-layer|tiny|pyramid-layer16|pyramid|diffkv|mikv]
+                  [--workload pyramid|llama-layer|tiny|pyramid-layer16|diffkv|mikv]
                   [--batch B] [--decode-steps S]     (smaller cases, for profiling)
 """
 from __future__ import annotations
@@ -91,16 +96,17 @@ def sources_sha256(kernel):
     return h.hexdigest()
 
 
-def _traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json) when
-    it was taken on this workload from the kernel's current sources; otherwise None."""
+def _traffic(kernel, workload, batch):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json) when it
+    was taken on this workload from the kernel's current sources, scaled from the batch it
+    was captured at to `batch` (the bytes of every unit are independent); otherwise None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel)
-    if not d or d.get("workload") != workload or d.get("source_sha256") != sources_sha256(kernel):
+    d = json.load(open(p)).get(kernel, {}).get(workload)
+    if not d or d.get("source_sha256") != sources_sha256(kernel):
         return None
-    return d.get("dram_bytes_per_launch")
+    return d["dram_bytes_per_launch"] * batch / d.get("batch", batch)
 
 
 def job_ms(step_ms, world, device):
@@ -331,9 +337,10 @@ class Sweep:
         # decode inputs of one step (the same for every layer), refreshed before each step
         self.dec = [inputs.make_decode_step(B, H, H, D, t, seed=seed, device=dev, key_std=kstd)
                     for t in range(steps)]
-        self.qd = torch.empty_like(self.dec[0][0])
-        self.kd = torch.empty_like(self.dec[0][1])
-        self.vd = torch.empty_like(self.dec[0][2])
+        # zeros until the first step is loaded (the capture's warm-up call decodes them)
+        self.qd = torch.zeros_like(self.dec[0][0])
+        self.kd = torch.zeros_like(self.dec[0][1])
+        self.vd = torch.zeros_like(self.dec[0][2])
         self.o_dec = torch.empty((L, B, H, D), dtype=torch.float16, device=dev)
         self.graph = None
         self.prefill_flops = 3 * D * T * T * B * H * L
@@ -361,11 +368,16 @@ class Sweep:
         with torch.cuda.graph(self.graph, stream=s):
             self._decode_layers(s)
 
-    def decode_step(self, t, s):
-        qd, kd, vd = self.dec[t]
+    def load_step(self, t, src=None):
+        """This step's decode inputs into the graph's input buffers (from `src`, host
+        buffers, when given)."""
+        qd, kd, vd = src if src is not None else self.dec[t]
         self.qd.copy_(qd, non_blocking=True)
         self.kd.copy_(kd, non_blocking=True)
         self.vd.copy_(vd, non_blocking=True)
+
+    def decode_step(self, t, s):
+        self.load_step(t)
         self.graph.replay()
 
     def decode_bytes(self):
@@ -382,6 +394,52 @@ class Sweep:
                 tot += (packed * per_tok + res * 2 * D * 2) * B * H + 4 * B * H * D * 2
         return tot / steps
 
+    def e2e(self, s, warmup, reps):
+        """The whole step through the public calls from pinned host buffers: H2D of the prompt
+        Q/K/V and of every step's decode inputs, D2H of every layer's decode output of every
+        step, all inside the timed region."""
+        steps, L = self.wl["steps"], len(self.layers)
+        pin = lambda t: t.cpu().pin_memory()
+        hq, hk, hv = pin(self.q), pin(self.k), pin(self.v)
+        hdec = [tuple(pin(x) for x in d) for d in self.dec]
+        ho = torch.empty((steps,) + tuple(self.o_dec.shape), dtype=self.o_dec.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+        h2d += sum(x.numel() * x.element_size() for d in hdec for x in d)
+        d2h = ho.numel() * ho.element_size()
+        times = []
+        for it in range(warmup + reps):
+            with torch.cuda.stream(s):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                self.q.copy_(hq, non_blocking=True)
+                self.k.copy_(hk, non_blocking=True)
+                self.v.copy_(hv, non_blocking=True)
+                self.prefill_build(s)
+                for t in range(steps):
+                    self.load_step(t, hdec[t])
+                    self.graph.replay()
+                    ho[t].copy_(self.o_dec, non_blocking=True)
+                b.record(s)
+            torch.cuda.synchronize()
+            if it >= warmup:
+                times.append(a.elapsed_time(b))
+        ms = statistics.mean(times)
+        return {"value": self.wl["B"] * steps / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps_timed": reps,
+                "note": f"{L} layers' decode outputs of each of the {steps} decode steps copied back"}
+
+
+def _l2_note(wl):
+    if wl.get("sweep"):
+        return "not flushed: the per-step working set (every layer's cache, about 13 GB) is larger than L2"
+    return "flushed (256 MB write) before the prefill and before every decode step; flush time excluded"
+
+
+def _config(args, wl, world):
+    """The config object of the JSON line (identical for both arms)."""
+    return {"workload": args.workload, **{k: v for k, v in wl.items() if v is not None},
+            "l2": _l2_note(wl), "parallelism": f"replicas x{world}"}
+
 
 def run_sweep(args, wl, rank, world):
     """Pyramid sweep: each step prefills and builds all layers, then decodes every layer for
@@ -391,18 +449,22 @@ def run_sweep(args, wl, rank, world):
     torch.cuda.set_device(dev)
     sw = Sweep(wl, dev, seed=rank)
     s = torch.cuda.Stream(device=dev)
-    steps = wl["steps"]
+    steps, L = wl["steps"], wl["n_layers"]
     hbm_peak, tf_peak, peak_src = _peaks()
 
     def one_step():
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        """One whole step; event pairs around the prefill + build and around each step's
+        graph replay (the decode launches alone, not the input copies)."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * steps)]
         with torch.cuda.stream(s):
             ev[0].record(s)
             sw.prefill_build(s)
             ev[1].record(s)
             for t in range(steps):
-                sw.decode_step(t, s)
-            ev[2].record(s)
+                sw.load_step(t)
+                ev[2 + 2 * t].record(s)
+                sw.graph.replay()
+                ev[3 + 2 * t].record(s)
         return ev
 
     with torch.cuda.stream(s):
@@ -418,20 +480,24 @@ def run_sweep(args, wl, rank, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
     pre_ms = dec_ms = 0.0
     with Clocks(dev.index) as clk:
+        t_start.record(s)
         for _ in range(args.steps):
             ev = one_step()
             torch.cuda.synchronize()
             pre_ms += ev[0].elapsed_time(ev[1])
-            dec_ms += ev[1].elapsed_time(ev[2])
+            dec_ms += sum(ev[2 + 2 * t].elapsed_time(ev[3 + 2 * t]) for t in range(steps))
+        t_end.record(s)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     st = sw.kvq.device_status(s)
     if st:
         raise RuntimeError(f"device status {st} after the timed steps")
-    step_ms = (pre_ms + dec_ms) / args.steps
+    step_ms = t_start.elapsed_time(t_end) / args.steps
     ms_max = job_ms(step_ms, world, dev)
     B = wl["B"]
     value = job_value(world, B * steps, ms_max)
@@ -439,35 +505,41 @@ def run_sweep(args, wl, rank, world):
     dbytes = sw.decode_bytes()
     achieved = dbytes / (dec_step_ms / 1e3) / 1e9
     pre_tf = sw.prefill_flops / (pre_ms / args.steps / 1e3) / 1e12      # includes select + build
+    e2e = sw.e2e(s, warmup=1, reps=min(2, args.steps))
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 in, f32 accumulate, packed INT2 cache",
         "data": "synthetic (seeded Gaussian Q/V, keys with LogNormal(0, 0.5) per-channel std; one prompt "
                 "shared by the layers)",
-        "config": {"workload": args.workload, **{k: v for k, v in wl.items() if v is not None},
-                   "l2": "not flushed: the per-step working set (every layer's cache, about 13 GB) is "
-                         "larger than L2", "parallelism": f"replicas x{world}"},
+        "config": _config(args, wl, world),
         "decode": {"tokens_per_s": B * steps / (dec_ms / args.steps / 1e3),
-                   "us_per_layer_step": dec_step_ms * 1e3 / wl["n_layers"],
-                   "bytes_per_step_all_layers": dbytes, "packed_kv_gbs": achieved,
+                   "us_per_layer_step": dec_step_ms * 1e3 / L,
+                   "bytes_per_layer_step": dbytes / L, "packed_kv_gbs": achieved,
                    "frac_hbm": achieved / hbm_peak, "launch": "one CUDA graph of every layer per step"},
         "prefill": {"ms_all_layers": pre_ms / args.steps, "tflops_incl_select_build": pre_tf,
                     "frac_tensor": pre_tf / tf_peak},
-        "segments_ms_per_step": {"prefill_build": pre_ms / args.steps, "decode": dec_ms / args.steps},
+        "segments_ms_per_step": {"prefill_build": pre_ms / args.steps, "decode": dec_ms / args.steps,
+                                 "decode_input_copies_and_gaps": step_ms - (pre_ms + dec_ms) / args.steps},
         "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
-                     "peak_source": f"{peak_src} hbm_gbs (of measured)"},
-        "e2e": None,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": _traffic("decode_kernel", args.workload, B),
+                     "per": "launch (one layer's decode, averaged over the 32 layers)",
+                     "peak_source": f"{peak_src} hbm_gbs (of measured)" if peak_src == "measured"
+                                    else "fallback 6800 GB/s"},
+        "roofline_prefill": {"kernel": "prefill_pass1_kernel + prefill_pass2_kernel (+ select, build)",
+                             "bound": "tensor", "achieved": pre_tf, "peak": tf_peak, "unit": "TFLOP/s",
+                             "frac": pre_tf / tf_peak, "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "e2e": e2e,
         "gpu_launches": sw.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:
-        cb = cpu_baseline(dict(wl, layer=wl["n_layers"] // 2), args)
+        cb = cpu_baseline(dict(wl, layer=L // 2), args)
         # one layer's oracle cost (layer 16's budget) for each of the layers
-        cb["value"] /= wl["n_layers"]
-        cb["seconds_per_step_estimated"] *= wl["n_layers"]
-        cb["sample"] += f", times {wl['n_layers']} layers"
+        cb["value"] /= L
+        cb["seconds_per_step_estimated"] *= L
+        cb["sample"] += f", times {L} layers"
         out["cpu_baseline"] = cb
         print(json.dumps(out), flush=True)
 
@@ -563,9 +635,7 @@ def run_ours(args, wl, rank, world):
         "scaling": "weak", "vs_baseline": None,
         "dtype": f"{wl['dtype']} in, f32 accumulate, packed {'INT2' if wl['policy'] == 'minikv' else ('K8V4/K4V2' if wl['policy'] == 'diffkv' else 'INT4/INT2')} cache",
         "data": "synthetic (seeded Gaussian Q/K/V, outlier key channels)",
-        "config": {"workload": args.workload, **{k: v for k, v in wl.items() if v is not None},
-                   "l2": "flushed (256 MB write) before the prefill and before every decode step; "
-                         "flush time excluded", "parallelism": f"replicas x{world}"},
+        "config": _config(args, wl, world),
         "decode": {"tokens_per_s": dec_tokens / (seg['decode'] / args.steps / 1e3),
                    "us_per_launch": dec_ms_per_launch * 1e3, "bytes_per_launch": dec_bytes,
                    "packed_kv_gbs": achieved, "frac_hbm": achieved / hbm_peak},
@@ -576,7 +646,8 @@ def run_ours(args, wl, rank, world):
         "segments_ms_per_step": {k2: v2 / args.steps for k2, v2 in seg.items()},
         "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": _traffic("decode_kernel", args.workload),
+                     "frac": achieved / hbm_peak,
+                     "traffic": _traffic("decode_kernel", args.workload, wl["B"]),
                      "peak_source": f"{peak_src} hbm_gbs (of measured)" if peak_src == "measured"
                                     else "fallback 6800 GB/s"},
         "roofline_prefill": {"kernel": "prefill_pass1_kernel + prefill_pass2_kernel", "bound": "tensor",
@@ -684,31 +755,59 @@ def oracle_step_seconds(wl, seed=0, rows=256, dec_steps=2):
 def cpu_baseline(wl, args):
     torch.set_num_threads(os.cpu_count() or 1)
     secs, sample = oracle_step_seconds(wl)
-    return {"value": wl["B"] * wl["steps"] / secs, "unit": UNIT, "cores": torch.get_num_threads(),
+    return {"value": wl["B"] * wl["steps"] / secs, "unit": UNIT, "cores": _oracle_cores(),
             "kind": "oracle", "sample": sample, "seconds_per_step_estimated": secs}
 
 
+def _oracle_cores():
+    """Threads the oracle's numpy matrix products may use (its Python loops use one)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
 def run_reference(args, wl, rank, world):
+    """The oracle arm: each step times the CPU oracle on a bounded sample of the workload's
+    step (see oracle_step_seconds) on the host cores.  ms_per_step is the time of what ran;
+    value is the full step's throughput estimated from it (the scale factor is printed)."""
     if rank != 0:
         return
     torch.set_num_threads(os.cpu_count() or 1)
+    n_layers = wl["n_layers"] if wl.get("sweep") else 1
+    wl_s = dict(wl, layer=wl["n_layers"] // 2) if wl.get("sweep") else wl
+
+    def sample():
+        t0 = time.perf_counter()
+        est, smp = oracle_step_seconds(wl_s, rows=64, dec_steps=1)
+        return time.perf_counter() - t0, est * n_layers, smp
+
     for _ in range(args.warmup):
-        oracle_step_seconds(wl, rows=64, dec_steps=1)
-    est, t0, sample = [], time.perf_counter(), ""
+        sample()
+    ran, est, smp, t0 = [], [], "", time.perf_counter()
     for _ in range(args.steps):
-        sec, sample = oracle_step_seconds(wl, rows=64, dec_steps=1)
-        est.append(sec)
+        r, e, smp = sample()
+        ran.append(r)
+        est.append(e)
+    if n_layers > 1:
+        smp += f", times {n_layers} layers (layer {wl['n_layers'] // 2}'s budget for each)"
     secs = statistics.mean(est)
     v = wl["B"] * wl["steps"] / secs
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(ran) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 attention, f32 quantiser",
         "data": "synthetic (seeded Gaussian Q/K/V, outlier key channels)",
-        "config": {"workload": args.workload, **{k: v2 for k, v2 in wl.items() if v2 is not None}},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
-                         "sample": sample},
+        "config": _config(args, wl, world),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": _oracle_cores(), "kind": "oracle",
+                         "sample": smp},
+        "scale_factor": secs / statistics.mean(ran),
+        "seconds_per_full_step_estimated": secs,
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": time.perf_counter() - t0}), flush=True)
 
@@ -719,7 +818,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama-layer", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="pyramid", choices=sorted(WORKLOADS))
     # smaller cases of a workload's kernels (profiling): the batch and the decode steps per
     # timed step; the JSON line's config records them
     ap.add_argument("--batch", type=int, default=None)
