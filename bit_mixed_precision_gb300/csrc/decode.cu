@@ -182,7 +182,11 @@ struct Smem {
     float wo[Cfg<NG>::W][NG][D];
     // logits of the warp's current group (CUDA-core per-token path: single heads only)
     float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 32 : 1];
-    uint4 qa[8][32];                     // per-token keys: the query's A fragments, [k-step][lane]
+    uint4 qa[NG >= 2 ? 8 : 1][32];       // per-token keys (GQA groups): the query's A fragments, [k-step][lane]
+    // single heads, MiniKV format: per warp the probabilities times each value group's
+    // scale (fp16, [group][token]) and a block of zeros that lanes without a column read
+    uint16_t ps[NG == 1 ? Cfg<NG>::W : 1][4][32];
+    uint32_t zero[NG == 1 ? 64 : 1];
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
     float lsum[NG];
@@ -1337,6 +1341,248 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
     flush_mma<NG, 128>(acc, sm);
 }
 
+// ---- MiniKV format with one query head per KV head (per-channel INT2 keys,
+// one scale row per 32 tokens; per-token INT2 values; D = 128, G = 32)
+//
+// A 2-bit code at bits 2i, 2i + 1 of a 16-bit half whose other bits are zero
+// is the fp16 subnormal c * 4^i * 2^-24, exactly.  One AND with a mask thus
+// turns two codes (one per half of a register) into an MMA operand, with no
+// shift and no conversion; the factor 4^i * 2^-24 is shared by a whole row of
+// the MMA and is taken out afterwards (keys: per token, in the logit
+// epilogue; values: per channel, once at the end).  Products of fp16 numbers
+// are exact in the float32 accumulators, subnormal or not.
+//
+// Keys: S = K Q' with the warp's 32 tokens as the M rows (two MMAs of 16
+// rows), the channels in eight k-steps of 16, and Q' = q * (channel scale)
+// split into fp16 hi / lo columns (N = 8: columns 0 and 1, the rest zero).
+// Lane (g, t) takes byte g & 3 of the words of word row g >> 2 (tokens
+// 4g .. 4g + 3 of the warp, at bits 2i of that byte) for channel pairs; one
+// byte permute per pair of channels and four masks give the four tokens:
+// rows g / g + 8 of MMA 0 are tokens 4g / 4g + 1, of MMA 1 tokens 4g + 2 /
+// 4g + 3.  Lane (g, 0) ends with the logits of tokens 4g .. 4g + 3.
+// Values: O^T = V^T P' with channels as M rows (eight M tiles), the 16
+// tokens of a k-step as K, and P' = p * (the token's scale of each
+// 32-channel group) as four fp16 columns, one per group.  Tile (w', P) holds
+// in row g channel 16 (w' + 4 (g >> 2)) + 4 (g & 3) + 2P and in row g + 8 the
+// next channel; lane (g, g >> 2) ends with both rows, in the column of their
+// group.  The zero points add sum_j p_j z_j per group.
+
+constexpr uint32_t kM0 = 0x00030003u, kM1 = 0x000C000Cu, kM2 = 0x00300030u, kM3 = 0x00C000C0u;
+
+struct Mk1Acc {
+    float m, l;              // running reference max (warp-uniform), this lane's share of the sum
+    float o[4][2][4];        // P.V accumulators: [word pair w'][row pair P][fragment]
+    float zs[4];             // sum of p * zero of this lane's tokens, per value group
+};
+
+template <int NG>
+__device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, size_t unit, int r, int i0,
+                             int i1, int n_local, uint8_t* stage_base, bool& ok) {
+    static_assert(NG == 1, "one query head per KV head");
+    constexpr int TPW = Cfg<NG>::TPW;
+    static_assert(TPW == 32, "one key scale row per warp and item");
+    const UnitState& us = sm.us;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // this warp's query fragments ([piece][k-step][t][reg], 512 B), probabilities (32 floats)
+    // and probability x value scale ([group][token] fp16)
+    uint32_t* qf = reinterpret_cast<uint32_t*>(&qf_rows<NG>(a, sm, warp)[0][0]);
+    float* pw = &sm.lg[warp][0][0];
+    uint16_t* psw = &sm.ps[warp][0][0];
+    // B-fragment sources: lanes g = 0 / 1 read the hi / lo query rows, g = 0..3 the value
+    // groups; the others read zeros (no per-step select)
+    const uint2* qfb = g < 2 ? reinterpret_cast<const uint2*>(qf) + g * 32 + t
+                             : reinterpret_cast<const uint2*>(sm.zero) + t;
+    const uint32_t* psb = g < 4 ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : sm.zero + t;
+    const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);   // channels 4 lane .. + 3
+    const uint32_t bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
+    Mk1Acc acc;
+    acc.m = kNegInf;
+    acc.l = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc.zs[i] = 0.0f;
+#pragma unroll
+        for (int P = 0; P < 2; ++P)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) acc.o[i][P][f] = 0.0f;
+    }
+    for (int i = i0; i < i1; ++i) {
+        ok = wait_item(a, sm, i, ok);
+        const int j0 = (r + i * a.cluster - us.base[tier]) * kSub;
+        const int n = min(kSub, us.cnt[tier] - j0);
+        const int tl = warp * TPW;
+        if (ok && tl < n) {
+            const View v = tier_view_c<2, KVQ_AXIS_CHANNEL, 2>((n + 31) & ~31, item_buf(a, stage_base, i));
+            const int nt = min(TPW, n - tl);
+            // -- Q' = q * scale of this scale row, as hi / lo fp16 fragments, and sum_c q z
+            float bias;
+            {
+                const uint2 s2 = *reinterpret_cast<const uint2*>(v.ks + (size_t)(tl >> 5) * 128 + 4 * lane);
+                const uint2 z2 = *reinterpret_cast<const uint2*>(v.kz + (size_t)(tl >> 5) * 128 + 4 * lane);
+                const float x0 = q4.x * h2lo(s2.x), x1 = q4.y * h2hi(s2.x);
+                const float x2 = q4.z * h2lo(s2.y), x3 = q4.w * h2hi(s2.y);
+                const uint32_t hi01 = pack_h2(x0, x1), hi23 = pack_h2(x2, x3);
+                const uint32_t lo01 = pack_h2(x0 - h2lo(hi01), x1 - h2hi(hi01));
+                const uint32_t lo23 = pack_h2(x2 - h2lo(hi23), x3 - h2hi(hi23));
+                bias = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
+                // channel c = 16 s + 8 half + 2 tt + e sits in register half of lane tt, k-step s
+                const int s_ = lane >> 2, half = (lane & 3) >> 1, tt = 2 * (lane & 1);
+                qf[(s_ * 4 + tt) * 2 + half] = hi01;
+                qf[(s_ * 4 + tt + 1) * 2 + half] = hi23;
+                qf[64 + (s_ * 4 + tt) * 2 + half] = lo01;
+                qf[64 + (s_ * 4 + tt + 1) * 2 + half] = lo23;
+                bias = warp_sum(bias);
+            }
+            __syncwarp();
+            // -- logits: two MMAs (tokens 4g + {0, 1} and 4g + {2, 3}), each over two
+            // accumulator chains of four k-steps
+            float R[2][2][4];
+#pragma unroll
+            for (int P = 0; P < 2; ++P)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) R[P][e][f] = 0.0f;
+            {
+                const uint32_t* rowp = v.kc + (size_t)((tl >> 4) + (g >> 2)) * 128;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint2 w0 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t);
+                    const uint2 w1 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t + 8);
+                    const uint2 b = qfb[s * 4];
+                    const uint32_t y0 = __byte_perm(w0.x, w0.y, bsel), y1 = __byte_perm(w1.x, w1.y, bsel);
+                    const uint32_t a0[4] = {y0 & kM0, y0 & kM1, y1 & kM0, y1 & kM1};
+                    const uint32_t a1[4] = {y0 & kM2, y0 & kM3, y1 & kM2, y1 & kM3};
+                    mma16816(R[0][s & 1], a0, b.x, b.y);
+                    mma16816(R[1][s & 1], a1, b.x, b.y);
+                }
+            }
+            // -- logits of tokens 4g + j (lanes t == 0): code factor 4^j * 2^-24 out, bias in
+            float lg[4];
+            lg[0] = fmaf((R[0][0][0] + R[0][1][0]) + (R[0][0][1] + R[0][1][1]), 16777216.0f, bias);  // 2^24
+            lg[1] = fmaf((R[0][0][2] + R[0][1][2]) + (R[0][0][3] + R[0][1][3]), 4194304.0f, bias);   // 2^22
+            lg[2] = fmaf((R[1][0][0] + R[1][1][0]) + (R[1][0][1] + R[1][1][1]), 1048576.0f, bias);   // 2^20
+            lg[3] = fmaf((R[1][0][2] + R[1][1][2]) + (R[1][0][3] + R[1][1][3]), 262144.0f, bias);    // 2^18
+            bool valid[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) valid[j] = t == 0 && 4 * g + j < nt;
+            float mx = fmaxf(fmaxf(valid[0] ? lg[0] : kNegInf, valid[1] ? lg[1] : kNegInf),
+                             fmaxf(valid[2] ? lg[2] : kNegInf, valid[3] ? lg[3] : kNegInf));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            mx = __shfl_sync(0xffffffffu, mx, 0);
+            // the reference moves only when the max rises by more than 2^8 (exact: the
+            // final division uses the same reference)
+            if (acc.m == kNegInf ? mx != kNegInf : mx > acc.m + 8.0f) {
+                const float corr = acc.m == kNegInf ? 0.0f : ex2_approx(acc.m - mx);
+                acc.m = mx;
+                acc.l *= corr;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    acc.zs[x] *= corr;
+#pragma unroll
+                    for (int P = 0; P < 2; ++P)
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) acc.o[x][P][f] *= corr;
+                }
+            }
+            {
+                float4 p;
+                p.x = valid[0] ? ex2_approx(lg[0] - acc.m) : 0.0f;
+                p.y = valid[1] ? ex2_approx(lg[1] - acc.m) : 0.0f;
+                p.z = valid[2] ? ex2_approx(lg[2] - acc.m) : 0.0f;
+                p.w = valid[3] ? ex2_approx(lg[3] - acc.m) : 0.0f;
+                acc.l += (p.x + p.y) + (p.z + p.w);
+                if (t == 0) *reinterpret_cast<float4*>(pw + 4 * g) = p;
+            }
+            __syncwarp();
+            // -- lane = token: p times each group's value scale into [group][token], and the
+            // zero points (stale slots past nt read as zero scale and zero point)
+            {
+                const float p = pw[lane];
+                const bool ok_t = lane < nt;
+                uint2 s2 = *reinterpret_cast<const uint2*>(v.vs + (size_t)(tl + lane) * 4);
+                uint2 z2 = *reinterpret_cast<const uint2*>(v.vz + (size_t)(tl + lane) * 4);
+                s2.x = ok_t ? s2.x : 0u;
+                s2.y = ok_t ? s2.y : 0u;
+                z2.x = ok_t ? z2.x : 0u;
+                z2.y = ok_t ? z2.y : 0u;
+                const uint32_t ps01 = pack_h2(p * h2lo(s2.x), p * h2hi(s2.x));
+                const uint32_t ps23 = pack_h2(p * h2lo(s2.y), p * h2hi(s2.y));
+                psw[0 * 32 + lane] = (uint16_t)(ps01 & 0xffffu);
+                psw[1 * 32 + lane] = (uint16_t)(ps01 >> 16);
+                psw[2 * 32 + lane] = (uint16_t)(ps23 & 0xffffu);
+                psw[3 * 32 + lane] = (uint16_t)(ps23 >> 16);
+                acc.zs[0] = fmaf(p, h2lo(z2.x), acc.zs[0]);
+                acc.zs[1] = fmaf(p, h2hi(z2.x), acc.zs[1]);
+                acc.zs[2] = fmaf(p, h2lo(z2.y), acc.zs[2]);
+                acc.zs[3] = fmaf(p, h2hi(z2.y), acc.zs[3]);
+            }
+            __syncwarp();
+            // -- P.V over two k-steps of 16 tokens: B = (p s) of tokens 16 ks + 2t, + 1
+            // (b0) and + 8, + 9 (b1) in column g (group g; zeros for g >= 4)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = 16 * ks + 2 * t;
+                const uint32_t b0 = psb[8 * ks], b1 = psb[8 * ks + 4];
+                const uint32_t* vrow = v.vc + (size_t)(tl + k0) * 8 + 4 * (g >> 2);
+                const uint4 xa = *reinterpret_cast<const uint4*>(vrow);
+                const uint4 xb = *reinterpret_cast<const uint4*>(vrow + 8);
+                const uint4 xc = *reinterpret_cast<const uint4*>(vrow + 64);
+                const uint4 xd = *reinterpret_cast<const uint4*>(vrow + 72);
+                const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
+                const uint32_t wc[4] = {xc.x, xc.y, xc.z, xc.w}, wd[4] = {xd.x, xd.y, xd.z, xd.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t ya = __byte_perm(wa[w], wb[w], bsel), yc = __byte_perm(wc[w], wd[w], bsel);
+                    const uint32_t a0[4] = {ya & kM0, ya & kM1, yc & kM0, yc & kM1};
+                    const uint32_t a1[4] = {ya & kM2, ya & kM3, yc & kM2, yc & kM3};
+                    mma16816(acc.o[w][0], a0, b0, b1);
+                    mma16816(acc.o[w][1], a1, b0, b1);
+                }
+            }
+            __syncwarp();                                        // pw / ps / qf are rewritten by the next item
+        }
+        release_item(a, sm, unit, r, i, n_local, stage_base);
+    }
+    // ---- merge the warp's state into its shared-memory state
+    acc.l = warp_sum(acc.l);
+#pragma unroll
+    for (int x = 0; x < 4; ++x) acc.zs[x] = warp_sum(acc.zs[x]);
+    float fo = 0.0f, fn = 0.0f;
+    {
+        const float mo = sm.wm[warp][0];
+        const float M = fmaxf(mo, acc.m);
+        fo = mo == kNegInf ? 0.0f : ex2_approx(mo - M);
+        fn = acc.m == kNegInf ? 0.0f : ex2_approx(acc.m - M);
+        __syncwarp();
+        if (lane == 0) {
+            sm.wl[warp][0] = sm.wl[warp][0] * fo + acc.l * fn;
+            sm.wm[warp][0] = M;
+        }
+    }
+    if (t == (g >> 2)) {
+        // lanes (g, g >> 2): rows g and g + 8 of every tile, column of their group
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+            for (int P = 0; P < 2; ++P) {
+                const int c = 16 * (w + 4 * (g >> 2)) + 4 * (g & 3) + 2 * P;
+                constexpr int slot_of_w[4] = {0, 0, 1, 1};
+                const int slot = slot_of_w[w];                       // the group is 2 (g >> 2) + slot
+                const float zg = (g >> 2) ? acc.zs[2 + slot] : acc.zs[slot];
+                const float lo_row = (P ? 1048576.0f : 16777216.0f);  // 2^(24 - 4P)
+                const float o0 = fmaf(acc.o[w][P][slot], lo_row, zg);
+                const float o1 = fmaf(acc.o[w][P][2 + slot], 0.25f * lo_row, zg);
+                float* dst = &sm.wo[warp][0][c];
+                dst[0] = dst[0] * fo + o0 * fn;
+                dst[1] = dst[1] * fo + o1 * fn;
+            }
+    }
+    __syncwarp();
+}
+
 // FAM selects the formats compiled into one kernel: bit 0 keys per channel
 // (MiniKV), bit 1 keys per token (DiffKV, MiKV tiers).
 template <int NG, int D, int FAM>
@@ -1345,7 +1591,9 @@ __device__ void dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_
     const TierArgs& ta = a.tier[t];
     const int kb = ta.k_bits, vb = ta.v_bits, ax = ta.k_axis;
     if ((FAM & 1) && ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) {
-        if constexpr (D == 128 && NG <= 4)
+        if constexpr (D == 128 && NG == 1)
+            run_tier_mk1<NG>(a, sm, t, unit, r, i0, i1, n_local, stage, ok);
+        else if constexpr (D == 128 && NG <= 4)
             run_tier_mma<2, KVQ_AXIS_CHANNEL, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok);
         else
             run_tier<2, KVQ_AXIS_CHANNEL, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok);
@@ -1564,6 +1812,7 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         sm.wl[x / NG][x % NG] = 0.0f;
     }
     for (int x = threadIdx.x; x < W * NG * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
+    for (int x = threadIdx.x; x < (int)(sizeof(sm.zero) / 4); x += blockDim.x) sm.zero[x] = 0u;
     __syncthreads();
 
     const UnitState& us = sm.us;
