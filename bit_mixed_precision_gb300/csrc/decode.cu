@@ -181,12 +181,12 @@ struct Smem {
     float wl[Cfg<NG>::W][NG];
     float wo[Cfg<NG>::W][NG][D];
     // logits of the warp's current group (CUDA-core per-token path: single heads only)
-    float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 32 : 1];
-    uint4 qa[NG >= 2 ? 8 : 1][32];       // per-token keys (GQA groups): the query's A fragments, [k-step][lane]
-    // single heads, MiniKV format: per warp the probabilities times each value group's
-    // scale (fp16, [group][token]) and a block of zeros that lanes without a column read
-    uint16_t ps[NG == 1 ? Cfg<NG>::W : 1][4][32];
-    uint32_t zero[NG == 1 ? 64 : 1];
+    // (single heads, MiniKV format: the warp's probabilities, 32 floats, then in the same
+    // bytes the probabilities times each value group's scale, fp16 [group][token])
+    float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 64 : 1];
+    // per-token keys (GQA groups): the query's A fragments, [k-step][lane]; single heads:
+    // zeros, read by the lanes that hold no column of a MiniKV-format B fragment
+    uint4 qa[NG >= 2 ? 8 : 1][32];
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
     float lsum[NG];
@@ -1387,12 +1387,13 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
     // and probability x value scale ([group][token] fp16)
     uint32_t* qf = reinterpret_cast<uint32_t*>(&qf_rows<NG>(a, sm, warp)[0][0]);
     float* pw = &sm.lg[warp][0][0];
-    uint16_t* psw = &sm.ps[warp][0][0];
+    uint16_t* psw = reinterpret_cast<uint16_t*>(pw);            // same bytes, after the probabilities are read
+    const uint32_t* zero = reinterpret_cast<const uint32_t*>(&sm.qa[0][0]);
     // B-fragment sources: lanes g = 0 / 1 read the hi / lo query rows, g = 0..3 the value
     // groups; the others read zeros (no per-step select)
     const uint2* qfb = g < 2 ? reinterpret_cast<const uint2*>(qf) + g * 32 + t
-                             : reinterpret_cast<const uint2*>(sm.zero) + t;
-    const uint32_t* psb = g < 4 ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : sm.zero + t;
+                             : reinterpret_cast<const uint2*>(zero) + t;
+    const uint32_t* psb = g < 4 ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : zero + t;
     const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);   // channels 4 lane .. + 3
     const uint32_t bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
     Mk1Acc acc;
@@ -1501,6 +1502,7 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
             // zero points (stale slots past nt read as zero scale and zero point)
             {
                 const float p = pw[lane];
+                __syncwarp();                                    // every lane has its p: ps overwrites pw
                 const bool ok_t = lane < nt;
                 uint2 s2 = *reinterpret_cast<const uint2*>(v.vs + (size_t)(tl + lane) * 4);
                 uint2 z2 = *reinterpret_cast<const uint2*>(v.vz + (size_t)(tl + lane) * 4);
@@ -1812,7 +1814,8 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         sm.wl[x / NG][x % NG] = 0.0f;
     }
     for (int x = threadIdx.x; x < W * NG * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
-    for (int x = threadIdx.x; x < (int)(sizeof(sm.zero) / 4); x += blockDim.x) sm.zero[x] = 0u;
+    if (NG == 1)
+        for (int x = threadIdx.x; x < (int)(sizeof(sm.qa) / 16); x += blockDim.x) (&sm.qa[0][0])[x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     const UnitState& us = sm.us;
