@@ -1396,6 +1396,24 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
     const uint32_t* psb = g < 4 ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : zero + t;
     const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);   // channels 4 lane .. + 3
     const uint32_t bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
+    // The copies of this tier's next items, one array per lane (lanes 0..5): a chunk of npad
+    // tokens stages array k at bytes [off_k npad, off_k npad + bytes_k npad) of its buffer,
+    // from base_k + (chunk index) * 128 bytes_k (compile-time sizes of the format).
+    const TierArgs& ta = a.tier[tier];
+    const uint8_t* cp_src = nullptr;
+    uint32_t cp_off = 0u, cp_bpt = 0u;
+    {
+        const size_t cap = (size_t)ta.cap;
+        switch (lane) {
+            case 0: cp_src = reinterpret_cast<const uint8_t*>(ta.k_codes + unit * (cap / 16) * 128); cp_off = 0; cp_bpt = 32; break;
+            case 1: cp_src = reinterpret_cast<const uint8_t*>(ta.k_scale + unit * (cap / 32) * 128); cp_off = 32; cp_bpt = 8; break;
+            case 2: cp_src = reinterpret_cast<const uint8_t*>(ta.k_zero + unit * (cap / 32) * 128); cp_off = 40; cp_bpt = 8; break;
+            case 3: cp_src = reinterpret_cast<const uint8_t*>(ta.v_codes + unit * cap * 8); cp_off = 48; cp_bpt = 32; break;
+            case 4: cp_src = reinterpret_cast<const uint8_t*>(ta.v_scale + unit * cap * 4); cp_off = 80; cp_bpt = 8; break;
+            case 5: cp_src = reinterpret_cast<const uint8_t*>(ta.v_zero + unit * cap * 4); cp_off = 88; cp_bpt = 8; break;
+            default: break;
+        }
+    }
     Mk1Acc acc;
     acc.m = kNegInf;
     acc.l = 0.0f;
@@ -1546,7 +1564,26 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
             }
             __syncwarp();                                        // pw / ps / qf are rewritten by the next item
         }
-        release_item(a, sm, unit, r, i, n_local, stage_base);
+        // every warp is done with item i: warp 0 requests item i + S into its buffer, the six
+        // copies of a chunk of this tier side by side (other items: the general path)
+        __syncthreads();
+        if (warp == 0 && i + a.stages < n_local && !sm.fail) {
+            const int inext = i + a.stages, kn = r + inext * a.cluster;
+            if (kn < us.base[tier + 1]) {
+                const int idx = kn - us.base[tier];
+                const int np = (min(kSub, us.cnt[tier] - idx * kSub) + 31) & ~31;
+                const int sb = inext & (a.stages - 1);
+                const uint32_t bar = smem_u32(&sm.bar[sb]);
+                if (lane == 0) mbar_expect_tx(bar, 96u * (uint32_t)np);
+                __syncwarp();
+                if (lane < 6)
+                    bulk_load(smem_u32(stage_base) + (uint32_t)sb * a.stage_bytes + cp_off * (uint32_t)np,
+                              cp_src + (size_t)idx * (kSub * cp_bpt), cp_bpt * (uint32_t)np, bar);
+            } else if (lane == 0) {
+                issue_item(a, us, unit, r, inext, stage_base, sm.bar);
+            }
+            if (lane == 0) sm.issued = inext + 1;
+        }
     }
     // ---- merge the warp's state into its shared-memory state
     acc.l = warp_sum(acc.l);
