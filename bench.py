@@ -2,7 +2,7 @@
 
 One step = the whole hot path over one batch of synthetic input: two-pass
 prefill (output + column scores), the prefill-end cache build (selection and
-INT2 packing for MiniKV, the tier split for DiffKV / MiKV), then every decode
+INT2 packing in one launch for MiniKV, the tier split for DiffKV / MiKV), then every decode
 step of the workload (attention over the packed cache + the policy tail).
 
 Default workload (`pyramid`): the 32-layer MiniKV pyramid sweep -- 32 layers of
@@ -223,7 +223,7 @@ class Hot:
             self.kh = torch.full((B * Hkv,), self.k_hh, dtype=torch.int32, device=dev)
             self.idx = torch.empty((B, Hkv, self.n_sel), dtype=torch.int32, device=dev)
             self.nout = torch.empty((B * Hkv,), dtype=torch.int32, device=dev)
-            self.launches_per_step = 2 + 1 + 3 + steps       # the residual flush runs inside decode
+            self.launches_per_step = 2 + 1 + steps           # the residual flush runs inside decode
         elif pol == "diffkv":
             f = inputs.dirichlet_fractions(B * Hkv, seed=seed)
             nc = T - nr
@@ -257,10 +257,9 @@ class Hot:
         kvq.prefill_attn_scores(self.q, self.k, self.v, self.scale,
                                 out=(self.o_pre, self.lse, self.cs), stream=s)
         if pol == "minikv":
-            kvq.select_tokens(self.cs, self.kh, self.w, kmax=self.k_hh, out=(self.idx, self.nout),
-                              stream=s)
-            kvq.requant_demote(self.cache, 0, k_src=self.k, v_src=self.v, sel_idx=self.idx,
-                               n_sel=self.n_sel, stream=s)
+            # selection + packing + residual in one launch (the prefill-end epilogue)
+            kvq.minikv_prefill_build(self.cache, self.k, self.v, self.cs, self.kh, self.w, kmax=self.k_hh,
+                                     idx_out=self.idx, stream=s)
         elif pol == "diffkv":
             kvq.requant_demote(self.cache, 0, k_src=self.k, v_src=self.v, colscore=self.cs,
                                n_high=self.n_high, n_low=self.n_low, stream=s)
@@ -344,16 +343,15 @@ class Sweep:
         self.o_dec = torch.empty((L, B, H, D), dtype=torch.float16, device=dev)
         self.graph = None
         self.prefill_flops = 3 * D * T * T * B * H * L
-        self.launches_per_step = L * (2 + 1 + 3 + steps)
+        self.launches_per_step = L * (2 + 1 + steps)
 
     def prefill_build(self, s):
         kvq = self.kvq
         for ly in self.layers:
             kvq.prefill_attn_scores(self.q, self.k, self.v, self.scale, out=(self.o_pre, self.lse, self.cs),
                                     stream=s)
-            kvq.select_tokens(self.cs, ly["kh"], ly["w"], kmax=ly["k_hh"], out=(ly["idx"], ly["nout"]), stream=s)
-            kvq.requant_demote(ly["cache"], 0, k_src=self.k, v_src=self.v, sel_idx=ly["idx"],
-                               n_sel=ly["n_sel"], stream=s)
+            kvq.minikv_prefill_build(ly["cache"], self.k, self.v, self.cs, ly["kh"], ly["w"], kmax=ly["k_hh"],
+                                     idx_out=ly["idx"], stream=s)
 
     def _decode_layers(self, s):
         for l, ly in enumerate(self.layers):

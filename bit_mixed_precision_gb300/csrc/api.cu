@@ -6,6 +6,8 @@
 
 #include <string>
 
+#include <algorithm>
+
 #include "kvq_internal.h"
 
 extern "C" cudaError_t kvq_internal_status_quant(cudaStream_t, uint32_t*);
@@ -278,6 +280,26 @@ kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params
         }
     }
     return kvq::run_policy(*c, mode, p, step, (cudaStream_t)stream);
+}
+
+kvq_status minikv_prefill_build(kvq_cache* c, const void* k, const void* v, int T, const float* score,
+                                const int32_t* k_hh, int kmax, int w_recent, int32_t* idx_out, void* stream) {
+    kvq_status st = check_cache(c, "minikv_prefill_build");
+    if (st != KVQ_OK) return st;
+    KVQ_REQUIRE(c->policy == KVQ_POLICY_MINIKV, KVQ_EINVAL, "minikv_prefill_build: not a MiniKV cache");
+    KVQ_REQUIRE(k && v && score && k_hh, KVQ_EINVAL, "minikv_prefill_build: null pointer");
+    KVQ_REQUIRE(aligned(k, 16) && aligned(v, 16) && aligned(c->res_k, 16) && aligned(c->res_v, 16), KVQ_EINVAL,
+                "minikv_prefill_build: k, v and the residual ring must be 16-byte aligned");
+    KVQ_REQUIRE(T > 0 && T <= 65536, KVQ_EINVAL, "minikv_prefill_build: T must be in [1, 65536]");
+    KVQ_REQUIRE(w_recent >= 0 && w_recent <= T && kmax >= 0, KVQ_EINVAL, "minikv_prefill_build: bad kmax / w_recent");
+    KVQ_REQUIRE((long long)kmax + w_recent <= 51200, KVQ_EUNSUPPORTED,
+                "minikv_prefill_build: kmax + w_recent = %lld positions exceed the 200 KB on-chip list",
+                (long long)kmax + w_recent);
+    const int nmax = std::min(kmax, T - w_recent) + w_recent;
+    KVQ_REQUIRE(std::max(0, nmax - c->nr) <= c->tier[0].cap, KVQ_EINVAL,
+                "minikv_prefill_build: tier 0 capacity %d < %d packed tokens", c->tier[0].cap,
+                std::max(0, nmax - c->nr));
+    return kvq::run_minikv_fused_build(*c, k, v, T, score, k_hh, kmax, w_recent, idx_out, (cudaStream_t)stream);
 }
 
 size_t kvq_tier_bytes(int units, int D, int G, int k_bits, int v_bits, int k_axis, int cap,

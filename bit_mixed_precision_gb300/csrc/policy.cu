@@ -193,6 +193,108 @@ __global__ void __launch_bounds__(kTailRows * 32) minikv_build_tail(PolicyArgs a
     }
 }
 
+// The whole prefill-end build of one unit in one CTA, straight from its
+// column scores: heavy hitters (radix select over positions < T - w, ties to
+// the lower position) plus the recent window into shared memory, ascending;
+// then the per-channel key groups and the per-token value groups of the
+// packed part, the residual rows, token ids and counters.  Same arithmetic
+// and layout as select_tokens followed by requant_demote(step 0).
+template <typename T, int KB, int VB>
+__global__ void __launch_bounds__(kTopkBlock) minikv_fused_build(PolicyArgs a, const float* __restrict__ score,
+                                                                 const int32_t* __restrict__ k_hh, int kmax, int w,
+                                                                 int32_t* __restrict__ idx_out) {
+    __shared__ TopkShared sh;
+    extern __shared__ int32_t sel[];                 // [kmax + w] selected positions, ascending
+    const size_t unit = blockIdx.x;
+    const int Tn = a.T, D = a.D, nc = Tn - w;
+    const float* sc = score + unit * (size_t)Tn;
+    int k = k_hh[unit];
+    if (k < 0 || k > kmax) {
+        if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
+        k = k < 0 ? 0 : kmax;
+    }
+    if (k > nc) k = nc;
+    if (k > 0) {
+        uint32_t kstar, take_eq;
+        block_radix_select([&](int i) { return orderable(sc[i]); }, nc, k, sh, &kstar, &take_eq);
+        uint32_t eq_base = 0, out_base = 0;
+        for (int c0 = 0; c0 < nc; c0 += blockDim.x) {
+            const int j = c0 + threadIdx.x;
+            const uint32_t kv = j < nc ? orderable(sc[j]) : 0u;
+            const uint32_t gt = (j < nc && kv > kstar) ? 1u : 0u;
+            const uint32_t eq = (j < nc && kv == kstar) ? 1u : 0u;
+            uint32_t eq_tot;
+            const uint32_t eq_rank = block_excl_scan(eq, sh, &eq_tot);
+            const uint32_t take = gt | (eq & (eq_base + eq_rank < take_eq ? 1u : 0u));
+            uint32_t sel_tot;
+            const uint32_t pos = block_excl_scan(take, sh, &sel_tot);
+            if (take) sel[out_base + pos] = j;
+            eq_base += eq_tot;
+            out_base += sel_tot;
+        }
+    }
+    for (int i = threadIdx.x; i < w; i += blockDim.x) sel[k + i] = nc + i;
+    __syncthreads();
+    const int n = k + w, nr = a.nr;
+    const int r0 = n <= nr ? n : nr + (n - nr) % 32, npk = n - r0;
+    const TierDev& t = a.tier[0];
+    if (idx_out)
+        for (int i = threadIdx.x; i < n; i += blockDim.x) idx_out[unit * (size_t)(kmax + w) + i] = sel[i];
+    const T* ks = reinterpret_cast<const T*>(a.k_src) + unit * (size_t)Tn * D;
+    const T* vs = reinterpret_cast<const T*>(a.v_src) + unit * (size_t)Tn * D;
+    // keys: channel c of packed group grp (32 selected tokens), one task per thread
+    const int kgroups = npk / 32;
+    for (int task = threadIdx.x; task < kgroups * D; task += blockDim.x) {
+        const int grp = task / D, c = task - grp * D;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = Elem<T>::to_f(ks[(size_t)sel[grp * 32 + i] * D + c]);
+        const QParams q = params32(v, KB);
+        pack32<KB>(v, q, t.k_codes + (unit * (size_t)(t.cap * KB / 32) + (size_t)grp * KB) * D + c, D);
+        const size_t so = (unit * (size_t)(t.cap / 32) + grp) * D + c;
+        t.k_scale[so] = q.s_bits;
+        t.k_zero[so] = q.z_bits;
+    }
+    // values: 32-channel group g of packed token i (four 16-byte loads)
+    const int vg = D / 32;
+    for (int task = threadIdx.x; task < npk * vg; task += blockDim.x) {
+        const int i = task / vg, g = task - i * vg;
+        const uint4* src = reinterpret_cast<const uint4*>(vs + (size_t)sel[i] * D + (size_t)g * 32);
+        float v[32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 wv = src[q4];
+            const T* e = reinterpret_cast<const T*>(&wv);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[8 * q4 + u] = Elem<T>::to_f(e[u]);
+        }
+        const QParams q = params32(v, VB);
+        const size_t orow = unit * (size_t)t.cap + i;
+        pack32<VB>(v, q, t.v_codes + orow * (D * VB / 32) + (size_t)g * VB, 1);
+        t.v_scale[orow * vg + g] = q.s_bits;
+        t.v_zero[orow * vg + g] = q.z_bits;
+    }
+    // residual rows (16-byte pieces), token ids, counters
+    const int vec = D * 2 / 16;
+    for (int task = threadIdx.x; task < r0 * 2 * vec; task += blockDim.x) {
+        const int i = task / (2 * vec), e = task - i * (2 * vec);
+        const int pos = sel[npk + i];
+        const bool isv = e >= vec;
+        const uint4* src = reinterpret_cast<const uint4*>((isv ? vs : ks) + (size_t)pos * D) + (isv ? e - vec : e);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(isv ? a.res_v : a.res_k) +
+                                              (unit * a.res_cap + i) * (size_t)D) + (isv ? e - vec : e);
+        *dst = *src;
+    }
+    for (int i = threadIdx.x; i < r0; i += blockDim.x) a.res_token_id[unit * a.res_cap + i] = sel[npk + i];
+    for (int i = threadIdx.x; i < npk; i += blockDim.x) t.token_id[unit * t.cap + i] = sel[i];
+    if (threadIdx.x == 0) {
+        t.count[unit] = npk;
+        a.res_start[unit] = 0;
+        a.res_len[unit] = r0;
+        a.seq_len[unit] = Tn;
+    }
+}
+
 // ----------------------------------------------------------------- DiffKV
 
 __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
@@ -590,6 +692,43 @@ kvq_status launched(const char* what) {
 }
 
 }  // namespace
+
+template <typename T>
+static cudaError_t launch_fused_t(const PolicyArgs& a, int units, int kb, int vb, const float* score,
+                                  const int32_t* k_hh, int kmax, int w, int32_t* idx_out, cudaStream_t s) {
+    const size_t smem = (size_t)(kmax + w) * sizeof(int32_t);
+    auto go = [&](auto kern) -> cudaError_t {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<units, kTopkBlock, smem, s>>>(a, score, k_hh, kmax, w, idx_out);
+        return cudaGetLastError();
+    };
+    if (kb == 2 && vb == 2) return go(minikv_fused_build<T, 2, 2>);
+    if (kb == 4 && vb == 4) return go(minikv_fused_build<T, 4, 4>);
+    if (kb == 4 && vb == 2) return go(minikv_fused_build<T, 4, 2>);
+    return cudaErrorInvalidValue;
+}
+
+kvq_status run_minikv_fused_build(const kvq_cache& c, const void* k, const void* v, int T, const float* score,
+                                  const int32_t* k_hh, int kmax, int w, int32_t* idx_out, cudaStream_t s) {
+    kvq_policy_params p{};
+    p.k_src = k;
+    p.v_src = v;
+    p.T = T;
+    PolicyArgs a = make_args(c, &p);
+    const int units = c.B * c.Hkv;
+    const kvq_tier& t = c.tier[0];
+    cudaError_t e = c.dtype == KVQ_BF16
+                        ? launch_fused_t<__nv_bfloat16>(a, units, t.k_bits, t.v_bits, score, k_hh, kmax, w, idx_out, s)
+                        : launch_fused_t<__half>(a, units, t.k_bits, t.v_bits, score, k_hh, kmax, w, idx_out, s);
+    if (e != cudaSuccess) {
+        set_error("minikv_prefill_build launch: %s", cudaGetErrorString(e));
+        return KVQ_ECUDA;
+    }
+    return KVQ_OK;
+}
 
 kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, int step,
                       cudaStream_t s) {

@@ -25,7 +25,7 @@ POLICY_MINIKV, POLICY_DIFFKV, POLICY_MIKV = 0, 1, 2
 MAX_TIERS = 2
 
 EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
-           "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
+           "minikv_prefill_build", "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
            "kvq_decode_workspace_bytes", "kvq_tier_bytes",
            "kvq_last_error", "kvq_device_status", "kvq_debug_withhold_copy", "kvq_version"]
 
@@ -86,6 +86,7 @@ def lib():
         L.select_tokens.argtypes = [vp, i32, i32, i32, vp, i32, i32, vp, vp, vp, sz, vp]
         L.requant_demote.argtypes = [ctypes.POINTER(KvqCache), i32, ctypes.POINTER(KvqPolicyParams),
                                      i32, vp]
+        L.minikv_prefill_build.argtypes = [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp, i32, i32, vp, vp]
         L.decode_attn_qkv.argtypes = [vp, vp, vp, ctypes.POINTER(KvqCache), f32, vp, vp, vp, sz, vp]
         L.decode_attn_qkv_static.argtypes = [vp, vp, vp, ctypes.POINTER(KvqCache), f32, vp, vp, vp]
         L.decode_attn_qkv_static.restype = ctypes.c_int
@@ -97,7 +98,7 @@ def lib():
         L.kvq_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.kvq_debug_withhold_copy.argtypes = [i32]
         for name in ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
-                     "requant_demote", "decode_attn_qkv", "kvq_device_status", "kvq_debug_withhold_copy"]:
+                     "minikv_prefill_build", "requant_demote", "decode_attn_qkv", "kvq_device_status", "kvq_debug_withhold_copy"]:
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -407,6 +408,28 @@ def requant_demote(cache, step, k_src=None, v_src=None, sel_idx=None, n_sel=0, c
                             n_low.data_ptr() if n_low is not None else None)
     _check(lib().requant_demote(ctypes.byref(cache.desc), cache.policy,
                                 ctypes.byref(p) if p is not None else None, step, _stream(stream)))
+
+
+def minikv_prefill_build(cache, k, v, score, k_hh, w_recent, kmax=None, idx_out=None, stream=None):
+    """MiniKV prefill-end build in one launch: heavy hitters + window from score [B, Hkv, T],
+    packed into tier 0 with the residual filled (select_tokens + requant_demote(step 0))."""
+    _cuda(k, v, score, k_hh, idx_out)
+    B, H, T, D = k.shape
+    if v.shape != k.shape or v.dtype != k.dtype or k.dtype != cache.dtype:
+        raise ValueError("k and v must share the cache's dtype and one shape")
+    if tuple(score.shape) != (B, H, T) or score.dtype != torch.float32:
+        raise ValueError(f"score must be float32 [{B}, {H}, {T}]")
+    if (B, H, D) != (cache.B, cache.Hkv, cache.D):
+        raise ValueError("k does not match the cache's B / Hkv / D")
+    if k_hh.dtype != torch.int32 or k_hh.numel() != B * H:
+        raise ValueError("k_hh must be int32 [B * Hkv]")
+    if kmax is None:
+        kmax = int(k_hh.max().item()) if k_hh.numel() else 0
+    if idx_out is not None and (idx_out.dtype != torch.int32 or idx_out.numel() != B * H * (kmax + w_recent)):
+        raise ValueError("idx_out must be int32 [B, Hkv, kmax + w_recent]")
+    _check(lib().minikv_prefill_build(ctypes.byref(cache.desc), _ptr(k), _ptr(v), T, _ptr(score), _ptr(k_hh),
+                                      int(kmax), int(w_recent), _ptr(idx_out), _stream(stream)))
+    return idx_out
 
 
 def decode_attn_qkv(q, k_new, v_new, cache, sm_scale=None, o=None, lse=None, stream=None):

@@ -214,6 +214,28 @@ kvq_status select_tokens(const float* score, int B, int H, int T, const int32_t*
                          int w_recent, int32_t* idx_out, int32_t* n_out,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* minikv_prefill_build -- the MiniKV prefill-end epilogue in one launch:
+ * select_tokens followed by requant_demote(step 0), fused ([MiniKV-J]
+ * key_machinery: selection persists from the end of prefill; [MiniKV-R]
+ * "Core claim": heavy hitters chosen once from the prefill column scores).
+ * One CTA per unit keeps the selected positions on chip and packs from them.
+ *   c: a MiniKV cache (tier 0 per-channel keys; G = 32).
+ *   k, v (device) [B, Hkv, T, D] activations in the cache's dtype, 16-byte
+ *   aligned; score (device) [B, Hkv, T] float32 (one row per KV head: reduce
+ *   GQA groups first, kvq_score_reduce); k_hh (device) [B*Hkv] budgets as in
+ *   select_tokens, kmax their upper bound, w_recent the window.
+ *   Per unit: n = min(k_hh, T - w) + w positions (heavy hitters ascending,
+ *   then T-w .. T-1); the first n - r0 are packed into tier 0 and the last
+ *   r0 = n <= nr ? n : nr + (n - nr) mod G stay in the residual ring, exactly
+ *   as requant_demote(step 0) with those positions as sel_idx would leave
+ *   the cache.  Tier 0 capacity must hold max(0, min(kmax, T - w) + w - nr)
+ *   tokens; (kmax + w_recent) * 4 bytes of shared memory per CTA, at most
+ *   200 KB (KVQ_EUNSUPPORTED beyond); T <= 65536.
+ *   idx_out (device, nullable) [B, Hkv, kmax + w_recent]: the positions, as
+ *   select_tokens writes them. */
+kvq_status minikv_prefill_build(kvq_cache* c, const void* k, const void* v, int T, const float* score,
+                                const int32_t* k_hh, int kmax, int w_recent, int32_t* idx_out, void* stream);
+
 /* requant_demote -- the policy tail of a step ([DiffKV-J] key_machinery and
  * Algorithm 1; [MiKV-R] re-quantisation paragraph; [MiniKV-R] nr).
  *   step == 0: build the cache at the end of prefill from p (k_src, v_src,

@@ -76,8 +76,9 @@ def test_fullsize_pyramid_layer16():
     _check_prefill(hot, [(3, 7), (15, 31)], np.array([0, 1, 4095, 9000, T - 1]))
     # build from seeded scores given to both sides
     cs = inputs.random_scores(B, H, T, seed=2, ties=64)
-    idx, _ = kvq.select_tokens(cs.cuda(), hot.kh, hot.w, kmax=hot.k_hh)
-    kvq.requant_demote(hot.cache, 0, k_src=hot.k, v_src=hot.v, sel_idx=idx, n_sel=hot.n_sel)
+    # the benchmark's prefill-end epilogue: selection and packing in one launch
+    idx = torch.empty((B, H, hot.n_sel), dtype=torch.int32, device="cuda")
+    kvq.minikv_prefill_build(hot.cache, hot.k, hot.v, cs.cuda(), hot.kh, hot.w, kmax=hot.k_hh, idx_out=idx)
     sample = [3 * H + 7, 15 * H + 31]
     units = {}
     gsel = idx.cpu().numpy().reshape(B * H, -1)

@@ -103,3 +103,72 @@ def test_minikv_llama_layer():
 def test_minikv_bf16():
     """bf16 prompt, decode inputs, residual ring and output (prompt 1024, 40 steps, nr = 0)."""
     _pipeline(B=2, H=2, T=1024, D=128, steps=40, nr=0, n_out=2, out_scale=8.0, seed=4, dtype=torch.bfloat16)
+
+
+def _cache_arrays(c):
+    t = c.tiers[0]
+    return [t.k_codes, t.k_scale, t.k_zero, t.v_codes, t.v_scale, t.v_zero, t.token_id, t.count,
+            c.res_k, c.res_v, c.res_token_id, c.res_start, c.res_len, c.seq_len]
+
+
+@pytest.mark.parametrize("nr,dtype", [(0, torch.float16), (128, torch.float16), (16, torch.bfloat16)])
+def test_fused_build_equals_two_launch_build(nr, dtype):
+    """minikv_prefill_build leaves every array of the cache exactly as select_tokens
+    followed by requant_demote(step 0) does (scores with many ties; ragged prompt)."""
+    B, H, T, D, G, w, k_hh = 2, 3, 700, 128, 32, 64, 177
+    x = inputs.make_qkv(B, H, H, T, D, dtype=dtype, seed=41, outliers=inputs.outlier_channels(H, D, 2, 41),
+                        outlier_scale=8.0)
+    k, v = x.k.cuda(), x.v.cuda()
+    cs = inputs.random_scores(B, H, T, seed=41, ties=24).cuda()
+    kh = torch.full((B * H,), k_hh, dtype=torch.int32, device="cuda")
+    n = k_hh + w
+    r0 = n if n <= nr else nr + (n - nr) % G
+    cap = ((n - r0) // G + 2) * G
+
+    def make():
+        return kvq.make_cache(B, H, H, D, G, dtype, kvq.POLICY_MINIKV, [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)],
+                              nr=nr)
+    two, fused = make(), make()
+    idx, _ = kvq.select_tokens(cs, kh, w, kmax=k_hh)
+    kvq.requant_demote(two, 0, k_src=k, v_src=v, sel_idx=idx, n_sel=n)
+    idx_f = torch.full((B, H, k_hh + w), -7, dtype=torch.int32, device="cuda")
+    kvq.minikv_prefill_build(fused, k, v, cs, kh, w, kmax=k_hh, idx_out=idx_f)
+    torch.cuda.synchronize()
+    assert kvq.device_status() == 0
+    assert torch.equal(idx, idx_f)
+    for a, b in zip(_cache_arrays(two), _cache_arrays(fused)):
+        assert torch.equal(a, b)
+
+
+def test_fused_build_per_unit_budgets_against_oracle():
+    """Per-unit heavy-hitter budgets (0, a few, most of the prompt): each unit's selection
+    equals the oracle's on the same float32 scores, and its packed words, scales, zeros,
+    ids and residual rows equal the oracle's MiniKV build."""
+    B, H, T, D, G, w, nr = 1, 4, 520, 128, 32, 40, 32
+    budgets = [0, 9, 200, 480]
+    x = inputs.make_qkv(B, H, H, T, D, seed=43)
+    cs = inputs.random_scores(B, H, T, seed=43, ties=16)
+    kh = torch.tensor(budgets, dtype=torch.int32, device="cuda")
+    cap = ((max(budgets) + w) // G + 2) * G
+    c = kvq.make_cache(B, H, H, D, G, torch.float16, kvq.POLICY_MINIKV, [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)],
+                       nr=nr)
+    kvq.minikv_prefill_build(c, x.k.cuda(), x.v.cuda(), cs.cuda(), kh, w)
+    torch.cuda.synchronize()
+    assert kvq.device_status() == 0
+    t = c.tiers[0]
+    for u in range(H):
+        sel = OS.select_unit(np_(cs[0, u]), min(budgets[u], T - w), w)
+        ref = OP.MiniKVUnit(np_(x.k[0, u]), np_(x.v[0, u]), sel, nr, G)
+        npk = len(ref.ids)
+        assert int(t.count[u]) == npk, f"unit {u}"
+        assert np.array_equal(t.token_id[u, :npk].cpu().numpy(), np.array(ref.ids, dtype=np.int32))
+        assert np.array_equal(u32(t.k_codes[u, :npk // 16]), ref.kw.view(np.uint32))
+        assert np.array_equal(u16(t.k_scale[u, :npk // G]), ref.ksc.view(np.uint16))
+        assert np.array_equal(u16(t.k_zero[u, :npk // G]), ref.kze.view(np.uint16))
+        assert np.array_equal(u32(t.v_codes[u, :npk]), ref.vw.view(np.uint32))
+        assert np.array_equal(u16(t.v_scale[u, :npk]), ref.vsc.view(np.uint16))
+        assert np.array_equal(u16(t.v_zero[u, :npk]), ref.vze.view(np.uint16))
+        r0 = len(ref.res)
+        assert int(c.res_len[u]) == r0 and int(c.res_start[u]) == 0 and int(c.seq_len[u]) == T
+        assert np.array_equal(c.res_token_id[u, :r0].cpu().numpy(), np.array([r[0] for r in ref.res], dtype=np.int32))
+        assert np.array_equal(np_(c.res_k[u, :r0]), np.stack([r[1] for r in ref.res]) if r0 else np.zeros((0, D)))
