@@ -184,6 +184,16 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
                     tr.k_bits, tr.v_bits, tr.k_axis);
         // the decode kernels take value groups (and per-token key groups) of 32 channels
         KVQ_REQUIRE(c->G == 32, KVQ_EUNSUPPORTED, "%s: tier %d: the decode kernels are built for G = 32", who, t);
+        if (tr.page_table) {
+            KVQ_REQUIRE(c->policy == KVQ_POLICY_DIFFKV, KVQ_EUNSUPPORTED, "%s: tier %d: only DiffKV tiers are paged",
+                        who, t);
+            KVQ_REQUIRE(tr.page_owner && tr.free_ring && tr.ring_ctr && tr.n_pages > 0 && tr.max_pages > 0,
+                        KVQ_EINVAL, "%s: tier %d: page pool arrays missing", who, t);
+            KVQ_REQUIRE((long long)tr.max_pages * KVQ_PAGE_TOKENS == tr.cap, KVQ_EINVAL,
+                        "%s: tier %d: a paged tier's cap must be max_pages * %d", who, t, KVQ_PAGE_TOKENS);
+            KVQ_REQUIRE((long long)c->B * c->Hkv * tr.max_pages <= (1LL << 31) - 1, KVQ_EINVAL,
+                        "%s: tier %d: page table too large", who, t);
+        }
     }
     KVQ_REQUIRE(c->res_cap > 0 && c->res_k && c->res_v && c->res_token_id && c->res_start && c->res_len &&
                     c->seq_len,
@@ -280,6 +290,26 @@ kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params
         }
     }
     return kvq::run_policy(*c, mode, p, step, (cudaStream_t)stream);
+}
+
+static bool any_paged(const kvq_cache* c) {
+    for (int t = 0; t < c->n_tiers; ++t)
+        if (c->tier[t].page_table) return true;
+    return false;
+}
+
+kvq_status kvq_pages_init(kvq_cache* c, void* stream) {
+    kvq_status st = check_cache(c, "kvq_pages_init");
+    if (st != KVQ_OK) return st;
+    KVQ_REQUIRE(any_paged(c), KVQ_EINVAL, "kvq_pages_init: the cache has no paged tier");
+    return kvq::run_pages_init(*c, (cudaStream_t)stream);
+}
+
+kvq_status kvq_pages_release(kvq_cache* c, const int32_t* release_mask, void* stream) {
+    kvq_status st = check_cache(c, "kvq_pages_release");
+    if (st != KVQ_OK) return st;
+    KVQ_REQUIRE(release_mask, KVQ_EINVAL, "kvq_pages_release: null mask");
+    return kvq::run_pages_release(*c, release_mask, (cudaStream_t)stream);
 }
 
 kvq_status minikv_prefill_build(kvq_cache* c, const void* k, const void* v, int T, const float* score,

@@ -78,6 +78,8 @@ struct TierArgs {
     int32_t* token_id;
     int32_t* count;
     int slot_base;              // offset of this tier in the logits row
+    const int32_t* page_table;  // paged tier: [unit][max_pages] physical page of each 128-slot chunk
+    int max_pages, n_pages;
 };
 
 struct DecodeArgs {
@@ -309,20 +311,33 @@ template <typename Fn>
 __device__ __forceinline__ void tier_ranges(const TierArgs& t, size_t unit, int j0, int npad, int D, int G,
                                             Fn fn) {
     const StageSizes z = tier_stage_sizes(t.k_axis, t.k_bits, t.v_bits, npad, D, G);
+    // a paged tier's chunk (128 slots) is one page: the page's rows stand in for the unit's
+    size_t urow = unit;
+    int cap = t.cap;
+    if (t.page_table) {
+        int pg = t.page_table[unit * (size_t)t.max_pages + j0 / KVQ_PAGE_TOKENS];
+        if (pg < 0 || pg >= t.n_pages) {
+            atomicOr(&g_status_decode, kDevCheck);
+            pg = 0;
+        }
+        urow = (size_t)pg;
+        j0 -= (j0 / KVQ_PAGE_TOKENS) * KVQ_PAGE_TOKENS;
+        cap = KVQ_PAGE_TOKENS;
+    }
     const void *kc_src, *ks_src, *kz_src;
     if (t.k_axis == KVQ_AXIS_CHANNEL) {
         const int per = 32 / t.k_bits;
-        kc_src = t.k_codes + (unit * (size_t)(t.cap / per) + j0 / per) * D;
-        const size_t so = (unit * (size_t)(t.cap / G) + j0 / G) * D;
+        kc_src = t.k_codes + (urow * (size_t)(cap / per) + j0 / per) * D;
+        const size_t so = (urow * (size_t)(cap / G) + j0 / G) * D;
         ks_src = t.k_scale + so;
         kz_src = t.k_zero + so;
     } else {
-        kc_src = t.k_codes + (unit * (size_t)t.cap + j0) * (D * t.k_bits / 32);
-        const size_t so = (unit * (size_t)t.cap + j0) * (D / G);
+        kc_src = t.k_codes + (urow * (size_t)cap + j0) * (D * t.k_bits / 32);
+        const size_t so = (urow * (size_t)cap + j0) * (D / G);
         ks_src = t.k_scale + so;
         kz_src = t.k_zero + so;
     }
-    const size_t vo = unit * (size_t)t.cap + j0;
+    const size_t vo = urow * (size_t)cap + j0;
     const uint32_t o_ks = a16(z.kc), o_kz = o_ks + a16(z.ks), o_vc = o_kz + a16(z.ks);
     const uint32_t o_vs = o_vc + a16(z.vc), o_vz = o_vs + a16(z.vs);
     fn(kc_src, z.kc, 0u);
@@ -679,7 +694,7 @@ __device__ __forceinline__ int local_at(int k, int r, int C) { return k > r ? (k
 __device__ void prefetch_start(const DecodeArgs& a, size_t unit, int r) {
     const int C = a.cluster, D = a.D;
     const TierArgs& t0 = a.tier[0];
-    const int nsub = (t0.cap + kSub - 1) / kSub;
+    const int nsub = t0.page_table ? 0 : (t0.cap + kSub - 1) / kSub;   // pages: unknown until read
     for (int k = r, i = 0; k < nsub && i < 2; k += C, ++i) {
         const int j0 = k * kSub;
         tier_ranges(t0, unit, j0, min(kSub, t0.cap - j0), D, a.G,
@@ -2202,6 +2217,9 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
         ta.v_zero = ct.v_zero;
         ta.token_id = ct.token_id;
         ta.count = ct.count;
+        ta.page_table = ct.page_table;
+        ta.max_pages = ct.max_pages;
+        ta.n_pages = ct.n_pages;
         ta.slot_base = slot;
         slot += ct.cap;
     }

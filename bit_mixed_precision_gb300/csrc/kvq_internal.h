@@ -45,6 +45,10 @@ cudaError_t static_decode_scratch(void** out);
 kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, int step,
                       cudaStream_t s);
 
+// DiffKV page pools: reset, and release of finished units.
+kvq_status run_pages_init(const kvq_cache& c, cudaStream_t s);
+kvq_status run_pages_release(const kvq_cache& c, const int32_t* mask, cudaStream_t s);
+
 // MiniKV prefill-end build from column scores in one launch (selection + packing + residual).
 kvq_status run_minikv_fused_build(const kvq_cache& c, const void* k, const void* v, int T, const float* score,
                                   const int32_t* k_hh, int kmax, int w, int32_t* idx_out, cudaStream_t s);

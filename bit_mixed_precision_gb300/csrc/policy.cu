@@ -53,7 +53,23 @@ struct TierDev {
     uint16_t* v_zero;
     int32_t* token_id;
     int32_t* count;
+    // paged tiers (page_table != nullptr): slot s of unit u lives in page
+    // page_table[u * max_pages + s / P] at row s mod P (P = KVQ_PAGE_TOKENS)
+    int32_t* page_table;
+    int32_t* page_owner;
+    int32_t* free_ring;
+    uint32_t* ring_ctr;
+    int max_pages, n_pages;
 };
+
+// Flat row of slot `slot` of unit `unit` in the tier's arrays (the page's row when paged).
+__device__ __forceinline__ size_t slot_row(const TierDev& t, size_t unit, int slot) {
+    if (t.page_table) {
+        const int pg = t.page_table[unit * (size_t)t.max_pages + (slot / KVQ_PAGE_TOKENS)];
+        return (size_t)pg * KVQ_PAGE_TOKENS + (size_t)(slot % KVQ_PAGE_TOKENS);
+    }
+    return unit * (size_t)t.cap + slot;
+}
 
 struct PolicyArgs {
     int B, Hq, Hkv, D, G, g, bf16, n_tiers, nr, hi_den;
@@ -90,13 +106,13 @@ __device__ void quant_row(Load load, int D, int G, int bits, uint32_t* codes, ui
 }
 
 __device__ __forceinline__ uint32_t* krow(const TierDev& t, size_t unit, int slot, int D) {
-    return t.k_codes + (unit * t.cap + slot) * (size_t)(D * t.k_bits / 32);
+    return t.k_codes + slot_row(t, unit, slot) * (size_t)(D * t.k_bits / 32);
 }
 __device__ __forceinline__ uint32_t* vrow(const TierDev& t, size_t unit, int slot, int D) {
-    return t.v_codes + (unit * t.cap + slot) * (size_t)(D * t.v_bits / 32);
+    return t.v_codes + slot_row(t, unit, slot) * (size_t)(D * t.v_bits / 32);
 }
 __device__ __forceinline__ size_t srow(const TierDev& t, size_t unit, int slot, int D, int G) {
-    return (unit * t.cap + slot) * (size_t)(D / G);
+    return slot_row(t, unit, slot) * (size_t)(D / G);
 }
 
 // Quantise raw token `pos` of a [units][T][D] source (or ring slot) into a
@@ -111,7 +127,7 @@ __device__ void put_raw_token(const PolicyArgs& a, const TierDev& t, size_t unit
     quant_row([&](int c) { return ld_act(vsrc, row_elem + c, bf); }, D, G, t.v_bits,
               vrow(t, unit, slot, D), t.v_scale + srow(t, unit, slot, D, G),
               t.v_zero + srow(t, unit, slot, D, G));
-    t.token_id[unit * t.cap + slot] = token_id;
+    t.token_id[slot_row(t, unit, slot)] = token_id;
 }
 
 // One warp: the same token into a tier slot, group-parallel for G = 32
@@ -145,7 +161,7 @@ __device__ void put_token_warp(const PolicyArgs& a, const TierDev& t, size_t uni
         (isv ? t.v_scale : t.k_scale)[so] = q.s_bits;
         (isv ? t.v_zero : t.k_zero)[so] = q.z_bits;
     }
-    if (lane == 0) t.token_id[unit * t.cap + slot] = token_id;
+    if (lane == 0) t.token_id[slot_row(t, unit, slot)] = token_id;
 }
 
 // ----------------------------------------------------------------- MiniKV
@@ -322,6 +338,21 @@ __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
     const float alpha_l = nl > 0 ? __fmul_rn(Tf, unorderable(k2)) : alpha_h;
     const TierDev& th = a.tier[0];
     const TierDev& tl = a.tier[1];
+    // slots each tier can hold for this unit: its capacity, or for a paged tier the pages
+    // the build gave it (fewer when the pool ran out)
+    __shared__ int lim_s[2];
+    if (threadIdx.x < 2) {
+        const TierDev& t = a.tier[threadIdx.x];
+        int lim = t.cap;
+        if (t.page_table) {
+            int k = 0;
+            while (k < t.max_pages && t.page_table[unit * (size_t)t.max_pages + k] >= 0) ++k;
+            lim = min(lim, k * KVQ_PAGE_TOKENS);
+        }
+        lim_s[threadIdx.x] = lim;
+    }
+    __syncthreads();
+    const uint32_t lim_h = (uint32_t)lim_s[0], lim_l = (uint32_t)lim_s[1];
     uint32_t eq1_base = 0, eq2_base = 0, hi_base = 0, lo_base = 0;
     for (int c0 = 0; c0 < nc; c0 += blockDim.x) {
         const int j = c0 + threadIdx.x;
@@ -338,11 +369,11 @@ __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
         const uint32_t ph = block_excl_scan(is_hi, sh, &tot_hi);
         const uint32_t pl = block_excl_scan(is_lo, sh, &tot_lo);
         const size_t row = (unit * T + j) * (size_t)D;
-        if (is_hi && hi_base + ph < (uint32_t)th.cap)
+        if (is_hi && hi_base + ph < lim_h)
             put_raw_token(a, th, unit, hi_base + ph, a.k_src, a.v_src, row, j);
-        if (is_lo && lo_base + pl < (uint32_t)tl.cap)
+        if (is_lo && lo_base + pl < lim_l)
             put_raw_token(a, tl, unit, lo_base + pl, a.k_src, a.v_src, row, j);
-        if ((is_hi && hi_base + ph >= (uint32_t)th.cap) || (is_lo && lo_base + pl >= (uint32_t)tl.cap))
+        if ((is_hi && hi_base + ph >= lim_h) || (is_lo && lo_base + pl >= lim_l))
             atomicOr(&g_status_policy, kDevCheck);
         eq1_base += tot1;
         eq2_base += tot2;
@@ -364,8 +395,8 @@ __global__ void __launch_bounds__(kTopkBlock) diffkv_build(PolicyArgs a) {
     }
     for (int i = threadIdx.x; i < W; i += blockDim.x) a.res_token_id[unit * a.res_cap + i] = nc + i;
     if (threadIdx.x == 0) {
-        th.count[unit] = min((int)hi_base, th.cap);
-        tl.count[unit] = min((int)lo_base, tl.cap);
+        th.count[unit] = min((int)hi_base, (int)lim_h);
+        tl.count[unit] = min((int)lo_base, (int)lim_l);
         a.res_start[unit] = 0;
         a.res_len[unit] = W;
         a.alpha[unit * 2] = alpha_h;
@@ -390,21 +421,171 @@ __global__ void diffkv_exit(PolicyArgs a) {
     const float th_h = __fdiv_rn(a.alpha[unit * 2], (float)N);
     const float th_l = __fdiv_rn(a.alpha[unit * 2 + 1], (float)N);
     const int cls = score >= th_h ? 0 : (score >= th_l ? 1 : 2);
+    bool stored = false;
     if (cls < 2) {
         const TierDev& t = a.tier[cls];
         const int slot = t.count[unit];
-        if (slot >= t.cap) {
+        bool room = slot < t.cap;
+        if (room && t.page_table && slot % KVQ_PAGE_TOKENS == 0) {
+            // the token opens a logical page: one page from the ring head
+            int pg = -1;
+            if (threadIdx.x == 0) {
+                const uint32_t h = atomicAdd(&t.ring_ctr[0], 1u);
+                const uint32_t tail = *(volatile uint32_t*)&t.ring_ctr[1];
+                if (h < tail) {
+                    pg = t.free_ring[h % (uint32_t)t.n_pages];
+                    const int li = slot / KVQ_PAGE_TOKENS;
+                    t.page_table[unit * (size_t)t.max_pages + li] = pg;
+                    t.page_owner[pg] = (int)unit * t.max_pages + li;
+                }
+            }
+            pg = __shfl_sync(0xffffffffu, pg, 0);
+            __syncwarp();                                  // the table entry before the row writes
+            room = pg >= 0;
+        }
+        if (!room) {
             if (threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
         } else {
             put_token_warp(a, t, unit, slot, a.res_k, a.res_v, (unit * cap + start) * (size_t)a.D, tc);
+            stored = true;
         }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        if (cls < 2 && a.tier[cls].count[unit] < a.tier[cls].cap) a.tier[cls].count[unit] += 1;
+        if (stored) a.tier[cls].count[unit] += 1;
         a.res_start[unit] = (start + 1) % cap;
         a.res_len[unit] = len - 1;
     }
+}
+
+// ---- DiffKV page pools ([DiffKV-J] unified pages, circular free page list,
+// bidirectional page table, parallel compaction): one CTA per pool operation.
+
+// Every page held by the units u with rel(u) goes back to the ring tail: units in
+// order, pages in logical order (each unit's run starts at the exclusive prefix
+// sum of the held counts).  Pages of a unit are a prefix of its table row.
+template <typename Rel>
+__device__ void pages_push(const TierDev& t, int units, Rel rel, TopkShared& sh, uint32_t* tail) {
+    const uint32_t n = (uint32_t)t.n_pages;
+    uint32_t base = 0;
+    for (int u0 = 0; u0 < units; u0 += blockDim.x) {
+        const int u = u0 + threadIdx.x;
+        uint32_t held = 0;
+        if (u < units && rel(u))
+            for (int i = 0; i < t.max_pages && t.page_table[(size_t)u * t.max_pages + i] >= 0; ++i) ++held;
+        uint32_t tot;
+        const uint32_t off = block_excl_scan(held, sh, &tot);
+        for (uint32_t i = 0; i < held; ++i) {
+            int32_t* e = &t.page_table[(size_t)u * t.max_pages + i];
+            const int pg = *e;
+            t.free_ring[(*tail + base + off + i) % n] = pg;
+            t.page_owner[pg] = -1;
+            *e = -1;
+        }
+        base += tot;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *tail += base;
+    __syncthreads();
+}
+
+// Prefill-end allocation of the paged tiers: every unit's old pages back to the
+// ring, then ceil(n / P) pages per unit for its n tokens of the tier (the same n
+// diffkv_build stores), one run per unit from the ring head in unit order.
+__global__ void __launch_bounds__(kTopkBlock) pages_build_alloc(PolicyArgs a) {
+    __shared__ TopkShared sh;
+    __shared__ uint32_t ctr[2];
+    const int units = a.B * a.Hkv, nc = a.T - a.nr;
+    for (int ti = 0; ti < a.n_tiers; ++ti) {
+        const TierDev& t = a.tier[ti];
+        if (!t.page_table) continue;
+        if (threadIdx.x == 0) {
+            ctr[0] = t.ring_ctr[0];
+            ctr[1] = t.ring_ctr[1];
+        }
+        __syncthreads();
+        pages_push(t, units, [](int) { return true; }, sh, &ctr[1]);
+        auto demand = [&](int u) -> uint32_t {
+            const int nh = max(0, min(a.n_high[u], nc));
+            const int n = ti == 0 ? nh : max(0, min(a.n_low[u], nc - nh));
+            return (uint32_t)min((n + KVQ_PAGE_TOKENS - 1) / KVQ_PAGE_TOKENS, t.max_pages);
+        };
+        uint32_t total = 0;
+        for (int u0 = 0; u0 < units; u0 += blockDim.x) {
+            const int u = u0 + threadIdx.x;
+            uint32_t tot;
+            (void)block_excl_scan(u < units ? demand(u) : 0u, sh, &tot);
+            total += tot;
+        }
+        const bool fits = total <= ctr[1] - ctr[0];
+        if (!fits && threadIdx.x == 0) atomicOr(&g_status_policy, kDevCheck);
+        const uint32_t n = (uint32_t)t.n_pages;
+        uint32_t base = 0;
+        for (int u0 = 0; fits && u0 < units; u0 += blockDim.x) {
+            const int u = u0 + threadIdx.x;
+            const uint32_t d = u < units ? demand(u) : 0u;
+            uint32_t tot;
+            const uint32_t off = block_excl_scan(d, sh, &tot);
+            for (uint32_t i = 0; i < d; ++i) {
+                const int pg = t.free_ring[(ctr[0] + base + off + i) % n];
+                t.page_table[(size_t)u * t.max_pages + i] = pg;
+                t.page_owner[pg] = u * t.max_pages + (int)i;
+            }
+            base += tot;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            t.ring_ctr[0] = ctr[0] + (fits ? total : 0u);
+            t.ring_ctr[1] = ctr[1];
+        }
+        __syncthreads();
+    }
+}
+
+// Every paged tier empty: ring = 0 .. n_pages-1, no owners, no table entries, counts 0.
+__global__ void pages_init_kernel(PolicyArgs a) {
+    const int units = a.B * a.Hkv;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (int ti = 0; ti < a.n_tiers; ++ti) {
+        const TierDev& t = a.tier[ti];
+        if (!t.page_table) continue;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)t.n_pages; i += stride) {
+            t.free_ring[i] = (int32_t)i;
+            t.page_owner[i] = -1;
+        }
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)units * t.max_pages; i += stride)
+            t.page_table[i] = -1;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)units; i += stride) t.count[i] = 0;
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            t.ring_ctr[0] = 0u;
+            t.ring_ctr[1] = (uint32_t)t.n_pages;
+        }
+    }
+}
+
+// A request is done: the units with mask[u] != 0 give their pages back (parallel
+// compaction at the ring tail) and are left empty.
+__global__ void __launch_bounds__(kTopkBlock) pages_release_kernel(PolicyArgs a, const int32_t* __restrict__ mask) {
+    __shared__ TopkShared sh;
+    __shared__ uint32_t tail;
+    const int units = a.B * a.Hkv;
+    for (int ti = 0; ti < a.n_tiers; ++ti) {
+        const TierDev& t = a.tier[ti];
+        if (t.page_table) {
+            if (threadIdx.x == 0) tail = t.ring_ctr[1];
+            __syncthreads();
+            pages_push(t, units, [&](int u) { return mask[u] != 0; }, sh, &tail);
+            if (threadIdx.x == 0) t.ring_ctr[1] = tail;
+        }
+        for (int u = threadIdx.x; u < units; u += blockDim.x)
+            if (mask[u]) t.count[u] = 0;
+    }
+    for (int u = threadIdx.x; u < units; u += blockDim.x)
+        if (mask[u]) {
+            a.res_len[u] = 0;
+            a.res_start[u] = 0;
+            a.seq_len[u] = 0;
+        }
 }
 
 // ----------------------------------------------------------------- MiKV
@@ -657,6 +838,12 @@ PolicyArgs make_args(const kvq_cache& c, const kvq_policy_params* p) {
         d.v_zero = s.v_zero;
         d.token_id = s.token_id;
         d.count = s.count;
+        d.page_table = s.page_table;
+        d.page_owner = s.page_owner;
+        d.free_ring = s.free_ring;
+        d.ring_ctr = s.ring_ctr;
+        d.max_pages = s.max_pages;
+        d.n_pages = s.n_pages;
     }
     a.res_k = c.res_k;
     a.res_v = c.res_v;
@@ -730,6 +917,18 @@ kvq_status run_minikv_fused_build(const kvq_cache& c, const void* k, const void*
     return KVQ_OK;
 }
 
+kvq_status run_pages_init(const kvq_cache& c, cudaStream_t s) {
+    PolicyArgs a = make_args(c, nullptr);
+    pages_init_kernel<<<152, 256, 0, s>>>(a);
+    return launched("kvq_pages_init");
+}
+
+kvq_status run_pages_release(const kvq_cache& c, const int32_t* mask, cudaStream_t s) {
+    PolicyArgs a = make_args(c, nullptr);
+    pages_release_kernel<<<1, kTopkBlock, 0, s>>>(a, mask);
+    return launched("kvq_pages_release");
+}
+
 kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, int step,
                       cudaStream_t s) {
     const int units = c.B * c.Hkv;
@@ -760,6 +959,7 @@ kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, 
     }
     if (mode == KVQ_POLICY_DIFFKV) {
         if (step == 0) {
+            if (c.tier[0].page_table || c.tier[1].page_table) pages_build_alloc<<<1, kTopkBlock, 0, s>>>(a);
             diffkv_build<<<units, kTopkBlock, 0, s>>>(a);
             return launched("DiffKV build");
         }

@@ -26,6 +26,7 @@ MAX_TIERS = 2
 
 EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
            "minikv_prefill_build", "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
+           "kvq_pages_init", "kvq_pages_release",
            "kvq_decode_workspace_bytes", "kvq_tier_bytes",
            "kvq_last_error", "kvq_device_status", "kvq_debug_withhold_copy", "kvq_version"]
 
@@ -42,7 +43,10 @@ class KvqTier(ctypes.Structure):
                 ("k_codes", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("k_zero", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("v_zero", ctypes.c_void_p),
-                ("token_id", ctypes.c_void_p), ("count", ctypes.c_void_p)]
+                ("token_id", ctypes.c_void_p), ("count", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("page_owner", ctypes.c_void_p),
+                ("free_ring", ctypes.c_void_p), ("ring_ctr", ctypes.c_void_p),
+                ("max_pages", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
 
 
 class KvqCache(ctypes.Structure):
@@ -87,6 +91,8 @@ def lib():
         L.requant_demote.argtypes = [ctypes.POINTER(KvqCache), i32, ctypes.POINTER(KvqPolicyParams),
                                      i32, vp]
         L.minikv_prefill_build.argtypes = [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp, i32, i32, vp, vp]
+        L.kvq_pages_init.argtypes = [ctypes.POINTER(KvqCache), vp]
+        L.kvq_pages_release.argtypes = [ctypes.POINTER(KvqCache), vp, vp]
         L.decode_attn_qkv.argtypes = [vp, vp, vp, ctypes.POINTER(KvqCache), f32, vp, vp, vp, sz, vp]
         L.decode_attn_qkv_static.argtypes = [vp, vp, vp, ctypes.POINTER(KvqCache), f32, vp, vp, vp]
         L.decode_attn_qkv_static.restype = ctypes.c_int
@@ -98,7 +104,7 @@ def lib():
         L.kvq_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.kvq_debug_withhold_copy.argtypes = [i32]
         for name in ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
-                     "minikv_prefill_build", "requant_demote", "decode_attn_qkv", "kvq_device_status", "kvq_debug_withhold_copy"]:
+                     "minikv_prefill_build", "requant_demote", "kvq_pages_init", "kvq_pages_release", "decode_attn_qkv", "kvq_device_status", "kvq_debug_withhold_copy"]:
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -273,6 +279,9 @@ class TierSpec:
     cap: int
 
 
+PAGE_TOKENS = 128
+
+
 @dataclass
 class Tier:
     spec: TierSpec
@@ -284,6 +293,22 @@ class Tier:
     v_zero: torch.Tensor
     token_id: torch.Tensor
     count: torch.Tensor
+    # paged tiers (DiffKV): the arrays above are [n_pages, PAGE_TOKENS, ...]
+    page_table: torch.Tensor = None     # [units, max_pages] int32
+    page_owner: torch.Tensor = None     # [n_pages] int32
+    free_ring: torch.Tensor = None      # [n_pages] int32
+    ring_ctr: torch.Tensor = None       # [2] (head, tail)
+    max_pages: int = 0
+    n_pages: int = 0
+
+    def rows_of(self, u):
+        """Flat row indices (into the arrays viewed as [rows, ...]) of unit u's slots 0..count-1."""
+        c = int(self.count[u].item())
+        if self.page_table is None:
+            return torch.arange(u * self.spec.cap, u * self.spec.cap + c)
+        pt = self.page_table[u].cpu()
+        s = torch.arange(c)
+        return pt[s // PAGE_TOKENS].long() * PAGE_TOKENS + s % PAGE_TOKENS
 
 
 @dataclass
@@ -325,10 +350,14 @@ class Cache:
         d.n_tiers = len(self.tiers)
         for i, t in enumerate(self.tiers):
             s = t.spec
+            pg = t.page_table is not None
             d.tier[i] = KvqTier(s.k_bits, s.v_bits, s.k_axis, s.cap, t.k_codes.data_ptr(),
                                 t.k_scale.data_ptr(), t.k_zero.data_ptr(), t.v_codes.data_ptr(),
                                 t.v_scale.data_ptr(), t.v_zero.data_ptr(), t.token_id.data_ptr(),
-                                t.count.data_ptr())
+                                t.count.data_ptr(),
+                                t.page_table.data_ptr() if pg else None, t.page_owner.data_ptr() if pg else None,
+                                t.free_ring.data_ptr() if pg else None, t.ring_ctr.data_ptr() if pg else None,
+                                t.max_pages, t.n_pages)
         d.res_cap, d.nr = self.res_cap, self.nr
         d.res_k, d.res_v = self.res_k.data_ptr(), self.res_v.data_ptr()
         d.res_token_id = self.res_token_id.data_ptr()
@@ -354,6 +383,21 @@ class Cache:
         return tot
 
 
+def _alloc_paged_tier(units, D, G, spec, n_pages, device):
+    """A tier whose slots live in a pool of n_pages pages of PAGE_TOKENS slots shared by the units."""
+    max_pages = (spec.cap + PAGE_TOKENS - 1) // PAGE_TOKENS
+    spec = TierSpec(spec.k_bits, spec.v_bits, spec.k_axis, max_pages * PAGE_TOKENS)
+    pool = _alloc_tier(n_pages, D, G, TierSpec(spec.k_bits, spec.v_bits, spec.k_axis, PAGE_TOKENS), device)
+    i32 = torch.int32
+    return Tier(spec, pool.k_codes, pool.k_scale, pool.k_zero, pool.v_codes, pool.v_scale, pool.v_zero,
+                pool.token_id, torch.zeros((units,), dtype=i32, device=device),
+                page_table=torch.full((units, max_pages), -1, dtype=i32, device=device),
+                page_owner=torch.full((n_pages,), -1, dtype=i32, device=device),
+                free_ring=torch.arange(n_pages, dtype=i32, device=device),
+                ring_ctr=torch.tensor([0, n_pages], dtype=torch.int32, device=device),
+                max_pages=max_pages, n_pages=n_pages)
+
+
 def _alloc_tier(units, D, G, spec, device):
     spec = TierSpec(spec.k_bits, spec.v_bits, spec.k_axis, (spec.cap + 31) // 32 * 32)
     cap = spec.cap
@@ -372,13 +416,19 @@ def _alloc_tier(units, D, G, spec, device):
 
 
 def make_cache(B, Hq, Hkv, D, G, dtype, policy, tiers, nr, res_cap=None, score_cap=0, hi_den=5,
-               device="cuda"):
-    """Allocates every array of a cache (torch device memory) and its descriptor."""
+               device="cuda", pages=None):
+    """Allocates every array of a cache (torch device memory) and its descriptor.  `pages`
+    (DiffKV): a pool size in pages per tier (None for a fixed per-unit tier); a paged
+    tier's spec.cap is then the most slots one unit may hold.  Paged caches are emptied
+    with pages_init before their first build."""
     units = B * Hkv
     if res_cap is None:
         res_cap = nr + G if policy == POLICY_MINIKV else nr + 1
+    pages = pages or [None] * len(tiers)
     c = Cache(B=B, Hq=Hq, Hkv=Hkv, D=D, G=G, dtype=dtype, policy=policy,
-              tiers=[_alloc_tier(units, D, G, s, device) for s in tiers], nr=nr, res_cap=res_cap,
+              tiers=[_alloc_tier(units, D, G, s, device) if n is None
+                     else _alloc_paged_tier(units, D, G, s, n, device) for s, n in zip(tiers, pages)],
+              nr=nr, res_cap=res_cap,
               res_k=torch.zeros((units, res_cap, D), dtype=dtype, device=device),
               res_v=torch.zeros((units, res_cap, D), dtype=dtype, device=device),
               res_token_id=torch.full((units, res_cap), -1, dtype=torch.int32, device=device),
@@ -393,6 +443,19 @@ def make_cache(B, Hq, Hkv, D, G, dtype, policy, tiers, nr, res_cap=None, score_c
         c.cum_score = torch.zeros((units, score_cap), dtype=torch.float32, device=device)
     c._make_desc()
     return c
+
+
+def pages_init(cache, stream=None):
+    """Empties every paged tier (free ring 0 .. n_pages-1, no owners, no table entries)."""
+    _check(lib().kvq_pages_init(ctypes.byref(cache.desc), _stream(stream)))
+
+
+def pages_release(cache, mask, stream=None):
+    """Returns every page of the units with mask[u] != 0 (int32 [B*Hkv] CUDA tensor)."""
+    _cuda(mask)
+    if mask.dtype != torch.int32 or mask.numel() != cache.units:
+        raise ValueError("mask must be int32 [B * Hkv]")
+    _check(lib().kvq_pages_release(ctypes.byref(cache.desc), _ptr(mask), _stream(stream)))
 
 
 def requant_demote(cache, step, k_src=None, v_src=None, sel_idx=None, n_sel=0, colscore=None,

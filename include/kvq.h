@@ -93,7 +93,31 @@ typedef struct {
     uint16_t* v_zero;           /* (device) */
     int32_t* token_id;          /* (device) */
     int32_t* count;             /* (device) */
+    /* Paged storage (DiffKV tiers only; page_table == NULL: the fixed per-unit
+     * layout above).  [DiffKV-J] key_machinery / core_discovery: a GPU-resident
+     * manager with unified pages, a circular free page list and a
+     * bidirectional page table, free pages compacted in parallel.  Here a page
+     * holds KVQ_PAGE_TOKENS slots of this tier; the tier's pool of n_pages
+     * pages is shared by every unit of the layer.  The arrays above are then
+     * laid out with the page in place of the unit and KVQ_PAGE_TOKENS in place
+     * of cap (k_codes [page][KVQ_PAGE_TOKENS][D*k_bits/32], ..., token_id
+     * [page][KVQ_PAGE_TOKENS]); count [u] stays per unit and cap is the
+     * logical capacity per unit, max_pages * KVQ_PAGE_TOKENS.
+     *   page_table [u][max_pages]: physical page of logical page i of unit u,
+     *     -1 if none (slot s of unit u lives in page page_table[u][s / P] at
+     *     row s mod P, P = KVQ_PAGE_TOKENS).
+     *   page_owner [n_pages]: u * max_pages + i for the page at logical
+     *     position i of unit u, -1 when free (the reverse direction).
+     *   free_ring [n_pages] and ring_ctr [2] = {head, tail}: the free pages are
+     *     free_ring[k mod n_pages] for head <= k < tail (monotone counters). */
+    int32_t* page_table;        /* (device) */
+    int32_t* page_owner;        /* (device) */
+    int32_t* free_ring;         /* (device) */
+    uint32_t* ring_ctr;         /* (device) */
+    int32_t max_pages, n_pages;
 } kvq_tier;
+
+#define KVQ_PAGE_TOKENS 128
 
 /* The compressed cache of one attention layer.  Plain struct of device
  * pointers, filled by the caller (sizes from kvq_cache_bytes()).
@@ -253,6 +277,15 @@ kvq_status minikv_prefill_build(kvq_cache* c, const void* k, const void* v, int 
  *             position) over tiers 0,1 plus that token form the set S; it
  *             enters INT4 (tier 0) if in S else INT2 (tier 1); INT4 tokens
  *             outside S are re-quantised to INT2 from their dequantised values.
+ *   Paged DiffKV tiers: step 0 first returns every page the units hold to
+ *   the free ring (units in order, pages in logical order), then gives each
+ *   unit ceil(n / KVQ_PAGE_TOKENS) pages for its n tokens of the tier, taken
+ *   from the ring head as one run per unit in unit order (exclusive prefix
+ *   sum of the demands), and records them in both directions of the page
+ *   table; a step whose leaving token opens a new page takes one page from
+ *   the ring head (an atomic pop; which unit gets which page then depends on
+ *   the order the units run in).  An empty ring is reported as KVQ_EDEVICE
+ *   by kvq_device_status and the token is not stored.
  *   p may be NULL for step > 0. */
 kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params* p, int step,
                           void* stream);
@@ -305,6 +338,21 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* c);
  *   the GPU, on any streams, race and give wrong results. */
 kvq_status decode_attn_qkv_static(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
                                   float sm_scale, void* o, float* lse_out, void* stream);
+
+/* kvq_pages_init -- empties every paged tier of the cache: the free ring
+ * holds pages 0 .. n_pages-1 in order (head 0, tail n_pages), every page is
+ * free (page_owner -1), every page table entry is -1 and every count 0.
+ * Call once before the first requant_demote(step 0) of a paged cache. */
+kvq_status kvq_pages_init(kvq_cache* c, void* stream);
+
+/* kvq_pages_release -- a request is done: every page of the units u with
+ * release_mask[u] != 0 (device, [B*Hkv] int32) goes back to the free ring,
+ * the units in order, each unit's pages in logical order, written at the
+ * ring tail at offsets given by an exclusive prefix sum of the released
+ * counts (the parallel compaction of [DiffKV-J]); their tier counts,
+ * residual and position are reset to empty.  Unpaged tiers only have their
+ * counts reset. */
+kvq_status kvq_pages_release(kvq_cache* c, const int32_t* release_mask, void* stream);
 
 /* Bytes each device array of a cache with these sizes needs; out[i] in the
  * order of the kvq_cache fields (see kvq_cache_layout in the Python

@@ -35,12 +35,33 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), n
 
 
-def test_struct_layout_matches_header():
+def test_struct_layout_matches_header(tmp_path):
+    """The binding's ctypes structs have the header's sizes and field offsets (compiled with
+    the host C compiler from include/kvq.h)."""
+    import shutil
+    import subprocess
     from bit_mixed_precision_gb300 import kvq
-    # 4 int32 + 8 pointers
-    assert ctypes.sizeof(kvq.KvqTier) == 16 + 8 * 8
-    # 8 int32, 2 tiers, 2 int32, 9 pointers, 2 int32
-    assert ctypes.sizeof(kvq.KvqCache) == 32 + 2 * 80 + 8 + 9 * 8 + 8
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    inc = os.path.join(ROOT, "include")
+    fields = {"kvq_tier": kvq.KvqTier, "kvq_cache": kvq.KvqCache, "kvq_policy_params": kvq.KvqPolicyParams}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kvq.h"', "int main(void) {"]
+    for cname, py in fields.items():
+        lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", inc, str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, py in fields.items():
+        assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)
 
 
 def test_host_validation_without_gpu(L):
