@@ -66,7 +66,7 @@ WORKLOADS = {
                     hh=None, layer=None, n_layers=32, rw=25, n_out=0, out_scale=1.0,
                     key_std=0.5, dtype="f16", sweep=True),
     "diffkv": dict(policy="diffkv", B=32, Hq=40, Hkv=8, D=128, T=8192, steps=512, nr=64, n_out=0,
-                   out_scale=1.0, dtype="f16"),
+                   out_scale=1.0, dtype="f16", paged=True),
     "mikv": dict(policy="mikv", B=64, Hq=32, Hkv=8, D=128, T=32768, steps=1024, nr=128, n_out=1,
                  out_scale=12.0, dtype="bf16"),
 }
@@ -230,10 +230,24 @@ class Hot:
             self.n_high = torch.from_numpy(np.floor(f[:, 0] * nc).astype(np.int32)).to(dev)
             self.n_low = torch.from_numpy(np.floor(f[:, 1] * nc).astype(np.int32)).to(dev)
             caps = [int(self.n_high.max()) + steps + G, int(self.n_low.max()) + steps + G]
+            pages = None
+            if wl.get("paged"):
+                # page pools sized for every unit's worst case over the run (its build tokens
+                # plus every window exit), instead of the largest unit's capacity for all
+                P = kvq.PAGE_TOKENS
+                pages = [int(((x.cpu().numpy().astype(np.int64) + steps + P - 1) // P).sum())
+                         for x in (self.n_high, self.n_low)]
             self.cache = kvq.make_cache(B, Hq, Hkv, D, G, self.dtype, kvq.POLICY_DIFFKV,
                                         [kvq.TierSpec(8, 4, kvq.AXIS_TOKEN, caps[0]),
-                                         kvq.TierSpec(4, 2, kvq.AXIS_TOKEN, caps[1])], nr=nr, device=dev)
-            self.launches_per_step = 2 + 1 + 2 * steps
+                                         kvq.TierSpec(4, 2, kvq.AXIS_TOKEN, caps[1])], nr=nr, device=dev,
+                                        pages=pages)
+            if pages:
+                kvq.pages_init(self.cache)
+            self.pool_bytes = self.cache.tier_nbytes()
+            self.fixed_bytes = sum(kvq.lib().kvq_tier_bytes(B * Hkv, D, G, s.k_bits, s.v_bits, s.k_axis,
+                                                            (c + 31) // 32 * 32, None)
+                                   for s, c in zip([kvq.TierSpec(8, 4, 1, 0), kvq.TierSpec(4, 2, 1, 0)], caps))
+            self.launches_per_step = 2 + 1 + (1 if wl.get("paged") else 0) + 2 * steps
         else:
             nq = T - nr + steps
             self.cache = kvq.make_cache(B, Hq, Hkv, D, G, self.dtype, kvq.POLICY_MIKV,
@@ -653,6 +667,8 @@ def run_ours(args, wl, rank, world):
                              "frac": pre_tf / tf_peak,
                              "peak_source": f"{peak_src} bf16_tflops (burst)"},
         "e2e": e2e,
+        **({"pages": {"pool_bytes": hot.pool_bytes, "fixed_capacity_bytes": hot.fixed_bytes,
+                      "page_tokens": kvq.PAGE_TOKENS}} if wl.get("paged") else {}),
         "gpu_launches": hot.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }

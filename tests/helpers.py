@@ -69,11 +69,13 @@ def selection_agrees(gpu_sel, ref_sel, ref_scores, k, w):
 
 def gpu_tier_rows(tier, u):
     """{token id: (k codes, k scale, k zero, v codes, v scale, v zero)} of unit u of a
-    per-token tier, as uint32 / uint16 arrays."""
-    c = int(tier.count[u].item())
-    ids = tier.token_id[u, :c].cpu().numpy()
-    kc, ks, kz = u32(tier.k_codes[u, :c]), u16(tier.k_scale[u, :c]), u16(tier.k_zero[u, :c])
-    vc, vs, vz = u32(tier.v_codes[u, :c]), u16(tier.v_scale[u, :c]), u16(tier.v_zero[u, :c])
+    per-token tier (fixed per-unit arrays or page pools), as uint32 / uint16 arrays."""
+    rows = tier.rows_of(u).to(tier.token_id.device)
+    c = len(rows)
+    pick = lambda x: x.reshape(-1, *x.shape[2:]).index_select(0, rows)
+    ids = pick(tier.token_id).cpu().numpy()
+    kc, ks, kz = u32(pick(tier.k_codes)), u16(pick(tier.k_scale)), u16(pick(tier.k_zero))
+    vc, vs, vz = u32(pick(tier.v_codes)), u16(pick(tier.v_scale)), u16(pick(tier.v_zero))
     return {int(ids[i]): (kc[i], ks[i], kz[i], vc[i], vs[i], vz[i]) for i in range(c)}
 
 

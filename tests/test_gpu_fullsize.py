@@ -34,9 +34,10 @@ pytestmark = pytest.mark.gpu
 G = 32
 
 
-def _hot(name, steps):
+def _hot(name, steps, **over):
     wl = dict(bench.WORKLOADS[name])
     wl["steps"] = steps
+    wl.update(over)
     return wl, bench.Hot(wl, torch.device("cuda", 0), seed=0)
 
 
@@ -106,11 +107,13 @@ def test_fullsize_pyramid_layer16():
         assert np.array_equal(u32(t0.v_codes[u, :npk]), units[u].vw.view(np.uint32))
 
 
-def test_fullsize_diffkv():
+@pytest.mark.parametrize("paged", [True, False])
+def test_fullsize_diffkv(paged):
     """DiffKV: GQA 40/8, batch 32, prompt 8192, K8V4 / K4V2 / prune with per-head
-    Dirichlet(2,5,3) fractions, 64-token window; 24 decode steps, one window exit each."""
+    Dirichlet(2,5,3) fractions, 64-token window; 24 decode steps, one window exit each;
+    the tiers in page pools (the benchmark's layout) and in fixed per-unit arrays."""
     steps = 24
-    wl, hot = _hot("diffkv", 512)
+    wl, hot = _hot("diffkv", 512, paged=paged)
     B, Hq, Hkv, D, T, W = wl["B"], wl["Hq"], wl["Hkv"], wl["D"], wl["T"], wl["nr"]
     g = Hq // Hkv
     _check_prefill(hot, [(0, 0), (31, 39)], np.array([0, 63, 5000, T - 1]))
@@ -137,6 +140,15 @@ def test_fullsize_diffkv():
     for u in sample:
         assert_tiers_equal(gpu_tier_rows(hot.cache.tiers[0], u), oracle_tier_rows(units[u].high), f"K8V4 u{u}")
         assert_tiers_equal(gpu_tier_rows(hot.cache.tiers[1], u), oracle_tier_rows(units[u].low), f"K4V2 u{u}")
+    if paged:
+        for tier in hot.cache.tiers:
+            pt = tier.page_table.cpu().numpy()
+            owner = tier.page_owner.cpu().numpy()
+            cnt = tier.count.cpu().numpy()
+            for u in range(B * Hkv):
+                k = int((pt[u] >= 0).sum())
+                assert k == (cnt[u] + kvq.PAGE_TOKENS - 1) // kvq.PAGE_TOKENS
+                assert np.array_equal(owner[pt[u, :k]], u * tier.max_pages + np.arange(k))
 
 
 def test_fullsize_mikv():
