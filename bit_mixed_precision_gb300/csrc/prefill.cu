@@ -42,6 +42,9 @@ constexpr uint32_t kKVHalf = kBN * 128;          // one 64-row x 64-column swizz
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
+// pass 2: two warpgroups sum the exponentials (each half of a tile's query columns), then
+// one TMA warp and one MMA warp
+constexpr int kP2Threads = 320;
 
 // Shared memory maps (offsets from a 1024-aligned base) for head dim D.
 template <int D> struct Layout {
@@ -59,7 +62,8 @@ template <int D> struct Layout {
     static constexpr uint32_t P2_K = 0;
     static constexpr uint32_t P2_Q = P2_K + kTileBytes;        // 2 stages
     static constexpr uint32_t P2_LSE = P2_Q + 2 * kTileBytes;  // 2 x 128 floats
-    static constexpr uint32_t P2_BAR = P2_LSE + 2 * kTile * 4;
+    static constexpr uint32_t P2_RED = P2_LSE + 2 * kTile * 4; // the second warpgroup's sums and flags
+    static constexpr uint32_t P2_BAR = P2_RED + 2 * kTile * 4;
     static constexpr uint32_t P2_SMEM = P2_BAR + 256 + 1024;
 };
 
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(192, 2)
 }
 
 template <typename T, int AB, int D>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(kP2Threads, 2)
     prefill_pass2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const float* __restrict__ lse, float* __restrict__ colscore, int T_len,
                          int Hq, int Hkv, int n_t, float scale_log2, int q_first) {
@@ -413,21 +417,21 @@ __global__ void __launch_bounds__(192, 2)
             mbar_init(BAR(C_QF + s), 1);
             mbar_init(BAR(C_QE + s), 1);
             mbar_init(BAR(C_SF + s), 1);
-            mbar_init(BAR(C_SFREE + s), 4);
+            mbar_init(BAR(C_SFREE + s), 8);
         }
         mbar_init(BAR(C_DRAIN), 1);
-        mbar_init(BAR(C_LSE), 128);
-        mbar_init(BAR(C_LSE + 1), 128);
+        mbar_init(BAR(C_LSE), 256);
+        mbar_init(BAR(C_LSE + 1), 256);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(smem_u32(tmem_slot), 256);
+    if (warp == 9) tmem_alloc(smem_u32(tmem_slot), 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(192, 2)
             for (int st = 0; st < 2; ++st)
                 if (last[st] >= 0) mbar_wait(BAR(C_QF + st), (last[st] >> 1) & 1, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t idS = idesc_f16(AB, 128, 128, 0);
             bool ok = mbar_wait(BAR(C_KF), 0, abort_flag);
@@ -477,21 +481,25 @@ __global__ void __launch_bounds__(192, 2)
             mbar_wait(BAR(C_DRAIN), 0, nullptr);
         }
     } else {
-        const int r = threadIdx.x;
+        // warpgroup wg (0: warps 0-3, 1: warps 4-7) sums query columns 64 wg .. 64 wg + 63 of
+        // every tile; thread r of either owns key r (TMEM lane r)
+        const int wg = warp >> 2;
+        const int r = threadIdx.x & (kTile - 1);
         const int j = kt * kTile + r;                       // key position of this thread
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int cb = 64 * wg;                             // this warpgroup's first column
         float acc = 0.0f;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int buf = it & 1;
             const int qt = kt + it0 + it;
             const int qi_own = qt * kTile + r;
-            // minus the base-2 lse of each query (-inf past the prompt: exponent -inf)
-            lse_s[buf * kTile + r] = qi_own < T_len && qi_own >= q_first
-                                         ? -(lse[(size_t)bh * T_len + qi_own] * kLog2e)
-                                         : -__int_as_float(0x7f800000);
-            // buffer buf is rewritten two tiles later, after every thread has
-            // arrived for the tile in between, i.e. finished reading this one
+            // minus the base-2 lse of each query (-inf past the prompt: exponent -inf);
+            // warpgroup 0 writes all 128, both arrive (so neither runs two tiles ahead)
+            if (wg == 0)
+                lse_s[buf * kTile + r] = qi_own < T_len && qi_own >= q_first
+                                             ? -(lse[(size_t)bh * T_len + qi_own] * kLog2e)
+                                             : -__int_as_float(0x7f800000);
             mbar_arrive(BAR(C_LSE + buf));
             if (!warp_wait(BAR(C_LSE + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
             if (!warp_wait(BAR(C_SF + buf), (it >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -504,8 +512,6 @@ __global__ void __launch_bounds__(192, 2)
             for (int e = 0; e < 8; ++e) tsp[e] = 0.0f;
             const int qbase = qt * kTile;
             const bool diag = it0 == 0 && it == 0;
-            // the 128 columns in four TMEM loads of 32, the next one in flight
-            // while the current one is summed
             // off the diagonal, exponents and sums go two queries per instruction
             // (packed float32 pairs; partial sum e of the pairs holds queries c with
             // c mod 8 = 2e, 2e + 1)
@@ -528,23 +534,19 @@ __global__ void __launch_bounds__(192, 2)
                     }
                 }
             };
-            const uint32_t tb = tmem + lane_base + (uint32_t)buf * 128u;
+            // this warpgroup's 64 columns in two TMEM loads of 32, the second in flight
+            // while the first is summed
+            const uint32_t tb = tmem + lane_base + (uint32_t)buf * 128u + (uint32_t)cb;
             float s0[32], s1[32];
             tmem_ld32(tb, s0);
             tmem_wait_ld();
             tmem_ld32(tb + 32u, s1);
-            sum32(s0, 0);
-            tmem_wait_ld();
-            tmem_ld32(tb + 64u, s0);
-            sum32(s1, 32);
-            tmem_wait_ld();
-            tmem_ld32(tb + 96u, s1);
-            sum32(s0, 64);
+            sum32(s0, cb);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C_SFREE + buf));
-            sum32(s1, 96);
+            sum32(s1, cb + 32);
             if (!diag) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) f2_unpack(tsp2[e], tsp[2 * e], tsp[2 * e + 1]);
@@ -552,12 +554,24 @@ __global__ void __launch_bounds__(192, 2)
             acc += ((tsp[0] + tsp[1]) + (tsp[2] + tsp[3])) + ((tsp[4] + tsp[5]) + (tsp[6] + tsp[7]));
         }
         if (!ok) give_up(abort_flag);
-        if (ok && j < T_len) colscore[(size_t)bh * T_len + j] = acc;
+        // warpgroup 1's sums join warpgroup 0's, which writes the column
+        float* red = reinterpret_cast<float*>(gbase + Lay::P2_RED);
+        int* red_ok = reinterpret_cast<int*>(gbase + Lay::P2_RED + kTile * 4);
+        if (wg == 1) {
+            red[r] = acc;
+            red_ok[r] = ok ? 1 : 0;
+        }
+        named_barrier_sync(1, 256);
+        if (wg == 0) {
+            ok = ok && red_ok[r] != 0;
+            acc += red[r];
+            if (ok && j < T_len) colscore[(size_t)bh * T_len + j] = acc;
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, 256);
+    if (warp == 9) tmem_dealloc(tmem, 256);
 }
 
 // ------------------------------------------------------------------ host
@@ -629,8 +643,8 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
         }
     }
     if (colscore) {
-        prefill_pass2_kernel<T, AB, D><<<g1, 192, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
-                                                                      Hkv, n_t, scale_log2, q_first);
+        prefill_pass2_kernel<T, AB, D><<<g1, kP2Threads, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
+                                                                             Hkv, n_t, scale_log2, q_first);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error("prefill pass 2 launch: %s", cudaGetErrorString(e));
