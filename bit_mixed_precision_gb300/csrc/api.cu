@@ -178,7 +178,8 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
         const bool ok_combo =
             (tr.k_axis == KVQ_AXIS_CHANNEL && tr.k_bits == 2 && tr.v_bits == 2) ||
             (c->D == 128 && tr.k_axis == KVQ_AXIS_TOKEN &&
-             ((tr.k_bits == 8 && tr.v_bits == 4) || (tr.k_bits == 4 && tr.v_bits == 2) ||
+             ((tr.k_bits == 8 && tr.v_bits == 4) || (tr.k_bits == 4 && tr.v_bits == 8) ||
+              (tr.k_bits == 4 && tr.v_bits == 2) ||
               (tr.k_bits == 4 && tr.v_bits == 4) || (tr.k_bits == 2 && tr.v_bits == 2)));
         KVQ_REQUIRE(ok_combo, KVQ_EUNSUPPORTED, "%s: tier %d format K%dV%d axis %d not built", who, t,
                     tr.k_bits, tr.v_bits, tr.k_axis);

@@ -1193,7 +1193,11 @@ __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const floa
         }
         // codes of channel c for the token pairs: f16x2 (1 + c_a / 2^VB, 1 + c_b / 2^VB)
         auto pair = [&](uint32_t wa, uint32_t wb, bool high) -> uint32_t {
-            if (VB == 4) {                               // channel nibble g of the word
+            if (VB == 8) {                               // channel byte g mod 4 of the word
+                const uint32_t b = (uint32_t)(g & 3);
+                const uint32_t x = __byte_perm(wa, wb, b | ((4u + b) << 8)) << 2;
+                return (x & 0x03FC03FCu) | 0x3C003C00u;
+            } else if (VB == 4) {                        // channel nibble g of the word
                 const uint32_t sel = (uint32_t)(g >> 1) | ((uint32_t)(4 + (g >> 1)) << 8);
                 const uint32_t x = __byte_perm(wa, wb, sel) << (6 - 4 * (g & 1));
                 return (x & 0x03C003C0u) | 0x3C003C00u;
@@ -1219,15 +1223,23 @@ __device__ __forceinline__ void mma_pv(const View& v, int tl, int nt, const floa
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const int grp = mt >> 1;
-            if (VB == 4 || (mt & 1) == 0) {
+            if (VB == 8) {
+                // words 4 mt .. 4 mt + 3 hold the tile's 16 channels, four per word: rows g take
+                // word 4 mt + g / 4, rows g + 8 word 4 mt + 2 + g / 4
+                const int wo = 4 * mt + (g >> 2);
+                xa = make_uint2(ra[wo], ra[wo + 2]);
+                xb = make_uint2(rb[wo], rb[wo + 2]);
+                xc = make_uint2(rc[wo], rc[wo + 2]);
+                xd = make_uint2(rd[wo], rd[wo + 2]);
+            } else if (VB == 4 || (mt & 1) == 0) {
                 const int w0 = VB == 4 ? 2 * mt : mt;
                 xa = *reinterpret_cast<const uint2*>(ra + w0);
                 xb = *reinterpret_cast<const uint2*>(rb + w0);
                 xc = *reinterpret_cast<const uint2*>(rc + w0);
                 xd = *reinterpret_cast<const uint2*>(rd + w0);
             }
-            auto lo = [&](const uint2& x) { return VB == 4 ? x.x : ((mt & 1) ? x.y : x.x); };
-            auto hi = [&](const uint2& x) { return VB == 4 ? x.y : ((mt & 1) ? x.y : x.x); };
+            auto lo = [&](const uint2& x) { return VB >= 4 ? x.x : ((mt & 1) ? x.y : x.x); };
+            auto hi = [&](const uint2& x) { return VB >= 4 ? x.y : ((mt & 1) ? x.y : x.x); };
             uint32_t af[4];
             af[0] = scaled(pair(lo(xa), lo(xb), false), sc0[grp]);
             af[1] = scaled(pair(hi(xa), hi(xb), true), sc0[grp]);
@@ -1655,11 +1667,13 @@ __device__ void dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_
     }
     if constexpr ((FAM & 2) && D == 128 && NG >= 2) {
         if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier_mma<8, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 8) { run_tier_mma<4, KVQ_AXIS_TOKEN, 8, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier_mma<4, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier_mma<4, KVQ_AXIS_TOKEN, 4, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier_mma<2, KVQ_AXIS_TOKEN, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
     } else if constexpr ((FAM & 2) && D == 128) {
         if (ax == KVQ_AXIS_TOKEN && kb == 8 && vb == 4) { run_tier<8, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
+        if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 8) { run_tier<4, KVQ_AXIS_TOKEN, 8, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 2) { run_tier<4, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 4 && vb == 4) { run_tier<4, KVQ_AXIS_TOKEN, 4, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }
         if (ax == KVQ_AXIS_TOKEN && kb == 2 && vb == 2) { run_tier<2, KVQ_AXIS_TOKEN, 2, D, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok); return; }

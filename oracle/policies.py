@@ -181,11 +181,14 @@ def diffkv_significance(colscore, T):
 
 
 class DiffKVUnit:
-    def __init__(self, k, v, colscore, n_high, n_low, window, group):
+    def __init__(self, k, v, colscore, n_high, n_low, window, group, high_bits=(8, 4), low_bits=(4, 2)):
+        """high_bits / low_bits: (key bits, value bits) of the two tiers; K8V4 / K4V2 as the
+        DiffKV pages give them, other pairs for the codec variants (the K4V8 mirror the
+        DiffKV verdict JSON lists among its negative results)."""
         T, d = k.shape
         self.W, self.group, self.d = window, group, d
-        self.high = TokenTier(8, 4, group, d)
-        self.low = TokenTier(4, 2, group, d)
+        self.high = TokenTier(high_bits[0], high_bits[1], group, d)
+        self.low = TokenTier(low_bits[0], low_bits[1], group, d)
         self.pruned = []
         nc = T - window
         sig = diffkv_significance(colscore, T)

@@ -138,3 +138,40 @@ def test_diffkv_pipeline():
         if agree[u]:
             assert_tiers_equal(gpu_tier_rows(cache.tiers[0], u), oracle_tier_rows(units[u].high))
             assert_tiers_equal(gpu_tier_rows(cache.tiers[1], u), oracle_tier_rows(units[u].low))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(10, 2), (2, 2)])
+def test_diffkv_k4v8_mirror(Hq, Hkv):
+    """The K4V8 mirror of the high tier (a codec variant the DiffKV pages report as a
+    negative result): build, window exits and decode against the oracle with the same
+    formats, on the tensor-core path (GQA 5) and the single-head CUDA-core path."""
+    B, T, D, steps = 2, 512, 128, 10
+    g = Hq // Hkv
+    x = inputs.make_qkv(B, Hq, Hkv, T + steps, D, seed=61)
+    cs = inputs.random_scores(B, Hq, T, seed=61) + 0.01
+    n_high, n_low = _counts(B, Hkv, T, 61)
+    caps = [int(max(n_high)) + steps + 1, int(max(n_low)) + steps + 1]
+    cache = kvq.make_cache(B, Hq, Hkv, D, G, torch.float16, kvq.POLICY_DIFFKV,
+                           [kvq.TierSpec(4, 8, kvq.AXIS_TOKEN, caps[0]), kvq.TierSpec(4, 2, kvq.AXIS_TOKEN, caps[1])],
+                           nr=W)
+    kvq.requant_demote(cache, 0, k_src=x.k[:, :, :T].contiguous().cuda(), v_src=x.v[:, :, :T].contiguous().cuda(),
+                       colscore=cs.cuda(), n_high=torch.from_numpy(n_high).cuda(), n_low=torch.from_numpy(n_low).cuda())
+    units = [OP.DiffKVUnit(np_(x.k[u // Hkv, u % Hkv, :T]), np_(x.v[u // Hkv, u % Hkv, :T]),
+                           np_(cs[u // Hkv, (u % Hkv) * g:(u % Hkv + 1) * g]), int(n_high[u]), int(n_low[u]), W, G,
+                           high_bits=(4, 8)) for u in range(B * Hkv)]
+    for u in range(B * Hkv):
+        assert_tiers_equal(gpu_tier_rows(cache.tiers[0], u), oracle_tier_rows(units[u].high), f"K4V8 u{u}")
+    scale = 1.0 / math.sqrt(D)
+    for t in range(steps):
+        qd = torch.randn((B, Hq, D), generator=torch.Generator().manual_seed(300 + t)).half()
+        kd, vd = x.k[:, :, T + t].contiguous(), x.v[:, :, T + t].contiguous()
+        od, _ = kvq.decode_attn_qkv(qd.cuda(), kd.cuda(), vd.cuda(), cache, scale)
+        kvq.requant_demote(cache, t + 1)
+        for u in range(B * Hkv):
+            ro, _, _ = units[u].step(T + t, np_(qd[u // Hkv, (u % Hkv) * g:(u % Hkv + 1) * g]),
+                                     np_(kd[u // Hkv, u % Hkv]), np_(vd[u // Hkv, u % Hkv]), scale)
+            assert_attn_close(od[u // Hkv, (u % Hkv) * g:(u % Hkv + 1) * g], ro, f"step {t} unit {u}")
+    assert kvq.device_status() == 0
+    for u in range(B * Hkv):
+        assert_tiers_equal(gpu_tier_rows(cache.tiers[0], u), oracle_tier_rows(units[u].high), f"K4V8 u{u}")
+        assert_tiers_equal(gpu_tier_rows(cache.tiers[1], u), oracle_tier_rows(units[u].low), f"K4V2 u{u}")
