@@ -168,8 +168,6 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
                         aligned(tr.v_codes, 16) && aligned(tr.v_scale, 16) && aligned(tr.v_zero, 16),
                     KVQ_EINVAL, "%s: tier %d arrays must be 16-byte aligned", who, t);
         if (tr.k_axis == KVQ_AXIS_CHANNEL)
-            KVQ_REQUIRE(c->G % 32 == 0, KVQ_EUNSUPPORTED, "%s: per-channel keys need G %% 32 == 0", who);
-        if (tr.k_axis == KVQ_AXIS_CHANNEL)
             KVQ_REQUIRE(tr.cap % c->G == 0, KVQ_EINVAL, "%s: tier %d cap must be a multiple of G", who, t);
         KVQ_REQUIRE(tr.k_codes && tr.k_scale && tr.k_zero && tr.v_codes && tr.v_scale && tr.v_zero &&
                         tr.token_id && tr.count,
@@ -183,8 +181,14 @@ static kvq_status check_cache(const kvq_cache* c, const char* who) {
               (tr.k_bits == 4 && tr.v_bits == 4) || (tr.k_bits == 2 && tr.v_bits == 2)));
         KVQ_REQUIRE(ok_combo, KVQ_EUNSUPPORTED, "%s: tier %d format K%dV%d axis %d not built", who, t,
                     tr.k_bits, tr.v_bits, tr.k_axis);
-        // the decode kernels take value groups (and per-token key groups) of 32 channels
-        KVQ_REQUIRE(c->G == 32, KVQ_EUNSUPPORTED, "%s: tier %d: the decode kernels are built for G = 32", who, t);
+        // the decode kernels take groups of 32 (channels of a value or per-token key, tokens of
+        // a per-channel key); the MiniKV single-head path (one query head per KV head, D = 128,
+        // 2-bit keys and values) also takes groups of 16
+        const bool g16 = c->G == 16 && tr.k_axis == KVQ_AXIS_CHANNEL && tr.k_bits == 2 && tr.v_bits == 2 &&
+                         c->D == 128 && c->Hq == c->Hkv;
+        KVQ_REQUIRE(c->G == 32 || g16, KVQ_EUNSUPPORTED,
+                    "%s: tier %d: G = %d is built for 2-bit MiniKV tiers with D = 128 and Hq == Hkv only", who, t,
+                    c->G);
         if (tr.page_table) {
             KVQ_REQUIRE(c->policy == KVQ_POLICY_DIFFKV, KVQ_EUNSUPPORTED, "%s: tier %d: only DiffKV tiers are paged",
                         who, t);
@@ -319,6 +323,7 @@ kvq_status minikv_prefill_build(kvq_cache* c, const void* k, const void* v, int 
     if (st != KVQ_OK) return st;
     KVQ_REQUIRE(c->policy == KVQ_POLICY_MINIKV, KVQ_EINVAL, "minikv_prefill_build: not a MiniKV cache");
     KVQ_REQUIRE(k && v && score && k_hh, KVQ_EINVAL, "minikv_prefill_build: null pointer");
+    KVQ_REQUIRE(c->G == 32, KVQ_EUNSUPPORTED, "minikv_prefill_build: built for G = 32 (requant_demote takes G = 16)");
     KVQ_REQUIRE(aligned(k, 16) && aligned(v, 16) && aligned(c->res_k, 16) && aligned(c->res_v, 16), KVQ_EINVAL,
                 "minikv_prefill_build: k, v and the residual ring must be 16-byte aligned");
     KVQ_REQUIRE(T > 0 && T <= 65536, KVQ_EINVAL, "minikv_prefill_build: T must be in [1, 65536]");

@@ -1396,36 +1396,54 @@ __device__ void run_tier_mma(const DecodeArgs& a, Smem<NG, 128>& sm, int t, size
 
 constexpr uint32_t kM0 = 0x00030003u, kM1 = 0x000C000Cu, kM2 = 0x00300030u, kM3 = 0x00C000C0u;
 
+template <int GK>
 struct Mk1Acc {
     float m, l;              // running reference max (warp-uniform), this lane's share of the sum
-    float o[4][2][4];        // P.V accumulators: [word pair w'][row pair P][fragment]
-    float zs[4];             // sum of p * zero of this lane's tokens, per value group
+    float o[4][2][4];        // P.V accumulators: [word quarter w'][row pair P][fragment]
+    float zs[128 / GK];      // sum of p * zero of this lane's tokens, per value group
 };
 
-template <int NG>
+// The staged chunk of the MiniKV format with group GK (compile-time sizes).
+template <int GK>
+__device__ __forceinline__ View mk1_view(int npad, const uint8_t* buf) {
+    return view_of(tier_stage_sizes(KVQ_AXIS_CHANNEL, 2, 2, npad, 128, GK), buf);
+}
+
+// GK = 32 (the configs) or 16 (the MiniKV review's default): with 16, a warp's 32 tokens
+// hold two key scale rows (q * scale columns 0, 1 and 2, 3 of the key MMAs, the logits of
+// tokens 16..31 in lanes t = 1) and the values eight 16-channel groups (all eight B
+// columns of the P.V MMAs).
+template <int NG, int GK>
 __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, size_t unit, int r, int i0,
                              int i1, int n_local, uint8_t* stage_base, bool& ok) {
     static_assert(NG == 1, "one query head per KV head");
+    static_assert(GK == 32 || GK == 16, "groups of 32 or 16");
     constexpr int TPW = Cfg<NG>::TPW;
-    static_assert(TPW == 32, "one key scale row per warp and item");
+    static_assert(TPW == 32, "32 tokens per warp and item");
+    constexpr int NKR = 32 / GK;            // key scale rows per warp
+    constexpr int NGV = 128 / GK;           // value groups per token
     const UnitState& us = sm.us;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    // this warp's query fragments ([piece][k-step][t][reg], 512 B), probabilities (32 floats)
-    // and probability x value scale ([group][token] fp16)
-    uint32_t* qf = reinterpret_cast<uint32_t*>(&qf_rows<NG>(a, sm, warp)[0][0]);
+    // this warp's query fragments ([piece = 2 row + hi/lo][k-step][t][reg], 512 B per key row),
+    // probabilities (32 floats) and probability x value scale ([group][token] fp16: over the
+    // probabilities for GK = 32, after the fragments for GK = 16)
+    uint32_t* qf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&sm) + a.qf_off +
+                                               (size_t)warp * (GK == 32 ? 512 : 1536));
     float* pw = &sm.lg[warp][0][0];
-    uint16_t* psw = reinterpret_cast<uint16_t*>(pw);            // same bytes, after the probabilities are read
+    uint16_t* psw = GK == 32 ? reinterpret_cast<uint16_t*>(pw) : reinterpret_cast<uint16_t*>(qf + 256);
     const uint32_t* zero = reinterpret_cast<const uint32_t*>(&sm.qa[0][0]);
-    // B-fragment sources: lanes g = 0 / 1 read the hi / lo query rows, g = 0..3 the value
-    // groups; the others read zeros (no per-step select)
-    const uint2* qfb = g < 2 ? reinterpret_cast<const uint2*>(qf) + g * 32 + t
-                             : reinterpret_cast<const uint2*>(zero) + t;
-    const uint32_t* psb = g < 4 ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : zero + t;
+    // B-fragment sources: lanes g < 2 NKR read the query pieces, g < NGV the value groups;
+    // the others read zeros (no per-step select)
+    const uint2* qfb = g < 2 * NKR ? reinterpret_cast<const uint2*>(qf) + g * 32 + t
+                                   : reinterpret_cast<const uint2*>(zero) + t;
+    const uint32_t* psb = g < NGV ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : zero + t;
+    const int tv = GK == 32 ? 0 : (g >> 2);       // the lane t that holds lane group g's logits
     const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);   // channels 4 lane .. + 3
     const uint32_t bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
-    // The copies of this tier's next items, one array per lane (lanes 0..5): a chunk of npad
+    // the copies of this tier's next items, one array per lane (lanes 0..5): a chunk of npad
     // tokens stages array k at bytes [off_k npad, off_k npad + bytes_k npad) of its buffer,
-    // from base_k + (chunk index) * 128 bytes_k (compile-time sizes of the format).
+    // from base_k + (chunk index) * 128 bytes_k (compile-time sizes of the format)
+    constexpr uint32_t kSB = 256 / GK;           // scale (or zero) bytes per token, keys and values
     const TierArgs& ta = a.tier[tier];
     const uint8_t* cp_src = nullptr;
     uint32_t cp_off = 0u, cp_bpt = 0u;
@@ -1433,52 +1451,56 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
         const size_t cap = (size_t)ta.cap;
         switch (lane) {
             case 0: cp_src = reinterpret_cast<const uint8_t*>(ta.k_codes + unit * (cap / 16) * 128); cp_off = 0; cp_bpt = 32; break;
-            case 1: cp_src = reinterpret_cast<const uint8_t*>(ta.k_scale + unit * (cap / 32) * 128); cp_off = 32; cp_bpt = 8; break;
-            case 2: cp_src = reinterpret_cast<const uint8_t*>(ta.k_zero + unit * (cap / 32) * 128); cp_off = 40; cp_bpt = 8; break;
-            case 3: cp_src = reinterpret_cast<const uint8_t*>(ta.v_codes + unit * cap * 8); cp_off = 48; cp_bpt = 32; break;
-            case 4: cp_src = reinterpret_cast<const uint8_t*>(ta.v_scale + unit * cap * 4); cp_off = 80; cp_bpt = 8; break;
-            case 5: cp_src = reinterpret_cast<const uint8_t*>(ta.v_zero + unit * cap * 4); cp_off = 88; cp_bpt = 8; break;
+            case 1: cp_src = reinterpret_cast<const uint8_t*>(ta.k_scale + unit * (cap / GK) * 128); cp_off = 32; cp_bpt = kSB; break;
+            case 2: cp_src = reinterpret_cast<const uint8_t*>(ta.k_zero + unit * (cap / GK) * 128); cp_off = 32 + kSB; cp_bpt = kSB; break;
+            case 3: cp_src = reinterpret_cast<const uint8_t*>(ta.v_codes + unit * cap * 8); cp_off = 32 + 2 * kSB; cp_bpt = 32; break;
+            case 4: cp_src = reinterpret_cast<const uint8_t*>(ta.v_scale + unit * cap * NGV); cp_off = 64 + 2 * kSB; cp_bpt = kSB; break;
+            case 5: cp_src = reinterpret_cast<const uint8_t*>(ta.v_zero + unit * cap * NGV); cp_off = 64 + 3 * kSB; cp_bpt = kSB; break;
             default: break;
         }
     }
-    Mk1Acc acc;
+    Mk1Acc<GK> acc;
     acc.m = kNegInf;
     acc.l = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        acc.zs[i] = 0.0f;
+    for (int x = 0; x < NGV; ++x) acc.zs[x] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int P = 0; P < 2; ++P)
 #pragma unroll
             for (int f = 0; f < 4; ++f) acc.o[i][P][f] = 0.0f;
-    }
     for (int i = i0; i < i1; ++i) {
         ok = wait_item(a, sm, i, ok);
         const int j0 = (r + i * a.cluster - us.base[tier]) * kSub;
         const int n = min(kSub, us.cnt[tier] - j0);
         const int tl = warp * TPW;
         if (ok && tl < n) {
-            const View v = tier_view_c<2, KVQ_AXIS_CHANNEL, 2>((n + 31) & ~31, item_buf(a, stage_base, i));
+            const View v = mk1_view<GK>((n + 31) & ~31, item_buf(a, stage_base, i));
             const int nt = min(TPW, n - tl);
-            // -- Q' = q * scale of this scale row, as hi / lo fp16 fragments, and sum_c q z
-            float bias;
-            {
-                const uint2 s2 = *reinterpret_cast<const uint2*>(v.ks + (size_t)(tl >> 5) * 128 + 4 * lane);
-                const uint2 z2 = *reinterpret_cast<const uint2*>(v.kz + (size_t)(tl >> 5) * 128 + 4 * lane);
+            // -- Q' = q * scale of each key scale row, as hi / lo fp16 fragments, and sum_c q z
+            float bias[NKR];
+#pragma unroll
+            for (int kr = 0; kr < NKR; ++kr) {
+                const size_t ro = (size_t)(tl / GK + kr) * 128 + 4 * lane;
+                const uint2 s2 = *reinterpret_cast<const uint2*>(v.ks + ro);
+                const uint2 z2 = *reinterpret_cast<const uint2*>(v.kz + ro);
                 const float x0 = q4.x * h2lo(s2.x), x1 = q4.y * h2hi(s2.x);
                 const float x2 = q4.z * h2lo(s2.y), x3 = q4.w * h2hi(s2.y);
                 const uint32_t hi01 = pack_h2(x0, x1), hi23 = pack_h2(x2, x3);
                 const uint32_t lo01 = pack_h2(x0 - h2lo(hi01), x1 - h2hi(hi01));
                 const uint32_t lo23 = pack_h2(x2 - h2lo(hi23), x3 - h2hi(hi23));
-                bias = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
+                bias[kr] = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
                 // channel c = 16 s + 8 half + 2 tt + e sits in register half of lane tt, k-step s
                 const int s_ = lane >> 2, half = (lane & 3) >> 1, tt = 2 * (lane & 1);
-                qf[(s_ * 4 + tt) * 2 + half] = hi01;
-                qf[(s_ * 4 + tt + 1) * 2 + half] = hi23;
-                qf[64 + (s_ * 4 + tt) * 2 + half] = lo01;
-                qf[64 + (s_ * 4 + tt + 1) * 2 + half] = lo23;
-                bias = warp_sum(bias);
+                uint32_t* qh = qf + 128 * kr;
+                qh[(s_ * 4 + tt) * 2 + half] = hi01;
+                qh[(s_ * 4 + tt + 1) * 2 + half] = hi23;
+                qh[64 + (s_ * 4 + tt) * 2 + half] = lo01;
+                qh[64 + (s_ * 4 + tt + 1) * 2 + half] = lo23;
+                bias[kr] = warp_sum(bias[kr]);
             }
+            const float bias_g = NKR == 1 ? bias[0] : ((g >> 2) ? bias[NKR - 1] : bias[0]);
             __syncwarp();
             // -- logits: two MMAs (tokens 4g + {0, 1} and 4g + {2, 3}), each over two
             // accumulator chains of four k-steps
@@ -1503,17 +1525,18 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
                     mma16816(R[1][s & 1], a1, b.x, b.y);
                 }
             }
-            // -- logits of tokens 4g + j (lanes t == 0): code factor 4^j * 2^-24 out, bias in
+            // -- logits of tokens 4g + j (lanes t == tv): code factor 4^j * 2^-24 out, bias in
             float lg[4];
-            lg[0] = fmaf((R[0][0][0] + R[0][1][0]) + (R[0][0][1] + R[0][1][1]), 16777216.0f, bias);  // 2^24
-            lg[1] = fmaf((R[0][0][2] + R[0][1][2]) + (R[0][0][3] + R[0][1][3]), 4194304.0f, bias);   // 2^22
-            lg[2] = fmaf((R[1][0][0] + R[1][1][0]) + (R[1][0][1] + R[1][1][1]), 1048576.0f, bias);   // 2^20
-            lg[3] = fmaf((R[1][0][2] + R[1][1][2]) + (R[1][0][3] + R[1][1][3]), 262144.0f, bias);    // 2^18
+            lg[0] = fmaf((R[0][0][0] + R[0][1][0]) + (R[0][0][1] + R[0][1][1]), 16777216.0f, bias_g);  // 2^24
+            lg[1] = fmaf((R[0][0][2] + R[0][1][2]) + (R[0][0][3] + R[0][1][3]), 4194304.0f, bias_g);   // 2^22
+            lg[2] = fmaf((R[1][0][0] + R[1][1][0]) + (R[1][0][1] + R[1][1][1]), 1048576.0f, bias_g);   // 2^20
+            lg[3] = fmaf((R[1][0][2] + R[1][1][2]) + (R[1][0][3] + R[1][1][3]), 262144.0f, bias_g);    // 2^18
             bool valid[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) valid[j] = t == 0 && 4 * g + j < nt;
+            for (int j = 0; j < 4; ++j) valid[j] = t == tv && 4 * g + j < nt;
             float mx = fmaxf(fmaxf(valid[0] ? lg[0] : kNegInf, valid[1] ? lg[1] : kNegInf),
                              fmaxf(valid[2] ? lg[2] : kNegInf, valid[3] ? lg[3] : kNegInf));
+            if (GK != 32) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -1525,13 +1548,13 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
                 acc.m = mx;
                 acc.l *= corr;
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    acc.zs[x] *= corr;
+                for (int x = 0; x < NGV; ++x) acc.zs[x] *= corr;
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
 #pragma unroll
                     for (int P = 0; P < 2; ++P)
 #pragma unroll
                         for (int f = 0; f < 4; ++f) acc.o[x][P][f] *= corr;
-                }
             }
             {
                 float4 p;
@@ -1540,35 +1563,40 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
                 p.z = valid[2] ? ex2_approx(lg[2] - acc.m) : 0.0f;
                 p.w = valid[3] ? ex2_approx(lg[3] - acc.m) : 0.0f;
                 acc.l += (p.x + p.y) + (p.z + p.w);
-                if (t == 0) *reinterpret_cast<float4*>(pw + 4 * g) = p;
+                if (t == tv) *reinterpret_cast<float4*>(pw + 4 * g) = p;
             }
             __syncwarp();
             // -- lane = token: p times each group's value scale into [group][token], and the
             // zero points (stale slots past nt read as zero scale and zero point)
             {
                 const float p = pw[lane];
-                __syncwarp();                                    // every lane has its p: ps overwrites pw
+                __syncwarp();                                    // every lane has its p: ps may overwrite pw
                 const bool ok_t = lane < nt;
-                uint2 s2 = *reinterpret_cast<const uint2*>(v.vs + (size_t)(tl + lane) * 4);
-                uint2 z2 = *reinterpret_cast<const uint2*>(v.vz + (size_t)(tl + lane) * 4);
-                s2.x = ok_t ? s2.x : 0u;
-                s2.y = ok_t ? s2.y : 0u;
-                z2.x = ok_t ? z2.x : 0u;
-                z2.y = ok_t ? z2.y : 0u;
-                const uint32_t ps01 = pack_h2(p * h2lo(s2.x), p * h2hi(s2.x));
-                const uint32_t ps23 = pack_h2(p * h2lo(s2.y), p * h2hi(s2.y));
-                psw[0 * 32 + lane] = (uint16_t)(ps01 & 0xffffu);
-                psw[1 * 32 + lane] = (uint16_t)(ps01 >> 16);
-                psw[2 * 32 + lane] = (uint16_t)(ps23 & 0xffffu);
-                psw[3 * 32 + lane] = (uint16_t)(ps23 >> 16);
-                acc.zs[0] = fmaf(p, h2lo(z2.x), acc.zs[0]);
-                acc.zs[1] = fmaf(p, h2hi(z2.x), acc.zs[1]);
-                acc.zs[2] = fmaf(p, h2lo(z2.y), acc.zs[2]);
-                acc.zs[3] = fmaf(p, h2hi(z2.y), acc.zs[3]);
+                uint32_t sw[NGV / 2], zw[NGV / 2];
+                if constexpr (NGV == 4) {
+                    const uint2 s2 = *reinterpret_cast<const uint2*>(v.vs + (size_t)(tl + lane) * 4);
+                    const uint2 z2 = *reinterpret_cast<const uint2*>(v.vz + (size_t)(tl + lane) * 4);
+                    sw[0] = s2.x; sw[1] = s2.y; zw[0] = z2.x; zw[1] = z2.y;
+                } else {
+                    const uint4 s4 = *reinterpret_cast<const uint4*>(v.vs + (size_t)(tl + lane) * 8);
+                    const uint4 z4 = *reinterpret_cast<const uint4*>(v.vz + (size_t)(tl + lane) * 8);
+                    sw[0] = s4.x; sw[1] = s4.y; sw[2] = s4.z; sw[3] = s4.w;
+                    zw[0] = z4.x; zw[1] = z4.y; zw[2] = z4.z; zw[3] = z4.w;
+                }
+#pragma unroll
+                for (int e = 0; e < NGV / 2; ++e) {
+                    sw[e] = ok_t ? sw[e] : 0u;
+                    zw[e] = ok_t ? zw[e] : 0u;
+                    const uint32_t ps2 = pack_h2(p * h2lo(sw[e]), p * h2hi(sw[e]));
+                    psw[(2 * e) * 32 + lane] = (uint16_t)(ps2 & 0xffffu);
+                    psw[(2 * e + 1) * 32 + lane] = (uint16_t)(ps2 >> 16);
+                    acc.zs[2 * e] = fmaf(p, h2lo(zw[e]), acc.zs[2 * e]);
+                    acc.zs[2 * e + 1] = fmaf(p, h2hi(zw[e]), acc.zs[2 * e + 1]);
+                }
             }
             __syncwarp();
             // -- P.V over two k-steps of 16 tokens: B = (p s) of tokens 16 ks + 2t, + 1
-            // (b0) and + 8, + 9 (b1) in column g (group g; zeros for g >= 4)
+            // (b0) and + 8, + 9 (b1) in column g (value group g; zeros past the groups)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int k0 = 16 * ks + 2 * t;
@@ -1601,7 +1629,7 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
                 const int np = (min(kSub, us.cnt[tier] - idx * kSub) + 31) & ~31;
                 const int sb = inext & (a.stages - 1);
                 const uint32_t bar = smem_u32(&sm.bar[sb]);
-                if (lane == 0) mbar_expect_tx(bar, 96u * (uint32_t)np);
+                if (lane == 0) mbar_expect_tx(bar, (64u + 4u * kSB) * (uint32_t)np);
                 __syncwarp();
                 if (lane < 6)
                     bulk_load(smem_u32(stage_base) + (uint32_t)sb * a.stage_bytes + cp_off * (uint32_t)np,
@@ -1615,7 +1643,7 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
     // ---- merge the warp's state into its shared-memory state
     acc.l = warp_sum(acc.l);
 #pragma unroll
-    for (int x = 0; x < 4; ++x) acc.zs[x] = warp_sum(acc.zs[x]);
+    for (int x = 0; x < NGV; ++x) acc.zs[x] = warp_sum(acc.zs[x]);
     float fo = 0.0f, fn = 0.0f;
     {
         const float mo = sm.wm[warp][0];
@@ -1628,23 +1656,26 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
             sm.wm[warp][0] = M;
         }
     }
-    if (t == (g >> 2)) {
-        // lanes (g, g >> 2): rows g and g + 8 of every tile, column of their group
+    // tile (w', P) row g holds channel 16 (w' + 4 (g >> 2)) + 4 (g & 3) + 2P, row g + 8 the
+    // next; their value group n (column n of the MMA) sits in lane t = n / 2, slot n mod 2
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < 4; ++w) {
+        constexpr int kQ = 64 / GK;                      // groups per 64 channels
+        const int n0 = (16 * w) / GK;                    // the group for g < 4; g >= 4 adds kQ
+        const int n = n0 + ((g >> 2) ? kQ : 0);
+        if (t != (n >> 1)) continue;
+        const int slot = n & 1;
+        const float zg = (g >> 2) ? acc.zs[n0 + kQ] : acc.zs[n0];
 #pragma unroll
-            for (int P = 0; P < 2; ++P) {
-                const int c = 16 * (w + 4 * (g >> 2)) + 4 * (g & 3) + 2 * P;
-                constexpr int slot_of_w[4] = {0, 0, 1, 1};
-                const int slot = slot_of_w[w];                       // the group is 2 (g >> 2) + slot
-                const float zg = (g >> 2) ? acc.zs[2 + slot] : acc.zs[slot];
-                const float lo_row = (P ? 1048576.0f : 16777216.0f);  // 2^(24 - 4P)
-                const float o0 = fmaf(acc.o[w][P][slot], lo_row, zg);
-                const float o1 = fmaf(acc.o[w][P][2 + slot], 0.25f * lo_row, zg);
-                float* dst = &sm.wo[warp][0][c];
-                dst[0] = dst[0] * fo + o0 * fn;
-                dst[1] = dst[1] * fo + o1 * fn;
-            }
+        for (int P = 0; P < 2; ++P) {
+            const int c = 16 * (w + 4 * (g >> 2)) + 4 * (g & 3) + 2 * P;
+            const float lo_row = (P ? 1048576.0f : 16777216.0f);  // 2^(24 - 4P)
+            const float o0 = fmaf(slot ? acc.o[w][P][1] : acc.o[w][P][0], lo_row, zg);
+            const float o1 = fmaf(slot ? acc.o[w][P][3] : acc.o[w][P][2], 0.25f * lo_row, zg);
+            float* dst = &sm.wo[warp][0][c];
+            dst[0] = dst[0] * fo + o0 * fn;
+            dst[1] = dst[1] * fo + o1 * fn;
+        }
     }
     __syncwarp();
 }
@@ -1657,8 +1688,10 @@ __device__ void dispatch_tier(const DecodeArgs& a, Smem<NG, D>& sm, int t, size_
     const TierArgs& ta = a.tier[t];
     const int kb = ta.k_bits, vb = ta.v_bits, ax = ta.k_axis;
     if ((FAM & 1) && ax == KVQ_AXIS_CHANNEL && kb == 2 && vb == 2) {
-        if constexpr (D == 128 && NG == 1)
-            run_tier_mk1<NG>(a, sm, t, unit, r, i0, i1, n_local, stage, ok);
+        if constexpr (D == 128 && NG == 1) {
+            if (a.G == 16) run_tier_mk1<NG, 16>(a, sm, t, unit, r, i0, i1, n_local, stage, ok);
+            else run_tier_mk1<NG, 32>(a, sm, t, unit, r, i0, i1, n_local, stage, ok);
+        }
         else if constexpr (D == 128 && NG <= 4)
             run_tier_mma<2, KVQ_AXIS_CHANNEL, 2, NG>(a, sm, t, unit, r, i0, i1, n_local, stage, lg_unit, ok);
         else
@@ -2063,8 +2096,10 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     // per-channel keys on the tensor cores: each warp's query x scale rows
     bool has_channel = false;
     for (int t = 0; t < c.n_tiers; ++t) has_channel |= c.tier[t].k_axis == KVQ_AXIS_CHANNEL;
+    // (single heads with G = 16: two key scale rows and eight value groups per warp, 1.5 KB)
     const uint32_t qf_bytes = (has_channel && D == 128 && NG <= 4)
-                                  ? (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t))
+                                  ? (NG == 1 && c.G == 16 ? (uint32_t)(Cfg<NG>::W * 1536)
+                                                          : (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)))
                                   : 0u;
     const uint32_t slot_bytes = (uint32_t)(NG * (D + 2) * sizeof(float));
     auto smem_for = [&](int C, int S) {
@@ -2077,7 +2112,8 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     auto kern = decode_kernel<NG, D, FAM>;
     static bool attr_done = false, wide_ok = false;
     if (!attr_done) {
-        const uint32_t qf_max = NG <= 4 ? (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)) : 0u;
+        const uint32_t qf_max = NG == 1 ? (uint32_t)(Cfg<NG>::W * 1536)
+                                        : (NG <= 4 ? (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)) : 0u);
         cudaError_t e = cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
             (int)std::min(smem_for(kMaxCluster, kMaxStages) - qf_bytes + qf_max, kSmemLimit));

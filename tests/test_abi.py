@@ -109,9 +109,10 @@ def test_tier_byte_accounting(L):
     assert L.kvq_tier_bytes(1, 128, 32, 2, 2, kvq.AXIS_CHANNEL, 40, out) == 0
 
 
-def test_decode_caches_need_groups_of_32(L):
-    """The decode kernels take value groups (and per-token key groups) of 32 channels: a cache
-    with another group size is refused on the host (the descriptor is never dereferenced)."""
+def test_decode_cache_group_sizes(L):
+    """The decode kernels take groups of 32; groups of 16 only on the single-head 2-bit
+    MiniKV path (D = 128, Hq == Hkv): other caches are refused on the host (the descriptor
+    is never dereferenced)."""
     from bit_mixed_precision_gb300 import kvq
     fake = 1 << 20                                  # aligned, never read
     size_max = ctypes.c_size_t(-1).value
@@ -135,9 +136,14 @@ def test_decode_caches_need_groups_of_32(L):
     for c in (mikv, minikv):
         c.G = 32
         assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) != size_max, L.kvq_last_error()
-        c.G = 64
-        assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == size_max
-        assert b"G = 32" in L.kvq_last_error()
+        for G in (64, 16):
+            c.G = G
+            assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == size_max
+            assert f"G = {G} is built for 2-bit MiniKV".encode() in L.kvq_last_error()
+    minikv.Hq = 1                                   # one query head per KV head: groups of 16 built
+    minikv.G = 16
+    assert L.kvq_decode_workspace_bytes(ctypes.byref(minikv)) != size_max, L.kvq_last_error()
+    minikv.G, minikv.Hq = 32, 4
     # workspace: MiniKV none; MiKV the step's logits [u][g][slots] (slots = tier caps + ring),
     # then (256-byte aligned) the lse per head [u][8] and the ring state [u][4]
     mikv.G = minikv.G = 32

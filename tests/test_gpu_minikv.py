@@ -105,6 +105,28 @@ def test_minikv_bf16():
     _pipeline(B=2, H=2, T=1024, D=128, steps=40, nr=0, n_out=2, out_scale=8.0, seed=4, dtype=torch.bfloat16)
 
 
+def test_minikv_group16():
+    """Groups of 16 (the MiniKV review's default): key scale rows every 16 tokens, eight value
+    groups per token, flushes every 16 steps past nr = 64 (prompt 1024, 40 steps)."""
+    _pipeline(B=2, H=3, T=1024, D=128, steps=40, nr=64, n_out=3, out_scale=10.0, seed=6, G=16)
+
+
+def test_group16_limits_are_reported():
+    """G = 16 is built for the single-head 2-bit MiniKV path only: other shapes are refused
+    before any launch."""
+    B, D, T, G = 1, 128, 256, 16
+    x = inputs.make_qkv(B, 2, 2, T, D, seed=3)
+    with pytest.raises(RuntimeError, match="G = 16"):
+        kvq.make_cache(B, 4, 2, D, G, torch.float16, kvq.POLICY_MINIKV,
+                       [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, 256)], nr=32)
+    c1 = kvq.make_cache(B, 2, 2, D, G, torch.float16, kvq.POLICY_MINIKV,
+                        [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, 256)], nr=32)
+    with pytest.raises(RuntimeError, match="G = 32"):
+        kvq.minikv_prefill_build(c1, x.k.contiguous().cuda(), x.v.contiguous().cuda(),
+                                 torch.ones((B, 2, T), device="cuda"),
+                                 torch.full((B * 2,), 32, dtype=torch.int32, device="cuda"), 32)
+
+
 def _cache_arrays(c):
     t = c.tiers[0]
     return [t.k_codes, t.k_scale, t.k_zero, t.v_codes, t.v_scale, t.v_zero, t.token_id, t.count,
