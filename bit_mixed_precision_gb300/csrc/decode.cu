@@ -52,6 +52,9 @@ constexpr uint32_t kSleepNs = 4000;  // longest single suspension of a waiting w
 // per-token tiers behind a 32k prompt, runs 7 % faster at C = 4 than at C = 8, i.e. with
 // about twice as many items per CTA as the others want)
 constexpr int kMinItemsPerCta = 34, kMinItemsPerCtaMikv = 64;
+// streamed decode: CTAs at most (the workspace holds one partial per (CTA, unit) pair, at
+// most ctas + units - 1 of them), and static items per CTA at least
+constexpr int kStreamMaxCtas = 1024, kStreamMinItems = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -110,6 +113,7 @@ struct DecodeArgs {
     int stages, stage_shift;    // staging buffers per CTA (2 or 4) and its log2
     int withhold_unit;          // failure-detection check: unit whose first CTA skips its first copy, or -1
     uint32_t qf_off, part_off, stage_off;  // dynamic shared memory offsets
+    float* stream_part;         // streamed decode: partial per (CTA, unit), in the workspace
 };
 
 __device__ __forceinline__ float ldf(const void* p, size_t i, bool bf16) {
@@ -196,6 +200,11 @@ struct Smem {
     int issued;                          // local items requested so far (thread 0 requests)
     int fail;                            // a wait gave up: nothing more is requested
     UnitState us;
+    // streamed decode: the item of each buffer (unit, kind, index, tokens), and the issuing
+    // thread's cursor (next static item, its unit's counters, whether that unit has an item)
+    int4 meta[kMaxStages];
+    int wu, wk, wrem;
+    int cu, ccnt, clen, cstart, cem;
 };
 
 // Online-softmax state of one warp for NG heads; o holds the lane's share.
@@ -1403,6 +1412,20 @@ struct Mk1Acc {
     float zs[128 / GK];      // sum of p * zero of this lane's tokens, per value group
 };
 
+template <int GK>
+__device__ __forceinline__ void mk1_acc_init(Mk1Acc<GK>& acc) {
+    acc.m = kNegInf;
+    acc.l = 0.0f;
+#pragma unroll
+    for (int x = 0; x < 128 / GK; ++x) acc.zs[x] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int P = 0; P < 2; ++P)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) acc.o[i][P][f] = 0.0f;
+}
+
 // The staged chunk of the MiniKV format with group GK (compile-time sizes).
 template <int GK>
 __device__ __forceinline__ View mk1_view(int npad, const uint8_t* buf) {
@@ -1413,237 +1436,198 @@ __device__ __forceinline__ View mk1_view(int npad, const uint8_t* buf) {
 // hold two key scale rows (q * scale columns 0, 1 and 2, 3 of the key MMAs, the logits of
 // tokens 16..31 in lanes t = 1) and the values eight 16-channel groups (all eight B
 // columns of the P.V MMAs).
-template <int NG, int GK>
-__device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, size_t unit, int r, int i0,
-                             int i1, int n_local, uint8_t* stage_base, bool& ok) {
-    static_assert(NG == 1, "one query head per KV head");
-    static_assert(GK == 32 || GK == 16, "groups of 32 or 16");
-    constexpr int TPW = Cfg<NG>::TPW;
-    static_assert(TPW == 32, "32 tokens per warp and item");
-    constexpr int NKR = 32 / GK;            // key scale rows per warp
-    constexpr int NGV = 128 / GK;           // value groups per token
-    const UnitState& us = sm.us;
+template <int GK>
+struct Mk1Ctx {
+    uint32_t* qf;            // this warp's query fragments ([piece][k-step][t][reg], 512 B per key row)
+    float* pw;               // this warp's 32 probabilities
+    uint16_t* psw;           // probability x value scale, fp16 [group][token]
+    const uint2* qfb;        // B-fragment source of the key MMAs (query pieces or zeros)
+    const uint32_t* psb;     // B-fragment source of the P.V MMAs (value groups or zeros)
+    float4 q4;               // query channels 4 lane .. 4 lane + 3 (base-2 scaled)
+    uint32_t bsel;           // byte permute of lane group g
+    int tv;                  // the lane t that holds lane group g's logits
+};
+
+template <int GK>
+__device__ __forceinline__ Mk1Ctx<GK> mk1_ctx(const DecodeArgs& a, Smem<1, 128>& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    // this warp's query fragments ([piece = 2 row + hi/lo][k-step][t][reg], 512 B per key row),
-    // probabilities (32 floats) and probability x value scale ([group][token] fp16: over the
-    // probabilities for GK = 32, after the fragments for GK = 16)
-    uint32_t* qf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&sm) + a.qf_off +
-                                               (size_t)warp * (GK == 32 ? 512 : 1536));
-    float* pw = &sm.lg[warp][0][0];
-    uint16_t* psw = GK == 32 ? reinterpret_cast<uint16_t*>(pw) : reinterpret_cast<uint16_t*>(qf + 256);
+    constexpr int NKR = 32 / GK, NGV = 128 / GK;
+    Mk1Ctx<GK> x;
+    // probabilities (32 floats) and probability x value scale: over the probabilities for
+    // GK = 32, after the fragments for GK = 16
+    x.qf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&sm) + a.qf_off +
+                                       (size_t)warp * (GK == 32 ? 512 : 1536));
+    x.pw = &sm.lg[warp][0][0];
+    x.psw = GK == 32 ? reinterpret_cast<uint16_t*>(x.pw) : reinterpret_cast<uint16_t*>(x.qf + 256);
     const uint32_t* zero = reinterpret_cast<const uint32_t*>(&sm.qa[0][0]);
-    // B-fragment sources: lanes g < 2 NKR read the query pieces, g < NGV the value groups;
-    // the others read zeros (no per-step select)
-    const uint2* qfb = g < 2 * NKR ? reinterpret_cast<const uint2*>(qf) + g * 32 + t
-                                   : reinterpret_cast<const uint2*>(zero) + t;
-    const uint32_t* psb = g < NGV ? reinterpret_cast<const uint32_t*>(psw + g * 32) + t : zero + t;
-    const int tv = GK == 32 ? 0 : (g >> 2);       // the lane t that holds lane group g's logits
-    const float4 q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);   // channels 4 lane .. + 3
-    const uint32_t bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
-    // the copies of this tier's next items, one array per lane (lanes 0..5): a chunk of npad
-    // tokens stages array k at bytes [off_k npad, off_k npad + bytes_k npad) of its buffer,
-    // from base_k + (chunk index) * 128 bytes_k (compile-time sizes of the format)
-    constexpr uint32_t kSB = 256 / GK;           // scale (or zero) bytes per token, keys and values
-    const TierArgs& ta = a.tier[tier];
-    const uint8_t* cp_src = nullptr;
-    uint32_t cp_off = 0u, cp_bpt = 0u;
+    // lanes g < 2 NKR read the query pieces, g < NGV the value groups; the others read
+    // zeros (no per-step select)
+    x.qfb = g < 2 * NKR ? reinterpret_cast<const uint2*>(x.qf) + g * 32 + t
+                        : reinterpret_cast<const uint2*>(zero) + t;
+    x.psb = g < NGV ? reinterpret_cast<const uint32_t*>(x.psw + g * 32) + t : zero + t;
+    x.tv = GK == 32 ? 0 : (g >> 2);
+    x.q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);
+    x.bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
+    return x;
+}
+
+// This warp's tokens [tl, tl + nt) (nt <= 32) of a staged chunk: logits, online softmax
+// and P.V into acc.
+template <int GK>
+__device__ __forceinline__ void mk1_item(const View& v, int tl, int nt, const Mk1Ctx<GK>& x, Mk1Acc<GK>& acc) {
+    constexpr int NKR = 32 / GK, NGV = 128 / GK;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float4 q4 = x.q4;
+    // -- Q' = q * scale of each key scale row, as hi / lo fp16 fragments, and sum_c q z
+    float bias[NKR];
+#pragma unroll
+    for (int kr = 0; kr < NKR; ++kr) {
+        const size_t ro = (size_t)(tl / GK + kr) * 128 + 4 * lane;
+        const uint2 s2 = *reinterpret_cast<const uint2*>(v.ks + ro);
+        const uint2 z2 = *reinterpret_cast<const uint2*>(v.kz + ro);
+        const float x0 = q4.x * h2lo(s2.x), x1 = q4.y * h2hi(s2.x);
+        const float x2 = q4.z * h2lo(s2.y), x3 = q4.w * h2hi(s2.y);
+        const uint32_t hi01 = pack_h2(x0, x1), hi23 = pack_h2(x2, x3);
+        const uint32_t lo01 = pack_h2(x0 - h2lo(hi01), x1 - h2hi(hi01));
+        const uint32_t lo23 = pack_h2(x2 - h2lo(hi23), x3 - h2hi(hi23));
+        bias[kr] = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
+        // channel c = 16 s + 8 half + 2 tt + e sits in register half of lane tt, k-step s
+        const int s_ = lane >> 2, half = (lane & 3) >> 1, tt = 2 * (lane & 1);
+        uint32_t* qh = x.qf + 128 * kr;
+        qh[(s_ * 4 + tt) * 2 + half] = hi01;
+        qh[(s_ * 4 + tt + 1) * 2 + half] = hi23;
+        qh[64 + (s_ * 4 + tt) * 2 + half] = lo01;
+        qh[64 + (s_ * 4 + tt + 1) * 2 + half] = lo23;
+        bias[kr] = warp_sum(bias[kr]);
+    }
+    const float bias_g = NKR == 1 ? bias[0] : ((g >> 2) ? bias[NKR - 1] : bias[0]);
+    __syncwarp();
+    // -- logits: two MMAs (tokens 4g + {0, 1} and 4g + {2, 3}), each over two accumulator
+    // chains of four k-steps
+    float R[2][2][4];
+#pragma unroll
+    for (int P = 0; P < 2; ++P)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int f = 0; f < 4; ++f) R[P][e][f] = 0.0f;
     {
-        const size_t cap = (size_t)ta.cap;
-        switch (lane) {
-            case 0: cp_src = reinterpret_cast<const uint8_t*>(ta.k_codes + unit * (cap / 16) * 128); cp_off = 0; cp_bpt = 32; break;
-            case 1: cp_src = reinterpret_cast<const uint8_t*>(ta.k_scale + unit * (cap / GK) * 128); cp_off = 32; cp_bpt = kSB; break;
-            case 2: cp_src = reinterpret_cast<const uint8_t*>(ta.k_zero + unit * (cap / GK) * 128); cp_off = 32 + kSB; cp_bpt = kSB; break;
-            case 3: cp_src = reinterpret_cast<const uint8_t*>(ta.v_codes + unit * cap * 8); cp_off = 32 + 2 * kSB; cp_bpt = 32; break;
-            case 4: cp_src = reinterpret_cast<const uint8_t*>(ta.v_scale + unit * cap * NGV); cp_off = 64 + 2 * kSB; cp_bpt = kSB; break;
-            case 5: cp_src = reinterpret_cast<const uint8_t*>(ta.v_zero + unit * cap * NGV); cp_off = 64 + 3 * kSB; cp_bpt = kSB; break;
-            default: break;
+        const uint32_t* rowp = v.kc + (size_t)((tl >> 4) + (g >> 2)) * 128;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t + 8);
+            const uint2 b = x.qfb[s * 4];
+            const uint32_t y0 = __byte_perm(w0.x, w0.y, x.bsel), y1 = __byte_perm(w1.x, w1.y, x.bsel);
+            const uint32_t a0[4] = {y0 & kM0, y0 & kM1, y1 & kM0, y1 & kM1};
+            const uint32_t a1[4] = {y0 & kM2, y0 & kM3, y1 & kM2, y1 & kM3};
+            mma16816(R[0][s & 1], a0, b.x, b.y);
+            mma16816(R[1][s & 1], a1, b.x, b.y);
         }
     }
-    Mk1Acc<GK> acc;
-    acc.m = kNegInf;
-    acc.l = 0.0f;
+    // -- logits of tokens 4g + j (lanes t == tv): code factor 4^j * 2^-24 out, bias in
+    float lg[4];
+    lg[0] = fmaf((R[0][0][0] + R[0][1][0]) + (R[0][0][1] + R[0][1][1]), 16777216.0f, bias_g);  // 2^24
+    lg[1] = fmaf((R[0][0][2] + R[0][1][2]) + (R[0][0][3] + R[0][1][3]), 4194304.0f, bias_g);   // 2^22
+    lg[2] = fmaf((R[1][0][0] + R[1][1][0]) + (R[1][0][1] + R[1][1][1]), 1048576.0f, bias_g);   // 2^20
+    lg[3] = fmaf((R[1][0][2] + R[1][1][2]) + (R[1][0][3] + R[1][1][3]), 262144.0f, bias_g);    // 2^18
+    bool valid[4];
 #pragma unroll
-    for (int x = 0; x < NGV; ++x) acc.zs[x] = 0.0f;
+    for (int j = 0; j < 4; ++j) valid[j] = t == x.tv && 4 * g + j < nt;
+    float mx = fmaxf(fmaxf(valid[0] ? lg[0] : kNegInf, valid[1] ? lg[1] : kNegInf),
+                     fmaxf(valid[2] ? lg[2] : kNegInf, valid[3] ? lg[3] : kNegInf));
+    if (GK != 32) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mx = __shfl_sync(0xffffffffu, mx, 0);
+    // the reference moves only when the max rises by more than 2^8 (exact: the final
+    // division uses the same reference)
+    if (acc.m == kNegInf ? mx != kNegInf : mx > acc.m + 8.0f) {
+        const float corr = acc.m == kNegInf ? 0.0f : ex2_approx(acc.m - mx);
+        acc.m = mx;
+        acc.l *= corr;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int k = 0; k < NGV; ++k) acc.zs[k] *= corr;
 #pragma unroll
-        for (int P = 0; P < 2; ++P)
-#pragma unroll
-            for (int f = 0; f < 4; ++f) acc.o[i][P][f] = 0.0f;
-    for (int i = i0; i < i1; ++i) {
-        ok = wait_item(a, sm, i, ok);
-        const int j0 = (r + i * a.cluster - us.base[tier]) * kSub;
-        const int n = min(kSub, us.cnt[tier] - j0);
-        const int tl = warp * TPW;
-        if (ok && tl < n) {
-            const View v = mk1_view<GK>((n + 31) & ~31, item_buf(a, stage_base, i));
-            const int nt = min(TPW, n - tl);
-            // -- Q' = q * scale of each key scale row, as hi / lo fp16 fragments, and sum_c q z
-            float bias[NKR];
-#pragma unroll
-            for (int kr = 0; kr < NKR; ++kr) {
-                const size_t ro = (size_t)(tl / GK + kr) * 128 + 4 * lane;
-                const uint2 s2 = *reinterpret_cast<const uint2*>(v.ks + ro);
-                const uint2 z2 = *reinterpret_cast<const uint2*>(v.kz + ro);
-                const float x0 = q4.x * h2lo(s2.x), x1 = q4.y * h2hi(s2.x);
-                const float x2 = q4.z * h2lo(s2.y), x3 = q4.w * h2hi(s2.y);
-                const uint32_t hi01 = pack_h2(x0, x1), hi23 = pack_h2(x2, x3);
-                const uint32_t lo01 = pack_h2(x0 - h2lo(hi01), x1 - h2hi(hi01));
-                const uint32_t lo23 = pack_h2(x2 - h2lo(hi23), x3 - h2hi(hi23));
-                bias[kr] = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
-                // channel c = 16 s + 8 half + 2 tt + e sits in register half of lane tt, k-step s
-                const int s_ = lane >> 2, half = (lane & 3) >> 1, tt = 2 * (lane & 1);
-                uint32_t* qh = qf + 128 * kr;
-                qh[(s_ * 4 + tt) * 2 + half] = hi01;
-                qh[(s_ * 4 + tt + 1) * 2 + half] = hi23;
-                qh[64 + (s_ * 4 + tt) * 2 + half] = lo01;
-                qh[64 + (s_ * 4 + tt + 1) * 2 + half] = lo23;
-                bias[kr] = warp_sum(bias[kr]);
-            }
-            const float bias_g = NKR == 1 ? bias[0] : ((g >> 2) ? bias[NKR - 1] : bias[0]);
-            __syncwarp();
-            // -- logits: two MMAs (tokens 4g + {0, 1} and 4g + {2, 3}), each over two
-            // accumulator chains of four k-steps
-            float R[2][2][4];
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int P = 0; P < 2; ++P)
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-#pragma unroll
-                    for (int f = 0; f < 4; ++f) R[P][e][f] = 0.0f;
-            {
-                const uint32_t* rowp = v.kc + (size_t)((tl >> 4) + (g >> 2)) * 128;
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint2 w0 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t);
-                    const uint2 w1 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t + 8);
-                    const uint2 b = qfb[s * 4];
-                    const uint32_t y0 = __byte_perm(w0.x, w0.y, bsel), y1 = __byte_perm(w1.x, w1.y, bsel);
-                    const uint32_t a0[4] = {y0 & kM0, y0 & kM1, y1 & kM0, y1 & kM1};
-                    const uint32_t a1[4] = {y0 & kM2, y0 & kM3, y1 & kM2, y1 & kM3};
-                    mma16816(R[0][s & 1], a0, b.x, b.y);
-                    mma16816(R[1][s & 1], a1, b.x, b.y);
-                }
-            }
-            // -- logits of tokens 4g + j (lanes t == tv): code factor 4^j * 2^-24 out, bias in
-            float lg[4];
-            lg[0] = fmaf((R[0][0][0] + R[0][1][0]) + (R[0][0][1] + R[0][1][1]), 16777216.0f, bias_g);  // 2^24
-            lg[1] = fmaf((R[0][0][2] + R[0][1][2]) + (R[0][0][3] + R[0][1][3]), 4194304.0f, bias_g);   // 2^22
-            lg[2] = fmaf((R[1][0][0] + R[1][1][0]) + (R[1][0][1] + R[1][1][1]), 1048576.0f, bias_g);   // 2^20
-            lg[3] = fmaf((R[1][0][2] + R[1][1][2]) + (R[1][0][3] + R[1][1][3]), 262144.0f, bias_g);    // 2^18
-            bool valid[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) valid[j] = t == tv && 4 * g + j < nt;
-            float mx = fmaxf(fmaxf(valid[0] ? lg[0] : kNegInf, valid[1] ? lg[1] : kNegInf),
-                             fmaxf(valid[2] ? lg[2] : kNegInf, valid[3] ? lg[3] : kNegInf));
-            if (GK != 32) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            mx = __shfl_sync(0xffffffffu, mx, 0);
-            // the reference moves only when the max rises by more than 2^8 (exact: the
-            // final division uses the same reference)
-            if (acc.m == kNegInf ? mx != kNegInf : mx > acc.m + 8.0f) {
-                const float corr = acc.m == kNegInf ? 0.0f : ex2_approx(acc.m - mx);
-                acc.m = mx;
-                acc.l *= corr;
-#pragma unroll
-                for (int x = 0; x < NGV; ++x) acc.zs[x] *= corr;
-#pragma unroll
-                for (int x = 0; x < 4; ++x)
-#pragma unroll
-                    for (int P = 0; P < 2; ++P)
-#pragma unroll
-                        for (int f = 0; f < 4; ++f) acc.o[x][P][f] *= corr;
-            }
-            {
-                float4 p;
-                p.x = valid[0] ? ex2_approx(lg[0] - acc.m) : 0.0f;
-                p.y = valid[1] ? ex2_approx(lg[1] - acc.m) : 0.0f;
-                p.z = valid[2] ? ex2_approx(lg[2] - acc.m) : 0.0f;
-                p.w = valid[3] ? ex2_approx(lg[3] - acc.m) : 0.0f;
-                acc.l += (p.x + p.y) + (p.z + p.w);
-                if (t == tv) *reinterpret_cast<float4*>(pw + 4 * g) = p;
-            }
-            __syncwarp();
-            // -- lane = token: p times each group's value scale into [group][token], and the
-            // zero points (stale slots past nt read as zero scale and zero point)
-            {
-                const float p = pw[lane];
-                __syncwarp();                                    // every lane has its p: ps may overwrite pw
-                const bool ok_t = lane < nt;
-                uint32_t sw[NGV / 2], zw[NGV / 2];
-                if constexpr (NGV == 4) {
-                    const uint2 s2 = *reinterpret_cast<const uint2*>(v.vs + (size_t)(tl + lane) * 4);
-                    const uint2 z2 = *reinterpret_cast<const uint2*>(v.vz + (size_t)(tl + lane) * 4);
-                    sw[0] = s2.x; sw[1] = s2.y; zw[0] = z2.x; zw[1] = z2.y;
-                } else {
-                    const uint4 s4 = *reinterpret_cast<const uint4*>(v.vs + (size_t)(tl + lane) * 8);
-                    const uint4 z4 = *reinterpret_cast<const uint4*>(v.vz + (size_t)(tl + lane) * 8);
-                    sw[0] = s4.x; sw[1] = s4.y; sw[2] = s4.z; sw[3] = s4.w;
-                    zw[0] = z4.x; zw[1] = z4.y; zw[2] = z4.z; zw[3] = z4.w;
-                }
-#pragma unroll
-                for (int e = 0; e < NGV / 2; ++e) {
-                    sw[e] = ok_t ? sw[e] : 0u;
-                    zw[e] = ok_t ? zw[e] : 0u;
-                    const uint32_t ps2 = pack_h2(p * h2lo(sw[e]), p * h2hi(sw[e]));
-                    psw[(2 * e) * 32 + lane] = (uint16_t)(ps2 & 0xffffu);
-                    psw[(2 * e + 1) * 32 + lane] = (uint16_t)(ps2 >> 16);
-                    acc.zs[2 * e] = fmaf(p, h2lo(zw[e]), acc.zs[2 * e]);
-                    acc.zs[2 * e + 1] = fmaf(p, h2hi(zw[e]), acc.zs[2 * e + 1]);
-                }
-            }
-            __syncwarp();
-            // -- P.V over two k-steps of 16 tokens: B = (p s) of tokens 16 ks + 2t, + 1
-            // (b0) and + 8, + 9 (b1) in column g (value group g; zeros past the groups)
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = 16 * ks + 2 * t;
-                const uint32_t b0 = psb[8 * ks], b1 = psb[8 * ks + 4];
-                const uint32_t* vrow = v.vc + (size_t)(tl + k0) * 8 + 4 * (g >> 2);
-                const uint4 xa = *reinterpret_cast<const uint4*>(vrow);
-                const uint4 xb = *reinterpret_cast<const uint4*>(vrow + 8);
-                const uint4 xc = *reinterpret_cast<const uint4*>(vrow + 64);
-                const uint4 xd = *reinterpret_cast<const uint4*>(vrow + 72);
-                const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
-                const uint32_t wc[4] = {xc.x, xc.y, xc.z, xc.w}, wd[4] = {xd.x, xd.y, xd.z, xd.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t ya = __byte_perm(wa[w], wb[w], bsel), yc = __byte_perm(wc[w], wd[w], bsel);
-                    const uint32_t a0[4] = {ya & kM0, ya & kM1, yc & kM0, yc & kM1};
-                    const uint32_t a1[4] = {ya & kM2, ya & kM3, yc & kM2, yc & kM3};
-                    mma16816(acc.o[w][0], a0, b0, b1);
-                    mma16816(acc.o[w][1], a1, b0, b1);
-                }
-            }
-            __syncwarp();                                        // pw / ps / qf are rewritten by the next item
+                for (int f = 0; f < 4; ++f) acc.o[k][P][f] *= corr;
+    }
+    {
+        float4 p;
+        p.x = valid[0] ? ex2_approx(lg[0] - acc.m) : 0.0f;
+        p.y = valid[1] ? ex2_approx(lg[1] - acc.m) : 0.0f;
+        p.z = valid[2] ? ex2_approx(lg[2] - acc.m) : 0.0f;
+        p.w = valid[3] ? ex2_approx(lg[3] - acc.m) : 0.0f;
+        acc.l += (p.x + p.y) + (p.z + p.w);
+        if (t == x.tv) *reinterpret_cast<float4*>(x.pw + 4 * g) = p;
+    }
+    __syncwarp();
+    // -- lane = token: p times each group's value scale into [group][token], and the zero
+    // points (stale slots past nt read as zero scale and zero point)
+    {
+        const float p = x.pw[lane];
+        __syncwarp();                                    // every lane has its p: ps may overwrite pw
+        const bool ok_t = lane < nt;
+        uint32_t sw[NGV / 2], zw[NGV / 2];
+        if constexpr (NGV == 4) {
+            const uint2 s2 = *reinterpret_cast<const uint2*>(v.vs + (size_t)(tl + lane) * 4);
+            const uint2 z2 = *reinterpret_cast<const uint2*>(v.vz + (size_t)(tl + lane) * 4);
+            sw[0] = s2.x; sw[1] = s2.y; zw[0] = z2.x; zw[1] = z2.y;
+        } else {
+            const uint4 s4 = *reinterpret_cast<const uint4*>(v.vs + (size_t)(tl + lane) * 8);
+            const uint4 z4 = *reinterpret_cast<const uint4*>(v.vz + (size_t)(tl + lane) * 8);
+            sw[0] = s4.x; sw[1] = s4.y; sw[2] = s4.z; sw[3] = s4.w;
+            zw[0] = z4.x; zw[1] = z4.y; zw[2] = z4.z; zw[3] = z4.w;
         }
-        // every warp is done with item i: warp 0 requests item i + S into its buffer, the six
-        // copies of a chunk of this tier side by side (other items: the general path)
-        __syncthreads();
-        if (warp == 0 && i + a.stages < n_local && !sm.fail) {
-            const int inext = i + a.stages, kn = r + inext * a.cluster;
-            if (kn < us.base[tier + 1]) {
-                const int idx = kn - us.base[tier];
-                const int np = (min(kSub, us.cnt[tier] - idx * kSub) + 31) & ~31;
-                const int sb = inext & (a.stages - 1);
-                const uint32_t bar = smem_u32(&sm.bar[sb]);
-                if (lane == 0) mbar_expect_tx(bar, (64u + 4u * kSB) * (uint32_t)np);
-                __syncwarp();
-                if (lane < 6)
-                    bulk_load(smem_u32(stage_base) + (uint32_t)sb * a.stage_bytes + cp_off * (uint32_t)np,
-                              cp_src + (size_t)idx * (kSub * cp_bpt), cp_bpt * (uint32_t)np, bar);
-            } else if (lane == 0) {
-                issue_item(a, us, unit, r, inext, stage_base, sm.bar);
-            }
-            if (lane == 0) sm.issued = inext + 1;
+#pragma unroll
+        for (int e = 0; e < NGV / 2; ++e) {
+            sw[e] = ok_t ? sw[e] : 0u;
+            zw[e] = ok_t ? zw[e] : 0u;
+            const uint32_t ps2 = pack_h2(p * h2lo(sw[e]), p * h2hi(sw[e]));
+            x.psw[(2 * e) * 32 + lane] = (uint16_t)(ps2 & 0xffffu);
+            x.psw[(2 * e + 1) * 32 + lane] = (uint16_t)(ps2 >> 16);
+            acc.zs[2 * e] = fmaf(p, h2lo(zw[e]), acc.zs[2 * e]);
+            acc.zs[2 * e + 1] = fmaf(p, h2hi(zw[e]), acc.zs[2 * e + 1]);
         }
     }
-    // ---- merge the warp's state into its shared-memory state
+    __syncwarp();
+    // -- P.V over two k-steps of 16 tokens: B = (p s) of tokens 16 ks + 2t, + 1 (b0) and
+    // + 8, + 9 (b1) in column g (value group g; zeros past the groups)
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const int k0 = 16 * ks + 2 * t;
+        const uint32_t b0 = x.psb[8 * ks], b1 = x.psb[8 * ks + 4];
+        const uint32_t* vrow = v.vc + (size_t)(tl + k0) * 8 + 4 * (g >> 2);
+        const uint4 xa = *reinterpret_cast<const uint4*>(vrow);
+        const uint4 xb = *reinterpret_cast<const uint4*>(vrow + 8);
+        const uint4 xc = *reinterpret_cast<const uint4*>(vrow + 64);
+        const uint4 xd = *reinterpret_cast<const uint4*>(vrow + 72);
+        const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
+        const uint32_t wc[4] = {xc.x, xc.y, xc.z, xc.w}, wd[4] = {xd.x, xd.y, xd.z, xd.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t ya = __byte_perm(wa[w], wb[w], x.bsel), yc = __byte_perm(wc[w], wd[w], x.bsel);
+            const uint32_t a0[4] = {ya & kM0, ya & kM1, yc & kM0, yc & kM1};
+            const uint32_t a1[4] = {ya & kM2, ya & kM3, yc & kM2, yc & kM3};
+            mma16816(acc.o[w][0], a0, b0, b1);
+            mma16816(acc.o[w][1], a1, b0, b1);
+        }
+    }
+    __syncwarp();                                        // pw / ps / qf are rewritten by the next item
+}
+
+// The warp's state merged into its shared-memory state (sm.wm / wl / wo of this warp).
+template <int GK>
+__device__ __forceinline__ void mk1_flush(Mk1Acc<GK>& acc, Smem<1, 128>& sm) {
+    constexpr int NGV = 128 / GK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     acc.l = warp_sum(acc.l);
 #pragma unroll
-    for (int x = 0; x < NGV; ++x) acc.zs[x] = warp_sum(acc.zs[x]);
+    for (int k = 0; k < NGV; ++k) acc.zs[k] = warp_sum(acc.zs[k]);
     float fo = 0.0f, fn = 0.0f;
     {
         const float mo = sm.wm[warp][0];
@@ -1678,6 +1662,70 @@ __device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, s
         }
     }
     __syncwarp();
+}
+
+// Local items [i0, i1) of the MiniKV tier, one query head per KV head.
+template <int NG, int GK>
+__device__ void run_tier_mk1(const DecodeArgs& a, Smem<NG, 128>& sm, int tier, size_t unit, int r, int i0,
+                             int i1, int n_local, uint8_t* stage_base, bool& ok) {
+    static_assert(NG == 1, "one query head per KV head");
+    static_assert(GK == 32 || GK == 16, "groups of 32 or 16");
+    constexpr int TPW = Cfg<NG>::TPW;
+    static_assert(TPW == 32, "32 tokens per warp and item");
+    constexpr int NGV = 128 / GK;
+    const UnitState& us = sm.us;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Mk1Ctx<GK> x = mk1_ctx<GK>(a, sm);
+    // the copies of this tier's next items, one array per lane (lanes 0..5): a chunk of npad
+    // tokens stages array k at bytes [off_k npad, off_k npad + bytes_k npad) of its buffer,
+    // from base_k + (chunk index) * 128 bytes_k (compile-time sizes of the format)
+    constexpr uint32_t kSB = 256 / GK;           // scale (or zero) bytes per token, keys and values
+    const TierArgs& ta = a.tier[tier];
+    const uint8_t* cp_src = nullptr;
+    uint32_t cp_off = 0u, cp_bpt = 0u;
+    {
+        const size_t cap = (size_t)ta.cap;
+        switch (lane) {
+            case 0: cp_src = reinterpret_cast<const uint8_t*>(ta.k_codes + unit * (cap / 16) * 128); cp_off = 0; cp_bpt = 32; break;
+            case 1: cp_src = reinterpret_cast<const uint8_t*>(ta.k_scale + unit * (cap / GK) * 128); cp_off = 32; cp_bpt = kSB; break;
+            case 2: cp_src = reinterpret_cast<const uint8_t*>(ta.k_zero + unit * (cap / GK) * 128); cp_off = 32 + kSB; cp_bpt = kSB; break;
+            case 3: cp_src = reinterpret_cast<const uint8_t*>(ta.v_codes + unit * cap * 8); cp_off = 32 + 2 * kSB; cp_bpt = 32; break;
+            case 4: cp_src = reinterpret_cast<const uint8_t*>(ta.v_scale + unit * cap * NGV); cp_off = 64 + 2 * kSB; cp_bpt = kSB; break;
+            case 5: cp_src = reinterpret_cast<const uint8_t*>(ta.v_zero + unit * cap * NGV); cp_off = 64 + 3 * kSB; cp_bpt = kSB; break;
+            default: break;
+        }
+    }
+    Mk1Acc<GK> acc;
+    mk1_acc_init(acc);
+    for (int i = i0; i < i1; ++i) {
+        ok = wait_item(a, sm, i, ok);
+        const int j0 = (r + i * a.cluster - us.base[tier]) * kSub;
+        const int n = min(kSub, us.cnt[tier] - j0);
+        const int tl = warp * TPW;
+        if (ok && tl < n)
+            mk1_item<GK>(mk1_view<GK>((n + 31) & ~31, item_buf(a, stage_base, i)), tl, min(TPW, n - tl), x, acc);
+        // every warp is done with item i: warp 0 requests item i + S into its buffer, the six
+        // copies of a chunk of this tier side by side (other items: the general path)
+        __syncthreads();
+        if (warp == 0 && i + a.stages < n_local && !sm.fail) {
+            const int inext = i + a.stages, kn = r + inext * a.cluster;
+            if (kn < us.base[tier + 1]) {
+                const int idx = kn - us.base[tier];
+                const int np = (min(kSub, us.cnt[tier] - idx * kSub) + 31) & ~31;
+                const int sb = inext & (a.stages - 1);
+                const uint32_t bar = smem_u32(&sm.bar[sb]);
+                if (lane == 0) mbar_expect_tx(bar, (64u + 4u * kSB) * (uint32_t)np);
+                __syncwarp();
+                if (lane < 6)
+                    bulk_load(smem_u32(stage_base) + (uint32_t)sb * a.stage_bytes + cp_off * (uint32_t)np,
+                              cp_src + (size_t)idx * (kSub * cp_bpt), cp_bpt * (uint32_t)np, bar);
+            } else if (lane == 0) {
+                issue_item(a, us, unit, r, inext, stage_base, sm.bar);
+            }
+            if (lane == 0) sm.issued = inext + 1;
+        }
+    }
+    mk1_flush<GK>(acc, sm);
 }
 
 // FAM selects the formats compiled into one kernel: bit 0 keys per channel
@@ -2056,9 +2104,317 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
     }
 }
 
+
+// ---- streamed decode: single heads, MiniKV format
+//
+// The units' items at full capacity form one static list: unit u owns items
+// [u n_i, (u + 1) n_i) (its n_c tier chunks, then its n_r ring pieces), and
+// CTA c takes the contiguous run [c per, (c + 1) per) of the list, as many CTAs
+// as are resident at once.  Every SM then streams the same share of the layer
+// whatever the batch, and a CTA's staging never drains between its units.  The
+// issuing warp walks the run, skipping items past a unit's live counts, and
+// publishes each requested item (unit, kind, index, tokens) beside its buffer;
+// the other warps follow those records.  Per (CTA, unit) the CTA writes its
+// partial state (max, sum, unnormalised output) to slot c + u of the
+// workspace; a second launch merges each unit's partials and does the unit's
+// end-of-step work (the new token into the ring, the MiniKV flush, counters).
+struct StreamArgs {
+    int n_c, n_r, n_i;           // tier chunks, ring pieces and items per unit at full capacity
+    long long per, total;        // static items per CTA, items of all units
+    float* part;                 // [ctas + units - 1][2 + 128] partial (max, sum, output) per (CTA, unit)
+};
+
+constexpr int kItChunk = 0, kItRing = 1, kItNone = 2, kItEnd = 3;
+
+// Issuing warp (every lane; the warps take turns): requests the CTA's next item into buffer k % S and
+// publishes its record; nothing but an end record once the run is done or a wait gave up.
+// Lanes 0..5 each copy one array of a tier chunk (at compile-time offsets of the format).
+template <int GK, int CH>
+__device__ __noinline__ void stream_issue(const DecodeArgs& a, const StreamArgs& s, Smem<1, 128>& sm, uint8_t* stage_base,
+                             int k, const uint8_t* cp_base, uint32_t cp_off, uint32_t cp_bpt) {
+    constexpr uint32_t kSB = 256 / GK;
+    const int lane = threadIdx.x & 31;
+    int kind = kItEnd, u = 0, idx = 0, n = 0;
+    if (lane == 0) {
+        // the cursor: unit and item of the next static item, static items left in the run
+        int uu = sm.wu, kk = sm.wk, rem = sm.fail ? 0 : sm.wrem;
+        while (rem > 0) {
+            if (uu != sm.cu) {
+                const int raw = a.tier[0].count[uu], rl = a.res_len[uu], rs = a.res_start[uu];
+                const int cnt = min(max(raw, 0), a.tier[0].cap), cap = a.res_cap;
+                const int len = min(max(rl, 0), cap - 1), st = min(max(rs, 0), cap - 1);
+                if (raw != cnt || rl != len || rs != st) atomicOr(&g_status_decode, kDevCheck);
+                sm.cu = uu;
+                sm.ccnt = cnt;
+                sm.clen = len;
+                sm.cstart = st;
+                sm.cem = 0;
+            }
+            const int cu = uu, ck = kk;
+            const bool last_of_unit = ck == s.n_i - 1 || rem == 1;
+            --rem;
+            if (++kk == s.n_i) {
+                kk = 0;
+                ++uu;
+            }
+            if (ck < s.n_c) {
+                const int nn = min(CH, sm.ccnt - ck * CH);
+                if (nn > 0) { kind = kItChunk; u = cu; idx = ck; n = nn; break; }
+            } else {
+                const int j0 = (ck - s.n_c) * kResItem;
+                const int nn = min(kResItem, sm.clen + 1 - j0);
+                if (nn > 0) { kind = kItRing; u = cu; idx = j0; n = nn; break; }
+            }
+            // a unit of the run with no live item still gets a record: its (empty) partial
+            if (last_of_unit && !sm.cem) { kind = kItNone; u = cu; break; }
+        }
+        sm.wu = uu;
+        sm.wk = kk;
+        sm.wrem = rem;
+        if (kind != kItEnd) sm.cem = 1;
+        sm.meta[k & (a.stages - 1)] = make_int4(u, kind, idx, n);
+    }
+    kind = __shfl_sync(0xffffffffu, kind, 0);
+    if (kind == kItEnd) return;
+    u = __shfl_sync(0xffffffffu, u, 0);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    n = __shfl_sync(0xffffffffu, n, 0);
+    const int sb = k & (a.stages - 1);
+    const uint32_t bar = smem_u32(&sm.bar[sb]);
+    const uint32_t dst = smem_u32(stage_base) + (uint32_t)sb * a.stage_bytes;
+    // failure-detection check: the first CTA withholds its first item's copies
+    const bool withhold = a.withhold_unit >= 0 && blockIdx.x == 0 && k == 0 && kind != kItNone;
+    if (kind == kItChunk) {
+        const int np = (n + 31) & ~31;
+        if (lane == 0 && !withhold) mbar_expect_tx(bar, (64u + 4u * kSB) * (uint32_t)np);
+        __syncwarp();
+        if (lane < 6 && !withhold)
+            bulk_load(dst + cp_off * (uint32_t)np,
+                      cp_base + ((size_t)u * a.tier[0].cap + (size_t)idx * CH) * cp_bpt, cp_bpt * (uint32_t)np, bar);
+    } else if (lane == 0 && !withhold) {
+        if (kind == kItRing)
+            stage_residual(a, (size_t)u, sm.clen, sm.cstart, idx, n, 128, stage_base + (size_t)sb * a.stage_bytes, bar);
+        else
+            mbar_arrive(bar);                            // no bytes: the buffer's phase completes at once
+    }
+    if (lane == 0) sm.issued = k + 1;
+}
+
+// Every warp is done with item i: warp i mod W (the turns spread the issuing work) requests
+// item i + S into its buffer.
+template <int GK, int CH>
+__device__ __forceinline__ void stream_release(const DecodeArgs& a, const StreamArgs& s, Smem<1, 128>& sm,
+                                               uint8_t* stage_base, int i, const uint8_t* cp_base,
+                                               uint32_t cp_off, uint32_t cp_bpt) {
+    __syncthreads();
+    if ((threadIdx.x >> 5) == (i & (Cfg<1>::W - 1)))
+        stream_issue<GK, CH>(a, s, sm, stage_base, i + a.stages, cp_base, cp_off, cp_bpt);
+}
+
+// Grid = (CTAs): CTA c streams the static items [c per, min((c + 1) per, total)); a tier
+// chunk is CH tokens (128 or 256: each warp takes 32 tokens of each 128).
+template <int GK, int CH>
+__global__ void __launch_bounds__(Cfg<1>::kThreads, Cfg<1>::MINB) decode_stream_kernel(DecodeArgs a, StreamArgs s) {
+    constexpr int D = 128, W = Cfg<1>::W, TPW = Cfg<1>::TPW, RPW = Cfg<1>::RPW;
+    constexpr uint32_t kSB = 256 / GK;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem<1, D>& sm = *reinterpret_cast<Smem<1, D>*>(smem_raw);
+    uint8_t* stage_base = smem_raw + a.stage_off;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool bf = a.bf16 != 0;
+    // lanes 0..5 of the issuing warp copy one array of a tier chunk each: unit u's chunk j
+    // starts (u cap + 128 j) bytes_per_token into the array
+    const TierArgs& ta = a.tier[0];
+    const uint8_t* cp_base = nullptr;
+    uint32_t cp_off = 0u, cp_bpt = 0u;
+    switch (lane) {
+        case 0: cp_base = reinterpret_cast<const uint8_t*>(ta.k_codes); cp_off = 0; cp_bpt = 32; break;
+        case 1: cp_base = reinterpret_cast<const uint8_t*>(ta.k_scale); cp_off = 32; cp_bpt = kSB; break;
+        case 2: cp_base = reinterpret_cast<const uint8_t*>(ta.k_zero); cp_off = 32 + kSB; cp_bpt = kSB; break;
+        case 3: cp_base = reinterpret_cast<const uint8_t*>(ta.v_codes); cp_off = 32 + 2 * kSB; cp_bpt = 32; break;
+        case 4: cp_base = reinterpret_cast<const uint8_t*>(ta.v_scale); cp_off = 64 + 2 * kSB; cp_bpt = kSB; break;
+        case 5: cp_base = reinterpret_cast<const uint8_t*>(ta.v_zero); cp_off = 64 + 3 * kSB; cp_bpt = kSB; break;
+        default: break;
+    }
+    grid_launch_dependents();                            // the merge launch may start as CTAs retire
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < a.stages; ++st) mbar_init(smem_u32(&sm.bar[st]), 1);
+        sm.fail = 0;
+        sm.issued = 0;
+        const long long g0 = (long long)blockIdx.x * s.per;
+        sm.wu = (int)(g0 / s.n_i);
+        sm.wk = (int)(g0 - (long long)sm.wu * s.n_i);
+        sm.wrem = (int)min(s.per, s.total - g0);
+        sm.cu = -1;
+        sm.cem = 0;
+        fence_mbar_init();
+    }
+    for (int x = threadIdx.x; x < (int)(sizeof(sm.qa) / 16); x += blockDim.x) (&sm.qa[0][0])[x] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (warp == 0)
+        for (int k = 0; k < a.stages; ++k) stream_issue<GK, CH>(a, s, sm, stage_base, k, cp_base, cp_off, cp_bpt);
+    __syncthreads();                                     // the first S records are visible
+
+    // A record is written when its item is requested, at least one CTA barrier before any
+    // warp reads it (S >= 2), so every warp takes the same path through the run.
+    bool ok = true;
+    int i = 0;
+    for (;;) {
+        const int4 m0 = sm.meta[i & (a.stages - 1)];
+        if (m0.y == kItEnd) break;
+        const int u = m0.x;
+        // the unit's query (base-2 logits; one query head per KV head) and fresh warp states
+        for (int x = threadIdx.x; x < D; x += blockDim.x) sm.q[0][x] = ldf(a.q, (size_t)u * D + x, bf) * a.scale_log2;
+        for (int x = threadIdx.x; x < W; x += blockDim.x) {
+            sm.wm[x][0] = kNegInf;
+            sm.wl[x][0] = 0.0f;
+        }
+        for (int x = threadIdx.x; x < W * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
+        __syncthreads();
+        int4 m = m0;
+        if (m.y == kItChunk) {
+            const Mk1Ctx<GK> x = mk1_ctx<GK>(a, sm);
+            Mk1Acc<GK> acc;
+            mk1_acc_init(acc);
+            do {
+                ok = wait_item(a, sm, i, ok);
+                const int n = m.w;
+                if constexpr (CH == kSub) {
+                    const int tl = warp * TPW;
+                    if (ok && tl < n)
+                        mk1_item<GK>(mk1_view<GK>((n + 31) & ~31, item_buf(a, stage_base, i)), tl, min(TPW, n - tl), x, acc);
+                } else if (ok) {
+                    const uint8_t* buf = item_buf(a, stage_base, i);
+#pragma unroll 1
+                    for (int h = 0; h < CH / kSub; ++h) {
+                        const int tl = h * kSub + warp * TPW;
+                        if (tl < n) mk1_item<GK>(mk1_view<GK>((n + 31) & ~31, buf), tl, min(TPW, n - tl), x, acc);
+                    }
+                }
+                stream_release<GK, CH>(a, s, sm, stage_base, i, cp_base, cp_off, cp_bpt);
+                m = sm.meta[++i & (a.stages - 1)];
+            } while (m.y == kItChunk && m.x == u);
+            mk1_flush<GK>(acc, sm);
+        }
+        if (m.y == kItRing && m.x == u) {
+            WarpAcc<1, D / 32> racc;
+            acc_init(racc);
+            do {
+                ok = wait_item(a, sm, i, ok);
+                const int n = m.w, w0 = warp * RPW;
+                if (ok && w0 < n) {
+                    const uint8_t* buf = item_buf(a, stage_base, i);
+                    const uint16_t* rk = reinterpret_cast<const uint16_t*>(buf);
+                    const uint16_t* rv = reinterpret_cast<const uint16_t*>(buf + a16((uint32_t)n * D * 2));
+                    residual_rows<1, D>(sm, rk + (size_t)w0 * D, rv + (size_t)w0 * D, min(RPW, n - w0), bf, racc,
+                                        nullptr, a.slots);
+                }
+                stream_release<GK, CH>(a, s, sm, stage_base, i, cp_base, cp_off, cp_bpt);
+                m = sm.meta[++i & (a.stages - 1)];
+            } while (m.y == kItRing && m.x == u);
+            flush_lane_values<1, D>(racc, sm);
+        }
+        if (m.y == kItNone && m.x == u) {                // nothing staged: its barrier completed at once
+            stream_release<GK, CH>(a, s, sm, stage_base, i, cp_base, cp_off, cp_bpt);
+            ++i;
+        }
+        __syncthreads();                                 // every warp's state is in shared memory
+        // the partial of (this CTA, u): slot blockIdx.x + u
+        float* pp = s.part + ((size_t)blockIdx.x + (size_t)u) * (D + 2);
+        for (int c = threadIdx.x; c < D; c += blockDim.x) {
+            float M = kNegInf;
+#pragma unroll
+            for (int w = 0; w < W; ++w) M = fmaxf(M, sm.wm[w][0]);
+            float L = 0.0f, O = 0.0f;
+            if (M != kNegInf) {
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    const float f = sm.wm[w][0] == kNegInf ? 0.0f : ex2_approx(sm.wm[w][0] - M);
+                    L = fmaf(sm.wl[w][0], f, L);
+                    O = fmaf(sm.wo[w][0][c], f, O);
+                }
+            }
+            pp[2 + c] = O;
+            if (c == 0) {
+                pp[0] = M;
+                pp[1] = L;
+            }
+        }
+        __syncthreads();                                 // before the next unit's query and states
+    }
+    __syncthreads();
+    if (sm.fail && threadIdx.x == 0) {
+        atomicOr(&g_status_decode, kDevTimeout);
+        // let every copy still in flight land before the buffers go away
+        const int S = a.stages, n = sm.issued;
+        for (int k = max(0, n - S); k < n; ++k)
+            (void)mbar_wait(smem_u32(&sm.bar[k & (S - 1)]), (uint32_t)(k >> a.stage_shift) & 1u, nullptr);
+    }
+}
+
+// Grid = (units), one thread per channel: the unit's partials (slots c + u of the CTAs whose
+// runs meet the unit) merged into o and lse, then its end-of-step work as the cluster
+// leader does it.  Launched as a programmatic dependent of the streamed launch: what does
+// not depend on it is read before the grid dependency wait.
+__global__ void __launch_bounds__(128) decode_stream_finalize(DecodeArgs a, StreamArgs s) {
+    constexpr int D = 128;
+    const int u = blockIdx.x, c = threadIdx.x;
+    const bool bf = a.bf16 != 0;
+    const int raw = a.tier[0].count[u], rl = a.res_len[u], rs = a.res_start[u], ps = a.pos[u];
+    const float kn = ldf(a.k_new, (size_t)u * D + c, bf), vn = ldf(a.v_new, (size_t)u * D + c, bf);
+    const long long first = (long long)u * s.n_i;
+    const int c0 = (int)(first / s.per), nseg = (int)((first + s.n_i - 1) / s.per) - c0 + 1;
+    const float* part = s.part + ((size_t)c0 + (size_t)u) * (D + 2);   // slot c + u, c = c0 .. c0 + nseg - 1
+    grid_dependency_wait();
+    // online merge of the partials (empty ones have sum 0)
+    float M = kNegInf, L = 0.0f, O = 0.0f;
+    for (int y = 0; y < nseg; ++y) {
+        const float* p = part + (size_t)y * (D + 2);
+        const float m = p[0], l = p[1], o = p[2 + c];
+        if (!(l > 0.0f)) continue;
+        if (m > M) {
+            const float f = M == kNegInf ? 0.0f : ex2_approx(M - m);
+            L = fmaf(L, f, l);
+            O = fmaf(O, f, o);
+            M = m;
+        } else {
+            const float w = ex2_approx(m - M);
+            L = fmaf(l, w, L);
+            O = fmaf(o, w, O);
+        }
+    }
+    stf(a.o, (size_t)u * D + c, O / L, bf);
+    if (c == 0 && a.lse_out) a.lse_out[u] = (M + __log2f(L)) * kLn2;
+    // the new token joins the ring, then the MiniKV flush when the ring is full
+    const int cap = a.res_cap, cnt = min(max(raw, 0), a.tier[0].cap);
+    const int len = min(max(rl, 0), cap - 1), start = min(max(rs, 0), cap - 1);
+    const size_t slot = (size_t)u * cap + (start + len) % cap;
+    stf(a.res_k, slot * D + c, kn, bf);
+    stf(a.res_v, slot * D + c, vn, bf);
+    if (c == 0) a.res_token_id[slot] = ps;
+    bool flushed = false;
+    if (len + 1 == a.nr + a.G) {                         // the same for every thread of the block
+        __syncthreads();                                 // the new row is in the ring
+        flushed = bf ? minikv_flush<__nv_bfloat16>(a, (size_t)u, start, cnt)
+                     : minikv_flush<__half>(a, (size_t)u, start, cnt);
+        if (!flushed && c == 0) atomicOr(&g_status_decode, kDevCheck);
+        __syncthreads();
+    }
+    if (c == 0) {
+        if (flushed) {
+            a.tier[0].count[u] = cnt + a.G;
+            a.res_start[u] = (start + a.G) % cap;
+            a.res_len[u] = len + 1 - a.G;
+        } else {
+            a.res_len[u] = len + 1;
+        }
+        a.pos[u] = ps + 1;
+    }
+}
+
 struct WsLayout {
     int slots;
-    size_t logits, lse2, meta, total;
+    size_t logits, lse2, meta, part, total;
 };
 
 WsLayout ws_layout(const kvq_cache& c) {
@@ -2070,6 +2426,11 @@ WsLayout ws_layout(const kvq_cache& c) {
     w.slots = slots;
     w.logits = 0;
     w.total = c.policy != KVQ_POLICY_MINIKV ? (size_t)units * g * slots * sizeof(float) : 0;
+    // MiniKV with one query head per KV head (streamed decode): a partial per (CTA, unit)
+    if (c.policy == KVQ_POLICY_MINIKV && g == 1 && c.D == 128) {
+        w.part = 0;
+        w.total = (size_t)(kStreamMaxCtas + units) * (c.D + 2) * sizeof(float);
+    }
     if (c.policy == KVQ_POLICY_MIKV) {
         w.lse2 = (w.total + 255) & ~(size_t)255;
         w.meta = w.lse2 + (size_t)units * 8 * sizeof(float);
@@ -2085,8 +2446,95 @@ int items_bound(const kvq_cache& c) {
     return n + (c.res_cap + kResItem - 1) / kResItem;
 }
 
+// Streamed decode (single heads, MiniKV format): as many CTAs as are resident at once, at
+// most kStreamMaxCtas; runs shorter than kStreamMinItems items per CTA take the cluster path.
+
+template <int GK>
+cudaError_t launch_stream(DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s, bool& used) {
+    constexpr int D = 128;
+    // tier chunks of 256 tokens where two buffers of them keep four CTAs per SM (G = 32)
+    constexpr int CH = GK == 32 ? 256 : 128;
+    used = false;
+    StreamArgs sa{};
+    sa.n_c = (c.tier[0].cap + CH - 1) / CH;
+    sa.n_r = (c.res_cap + kResItem - 1) / kResItem;
+    sa.n_i = sa.n_c + sa.n_r;
+    sa.total = (long long)units * sa.n_i;
+    sa.part = a.stream_part;
+    uint32_t stage = std::max(tier_stage_sizes(KVQ_AXIS_CHANNEL, 2, 2, CH, D, GK).total(),
+                              2u * a16((uint32_t)kResItem * D * 2));
+    stage = (stage + 127u) & ~127u;
+    const uint32_t sm_bytes = (uint32_t)((sizeof(Smem<1, D>) + 127) & ~(size_t)127);
+    const uint32_t qf_bytes = (uint32_t)(Cfg<1>::W * (GK == 16 ? 1536 : 512));
+    constexpr uint32_t kSmemLimit = 227u * 1024u;
+    auto smem_for = [&](int S) { return sm_bytes + qf_bytes + (uint32_t)S * stage; };
+    auto kern = decode_stream_kernel<GK, CH>;
+    // resident CTAs per SM with 2 and 4 staging buffers, and the SM count, per device
+    constexpr int kDevs = 16;
+    static int per_sm[kDevs][2], sms[kDevs];
+    static bool known[kDevs] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kDevs) return cudaSuccess;             // not used: the cluster path
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!known[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)std::min(smem_for(kMaxStages), kSmemLimit));
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+            for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+                per_sm[dev][k] = 0;
+                if (smem_for(2 << k) <= kSmemLimit)
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev][k], kern, Cfg<1>::kThreads,
+                                                                      smem_for(2 << k));
+            }
+            if (e != cudaSuccess) return e;
+            known[dev] = true;
+        }
+    }
+    // four buffers where they cost no resident CTA
+    const int S = per_sm[dev][1] >= per_sm[dev][0] && per_sm[dev][1] > 0 ? 4 : 2;
+    const long long resident = (long long)per_sm[dev][S == 4 ? 1 : 0] * sms[dev];
+    int ctas = (int)std::min<long long>(resident, kStreamMaxCtas);
+    if (ctas < 1 || sa.total < (long long)kStreamMinItems * ctas) return cudaSuccess;
+    sa.per = (sa.total + ctas - 1) / ctas;
+    ctas = (int)((sa.total + sa.per - 1) / sa.per);
+    a.cluster = 1;
+    a.stages = S;
+    a.stage_shift = S == 4 ? 2 : 1;
+    a.stage_bytes = stage;
+    a.qf_off = sm_bytes;
+    a.part_off = sm_bytes + qf_bytes;
+    a.stage_off = sm_bytes + qf_bytes;
+    kern<<<ctas, Cfg<1>::kThreads, smem_for(S), s>>>(a, sa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)units);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    used = true;
+    return cudaLaunchKernelEx(&cfg, decode_stream_finalize, a, sa);
+}
+
 template <int NG, int D, int FAM>
 cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s) {
+    if constexpr (NG == 1 && D == 128 && FAM == 1) {
+        if (c.policy == KVQ_POLICY_MINIKV && a.stream_part) {
+            bool used = false;
+            const cudaError_t e = c.G == 16 ? launch_stream<16>(a, c, units, s, used)
+                                            : launch_stream<32>(a, c, units, s, used);
+            if (e != cudaSuccess || used) return e;
+        }
+    }
     uint32_t stage = 2u * a16((uint32_t)kResItem * D * 2);
     for (int t = 0; t < c.n_tiers; ++t)
         stage = std::max(stage, tier_stage_sizes(c.tier[t].k_axis, c.tier[t].k_bits, c.tier[t].v_bits,
@@ -2290,6 +2738,9 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, c
                                              : nullptr;
     a.lse2_ws = c.policy == KVQ_POLICY_MIKV ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + w.lse2) : nullptr;
     a.meta_ws = c.policy == KVQ_POLICY_MIKV ? reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + w.meta) : nullptr;
+    a.stream_part = c.policy == KVQ_POLICY_MINIKV && a.g == 1 && c.D == 128 && ws
+                        ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + w.part)
+                        : nullptr;
     bool channel_only = true;
     for (int t = 0; t < c.n_tiers; ++t) channel_only &= c.tier[t].k_axis == KVQ_AXIS_CHANNEL;
     if (c.D == 64) return a.g == 1 ? launch_typed<1, 64, 1>(a, c, units, s) : cudaErrorInvalidConfiguration;

@@ -154,6 +154,16 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
     }
 }
 
+// Programmatic dependent launch: lets the grid launched after this one (with the
+// programmatic stream serialization attribute) start, and waits for the grid this one
+// depends on to complete with its memory visible.  Both are no-ops for grids launched
+// without the attribute.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
