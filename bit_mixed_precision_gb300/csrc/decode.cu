@@ -1536,14 +1536,14 @@ __device__ __forceinline__ void mk1_item(const View& v, int tl, int nt, const Mk
     for (int j = 0; j < 4; ++j) valid[j] = t == x.tv && 4 * g + j < nt;
     float mx = fmaxf(fmaxf(valid[0] ? lg[0] : kNegInf, valid[1] ? lg[1] : kNegInf),
                      fmaxf(valid[2] ? lg[2] : kNegInf, valid[3] ? lg[3] : kNegInf));
-    if (GK != 32) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    mx = __shfl_sync(0xffffffffu, mx, 0);
     // the reference moves only when the max rises by more than 2^8 (exact: the final
-    // division uses the same reference)
-    if (acc.m == kNegInf ? mx != kNegInf : mx > acc.m + 8.0f) {
+    // division uses the same reference); the warp's max is formed only then
+    if (__any_sync(0xffffffffu, acc.m == kNegInf ? mx != kNegInf : mx > acc.m + 8.0f)) {
+        if (GK != 32) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        mx = __shfl_sync(0xffffffffu, mx, 0);
         const float corr = acc.m == kNegInf ? 0.0f : ex2_approx(acc.m - mx);
         acc.m = mx;
         acc.l *= corr;
