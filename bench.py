@@ -80,6 +80,11 @@ def _peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+# what decode_attn_qkv launches: single-head MiniKV caches with at least 8 items per resident
+# CTA stream (two launches), every other cache runs the cluster kernel
+DECODE_KERNELS = ("decode_attn_qkv: decode_stream_kernel + decode_stream_finalize (single-head MiniKV, "
+                  "8+ items per resident CTA), else decode_kernel")
+
 KERNEL_SOURCES = {
     "decode_kernel": ["bit_mixed_precision_gb300/csrc/decode.cu", "bit_mixed_precision_gb300/csrc/kvq_common.cuh",
                       "bit_mixed_precision_gb300/csrc/pack_device.cuh"],
@@ -533,7 +538,7 @@ def run_sweep(args, wl, rank, world):
                     "frac_tensor": pre_tf / tf_peak},
         "segments_ms_per_step": {"prefill_build": pre_ms / args.steps, "decode": dec_ms / args.steps,
                                  "decode_input_copies_and_gaps": step_ms - (pre_ms + dec_ms) / args.steps},
-        "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": DECODE_KERNELS, "bound": "hbm", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": _traffic("decode_kernel", args.workload, B),
                      "per": "launch (one layer's decode, averaged over the 32 layers)",
@@ -656,7 +661,7 @@ def run_ours(args, wl, rank, world):
                                      "query-key pairs) of pass-1 QK^T and PV and of pass-2 QK^T, "
                                      "2 flops per multiply-add"},
         "segments_ms_per_step": {k2: v2 / args.steps for k2, v2 in seg.items()},
-        "roofline": {"kernel": "decode_kernel (decode_attn_qkv)", "bound": "hbm",
+        "roofline": {"kernel": DECODE_KERNELS, "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak,
                      "traffic": _traffic("decode_kernel", args.workload, wl["B"]),

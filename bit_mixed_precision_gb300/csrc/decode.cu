@@ -188,8 +188,8 @@ struct Smem {
     float wo[Cfg<NG>::W][NG][D];
     // logits of the warp's current group (CUDA-core per-token path: single heads only)
     // (single heads, MiniKV format: the warp's probabilities, 32 floats, then in the same
-    // bytes the probabilities times each value group's scale, fp16 [group][token])
-    float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 64 : 1];
+    // bytes the probabilities times each value group's scale, fp16 [group][40: 32 tokens])
+    float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 80 : 1];
     // per-token keys (GQA groups): the query's A fragments, [k-step][lane]; single heads:
     // zeros, read by the lanes that hold no column of a MiniKV-format B fragment
     uint4 qa[NG >= 2 ? 8 : 1][32];
@@ -1436,17 +1436,30 @@ __device__ __forceinline__ View mk1_view(int npad, const uint8_t* buf) {
 // hold two key scale rows (q * scale columns 0, 1 and 2, 3 of the key MMAs, the logits of
 // tokens 16..31 in lanes t = 1) and the values eight 16-channel groups (all eight B
 // columns of the P.V MMAs).
+// Shared-memory strides chosen so that the lanes of one fragment load hit distinct banks: a
+// query piece (hi or lo of one key scale row: [k-step][t][reg], 64 words) every 72 words, a
+// value group's 32 fp16 (p x scale) every 40 halves.
+constexpr int kQfPiece = 72, kPsGroup = 40;
+
 template <int GK>
 struct Mk1Ctx {
-    uint32_t* qf;            // this warp's query fragments ([piece][k-step][t][reg], 512 B per key row)
+    uint32_t* qf;            // this warp's query fragments, one piece every kQfPiece words
     float* pw;               // this warp's 32 probabilities
-    uint16_t* psw;           // probability x value scale, fp16 [group][token]
-    const uint2* qfb;        // B-fragment source of the key MMAs (query pieces or zeros)
-    const uint32_t* psb;     // B-fragment source of the P.V MMAs (value groups or zeros)
+    uint16_t* psw;           // probability x value scale, fp16, one group every kPsGroup halves
+    const uint2* qfb;        // B-fragment source of the key MMAs (a query piece)
+    const uint32_t* psb;     // B-fragment source of the P.V MMAs (a value group)
     float4 q4;               // query channels 4 lane .. 4 lane + 3 (base-2 scaled)
-    uint32_t bsel;           // byte permute of lane group g
+    uint32_t bsel;           // byte permute of lane group g (key codes)
+    uint32_t vsel;           // byte permute of the value codes (operands swapped for t >= 2)
+    int voff;                // word offset of the first value row a lane loads (t >= 2: the second)
     int tv;                  // the lane t that holds lane group g's logits
 };
+
+// Bytes of a warp's query fragments and (groups of 16) value-group products.
+template <int GK>
+constexpr uint32_t mk1_qf_warp_bytes() {
+    return GK == 32 ? 2u * kQfPiece * 4u : 4u * kQfPiece * 4u + 8u * kPsGroup * 2u;
+}
 
 template <int GK>
 __device__ __forceinline__ Mk1Ctx<GK> mk1_ctx(const DecodeArgs& a, Smem<1, 128>& sm) {
@@ -1456,18 +1469,19 @@ __device__ __forceinline__ Mk1Ctx<GK> mk1_ctx(const DecodeArgs& a, Smem<1, 128>&
     // probabilities (32 floats) and probability x value scale: over the probabilities for
     // GK = 32, after the fragments for GK = 16
     x.qf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(&sm) + a.qf_off +
-                                       (size_t)warp * (GK == 32 ? 512 : 1536));
+                                       (size_t)warp * mk1_qf_warp_bytes<GK>());
     x.pw = &sm.lg[warp][0][0];
-    x.psw = GK == 32 ? reinterpret_cast<uint16_t*>(x.pw) : reinterpret_cast<uint16_t*>(x.qf + 256);
-    const uint32_t* zero = reinterpret_cast<const uint32_t*>(&sm.qa[0][0]);
-    // lanes g < 2 NKR read the query pieces, g < NGV the value groups; the others read
-    // zeros (no per-step select)
-    x.qfb = g < 2 * NKR ? reinterpret_cast<const uint2*>(x.qf) + g * 32 + t
-                        : reinterpret_cast<const uint2*>(zero) + t;
-    x.psb = g < NGV ? reinterpret_cast<const uint32_t*>(x.psw + g * 32) + t : zero + t;
+    x.psw = GK == 32 ? reinterpret_cast<uint16_t*>(x.pw) : reinterpret_cast<uint16_t*>(x.qf + 4 * kQfPiece);
+    // column g of the B fragments: the query piece / value group g; columns past them feed
+    // MMA outputs nobody reads, so those lanes repeat a real piece / group (finite values,
+    // and their loads coincide with another lane's)
+    x.qfb = reinterpret_cast<const uint2*>(x.qf + (g & (2 * NKR - 1)) * kQfPiece) + t;
+    x.psb = reinterpret_cast<const uint32_t*>(x.psw + (g & (NGV - 1)) * kPsGroup) + t;
     x.tv = GK == 32 ? 0 : (g >> 2);
     x.q4 = *reinterpret_cast<const float4*>(&sm.q[0][4 * lane]);
     x.bsel = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
+    x.vsel = t >= 2 ? ((uint32_t)(4 + (g & 3)) | ((uint32_t)(g & 3) << 8)) : x.bsel;
+    x.voff = t >= 2 ? 8 : 0;
     return x;
 }
 
@@ -1493,11 +1507,11 @@ __device__ __forceinline__ void mk1_item(const View& v, int tl, int nt, const Mk
         bias[kr] = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
         // channel c = 16 s + 8 half + 2 tt + e sits in register half of lane tt, k-step s
         const int s_ = lane >> 2, half = (lane & 3) >> 1, tt = 2 * (lane & 1);
-        uint32_t* qh = x.qf + 128 * kr;
+        uint32_t* qh = x.qf + 2 * kQfPiece * kr;
         qh[(s_ * 4 + tt) * 2 + half] = hi01;
         qh[(s_ * 4 + tt + 1) * 2 + half] = hi23;
-        qh[64 + (s_ * 4 + tt) * 2 + half] = lo01;
-        qh[64 + (s_ * 4 + tt + 1) * 2 + half] = lo23;
+        qh[kQfPiece + (s_ * 4 + tt) * 2 + half] = lo01;
+        qh[kQfPiece + (s_ * 4 + tt + 1) * 2 + half] = lo23;
         bias[kr] = warp_sum(bias[kr]);
     }
     const float bias_g = NKR == 1 ? bias[0] : ((g >> 2) ? bias[NKR - 1] : bias[0]);
@@ -1588,29 +1602,30 @@ __device__ __forceinline__ void mk1_item(const View& v, int tl, int nt, const Mk
             sw[e] = ok_t ? sw[e] : 0u;
             zw[e] = ok_t ? zw[e] : 0u;
             const uint32_t ps2 = pack_h2(p * h2lo(sw[e]), p * h2hi(sw[e]));
-            x.psw[(2 * e) * 32 + lane] = (uint16_t)(ps2 & 0xffffu);
-            x.psw[(2 * e + 1) * 32 + lane] = (uint16_t)(ps2 >> 16);
+            x.psw[(2 * e) * kPsGroup + lane] = (uint16_t)(ps2 & 0xffffu);
+            x.psw[(2 * e + 1) * kPsGroup + lane] = (uint16_t)(ps2 >> 16);
             acc.zs[2 * e] = fmaf(p, h2lo(zw[e]), acc.zs[2 * e]);
             acc.zs[2 * e + 1] = fmaf(p, h2hi(zw[e]), acc.zs[2 * e + 1]);
         }
     }
     __syncwarp();
     // -- P.V over two k-steps of 16 tokens: B = (p s) of tokens 16 ks + 2t, + 1 (b0) and
-    // + 8, + 9 (b1) in column g (value group g; zeros past the groups)
+    // + 8, + 9 (b1) in column g (value group g).  Lanes t >= 2 load the rows of tokens
+    // k0 + 1 and k0 first (no bank shared with lanes t < 2) and swap the permute's operands.
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         const int k0 = 16 * ks + 2 * t;
         const uint32_t b0 = x.psb[8 * ks], b1 = x.psb[8 * ks + 4];
         const uint32_t* vrow = v.vc + (size_t)(tl + k0) * 8 + 4 * (g >> 2);
-        const uint4 xa = *reinterpret_cast<const uint4*>(vrow);
-        const uint4 xb = *reinterpret_cast<const uint4*>(vrow + 8);
-        const uint4 xc = *reinterpret_cast<const uint4*>(vrow + 64);
-        const uint4 xd = *reinterpret_cast<const uint4*>(vrow + 72);
+        const uint4 xa = *reinterpret_cast<const uint4*>(vrow + x.voff);
+        const uint4 xb = *reinterpret_cast<const uint4*>(vrow + (8 - x.voff));
+        const uint4 xc = *reinterpret_cast<const uint4*>(vrow + 64 + x.voff);
+        const uint4 xd = *reinterpret_cast<const uint4*>(vrow + (72 - x.voff));
         const uint32_t wa[4] = {xa.x, xa.y, xa.z, xa.w}, wb[4] = {xb.x, xb.y, xb.z, xb.w};
         const uint32_t wc[4] = {xc.x, xc.y, xc.z, xc.w}, wd[4] = {xd.x, xd.y, xd.z, xd.w};
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const uint32_t ya = __byte_perm(wa[w], wb[w], x.bsel), yc = __byte_perm(wc[w], wd[w], x.bsel);
+            const uint32_t ya = __byte_perm(wa[w], wb[w], x.vsel), yc = __byte_perm(wc[w], wd[w], x.vsel);
             const uint32_t a0[4] = {ya & kM0, ya & kM1, yc & kM0, yc & kM1};
             const uint32_t a1[4] = {ya & kM2, ya & kM3, yc & kM2, yc & kM3};
             mma16816(acc.o[w][0], a0, b0, b1);
@@ -2465,7 +2480,7 @@ cudaError_t launch_stream(DecodeArgs& a, const kvq_cache& c, int units, cudaStre
                               2u * a16((uint32_t)kResItem * D * 2));
     stage = (stage + 127u) & ~127u;
     const uint32_t sm_bytes = (uint32_t)((sizeof(Smem<1, D>) + 127) & ~(size_t)127);
-    const uint32_t qf_bytes = (uint32_t)(Cfg<1>::W * (GK == 16 ? 1536 : 512));
+    const uint32_t qf_bytes = (uint32_t)Cfg<1>::W * mk1_qf_warp_bytes<GK>();
     constexpr uint32_t kSmemLimit = 227u * 1024u;
     auto smem_for = [&](int S) { return sm_bytes + qf_bytes + (uint32_t)S * stage; };
     auto kern = decode_stream_kernel<GK, CH>;
@@ -2544,10 +2559,11 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     // per-channel keys on the tensor cores: each warp's query x scale rows
     bool has_channel = false;
     for (int t = 0; t < c.n_tiers; ++t) has_channel |= c.tier[t].k_axis == KVQ_AXIS_CHANNEL;
-    // (single heads with G = 16: two key scale rows and eight value groups per warp, 1.5 KB)
+    // (single heads: query pieces and, with G = 16, the value-group products of each warp)
     const uint32_t qf_bytes = (has_channel && D == 128 && NG <= 4)
-                                  ? (NG == 1 && c.G == 16 ? (uint32_t)(Cfg<NG>::W * 1536)
-                                                          : (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)))
+                                  ? (NG == 1 ? (uint32_t)Cfg<NG>::W * (c.G == 16 ? mk1_qf_warp_bytes<16>()
+                                                                                  : mk1_qf_warp_bytes<32>())
+                                             : (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)))
                                   : 0u;
     const uint32_t slot_bytes = (uint32_t)(NG * (D + 2) * sizeof(float));
     auto smem_for = [&](int C, int S) {
@@ -2560,7 +2576,7 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
     auto kern = decode_kernel<NG, D, FAM>;
     static bool attr_done = false, wide_ok = false;
     if (!attr_done) {
-        const uint32_t qf_max = NG == 1 ? (uint32_t)(Cfg<NG>::W * 1536)
+        const uint32_t qf_max = NG == 1 ? (uint32_t)Cfg<NG>::W * mk1_qf_warp_bytes<16>()
                                         : (NG <= 4 ? (uint32_t)(Cfg<NG>::W * 2 * NG * 128 * sizeof(uint16_t)) : 0u);
         cudaError_t e = cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
