@@ -67,7 +67,7 @@ template <int D> struct Layout {
     static constexpr uint32_t P2_SMEM = P2_BAR + 256 + 1024;
 };
 
-enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SFREE = 9, B_PF = 11, B_OD = 13,
+enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SCONS = 8, B_SFREE = 9, B_PF = 11, B_OD = 13,
              B_DRAIN = 14, B_VC = 15, P1_NBAR = 17 };
 enum P2Bar { C_KF = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_SFREE = 7, C_DRAIN = 9, C_LSE = 10,
              P2_NBAR = 12 };
@@ -149,10 +149,11 @@ __global__ void __launch_bounds__(192, 2)
             mbar_init(BAR(B_KF + s), 1);
             mbar_init(BAR(B_VF + s), 1);
             mbar_init(BAR(B_KVE + s), 1);
-            mbar_init(BAR(B_SF + s), 1);
-            mbar_init(BAR(B_SFREE + s), 1);              // P.V of the buffer's tile done
-            mbar_init(BAR(B_PF + s), 4);                 // P of the buffer's tile written
+            mbar_init(BAR(B_SFREE + s), 1);              // P.V of the P buffer's tile done
+            mbar_init(BAR(B_PF + s), 4);                 // P of the P buffer's tile written
         }
+        mbar_init(BAR(B_SF), 1);                         // S of the tile computed
+        mbar_init(BAR(B_SCONS), 4);                      // S of the tile loaded by every softmax warp
         mbar_init(BAR(B_OD), 1);
         mbar_init(BAR(B_DRAIN), 1);
         mbar_init(BAR(B_VC), 4);
@@ -165,7 +166,10 @@ __global__ void __launch_bounds__(192, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 2 * kBN;                 // S buffers at columns 0 and 64
+    // TMEM columns: S of the current tile [0, 64), P (fp16, two keys per column) of even and
+    // odd tiles [64, 96) and [96, 128), O [128, 256).  The S buffer is free again as soon as
+    // every softmax warp has loaded it, so the next QK^T overlaps the softmax.
+    const uint32_t tO = tmem + 2 * kBN;
 
     if (warp == 4) {
         if (lane == 0) {
@@ -207,15 +211,15 @@ __global__ void __launch_bounds__(192, 2)
             // P is always fp16; bf16 V tiles are converted to fp16 in smem first
             const uint32_t idPV = idesc_f16(0, 128, D, 1);
             bool ok = mbar_wait(BAR(B_Q), 0, abort_flag);
-            // O += P V with P (fp16, two keys per 32-bit column) read from the
-            // first 32 columns of the tile's S buffer
+            // O += P V with P (fp16, two keys per 32-bit column) read from the P
+            // buffer of the tile's parity
             auto issue_pv = [&](int jj) -> bool {
                 if (!mbar_wait(BAR(B_PF + (jj & 1)), (jj >> 1) & 1, abort_flag)) return false;
                 if (!mbar_wait(BAR((AB ? B_VC : B_VF) + (jj & 1)), (jj >> 1) & 1, abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t vt = sV + (uint32_t)(jj & 1) * kKVBytes;
-                const uint32_t tP = tmem + (uint32_t)(jj & 1) * kBN;
+                const uint32_t tP = tmem + (uint32_t)kBN + (uint32_t)(jj & 1) * (kBN / 2);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     tc_mma_f16_ta(tO, tP + (uint32_t)kk * 8u, mnmajor_desc(vt, kk, kKVHalf), idPV,
@@ -228,17 +232,16 @@ __global__ void __launch_bounds__(192, 2)
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int st = j & 1;
                 if (!mbar_wait(BAR(B_KF + st), (j >> 1) & 1, abort_flag)) { ok = false; break; }
-                if (j >= 2 && !mbar_wait(BAR(B_SFREE + st), ((j - 2) >> 1) & 1, abort_flag)) {
+                if (j >= 1 && !mbar_wait(BAR(B_SCONS), (j - 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tS = tmem + (uint32_t)st * kBN;
                 const uint32_t kt = sK + (uint32_t)st * kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_f16(tS, kmajor_desc(sQ, kk), kmajor_desc(kt, kk, kKVHalf), idS, kk > 0 ? 1u : 0u);
-                tc_commit(BAR(B_SF + st));
+                    tc_mma_f16(tmem, kmajor_desc(sQ, kk), kmajor_desc(kt, kk, kKVHalf), idS, kk > 0 ? 1u : 0u);
+                tc_commit(BAR(B_SF));
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
             if (ok) ok = issue_pv(n_kv - 1);
@@ -257,13 +260,17 @@ __global__ void __launch_bounds__(192, 2)
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const int sb = j & 1;
-            if (!warp_wait(BAR(B_SF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!warp_wait(BAR(B_SF), j & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             float s[kBN];
 #pragma unroll
             for (int c4 = 0; c4 < kBN / 32; ++c4)
-                tmem_ld32(tmem + lane_base + (uint32_t)sb * kBN + (uint32_t)c4 * 32u, s + c4 * 32);
+                tmem_ld32(tmem + lane_base + (uint32_t)c4 * 32u, s + c4 * 32);
             tmem_wait_ld();
+            // S is in registers: the next tile's QK^T may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_SCONS));
             if (AB) {
                 // bf16 -> fp16 of this thread's share of the V tile (exact for |v| < 65504)
                 if (!warp_wait(BAR(B_VF + sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -326,8 +333,8 @@ __global__ void __launch_bounds__(192, 2)
                 if (j >= 1) l *= ex2_approx(m_used - m_new);
                 m_used = m_new;
             }
-            // P (fp16) over the first 32 columns of this tile's S buffer: column c
-            // holds keys 2c (low half) and 2c + 1 (high half) of row r.  Exponents
+            // P (fp16) in the 32 columns of the P buffer of this tile's parity: column
+            // c holds keys 2c (low half) and 2c + 1 (high half) of row r.  Exponents
             // s * scale - m and the row sum go two keys per instruction (packed
             // float32 pairs); the eight partial sums are those of keys c mod 8.
             unsigned long long rsp2[4] = {0ull, 0ull, 0ull, 0ull};
@@ -345,7 +352,10 @@ __global__ void __launch_bounds__(192, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) f2_unpack(rsp2[e], rsp[2 * e], rsp[2 * e + 1]);
             l += ((rsp[0] + rsp[1]) + (rsp[2] + rsp[3])) + ((rsp[4] + rsp[5]) + (rsp[6] + rsp[7]));
-            tmem_st32(tmem + lane_base + (uint32_t)sb * kBN, pk);
+            // the P buffer of this parity is free once P.V of tile j - 2 is done
+            if (j >= 2 && !warp_wait(BAR(B_SFREE + sb), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            tmem_st32(tmem + lane_base + (uint32_t)kBN + (uint32_t)sb * (kBN / 2), pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
