@@ -67,6 +67,7 @@ template <int D> struct Layout {
     static constexpr uint32_t P2_SMEM = P2_BAR + 256 + 1024;
 };
 
+constexpr int kKVPrefetch = 4;     // pass 1: K/V tiles prefetched into L2 this far ahead
 enum P1Bar { B_Q = 0, B_KF = 1, B_VF = 3, B_KVE = 5, B_SF = 7, B_SCONS = 8, B_SFREE = 9, B_PF = 11, B_OD = 13,
              B_DRAIN = 14, B_VC = 15, P1_NBAR = 17 };
 enum P2Bar { C_KF = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_SFREE = 7, C_DRAIN = 9, C_LSE = 10,
@@ -195,6 +196,13 @@ __global__ void __launch_bounds__(192, 2)
                 for (int hf = 0; hf < kHalves; ++hf)
                     tma_load_3d(vdst + hf * kKVHalf, &tv, 64 * hf, j * kBN, bhkv, BAR(B_VF + st));
                 last[st] = j;
+                // the tile requested kKVPrefetch tiles from now waits for a P.V to free its
+                // buffer: have it in L2 by then
+                if (j + kKVPrefetch < n_kv)
+                    for (int hf = 0; hf < kHalves; ++hf) {
+                        tma_prefetch_3d(&tk, 64 * hf, (j + kKVPrefetch) * kBN, bhkv);
+                        tma_prefetch_3d(&tv, 64 * hf, (j + kKVPrefetch) * kBN, bhkv);
+                    }
             }
             // every issued copy has landed before the CTA may exit
             mbar_wait(BAR(B_Q), 0, nullptr);
