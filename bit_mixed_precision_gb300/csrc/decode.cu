@@ -1505,13 +1505,11 @@ __device__ __forceinline__ void mk1_item(const View& v, int tl, int nt, const Mk
         const uint32_t lo01 = pack_h2(x0 - h2lo(hi01), x1 - h2hi(hi01));
         const uint32_t lo23 = pack_h2(x2 - h2lo(hi23), x3 - h2hi(hi23));
         bias[kr] = fmaf(q4.x, h2lo(z2.x), fmaf(q4.y, h2hi(z2.x), fmaf(q4.z, h2lo(z2.y), q4.w * h2hi(z2.y))));
-        // channel c = 16 s + 8 half + 2 tt + e sits in register half of lane tt, k-step s
-        const int s_ = lane >> 2, half = (lane & 3) >> 1, tt = 2 * (lane & 1);
+        // the MMA's k = 2t, 2t + 1, 2t + 8, 2t + 9 of k-step s are channels 16 s + 4t .. + 3:
+        // lane 4s + t holds exactly the B registers of lane t at k-step s
         uint32_t* qh = x.qf + 2 * kQfPiece * kr;
-        qh[(s_ * 4 + tt) * 2 + half] = hi01;
-        qh[(s_ * 4 + tt + 1) * 2 + half] = hi23;
-        qh[kQfPiece + (s_ * 4 + tt) * 2 + half] = lo01;
-        qh[kQfPiece + (s_ * 4 + tt + 1) * 2 + half] = lo23;
+        reinterpret_cast<uint2*>(qh)[lane] = make_uint2(hi01, hi23);
+        reinterpret_cast<uint2*>(qh + kQfPiece)[lane] = make_uint2(lo01, lo23);
         bias[kr] = warp_sum(bias[kr]);
     }
     const float bias_g = NKR == 1 ? bias[0] : ((g >> 2) ? bias[NKR - 1] : bias[0]);
@@ -1529,10 +1527,10 @@ __device__ __forceinline__ void mk1_item(const View& v, int tl, int nt, const Mk
         const uint32_t* rowp = v.kc + (size_t)((tl >> 4) + (g >> 2)) * 128;
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-            const uint2 w0 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t);
-            const uint2 w1 = *reinterpret_cast<const uint2*>(rowp + 16 * s + 2 * t + 8);
+            // channels 16 s + 4t .. + 3 (the k order above): one 16-byte load
+            const uint4 w = *reinterpret_cast<const uint4*>(rowp + 16 * s + 4 * t);
             const uint2 b = x.qfb[s * 4];
-            const uint32_t y0 = __byte_perm(w0.x, w0.y, x.bsel), y1 = __byte_perm(w1.x, w1.y, x.bsel);
+            const uint32_t y0 = __byte_perm(w.x, w.y, x.bsel), y1 = __byte_perm(w.z, w.w, x.bsel);
             const uint32_t a0[4] = {y0 & kM0, y0 & kM1, y1 & kM0, y1 & kM1};
             const uint32_t a1[4] = {y0 & kM2, y0 & kM3, y1 & kM2, y1 & kM3};
             mma16816(R[0][s & 1], a0, b.x, b.y);
