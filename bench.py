@@ -228,7 +228,8 @@ class Hot:
             self.kh = torch.full((B * Hkv,), self.k_hh, dtype=torch.int32, device=dev)
             self.idx = torch.empty((B, Hkv, self.n_sel), dtype=torch.int32, device=dev)
             self.nout = torch.empty((B * Hkv,), dtype=torch.int32, device=dev)
-            self.launches_per_step = 2 + 1 + steps           # the residual flush runs inside decode
+            # prefill passes, the build, then every decode call (the flush runs inside it)
+            self.launches_per_step = 2 + 1 + steps * kvq.decode_launches(self.cache)
         elif pol == "diffkv":
             f = inputs.dirichlet_fractions(B * Hkv, seed=seed)
             nc = T - nr
@@ -252,14 +253,16 @@ class Hot:
             self.fixed_bytes = sum(kvq.lib().kvq_tier_bytes(B * Hkv, D, G, s.k_bits, s.v_bits, s.k_axis,
                                                             (c + 31) // 32 * 32, None)
                                    for s, c in zip([kvq.TierSpec(8, 4, 1, 0), kvq.TierSpec(4, 2, 1, 0)], caps))
-            self.launches_per_step = 2 + 1 + (1 if wl.get("paged") else 0) + 2 * steps
+            self.launches_per_step = (2 + 1 + (1 if wl.get("paged") else 0)
+                                      + steps * (kvq.decode_launches(self.cache) + 1))   # + policy step
         else:
             nq = T - nr + steps
             self.cache = kvq.make_cache(B, Hq, Hkv, D, G, self.dtype, kvq.POLICY_MIKV,
                                         [kvq.TierSpec(4, 4, kvq.AXIS_TOKEN, nq // 5 + 64),
                                          kvq.TierSpec(2, 2, kvq.AXIS_TOKEN, nq + 64)],
                                         nr=nr, score_cap=T + steps + 1, hi_den=5, device=dev)
-            self.launches_per_step = 2 + 1 + 3 * steps          # decode, score update, policy step
+            # decode (and its score update), policy step
+            self.launches_per_step = 2 + 1 + steps * (kvq.decode_launches(self.cache) + 1)
         self.o_pre = torch.empty_like(self.q)
         self.lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
         self.cs = torch.empty_like(self.lse)
@@ -362,7 +365,7 @@ class Sweep:
         self.o_dec = torch.empty((L, B, H, D), dtype=torch.float16, device=dev)
         self.graph = None
         self.prefill_flops = 3 * D * T * T * B * H * L
-        self.launches_per_step = L * (2 + 1 + steps)
+        self.launches_per_step = sum(2 + 1 + steps * kvq.decode_launches(ly["cache"]) for ly in self.layers)
 
     def prefill_build(self, s):
         kvq = self.kvq

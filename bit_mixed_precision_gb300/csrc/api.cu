@@ -227,6 +227,11 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* c) {
     return kvq::decode_workspace_bytes(*c);
 }
 
+int kvq_decode_launches(const kvq_cache* c) {
+    if (check_cache(c, "kvq_decode_launches") != KVQ_OK) return -1;
+    return kvq::decode_launches(*c);
+}
+
 kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
                            float sm_scale, void* o, float* lse_out, void* ws, size_t ws_bytes,
                            void* stream) {

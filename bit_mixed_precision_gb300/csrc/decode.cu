@@ -55,6 +55,9 @@ constexpr int kMinItemsPerCta = 34, kMinItemsPerCtaMikv = 64;
 // streamed decode: CTAs at most (the workspace holds one partial per (CTA, unit) pair, at
 // most ctas + units - 1 of them), and static items per CTA at least
 constexpr int kStreamMaxCtas = 1024, kStreamMinItems = 8;
+// streamed decode: tier chunk tokens (256 where two buffers of them keep four CTAs per SM)
+template <int GK>
+constexpr int kStreamChunk = GK == 32 ? 256 : 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
@@ -2462,25 +2465,30 @@ int items_bound(const kvq_cache& c) {
 // Streamed decode (single heads, MiniKV format): as many CTAs as are resident at once, at
 // most kStreamMaxCtas; runs shorter than kStreamMinItems items per CTA take the cluster path.
 
+// The streamed launch's shape for a cache (device-dependent: resident CTAs per SM).
+struct StreamPlan {
+    bool used;                   // false: the cluster path
+    StreamArgs sa;
+    int ctas, S;
+    uint32_t stage, sm_bytes, qf_bytes, smem;
+};
+
 template <int GK>
-cudaError_t launch_stream(DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s, bool& used) {
-    constexpr int D = 128;
-    // tier chunks of 256 tokens where two buffers of them keep four CTAs per SM (G = 32)
-    constexpr int CH = GK == 32 ? 256 : 128;
-    used = false;
-    StreamArgs sa{};
+cudaError_t stream_plan(const kvq_cache& c, int units, StreamPlan& p) {
+    constexpr int D = 128, CH = kStreamChunk<GK>;
+    p = StreamPlan{};
+    StreamArgs& sa = p.sa;
     sa.n_c = (c.tier[0].cap + CH - 1) / CH;
     sa.n_r = (c.res_cap + kResItem - 1) / kResItem;
     sa.n_i = sa.n_c + sa.n_r;
     sa.total = (long long)units * sa.n_i;
-    sa.part = a.stream_part;
     uint32_t stage = std::max(tier_stage_sizes(KVQ_AXIS_CHANNEL, 2, 2, CH, D, GK).total(),
                               2u * a16((uint32_t)kResItem * D * 2));
-    stage = (stage + 127u) & ~127u;
-    const uint32_t sm_bytes = (uint32_t)((sizeof(Smem<1, D>) + 127) & ~(size_t)127);
-    const uint32_t qf_bytes = (uint32_t)Cfg<1>::W * mk1_qf_warp_bytes<GK>();
+    p.stage = (stage + 127u) & ~127u;
+    p.sm_bytes = (uint32_t)((sizeof(Smem<1, D>) + 127) & ~(size_t)127);
+    p.qf_bytes = (uint32_t)Cfg<1>::W * mk1_qf_warp_bytes<GK>();
     constexpr uint32_t kSmemLimit = 227u * 1024u;
-    auto smem_for = [&](int S) { return sm_bytes + qf_bytes + (uint32_t)S * stage; };
+    auto smem_for = [&](int S) { return p.sm_bytes + p.qf_bytes + (uint32_t)S * p.stage; };
     auto kern = decode_stream_kernel<GK, CH>;
     // resident CTAs per SM with 2 and 4 staging buffers, and the SM count, per device
     constexpr int kDevs = 16;
@@ -2508,20 +2516,33 @@ cudaError_t launch_stream(DecodeArgs& a, const kvq_cache& c, int units, cudaStre
         }
     }
     // four buffers where they cost no resident CTA
-    const int S = per_sm[dev][1] >= per_sm[dev][0] && per_sm[dev][1] > 0 ? 4 : 2;
-    const long long resident = (long long)per_sm[dev][S == 4 ? 1 : 0] * sms[dev];
+    p.S = per_sm[dev][1] >= per_sm[dev][0] && per_sm[dev][1] > 0 ? 4 : 2;
+    const long long resident = (long long)per_sm[dev][p.S == 4 ? 1 : 0] * sms[dev];
     int ctas = (int)std::min<long long>(resident, kStreamMaxCtas);
     if (ctas < 1 || sa.total < (long long)kStreamMinItems * ctas) return cudaSuccess;
     sa.per = (sa.total + ctas - 1) / ctas;
-    ctas = (int)((sa.total + sa.per - 1) / sa.per);
+    p.ctas = (int)((sa.total + sa.per - 1) / sa.per);
+    p.smem = smem_for(p.S);
+    p.used = true;
+    return cudaSuccess;
+}
+
+template <int GK>
+cudaError_t launch_stream(DecodeArgs& a, const kvq_cache& c, int units, cudaStream_t s, bool& used) {
+    constexpr int D = 128;
+    used = false;
+    StreamPlan p;
+    cudaError_t e = stream_plan<GK>(c, units, p);
+    if (e != cudaSuccess || !p.used) return e;
+    p.sa.part = a.stream_part;
     a.cluster = 1;
-    a.stages = S;
-    a.stage_shift = S == 4 ? 2 : 1;
-    a.stage_bytes = stage;
-    a.qf_off = sm_bytes;
-    a.part_off = sm_bytes + qf_bytes;
-    a.stage_off = sm_bytes + qf_bytes;
-    kern<<<ctas, Cfg<1>::kThreads, smem_for(S), s>>>(a, sa);
+    a.stages = p.S;
+    a.stage_shift = p.S == 4 ? 2 : 1;
+    a.stage_bytes = p.stage;
+    a.qf_off = p.sm_bytes;
+    a.part_off = p.sm_bytes + p.qf_bytes;
+    a.stage_off = p.sm_bytes + p.qf_bytes;
+    decode_stream_kernel<GK, kStreamChunk<GK>><<<p.ctas, Cfg<1>::kThreads, p.smem, s>>>(a, p.sa);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -2535,7 +2556,7 @@ cudaError_t launch_stream(DecodeArgs& a, const kvq_cache& c, int units, cudaStre
     cfg.attrs = at;
     cfg.numAttrs = 1;
     used = true;
-    return cudaLaunchKernelEx(&cfg, decode_stream_finalize, a, sa);
+    return cudaLaunchKernelEx(&cfg, decode_stream_finalize, a, p.sa);
 }
 
 template <int NG, int D, int FAM>
@@ -2684,6 +2705,18 @@ cudaError_t launch_typed(DecodeArgs& a, const kvq_cache& c, int units, cudaStrea
 }  // namespace
 
 size_t decode_workspace_bytes(const kvq_cache& c) { return ws_layout(c).total; }
+
+int decode_launches(const kvq_cache& c) {
+    const int units = c.B * c.Hkv;
+    int n = c.policy == KVQ_POLICY_MIKV ? 2 : 1;               // MiKV: the score kernel after the step
+    if (c.policy == KVQ_POLICY_MINIKV && c.Hq == c.Hkv && c.D == 128) {
+        StreamPlan p;
+        const cudaError_t e = c.G == 16 ? stream_plan<16>(c, units, p) : stream_plan<32>(c, units, p);
+        if (e != cudaSuccess) return -1;
+        if (p.used) n = 2;                                     // streamed: the merge launch after it
+    }
+    return n;
+}
 
 namespace {
 std::atomic<int> g_withhold_copy{0};

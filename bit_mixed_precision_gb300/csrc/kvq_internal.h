@@ -35,6 +35,7 @@ cudaError_t launch_score_reduce(const float* cs, int B, int Hq, int Hkv, int T, 
                                 float* out, cudaStream_t s);
 
 size_t decode_workspace_bytes(const kvq_cache& c);
+int decode_launches(const kvq_cache& c);
 void set_withhold_copy(int on);
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new, const kvq_cache& c,
                           float sm_scale, void* o, float* lse_out, void* ws, cudaStream_t s);

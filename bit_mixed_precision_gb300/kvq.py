@@ -27,7 +27,7 @@ MAX_TIERS = 2
 EXPORTS = ["kv_quant_pack", "prefill_attn_scores", "prefill_window_scores", "kvq_score_reduce", "select_tokens",
            "minikv_prefill_build", "requant_demote", "decode_attn_qkv", "decode_attn_qkv_static",
            "kvq_pages_init", "kvq_pages_release",
-           "kvq_decode_workspace_bytes", "kvq_tier_bytes",
+           "kvq_decode_workspace_bytes", "kvq_decode_launches", "kvq_tier_bytes",
            "kvq_last_error", "kvq_device_status", "kvq_debug_withhold_copy", "kvq_version"]
 
 
@@ -98,6 +98,8 @@ def lib():
         L.decode_attn_qkv_static.restype = ctypes.c_int
         L.kvq_decode_workspace_bytes.argtypes = [ctypes.POINTER(KvqCache)]
         L.kvq_decode_workspace_bytes.restype = sz
+        L.kvq_decode_launches.argtypes = [ctypes.POINTER(KvqCache)]
+        L.kvq_decode_launches.restype = ctypes.c_int
         L.kvq_tier_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
         L.kvq_tier_bytes.restype = sz
         L.kvq_last_error.restype = ctypes.c_char_p
@@ -512,6 +514,14 @@ def decode_attn_qkv(q, k_new, v_new, cache, sm_scale=None, o=None, lse=None, str
 
 
 STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_launches(cache):
+    """Kernel launches one decode_attn_qkv call makes for the cache on the current device."""
+    n = lib().kvq_decode_launches(ctypes.byref(cache.desc))
+    if n < 0:
+        raise KvqError(KVQ_EINVAL, lib().kvq_last_error().decode())
+    return n
 
 
 def decode_attn_qkv_static(q, k_new, v_new, cache, sm_scale=None, o=None, lse=None, stream=None):

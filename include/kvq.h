@@ -303,15 +303,28 @@ kvq_status requant_demote(kvq_cache* c, kvq_policy mode, const kvq_policy_params
  *   tokens its G oldest are packed into tier 0 (keys per channel, values per
  *   token) and leave the ring.  seq_len and res_len advance by one.
  *   ws (device) of at least kvq_decode_workspace_bytes(c) bytes, 256-byte
- *   aligned (may be NULL when that is 0, as for MiniKV); its content between
- *   calls is irrelevant. */
+ *   aligned (may be NULL when that is 0); its content between calls is
+ *   irrelevant.
+ *   Launches: MiniKV caches with one query head per KV head and D = 128 whose
+ *   units hold at least 8 chunk or ring items per resident CTA run as one
+ *   list split evenly over the resident CTAs, then a merge launch (the merge,
+ *   the ring append, the flush and the counters); every other cache runs one
+ *   thread-block cluster per unit (MiKV: then a score launch).
+ *   kvq_decode_launches(c) gives the count. */
 kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
                            float sm_scale, void* o, float* lse_out, void* ws, size_t ws_bytes,
                            void* stream);
 
 /* Bytes of decode workspace the cache needs (DiffKV, MiKV: the step's
- * logits; MiniKV: 0), or (size_t)-1 on an invalid cache. */
+ * logits; MiniKV with one query head per KV head and D = 128: one partial
+ * state, 528 bytes, per (CTA, unit, warp) of the list launch, for at most
+ * 1024 CTAs; other MiniKV caches: 0), or (size_t)-1 on an invalid cache. */
 size_t kvq_decode_workspace_bytes(const kvq_cache* c);
+
+/* Kernel launches one decode_attn_qkv call on the current device makes for
+ * the cache (1 or 2), or -1 on an invalid cache or a failed device query.
+ * Host-only: queries the device's occupancy, launches nothing. */
+int kvq_decode_launches(const kvq_cache* c);
 
 /* Size of the scratch array built into the library for decode_attn_qkv_static. */
 #define KVQ_STATIC_SCRATCH_BYTES (16u << 20)

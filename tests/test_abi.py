@@ -95,6 +95,7 @@ def test_host_validation_without_gpu(L):
     assert L.decode_attn_qkv(vp, vp, vp, ctypes.byref(c), ctypes.c_float(0.1), vp, None, vp, 1 << 20,
                              None) == kvq.KVQ_EINVAL
     assert L.kvq_decode_workspace_bytes(ctypes.byref(c)) == ctypes.c_size_t(-1).value
+    assert L.kvq_decode_launches(ctypes.byref(c)) == -1
     assert L.kvq_version() == 100
 
 

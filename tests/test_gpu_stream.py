@@ -24,6 +24,7 @@ def _decode_against_oracle(cache, x, T, units, G, seed):
     scale = 1.0 / math.sqrt(D)
     n_chunks = (cache.tiers[0].spec.cap + 127) // 128
     assert B * H * (n_chunks + (cache.res_cap + 7) // 8) >= 8 * 1024
+    assert kvq.decode_launches(cache) == 2, "the list launch and its merge launch" 
     for t in range(STEPS):
         qd, kd, vd = (z.cuda() for z in inputs.make_decode_step(B, H, H, D, t, seed=seed))
         od, ld = kvq.decode_attn_qkv(qd, kd, vd, cache, scale)
