@@ -317,8 +317,9 @@ kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, 
 
 /* Bytes of decode workspace the cache needs (DiffKV, MiKV: the step's
  * logits; MiniKV with one query head per KV head and D = 128: one partial
- * state, 528 bytes, per (CTA, unit, warp) of the list launch, for at most
- * 1024 CTAs; other MiniKV caches: 0), or (size_t)-1 on an invalid cache. */
+ * state (max, sum, 128 outputs: 520 bytes) per (CTA, unit) pair of the list
+ * launch, for at most 1024 CTAs; other MiniKV caches: 0), or (size_t)-1 on
+ * an invalid cache. */
 size_t kvq_decode_workspace_bytes(const kvq_cache* c);
 
 /* Kernel launches one decode_attn_qkv call on the current device makes for
