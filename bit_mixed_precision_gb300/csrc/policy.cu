@@ -655,7 +655,60 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_build(PolicyArgs a) {
 struct MikvShared {
     TopkShared tk;
     uint32_t cnt_eq;
+    uint32_t kmin, kmax;                 // the population's smallest and largest ranking keys
 };
+
+// One warp: INT4 slot i of tier th dequantised and re-quantised into slot `slot` of tier
+// tl, group-parallel for G = 32 (lanes 0 .. D/32 - 1 the key groups, the next D/32 lanes
+// the value groups); other group sizes run serially on lane 0.
+__device__ void requant_row_warp(const PolicyArgs& a, const TierDev& th, const TierDev& tl, size_t unit, int i,
+                                 int slot) {
+    const int lane = threadIdx.x & 31;
+    const int D = a.D, G = a.G, ng = D / G;
+    const uint32_t* k4 = krow(th, unit, i, D);
+    const uint32_t* v4 = vrow(th, unit, i, D);
+    const size_t s4 = srow(th, unit, i, D, G);
+    if (G != 32 || 2 * ng > 32) {
+        if (lane == 0) {
+            quant_row([&](int c) {
+                          return dequant(code_at(k4, c, th.k_bits), h2f_bits(th.k_scale[s4 + c / G]),
+                                         h2f_bits(th.k_zero[s4 + c / G]));
+                      },
+                      D, G, tl.k_bits, krow(tl, unit, slot, D), tl.k_scale + srow(tl, unit, slot, D, G),
+                      tl.k_zero + srow(tl, unit, slot, D, G));
+            quant_row([&](int c) {
+                          return dequant(code_at(v4, c, th.v_bits), h2f_bits(th.v_scale[s4 + c / G]),
+                                         h2f_bits(th.v_zero[s4 + c / G]));
+                      },
+                      D, G, tl.v_bits, vrow(tl, unit, slot, D), tl.v_scale + srow(tl, unit, slot, D, G),
+                      tl.v_zero + srow(tl, unit, slot, D, G));
+            tl.token_id[unit * tl.cap + slot] = th.token_id[unit * th.cap + i];
+        }
+        return;
+    }
+    if (lane < 2 * ng) {
+        const bool isv = lane >= ng;
+        const int grp = isv ? lane - ng : lane;
+        const uint32_t* src = isv ? v4 : k4;
+        const int sb = isv ? th.v_bits : th.k_bits, db = isv ? tl.v_bits : tl.k_bits;
+        const float sc = h2f_bits((isv ? th.v_scale : th.k_scale)[s4 + grp]);
+        const float zp = h2f_bits((isv ? th.v_zero : th.k_zero)[s4 + grp]);
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = dequant(code_at(src, grp * 32 + c, sb), sc, zp);
+        const QParams q = params32(v, db);
+        uint32_t* codes = (isv ? vrow(tl, unit, slot, D) : krow(tl, unit, slot, D)) + grp * db;
+        switch (db) {
+            case 2: pack32<2>(v, q, codes, 1); break;
+            case 4: pack32<4>(v, q, codes, 1); break;
+            default: pack32<8>(v, q, codes, 1); break;
+        }
+        const size_t so = srow(tl, unit, slot, D, G) + grp;
+        (isv ? tl.v_scale : tl.k_scale)[so] = q.s_bits;
+        (isv ? tl.v_zero : tl.k_zero)[so] = q.z_bits;
+    }
+    if (lane == 0) tl.token_id[unit * tl.cap + slot] = th.token_id[unit * th.cap + i];
+}
 
 // Oldest residual token leaves; the top floor(N_q / hi_den) by cumulative
 // score (ties to the lower position) is recomputed; INT4 tokens outside it
@@ -683,15 +736,40 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a, int key_ca
     // the ranking keys of the population, gathered once into shared memory when
     // they fit (every pass of the selection then reads them from there)
     uint32_t* kc = reinterpret_cast<uint32_t*>(holes + th.cap);
+    int start_shift = 24;                              // the radix digit the selection starts at
+    uint32_t kpfx = 0;
     if (key_cache) {
-        for (int i = threadIdx.x; i < nq; i += blockDim.x) kc[i] = orderable(cum[id_of(i)]);
+        if (threadIdx.x == 0) {
+            sh.kmin = 0xffffffffu;
+            sh.kmax = 0u;
+        }
         __syncthreads();
+        uint32_t mn = 0xffffffffu, mx = 0u;
+        for (int i = threadIdx.x; i < nq; i += blockDim.x) {
+            const uint32_t kv = orderable(cum[id_of(i)]);
+            kc[i] = kv;
+            mn = min(mn, kv);
+            mx = max(mx, kv);
+        }
+        mn = __reduce_min_sync(0xffffffffu, mn);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        if ((threadIdx.x & 31) == 0) {
+            atomicMin(&sh.kmin, mn);
+            atomicMax(&sh.kmax, mx);
+        }
+        __syncthreads();
+        // the keys share their leading bits down to the first one where min and max differ:
+        // the selection starts at the 8-bit digit holding that bit
+        const uint32_t diff = sh.kmin ^ sh.kmax;
+        const int lead = diff ? __clz(diff) : 32;
+        start_shift = lead >= 32 ? 0 : 24 - 8 * (lead / 8);
+        kpfx = sh.kmin;
     }
     auto key = [&](int i) { return key_cache ? kc[i] : orderable(cum[id_of(i)]); };
     uint32_t k1 = 0xffffffffu, t1 = 0;
     uint32_t id_star = 0xffffffffu;                    // ties: position <= id_star are in
     if (n4 > 0) {
-        block_radix_select(key, nq, n4, sh.tk, &k1, &t1);
+        block_radix_select(key, nq, n4, sh.tk, &k1, &t1, start_shift, kpfx);
         if (threadIdx.x == 0) sh.cnt_eq = 0;
         __syncthreads();
         uint32_t local = 0;
@@ -720,34 +798,25 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a, int key_ca
     const int c0_new_pred = 0;
     (void)c0_new_pred;
     const int lo_first = c1 + (e_in ? 0 : 1);
+    // (each chunk's demoted slots are listed in `holes`, free until the hole filling below,
+    // then re-quantised one row per warp)
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     for (int s0 = 0; s0 < c0; s0 += blockDim.x) {
         const int i = s0 + threadIdx.x;
         const uint32_t dem = (i < c0 && !in_top(i)) ? 1u : 0u;
         uint32_t tot;
         const uint32_t r = block_excl_scan(dem, sh.tk, &tot);
-        if (dem) {
-            const int slot = lo_first + (int)(dem_base + r);
+        if (dem) holes[r] = i;                         // tot <= c0 <= the tier-0 capacity
+        __syncthreads();
+        for (int e = warp; e < (int)tot; e += nwarps) {
+            const int slot = lo_first + (int)dem_base + e;
             if (slot < tl.cap) {
-                const uint32_t* k4 = krow(th, unit, i, D);
-                const uint32_t* v4 = vrow(th, unit, i, D);
-                const size_t s4 = srow(th, unit, i, D, G);
-                quant_row([&](int c) {
-                              return dequant(code_at(k4, c, th.k_bits), h2f_bits(th.k_scale[s4 + c / G]),
-                                             h2f_bits(th.k_zero[s4 + c / G]));
-                          },
-                          D, G, tl.k_bits, krow(tl, unit, slot, D), tl.k_scale + srow(tl, unit, slot, D, G),
-                          tl.k_zero + srow(tl, unit, slot, D, G));
-                quant_row([&](int c) {
-                              return dequant(code_at(v4, c, th.v_bits), h2f_bits(th.v_scale[s4 + c / G]),
-                                             h2f_bits(th.v_zero[s4 + c / G]));
-                          },
-                          D, G, tl.v_bits, vrow(tl, unit, slot, D), tl.v_scale + srow(tl, unit, slot, D, G),
-                          tl.v_zero + srow(tl, unit, slot, D, G));
-                tl.token_id[unit * tl.cap + slot] = th.token_id[unit * th.cap + i];
-            } else {
+                requant_row_warp(a, th, tl, unit, holes[e], slot);
+            } else if ((threadIdx.x & 31) == 0) {
                 atomicOr(&g_status_policy, kDevCheck);
             }
         }
+        __syncthreads();
         dem_base += tot;
     }
     const int n_dem = (int)dem_base;
