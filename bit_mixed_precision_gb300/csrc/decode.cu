@@ -55,6 +55,9 @@ constexpr int kMinItemsPerCta = 34, kMinItemsPerCtaMikv = 64;
 // streamed decode: CTAs at most (the workspace holds one partial per (CTA, unit) pair, at
 // most ctas + units - 1 of them), and static items per CTA at least
 constexpr int kStreamMaxCtas = 1024, kStreamMinItems = 8;
+// streamed decode: residual rows per ring item (eight per warp: fewer items per unit than the
+// cluster path's 8-row pieces, which spread the ring over the cluster's CTAs)
+constexpr int kResItemS = 32;
 // streamed decode: tier chunk tokens (256 where two buffers of them keep four CTAs per SM)
 template <int GK>
 constexpr int kStreamChunk = GK == 32 ? 256 : 128;
@@ -628,12 +631,12 @@ __device__ __forceinline__ void row_vals(const uint16_t* row, bool bf, float (&x
 
 // Rows [0, nt) (nt <= RPW) of the warp's slice: logits, online softmax and
 // P.V; the logits go to lg_out (row-indexed) when asked.
-template <int NG, int D>
+template <int NG, int D, int RPW = Cfg<NG>::RPW>
 __device__ __forceinline__ void residual_rows(const Smem<NG, D>& sm, const uint16_t* rk,
                                               const uint16_t* rv, int nt, bool bf,
                                               WarpAcc<NG, D / 32>& acc, float* lg_out, int slots) {
     constexpr int CPL = D / 32;
-    constexpr int RPW = Cfg<NG>::RPW, LPR = 32 / RPW;   // rows per warp, lanes per row
+    constexpr int LPR = 32 / RPW;                  // lanes per row (RPW rows per warp)
     const int lane = threadIdx.x & 31;
     const int c0 = lane * CPL;
     const int t = lane / LPR;                      // the row this lane reports
@@ -2177,8 +2180,8 @@ __device__ __noinline__ void stream_issue(const DecodeArgs& a, const StreamArgs&
                 const int nn = min(CH, sm.ccnt - ck * CH);
                 if (nn > 0) { kind = kItChunk; u = cu; idx = ck; n = nn; break; }
             } else {
-                const int j0 = (ck - s.n_c) * kResItem;
-                const int nn = min(kResItem, sm.clen + 1 - j0);
+                const int j0 = (ck - s.n_c) * kResItemS;
+                const int nn = min(kResItemS, sm.clen + 1 - j0);
                 if (nn > 0) { kind = kItRing; u = cu; idx = j0; n = nn; break; }
             }
             // a unit of the run with no live item still gets a record: its (empty) partial
@@ -2231,7 +2234,7 @@ __device__ __forceinline__ void stream_release(const DecodeArgs& a, const Stream
 // chunk is CH tokens (128 or 256: each warp takes 32 tokens of each 128).
 template <int GK, int CH>
 __global__ void __launch_bounds__(Cfg<1>::kThreads, Cfg<1>::MINB) decode_stream_kernel(DecodeArgs a, StreamArgs s) {
-    constexpr int D = 128, W = Cfg<1>::W, TPW = Cfg<1>::TPW, RPW = Cfg<1>::RPW;
+    constexpr int D = 128, W = Cfg<1>::W, TPW = Cfg<1>::TPW;
     constexpr uint32_t kSB = 256 / GK;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem<1, D>& sm = *reinterpret_cast<Smem<1, D>*>(smem_raw);
@@ -2317,13 +2320,14 @@ __global__ void __launch_bounds__(Cfg<1>::kThreads, Cfg<1>::MINB) decode_stream_
             acc_init(racc);
             do {
                 ok = wait_item(a, sm, i, ok);
-                const int n = m.w, w0 = warp * RPW;
+                constexpr int RPS = kResItemS / W;       // ring rows per warp and item
+                const int n = m.w, w0 = warp * RPS;
                 if (ok && w0 < n) {
                     const uint8_t* buf = item_buf(a, stage_base, i);
                     const uint16_t* rk = reinterpret_cast<const uint16_t*>(buf);
                     const uint16_t* rv = reinterpret_cast<const uint16_t*>(buf + a16((uint32_t)n * D * 2));
-                    residual_rows<1, D>(sm, rk + (size_t)w0 * D, rv + (size_t)w0 * D, min(RPW, n - w0), bf, racc,
-                                        nullptr, a.slots);
+                    residual_rows<1, D, RPS>(sm, rk + (size_t)w0 * D, rv + (size_t)w0 * D, min(RPS, n - w0), bf,
+                                             racc, nullptr, a.slots);
                 }
                 stream_release<GK, CH>(a, s, sm, stage_base, i, cp_base, cp_off, cp_bpt);
                 m = sm.meta[++i & (a.stages - 1)];
@@ -2479,11 +2483,11 @@ cudaError_t stream_plan(const kvq_cache& c, int units, StreamPlan& p) {
     p = StreamPlan{};
     StreamArgs& sa = p.sa;
     sa.n_c = (c.tier[0].cap + CH - 1) / CH;
-    sa.n_r = (c.res_cap + kResItem - 1) / kResItem;
+    sa.n_r = (c.res_cap + kResItemS - 1) / kResItemS;
     sa.n_i = sa.n_c + sa.n_r;
     sa.total = (long long)units * sa.n_i;
     uint32_t stage = std::max(tier_stage_sizes(KVQ_AXIS_CHANNEL, 2, 2, CH, D, GK).total(),
-                              2u * a16((uint32_t)kResItem * D * 2));
+                              2u * a16((uint32_t)kResItemS * D * 2));
     p.stage = (stage + 127u) & ~127u;
     p.sm_bytes = (uint32_t)((sizeof(Smem<1, D>) + 127) & ~(size_t)127);
     p.qf_bytes = (uint32_t)Cfg<1>::W * mk1_qf_warp_bytes<GK>();

@@ -16,14 +16,16 @@ from tests.helpers import assert_attn_close, np_, u16, u32
 
 pytestmark = pytest.mark.gpu
 
-# 64 units x at least 128 static items each = 8192 = 8 items for each of 1024 CTAs
-B, H, D, W, STEPS = 2, 32, 128, 512, 40
+# 128 units x at least 64 static items each (chunks of 256 tokens for G = 32, 128 for G = 16,
+# then ring pieces of 32 rows) >= 8192 = 8 items for each of 1024 CTAs
+B, H, D, W, STEPS = 4, 32, 128, 512, 40
 
 
 def _decode_against_oracle(cache, x, T, units, G, seed):
     scale = 1.0 / math.sqrt(D)
-    n_chunks = (cache.tiers[0].spec.cap + 127) // 128
-    assert B * H * (n_chunks + (cache.res_cap + 7) // 8) >= 8 * 1024
+    ch = 256 if G == 32 else 128
+    n_items = (cache.tiers[0].spec.cap + ch - 1) // ch + (cache.res_cap + 31) // 32
+    assert B * H * n_items >= 8 * 1024
     assert kvq.decode_launches(cache) == 2, "the list launch and its merge launch" 
     for t in range(STEPS):
         qd, kd, vd = (z.cuda() for z in inputs.make_decode_step(B, H, H, D, t, seed=seed))
