@@ -2145,12 +2145,14 @@ struct StreamArgs {
 
 constexpr int kItChunk = 0, kItRing = 1, kItNone = 2, kItEnd = 3;
 
-// Issuing warp (every lane; the warps take turns): requests the CTA's next item into buffer k % S and
-// publishes its record; nothing but an end record once the run is done or a wait gave up.
-// Lanes 0..5 each copy one array of a tier chunk (at compile-time offsets of the format).
+// Issuing warp (every lane; the warps take turns): requests the CTA's next item into
+// buffer k % S and publishes its record; nothing but an end record once the run is done or
+// a wait gave up.  Lanes 0..5 each copy one array of a tier chunk (at compile-time offsets
+// of the format).  Not inlined: its registers stay out of the item loop's.
 template <int GK, int CH>
-__device__ __noinline__ void stream_issue(const DecodeArgs& a, const StreamArgs& s, Smem<1, 128>& sm, uint8_t* stage_base,
-                             int k, const uint8_t* cp_base, uint32_t cp_off, uint32_t cp_bpt) {
+__device__ __noinline__ void stream_issue(const DecodeArgs& a, const StreamArgs& s, Smem<1, 128>& sm,
+                                          uint8_t* stage_base, int k, const uint8_t* cp_base, uint32_t cp_off,
+                                          uint32_t cp_bpt) {
     constexpr uint32_t kSB = 256 / GK;
     const int lane = threadIdx.x & 31;
     int kind = kItEnd, u = 0, idx = 0, n = 0;
