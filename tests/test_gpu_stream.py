@@ -21,14 +21,14 @@ pytestmark = pytest.mark.gpu
 B, H, D, W, STEPS = 4, 32, 128, 512, 40
 
 
-def _decode_against_oracle(cache, x, T, units, G, seed):
+def _decode_against_oracle(cache, x, T, units, G, seed, dtype=torch.float16):
     scale = 1.0 / math.sqrt(D)
     ch = 256 if G == 32 else 128
     n_items = (cache.tiers[0].spec.cap + ch - 1) // ch + (cache.res_cap + 31) // 32
     assert B * H * n_items >= 8 * 1024
     assert kvq.decode_launches(cache) == 2, "the list launch and its merge launch" 
     for t in range(STEPS):
-        qd, kd, vd = (z.cuda() for z in inputs.make_decode_step(B, H, H, D, t, seed=seed))
+        qd, kd, vd = (z.cuda() for z in inputs.make_decode_step(B, H, H, D, t, dtype=dtype, seed=seed))
         od, ld = kvq.decode_attn_qkv(qd, kd, vd, cache, scale)
         torch.cuda.synchronize()
         for u, ref in units.items():
@@ -76,15 +76,15 @@ def test_stream_per_unit_budgets():
     _decode_against_oracle(cache, x, T, units, G, seed)
 
 
-def test_stream_group16():
-    """Groups of 16, one budget for every unit (selection + two-launch build), nr = 64:
-    flushes every 16 steps once the ring holds 80 tokens."""
-    T, G, nr, seed, k_hh = 17000, 16, 64, 23, 15000
-    x = inputs.make_qkv(B, H, H, T, D, seed=seed)
+def test_stream_group16_bf16():
+    """Groups of 16 and a bf16 prompt, ring and output, one budget for every unit (selection +
+    two-launch build), nr = 64: flushes every 16 steps once the ring holds 80 tokens."""
+    T, G, nr, seed, k_hh, dt = 17000, 16, 64, 23, 15000, torch.bfloat16
+    x = inputs.make_qkv(B, H, H, T, D, dtype=dt, seed=seed)
     cs = inputs.random_scores(B, H, T, seed=seed + 1)
     n_sel = k_hh + W
     cap = ((n_sel + STEPS) // G + 2) * G
-    cache = kvq.make_cache(B, H, H, D, G, torch.float16, kvq.POLICY_MINIKV,
+    cache = kvq.make_cache(B, H, H, D, G, dt, kvq.POLICY_MINIKV,
                            [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=nr)
     idx, _ = kvq.select_tokens(cs.cuda(), torch.full((B * H,), k_hh, dtype=torch.int32, device="cuda"), W)
     kvq.requant_demote(cache, 0, k_src=x.k.cuda(), v_src=x.v.cuda(), sel_idx=idx, n_sel=n_sel)
@@ -95,4 +95,4 @@ def test_stream_group16():
         sel = OS.select_unit(np_(cs[b, h]), k_hh, W)
         assert np.array_equal(np.sort(gsel[u]), sel), f"selection of unit {u}"
         units[u] = OP.MiniKVUnit(np_(x.k[b, h]), np_(x.v[b, h]), sel, nr, G)
-    _decode_against_oracle(cache, x, T, units, G, seed)
+    _decode_against_oracle(cache, x, T, units, G, seed, dt)
