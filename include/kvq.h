@@ -348,8 +348,9 @@ int kvq_decode_launches(const kvq_cache* c);
  *   teardown of the primary context) it is stale, so a process that resets
  *   a device must not call decode_attn_qkv_static on it again.
  *   All calls share the one array (DiffKV and MiKV keep the step's logits
- *   there; MiniKV needs none): two DiffKV/MiKV calls whose work overlaps on
- *   the GPU, on any streams, race and give wrong results. */
+ *   there, MiniKV caches with one query head per KV head their list launch's
+ *   partials; other MiniKV caches need none): two such calls whose work
+ *   overlaps on the GPU, on any streams, race and give wrong results. */
 kvq_status decode_attn_qkv_static(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
                                   float sm_scale, void* o, float* lse_out, void* stream);
 

@@ -1,7 +1,8 @@
 """decode_attn_qkv_static: the decode entry point for callers that cannot give the
 library scratch memory (an engine whose allocator already owns all free device
 memory, or C code without a device allocator).  DiffKV and MiKV caches keep the
-step's logits in scratch, so those two run here: two calls in a row, each checked
+step's logits in scratch, and single-head MiniKV caches large enough for the streamed
+launch keep its partials there, so those run here: two calls in a row, each checked
 against the CPU oracle (outputs, cumulative scores, tier contents) and against the
 caller-workspace entry point on a twin cache.
 
@@ -126,6 +127,45 @@ def test_static_scratch_diffkv_two_calls():
             assert_attn_close(o_st[0, u * g:(u + 1) * g], ro, f"call {t} unit {u}")
             assert_tiers_equal(gpu_tier_rows(st.tiers[0], u), oracle_tier_rows(units[u].high), f"K8V4 u{u}")
             assert_tiers_equal(gpu_tier_rows(st.tiers[1], u), oracle_tier_rows(units[u].low), f"K4V2 u{u}")
+    assert kvq.device_status() == 0
+
+
+def test_static_scratch_minikv_streamed_two_calls():
+    """MiniKV with one query head per KV head, large enough for the streamed launch: its
+    per-(CTA, unit) partials live in the scratch.  Two calls in a row against the oracle
+    (sampled units) and against the caller-workspace call on a twin cache (every unit)."""
+    from oracle import select as OS
+    B, H, T, D, W, k_hh, steps = 4, 32, 17000, 128, 512, 16000, 2
+    x = inputs.make_qkv(B, H, H, T, D, seed=37)
+    cs = inputs.random_scores(B, H, T, seed=38)
+    cap = ((k_hh + W + steps) // G + 2) * G
+
+    def make():
+        c = kvq.make_cache(B, H, H, D, G, torch.float16, kvq.POLICY_MINIKV,
+                           [kvq.TierSpec(2, 2, kvq.AXIS_CHANNEL, cap)], nr=0)
+        kvq.minikv_prefill_build(c, x.k.cuda(), x.v.cuda(), cs.cuda(),
+                                 torch.full((B * H,), k_hh, dtype=torch.int32, device="cuda"), W)
+        return c
+
+    st, ws = make(), make()
+    _scratch_used(st)
+    assert kvq.decode_launches(st) == 2, "the streamed launch and its merge launch"
+    sample = [0, 37, B * H - 1]
+    units = {u: OP.MiniKVUnit(np_(x.k[u // H, u % H]), np_(x.v[u // H, u % H]),
+                              OS.select_unit(np_(cs[u // H, u % H]), k_hh, W), 0, G) for u in sample}
+    scale = 1.0 / math.sqrt(D)
+    for t in range(steps):
+        qd, kd, vd = (z.cuda() for z in inputs.make_decode_step(B, H, H, D, t, seed=37))
+        o1, l1 = kvq.decode_attn_qkv_static(qd, kd, vd, st, scale)
+        o2, l2 = kvq.decode_attn_qkv(qd, kd, vd, ws, scale)
+        torch.cuda.synchronize()
+        _twin_outputs(o1, o2, f"step {t}: static vs caller workspace")
+        for u in sample:
+            b, h = u // H, u % H
+            ro, rl = units[u].step(T + t, np_(qd[b, h:h + 1]), np_(kd[b, h]), np_(vd[b, h]), scale)
+            assert_attn_close(o1[b, h], ro[0], f"step {t} unit {u}")
+            assert abs(float(l1[b, h]) - rl[0]) < 1e-3
+    assert torch.equal(st.res_len, ws.res_len) and torch.equal(st.tiers[0].count, ws.tiers[0].count)
     assert kvq.device_status() == 0
 
 
