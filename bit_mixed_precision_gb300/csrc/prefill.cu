@@ -45,6 +45,7 @@ constexpr float kRescaleLog2 = 8.0f;
 // pass 2: two warpgroups sum the exponentials (each half of a tile's query columns), then
 // one TMA warp and one MMA warp
 constexpr int kP2Threads = 320;
+constexpr int kP2TileFastTiles = 128;  // pass 2: head-major launch order from this many 128-row tiles
 
 // Shared memory maps (offsets from a 1024-aligned base) for head dim D.
 template <int D> struct Layout {
@@ -406,7 +407,7 @@ template <typename T, int AB, int D>
 __global__ void __launch_bounds__(kP2Threads, 2)
     prefill_pass2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const float* __restrict__ lse, float* __restrict__ colscore, int T_len,
-                         int Hq, int Hkv, int n_t, float scale_log2, int q_first) {
+                         int Hq, int Hkv, int n_t, float scale_log2, int q_first, int tile_fast) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -422,8 +423,10 @@ __global__ void __launch_bounds__(kP2Threads, 2)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lay::P2_BAR + 8 * P2_NBAR + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int kt = (int)blockIdx.y;
+    // tile_fast: blockIdx.x runs over the head's key tiles, blockIdx.y over heads (the CTAs
+    // resident together then read a few heads' Q and lse, and reuse them in L2)
+    const int bh = tile_fast ? (int)blockIdx.y : (int)blockIdx.x;
+    const int kt = tile_fast ? (int)blockIdx.x : (int)blockIdx.y;
     const int b = bh / Hq, hq = bh % Hq;
     const int bhkv = b * Hkv + hq / (Hq / Hkv);
     // query tiles kt + it0 .. n_t - 1: at or below the diagonal and reaching query q_first
@@ -663,8 +666,14 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
         }
     }
     if (colscore) {
-        prefill_pass2_kernel<T, AB, D><<<g1, kP2Threads, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
-                                                                             Hkv, n_t, scale_log2, q_first);
+        // pass 2 in head-major order for long prompts (measured: 10 % faster at 16k tokens and
+        // 7 % at 32k; 12 % slower at 8k and 20 % at 4k, where the heads' query tiles stay in
+        // L2 in either order)
+        const int tile_fast = (B * Hq <= 65535 && n_t >= kP2TileFastTiles) ? 1 : 0;
+        const dim3 g2 = tile_fast ? dim3(n_t, B * Hq) : g1;
+        prefill_pass2_kernel<T, AB, D><<<g2, kP2Threads, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
+                                                                             Hkv, n_t, scale_log2, q_first,
+                                                                             tile_fast);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error("prefill pass 2 launch: %s", cudaGetErrorString(e));
