@@ -26,6 +26,8 @@
 // KVQ_ETIMEOUT in the device status word.
 #include <mutex>
 
+#include <algorithm>
+
 #include "kvq_common.cuh"
 #include "kvq_internal.h"
 
@@ -45,7 +47,7 @@ constexpr float kRescaleLog2 = 8.0f;
 // pass 2: two warpgroups sum the exponentials (each half of a tile's query columns), then
 // one TMA warp and one MMA warp
 constexpr int kP2Threads = 320;
-constexpr int kP2TileFastTiles = 128;  // pass 2: head-major launch order from this many 128-row tiles
+constexpr long long kL2OrderBytes = 128ll << 20;  // about L2 (129 MB): the prefill launch order's threshold
 
 // Shared memory maps (offsets from a 1024-aligned base) for head dim D.
 template <int D> struct Layout {
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(192, 2)
     prefill_pass1_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, T* __restrict__ o,
                          float* __restrict__ lse, int T_len, int Hq, int Hkv, int n_qt,
-                         float scale_log2) {
+                         float scale_log2, int tile_fast) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     if (raw & 1023u) {                                  // layout assumption broken: do nothing
@@ -140,8 +142,10 @@ __global__ void __launch_bounds__(192, 2)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Lay::P1_BAR + 8 * P1_NBAR + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int qt = n_qt - 1 - (int)blockIdx.y;
+    // tile_fast: blockIdx.x runs over the head's query tiles, blockIdx.y over heads (the CTAs
+    // resident together then read a few heads' K/V and reuse it in L2)
+    const int bh = tile_fast ? (int)blockIdx.y : (int)blockIdx.x;
+    const int qt = n_qt - 1 - (tile_fast ? (int)blockIdx.x : (int)blockIdx.y);
     const int b = bh / Hq, hq = bh % Hq;
     const int bhkv = b * Hkv + hq / (Hq / Hkv);
     // 64-key tiles up to the diagonal, none wholly past the end of the prompt
@@ -655,10 +659,28 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
     const int n_t = (T_len + kTile - 1) / kTile;
     const float scale_log2 = sm_scale * kLog2e;
     dim3 g1(B * Hq, n_t);
+    // Launch order.  Head-minor (the default) runs every head's same tile together; when the
+    // heads resident at once (two CTAs per SM) hold more K/V (pass 1) or Q (pass 2) than L2,
+    // each tile would be read from HBM once per query (key) tile of its head, so the order
+    // turns head-major: a head's tiles in consecutive CTAs, sharing its tiles in L2.
+    // Measured: the 16k-token, 512-head pyramid layer much faster; head-major loses 20-33 %
+    // where the heads' tiles already stay in L2 (4k tokens, 32 heads).
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        sms = 152;
+    }
+    const long long heads_resident = std::min<long long>((long long)B * Hq, 2LL * sms);
+    const long long g_size = Hq / Hkv;
+    auto head_major = [&](long long bytes_per_head) {
+        return B * Hq <= 65535 && heads_resident * bytes_per_head > kL2OrderBytes;
+    };
+    const int tf1 = head_major((long long)T_len * D * 2 * 2 / g_size) ? 1 : 0;   // K and V, shared by the group
+    const int tf2 = head_major((long long)T_len * (D * 2 + 4)) ? 1 : 0;          // Q and lse
     cudaError_t e = cudaSuccess;
     if (o) {
-        prefill_pass1_kernel<T, AB, D><<<g1, 192, Lay::P1_SMEM, s>>>(mq, mk64, mv64, (T*)o, lse, T_len, Hq,
-                                                                      Hkv, n_t, scale_log2);
+        prefill_pass1_kernel<T, AB, D><<<tf1 ? dim3(n_t, B * Hq) : g1, 192, Lay::P1_SMEM, s>>>(
+            mq, mk64, mv64, (T*)o, lse, T_len, Hq, Hkv, n_t, scale_log2, tf1);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error("prefill pass 1 launch: %s", cudaGetErrorString(e));
@@ -666,14 +688,10 @@ kvq_status run_typed(const void* q, const void* k, const void* v, int B, int Hq,
         }
     }
     if (colscore) {
-        // pass 2 in head-major order for long prompts (measured: 10 % faster at 16k tokens and
-        // 7 % at 32k; 12 % slower at 8k and 20 % at 4k, where the heads' query tiles stay in
-        // L2 in either order)
-        const int tile_fast = (B * Hq <= 65535 && n_t >= kP2TileFastTiles) ? 1 : 0;
-        const dim3 g2 = tile_fast ? dim3(n_t, B * Hq) : g1;
-        prefill_pass2_kernel<T, AB, D><<<g2, kP2Threads, Lay::P2_SMEM, s>>>(mq, mk, lse, colscore, T_len, Hq,
-                                                                             Hkv, n_t, scale_log2, q_first,
-                                                                             tile_fast);
+        // (pass 2 measured: head-major 10 % faster at 16k tokens with 64 heads and 7 % at 32k
+        // with 32; 12 % slower at 8k and 20 % at 4k with 32 heads)
+        prefill_pass2_kernel<T, AB, D><<<tf2 ? dim3(n_t, B * Hq) : g1, kP2Threads, Lay::P2_SMEM, s>>>(
+            mq, mk, lse, colscore, T_len, Hq, Hkv, n_t, scale_log2, q_first, tf2);
         e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error("prefill pass 2 launch: %s", cudaGetErrorString(e));
