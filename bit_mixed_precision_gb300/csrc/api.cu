@@ -229,7 +229,9 @@ size_t kvq_decode_workspace_bytes(const kvq_cache* c) {
 
 int kvq_decode_launches(const kvq_cache* c) {
     if (check_cache(c, "kvq_decode_launches") != KVQ_OK) return -1;
-    return kvq::decode_launches(*c);
+    const int n = kvq::decode_launches(*c);
+    if (n < 0) set_error("kvq_decode_launches: the device occupancy query failed");
+    return n;
 }
 
 kvq_status decode_attn_qkv(const void* q, const void* k_new, const void* v_new, kvq_cache* c,
