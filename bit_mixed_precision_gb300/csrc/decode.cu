@@ -196,8 +196,7 @@ struct Smem {
     // (single heads, MiniKV format: the warp's probabilities, 32 floats, then in the same
     // bytes the probabilities times each value group's scale, fp16 [group][40: 32 tokens])
     float lg[NG == 1 ? Cfg<NG>::W : 1][1][NG == 1 ? 80 : 1];
-    // per-token keys (GQA groups): the query's A fragments, [k-step][lane]; single heads:
-    // zeros, read by the lanes that hold no column of a MiniKV-format B fragment
+    // per-token keys (GQA groups): the query's A fragments, [k-step][lane] (single heads: unused)
     uint4 qa[NG >= 2 ? 8 : 1][32];
     float cw[kMaxCluster][NG];           // leader: weight of each CTA partial
     float lse2[NG];                      // base-2 log-sum-exp of the step (broadcast by the leader)
@@ -1980,8 +1979,6 @@ __global__ void __launch_bounds__(Cfg<NG>::kThreads, Cfg<NG>::MINB) decode_kerne
         sm.wl[x / NG][x % NG] = 0.0f;
     }
     for (int x = threadIdx.x; x < W * NG * D; x += blockDim.x) (&sm.wo[0][0][0])[x] = 0.0f;
-    if (NG == 1)
-        for (int x = threadIdx.x; x < (int)(sizeof(sm.qa) / 16); x += blockDim.x) (&sm.qa[0][0])[x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     const UnitState& us = sm.us;
@@ -2244,7 +2241,7 @@ __global__ void __launch_bounds__(Cfg<1>::kThreads, Cfg<1>::MINB) decode_stream_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool bf = a.bf16 != 0;
     // lanes 0..5 of the issuing warp copy one array of a tier chunk each: unit u's chunk j
-    // starts (u cap + 128 j) bytes_per_token into the array
+    // starts (u cap + CH j) bytes_per_token into the array
     const TierArgs& ta = a.tier[0];
     const uint8_t* cp_base = nullptr;
     uint32_t cp_off = 0u, cp_bpt = 0u;
@@ -2270,7 +2267,6 @@ __global__ void __launch_bounds__(Cfg<1>::kThreads, Cfg<1>::MINB) decode_stream_
         sm.cem = 0;
         fence_mbar_init();
     }
-    for (int x = threadIdx.x; x < (int)(sizeof(sm.qa) / 16); x += blockDim.x) (&sm.qa[0][0])[x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     if (warp == 0)
         for (int k = 0; k < a.stages; ++k) stream_issue<GK, CH>(a, s, sm, stage_base, k, cp_base, cp_off, cp_bpt);
