@@ -713,10 +713,10 @@ __device__ void requant_row_warp(const PolicyArgs& a, const TierDev& th, const T
 // Oldest residual token leaves; the top floor(N_q / hi_den) by cumulative
 // score (ties to the lower position) is recomputed; INT4 tokens outside it
 // are re-quantised to INT2 from their dequantised values.
-__global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a, int key_cache) {
-    __shared__ MikvShared sh;
-    extern __shared__ int32_t holes[];                 // [cap of tier 0], then (key_cache) the keys
-    const size_t unit = blockIdx.x;
+// One CTA (any multiple of 32 threads up to 1024) on one unit; `holes` holds the tier-0
+// capacity in ints, then (key_cache) the population's keys.
+__device__ __forceinline__ void mikv_step_unit(const PolicyArgs& a, size_t unit, int key_cache, int32_t* holes,
+                                               MikvShared& sh) {
     const int len = a.res_len[unit];
     if (len <= a.nr) return;
     const int D = a.D, G = a.G, cap = a.res_cap;
@@ -880,6 +880,367 @@ __global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a, int key_ca
     (void)bf;
 }
 
+// The same, without the key cache, as one out-of-line copy for the sampled step's fallbacks.
+__device__ __noinline__ void mikv_step_general(const PolicyArgs& a, size_t unit, int32_t* holes, MikvShared& sh) {
+    mikv_step_unit(a, unit, 0, holes, sh);
+}
+
+__global__ void __launch_bounds__(kTopkBlock) mikv_step(PolicyArgs a, int key_cache) {
+    __shared__ MikvShared sh;
+    extern __shared__ int32_t holes[];
+    mikv_step_unit(a, blockIdx.x, key_cache, holes, sh);
+}
+
+// ------------------------------------------------- MiKV step by sample selection
+//
+// MiKV evicts nothing and tokens leave the residual window in position order, so when the
+// leaving token is position e = c0 + c1 the population is exactly positions 0 .. e and its
+// ranking keys are the first e + 1 cumulative scores, read in order (no gather by token
+// id).  The ranking value of position p is R(p) = key(p) * 2^32 + (2^32 - 1 - p): larger
+// ranks higher, equal scores go to the lower position, and no two values are equal.  The
+// top floor((e + 1) / hi_den) is {R >= R*}, and R* comes from a sample selection:
+//  1. a strided sample of 256 keys, ranked in shared memory, gives seven boundary keys around
+//     the sample rank where R* is expected;
+//  2. one pass counts the keys at or above each boundary, which places R* between two
+//     neighbouring boundaries (or above or below all of them) and gives its rank there;
+//  3. a second pass (the scores are in L2 by then) gathers the values between those two
+//     (the band), and a radix select inside the band gives R* exactly.
+// A band larger than its buffer, or a population that is not positions 0 .. e, takes the
+// general step above, with the same result.
+
+constexpr int kMikvThreads = 256;
+constexpr int kMikvSample = 256;                     // sampled keys (one thread ranks each)
+constexpr int kMikvNB = 7;                           // boundaries
+constexpr int kMikvStep = 10;                        // sample ranks between boundaries
+constexpr int kMikvBand = 4096;                      // band buffer, 64-bit values
+static_assert(kMikvSample == kMikvThreads, "one thread per sampled key");
+static_assert(2 * kMikvSample * 4 <= kMikvBand * 8, "sample in the band buffer");
+
+struct MikvSampledShared {
+    MikvShared gen;
+    uint32_t cnt[kMikvNB];                           // keys at or above each boundary
+    uint32_t bnd[kMikvNB];                           // the boundary keys, non-increasing
+    uint32_t nb_got;
+    int bad;
+};
+
+// One count per lane with `on` into h[bin], by all 32 lanes of a warp together: lanes that
+// share a bin add once (neighbouring positions' scores are close, so a warp's lanes often
+// fall into one bin, which would serialise their atomics).
+__device__ __forceinline__ void warp_hist_add(uint32_t* h, uint32_t bin, bool on) {
+    const uint32_t m = __ballot_sync(0xffffffffu, on);
+    if (!m) return;
+    const int lane = threadIdx.x & 31;
+    const int first = __ffs(m) - 1;
+    const uint32_t b0 = __shfl_sync(0xffffffffu, bin, first);
+    if (__all_sync(0xffffffffu, !on || bin == b0)) {
+        if (lane == first) atomicAdd(&h[b0], (uint32_t)__popc(m));
+    } else {
+        const uint32_t peers = __match_any_sync(0xffffffffu, on ? bin : 0xffffffffu);
+        if (on && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+    }
+}
+
+// The r-th largest (1 <= r <= n) of n distinct 64-bit values that all lie in [lo, hi]:
+// 8-bit digits from the highest bit where lo and hi differ; once the chosen bin holds a
+// single value, that value is the answer.
+__device__ unsigned long long band_select(const unsigned long long* v, int n, uint32_t r, unsigned long long lo,
+                                          unsigned long long hi, TopkShared& sh) {
+    const unsigned long long diff = lo ^ hi;
+    const int top = diff ? 63 - __clzll((long long)diff) : 0;
+    unsigned long long mask = top >= 63 ? 0ull : ~0ull << (top + 1);
+    unsigned long long prefix = lo & mask;
+    uint32_t remaining = r;
+    for (int s_ = top - 7;; s_ -= 8) {
+        const int s = s_ < 0 ? 0 : s_;
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
+        __syncthreads();
+        for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+            const int i = i0 + threadIdx.x;
+            const unsigned long long x = i < n ? v[i] : 0ull;
+            warp_hist_add(sh.hist, (uint32_t)(x >> s) & 255u, i < n && (x & mask) == prefix);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) radix_pick_bin(sh, remaining);
+        __syncthreads();
+        const uint32_t bin = sh.bcast[0];
+        prefix |= (unsigned long long)bin << s;
+        mask |= 255ull << s;
+        remaining = sh.bcast[1];
+        const uint32_t in_bin = sh.hist[bin];
+        __syncthreads();
+        if (s == 0) return prefix;
+        if (in_bin == 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const unsigned long long x = v[i];
+                if ((x & mask) == prefix) {
+                    sh.bcast[2] = (uint32_t)(x >> 32);
+                    sh.bcast[3] = (uint32_t)x;
+                }
+            }
+            __syncthreads();
+            const unsigned long long out = ((unsigned long long)sh.bcast[2] << 32) | sh.bcast[3];
+            __syncthreads();
+            return out;
+        }
+    }
+}
+
+// Bytes of the front of the sampled step's dynamic shared memory: the band, which later
+// holds the demoted slots (or the general step's holes: the tier-0 capacity in ints).
+__host__ __device__ __forceinline__ size_t mikv_front_bytes(int cap0) {
+    const size_t b = (size_t)kMikvBand * 8, h = (size_t)cap0 * 4;
+    return ((b > h ? b : h) + 15) & ~(size_t)15;
+}
+
+__device__ __forceinline__ unsigned long long rank_value(float score, int p) {
+    return ((unsigned long long)orderable(score) << 32) | (0xffffffffu - (uint32_t)p);
+}
+
+// Launched with kMikvThreads threads; dynamic shared memory: mikv_front_bytes (the sample,
+// then the band, then the demoted slots or the general step's holes), then one bit per
+// tier-0 slot (kept).
+__global__ void __launch_bounds__(kMikvThreads, 4) mikv_step_sampled(PolicyArgs a) {
+    __shared__ MikvSampledShared sh;
+    extern __shared__ __align__(16) uint8_t mikv_dyn[];
+    const size_t unit = blockIdx.x;
+    const TierDev& th = a.tier[0];
+    const TierDev& tl = a.tier[1];
+    unsigned long long* band = reinterpret_cast<unsigned long long*>(mikv_dyn);
+    int32_t* dem = reinterpret_cast<int32_t*>(mikv_dyn);      // once the band is done with
+    uint32_t* keep = reinterpret_cast<uint32_t*>(mikv_dyn + mikv_front_bytes(th.cap));
+    const int len = a.res_len[unit];
+    if (len <= a.nr) return;
+    const int cap = a.res_cap, start = a.res_start[unit];
+    const int e_id = a.res_token_id[unit * cap + start];
+    const int c0 = th.count[unit], c1 = tl.count[unit];
+    const int nq = c0 + c1 + 1;
+    const int n4 = nq / a.hi_den;
+    if (n4 < 1 || e_id != c0 + c1 || nq > a.score_cap) {
+        mikv_step_general(a, unit, dem, sh.gen);
+        return;
+    }
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+    const float* cum = a.cum_score + unit * (size_t)a.score_cap;
+
+    // 1. the sample: the key of position floor(j n / S) with its low 8 bits replaced by j
+    //    (distinct values; any values serve as edges), ranked in shared memory
+    const int S = min(kMikvSample, nq);
+    uint32_t* skey = reinterpret_cast<uint32_t*>(band);  // [kMikvSample], zero past S
+    uint32_t* srt = skey + kMikvSample;
+    skey[tid] = tid < S ? (orderable(cum[(int)(((long long)tid * nq) / S)]) & 0xffffff00u) | (uint32_t)tid : 0u;
+    if (tid < kMikvNB) sh.cnt[tid] = 0u;
+    if (tid == 0) {
+        sh.nb_got = 0;
+        sh.bad = 0;
+    }
+    __syncthreads();
+    {
+        // this thread's sample rank: the sampled values above it (the zeros past S never are)
+        const uint32_t x = skey[tid];
+        const uint4* s4 = reinterpret_cast<const uint4*>(skey);
+        uint32_t rk = 0;
+#pragma unroll 4
+        for (int i = 0; i < kMikvSample / 4; ++i) {
+            const uint4 y = s4[i];
+            rk += (y.x > x ? 1u : 0u) + (y.y > x ? 1u : 0u) + (y.z > x ? 1u : 0u) + (y.w > x ? 1u : 0u);
+        }
+        if (tid < S) srt[rk] = x;
+    }
+    __syncthreads();
+
+    // 2. keys at or above each of kMikvNB boundaries: the sample's keys kMikvStep ranks
+    //    apart around where R* is expected, counted in registers (no shared-memory traffic
+    //    per key).  Positions past the end read as the pattern 0xffffffff, whose key is 0,
+    //    below every boundary.
+    const int rho = (int)(((long long)n4 * S + nq / 2) / nq);
+    uint32_t bnd[kMikvNB], cnt[kMikvNB];
+#pragma unroll
+    for (int i = 0; i < kMikvNB; ++i) {
+        bnd[i] = max(srt[min(max(rho + (i - kMikvNB / 2) * kMikvStep, 0), S - 1)], 1u);
+        cnt[i] = 0u;
+    }
+    if (tid < kMikvNB) sh.bnd[tid] = bnd[tid];
+    const uint32_t* cumw = reinterpret_cast<const uint32_t*>(cum);
+    constexpr int kU = 16;
+    for (int p0 = 0; p0 < nq; p0 += nt * kU) {
+        uint32_t w[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int p = p0 + u * nt + tid;
+            w[u] = p < nq ? cumw[p] : 0xffffffffu;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const uint32_t kv = orderable(__uint_as_float(w[u]));
+#pragma unroll
+            for (int i = 0; i < kMikvNB; ++i) cnt[i] += kv >= bnd[i] ? 1u : 0u;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kMikvNB; ++i) {
+        const uint32_t t = __reduce_add_sync(0xffffffffu, cnt[i]);
+        if (lane == 0) atomicAdd(&sh.cnt[i], t);
+    }
+    __syncthreads();
+    // the first boundary with at least n4 keys at or above it bounds R* from below, the one
+    // before it (if any) from above; the keys between them are the band
+    int ib = kMikvNB;
+    for (int i = kMikvNB - 1; i >= 0; --i)
+        if (sh.cnt[i] >= (uint32_t)n4) ib = i;
+    const uint32_t above = ib > 0 ? sh.cnt[ib - 1] : 0u;
+    const uint32_t nb = (ib < kMikvNB ? sh.cnt[ib] : (uint32_t)nq) - above;
+    const uint32_t r = (uint32_t)n4 - above;           // R*'s rank in the band (1 = largest)
+    const uint32_t lo_key = ib < kMikvNB ? sh.bnd[ib] : 0u;
+    const unsigned long long hi_key = ib > 0 ? (unsigned long long)sh.bnd[ib - 1] : (1ull << 32);   // exclusive
+    if (nb > (uint32_t)kMikvBand || r < 1u || r > nb || hi_key == 0ull) {
+        __syncthreads();
+        mikv_step_general(a, unit, dem, sh.gen);
+        return;
+    }
+
+    // 3. the band, then R* inside it
+    for (int p0 = 0; p0 < nq; p0 += nt * kU) {
+        float v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int p = p0 + u * nt + tid;
+            v[u] = p < nq ? cum[p] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int p = p0 + u * nt + tid;
+            const uint32_t kv = orderable(v[u]);
+            const bool inb = p < nq && kv >= lo_key && (unsigned long long)kv < hi_key;
+            const uint32_t bal = __ballot_sync(0xffffffffu, inb);
+            if (bal) {
+                uint32_t base = 0;
+                if (lane == 0) base = atomicAdd(&sh.nb_got, (uint32_t)__popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (inb) {
+                    const uint32_t at = base + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+                    if (at < (uint32_t)kMikvBand) band[at] = rank_value(v[u], p);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (sh.nb_got != nb) {                               // the scores changed under the step
+        __syncthreads();
+        mikv_step_general(a, unit, dem, sh.gen);
+        return;
+    }
+    const unsigned long long rstar = band_select(band, (int)nb, r, (unsigned long long)lo_key << 32,
+                                                 ((hi_key - 1ull) << 32) | 0xffffffffull, sh.gen.tk);
+
+    // INT4 slots still in the top set (one bit per slot), from their positions' scores
+    const int nwords = (c0 + 31) >> 5;
+    for (int s0 = 0; s0 < c0; s0 += nt * 8) {
+        int pid[8];
+        float sv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int sl = s0 + u * nt + tid;
+            pid[u] = sl < c0 ? th.token_id[unit * th.cap + sl] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool ok = pid[u] >= 0 && pid[u] < e_id;
+            if (s0 + u * nt + tid < c0 && !ok) sh.bad = 1;
+            sv[u] = ok ? cum[pid[u]] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool kept = pid[u] >= 0 && pid[u] < e_id && rank_value(sv[u], pid[u]) >= rstar;
+            const uint32_t bal = __ballot_sync(0xffffffffu, kept);
+            const int wd = ((s0 + u * nt) >> 5) + warp;
+            if (lane == 0 && wd < nwords) keep[wd] = bal;
+        }
+    }
+    __syncthreads();
+    if (sh.bad) {                                      // a tier-0 token outside positions 0 .. e - 1
+        __syncthreads();
+        mikv_step_general(a, unit, dem, sh.gen);
+        return;
+    }
+    const bool e_in = rank_value(cum[e_id], e_id) >= rstar;
+
+    // demoted slots in slot order
+    uint32_t dem_base = 0;
+    for (int w0 = 0; w0 < nwords; w0 += nt) {
+        const int w = w0 + tid;
+        uint32_t dm = 0u;
+        if (w < nwords) {
+            const int nv = min(32, c0 - 32 * w);
+            dm = ~keep[w] & (nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u));
+        }
+        uint32_t tot;
+        uint32_t at = dem_base + block_excl_scan((uint32_t)__popc(dm), sh.gen.tk, &tot);
+        while (dm) {
+            dem[at++] = 32 * w + (__ffs(dm) - 1);
+            dm &= dm - 1u;
+        }
+        dem_base += tot;
+    }
+    __syncthreads();
+    const int n_dem = (int)dem_base;
+    const int D = a.D, G = a.G;
+    // re-quantised to INT2 after the leaving token's tier-1 slot (when it goes there)
+    const int lo_first = c1 + (e_in ? 0 : 1);
+    for (int e = warp; e < n_dem; e += nw) {
+        const int slot = lo_first + e;
+        if (slot < tl.cap) requant_row_warp(a, th, tl, unit, dem[e], slot);
+        else if (lane == 0) atomicOr(&g_status_policy, kDevCheck);
+    }
+    __syncthreads();
+    // kept slots at or above c0 - n_dem fill the demoted slots below it (a prefix of `dem`)
+    const int c0n = c0 - n_dem;
+    const int kw = D * th.k_bits / 32, vw = D * th.v_bits / 32, ng = D / G;
+    uint32_t mov_base = 0;
+    for (int s0 = c0n; s0 < c0; s0 += nt) {
+        const int i = s0 + tid;
+        const uint32_t mov = (i < c0 && ((keep[i >> 5] >> (i & 31)) & 1u)) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t r = block_excl_scan(mov, sh.gen.tk, &tot);
+        if (mov) {
+            const int dst = dem[mov_base + r];
+            uint32_t* kd = krow(th, unit, dst, D);
+            const uint32_t* ks = krow(th, unit, i, D);
+            for (int w = 0; w < kw; ++w) kd[w] = ks[w];
+            uint32_t* vd = vrow(th, unit, dst, D);
+            const uint32_t* vs = vrow(th, unit, i, D);
+            for (int w = 0; w < vw; ++w) vd[w] = vs[w];
+            const size_t sd = srow(th, unit, dst, D, G), ss = srow(th, unit, i, D, G);
+            for (int w = 0; w < ng; ++w) {
+                th.k_scale[sd + w] = th.k_scale[ss + w];
+                th.k_zero[sd + w] = th.k_zero[ss + w];
+                th.v_scale[sd + w] = th.v_scale[ss + w];
+                th.v_zero[sd + w] = th.v_zero[ss + w];
+            }
+            th.token_id[unit * th.cap + dst] = th.token_id[unit * th.cap + i];
+        }
+        mov_base += tot;
+    }
+    __syncthreads();
+    // the leaving token, quantised from its full-precision values (warp 0)
+    if (tid < 32) {
+        const size_t row = (unit * cap + start) * (size_t)D;
+        if (e_in) {
+            if (c0n < th.cap) put_token_warp(a, th, unit, c0n, a.res_k, a.res_v, row, e_id);
+            else if (tid == 0) atomicOr(&g_status_policy, kDevCheck);
+        } else {
+            if (c1 < tl.cap) put_token_warp(a, tl, unit, c1, a.res_k, a.res_v, row, e_id);
+            else if (tid == 0) atomicOr(&g_status_policy, kDevCheck);
+        }
+    }
+    if (tid == 0) {
+        th.count[unit] = min(c0n + (e_in ? 1 : 0), th.cap);
+        tl.count[unit] = min(c1 + n_dem + (e_in ? 0 : 1), tl.cap);
+        a.res_start[unit] = (start + 1) % cap;
+        a.res_len[unit] = len - 1;
+    }
+}
+
 PolicyArgs make_args(const kvq_cache& c, const kvq_policy_params* p) {
     PolicyArgs a{};
     a.B = c.B;
@@ -1039,10 +1400,23 @@ kvq_status run_policy(const kvq_cache& c, int mode, const kvq_policy_params* p, 
         mikv_build<<<units, kTopkBlock, 0, s>>>(a);
         return launched("MiKV build");
     }
+    constexpr size_t kMaxDyn = 200 * 1024;
+    const size_t cap0 = (size_t)c.tier[0].cap;
+    const size_t dyn_s = mikv_front_bytes((int)cap0) + (cap0 + 31) / 32 * sizeof(uint32_t);
+    if (dyn_s <= kMaxDyn) {
+        if (dyn_s > 48 * 1024) {
+            static bool attr_s = false;
+            if (!attr_s) {
+                cudaFuncSetAttribute(mikv_step_sampled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDyn);
+                attr_s = true;
+            }
+        }
+        mikv_step_sampled<<<units, kMikvThreads, dyn_s, s>>>(a);
+        return launched("MiKV step");
+    }
     // holes of tier 0, then the population's keys when both fit in shared memory
     const size_t holes = (size_t)c.tier[0].cap * sizeof(int32_t);
     const size_t keys = ((size_t)c.tier[0].cap + c.tier[1].cap + 1) * sizeof(uint32_t);
-    constexpr size_t kMaxDyn = 200 * 1024;
     const int key_cache = holes + keys <= kMaxDyn ? 1 : 0;
     const size_t dyn = key_cache ? holes + keys : holes;
     if (dyn > 48 * 1024) {

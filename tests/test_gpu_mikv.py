@@ -31,10 +31,14 @@ def _check_units(cache, units):
         assert_tiers_equal(gpu_tier_rows(cache.tiers[1], u), oracle_tier_rows(un.lo), f"INT2 u{u}")
 
 
-def test_mikv_decisions_bit_exact():
+@pytest.mark.parametrize("T,flat", [(700, False), (700, True), (2600, True)])
+def test_mikv_decisions_bit_exact(T, flat):
     """Identical float32 cumulative scores (with many ties) on both sides: the INT4/INT2
-    split, every demotion and every re-quantised code are identical."""
-    B, Hq, Hkv, T, D, steps, nr = 2, 8, 2, 700, 128, 10, 16
+    split, every demotion and every re-quantised code are identical.  With `flat`, every
+    third step gives all tokens the same score (the ranking is then by position alone); at
+    2600 tokens that tie is wider than the step's band buffer, so those steps take the
+    general selection."""
+    B, Hq, Hkv, D, steps, nr = 2, 8, 2, 128, 10, 16
     g = Hq // Hkv
     x = inputs.make_qkv(B, Hq, Hkv, T + steps, D, dtype=torch.bfloat16, seed=11,
                         outliers=inputs.outlier_channels(Hkv, D, 1, 11), outlier_scale=12.0)
@@ -65,6 +69,8 @@ def test_mikv_decisions_bit_exact():
             # replace every cumulative score by the same synthetic values on both sides,
             # coarse enough to tie often
             vals = (np.floor(r.random(T + t + 1) * 24) / 8).astype(np.float32)
+            if flat and t % 3 == 2:
+                vals[:] = 1.5
             for j in range(T + t + 1):
                 units[u].cs[j] = vals[j]
             cache.cum_score[u, :T + t + 1] = torch.from_numpy(vals).cuda()
